@@ -1,0 +1,408 @@
+"""Benchmark of the KDA recurrence hot path on one GB300 per rank.
+
+Default workload (N=1): one decode step of one KDA layer for 64 sequences,
+96 heads, d_k = d_v = 128: the short conv (3-token bf16 ring, SiLU) followed
+by the decode step on a 384 MiB fp32 state. `value` is whole-job algorithmic
+bytes per second (GB/s) over the step; `prefill` reports the chunked prefill
+of a 4096-token sequence (96 heads, d=128, C=64) in tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs as one process per GPU under torchrun; every rank runs an
+independent replica (the path needs no exchange), rank 0 prints the line.
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_attention_recurrence_02_gb300 import synth  # noqa: E402
+
+METRIC = "KDA decode state GB/s & prefill tokens/s (H=96,d=128) vs HBM/TC roofline"
+DEC = synth.DECODE
+PRE = synth.PREFILL
+B, H, D = DEC["B"], DEC["H"], DEC["D"]
+UNITS = B * H
+# Algorithmic bytes of one decode step per (sequence, head), conv included:
+# state read + write, q/k/v in (bf16), g (fp32), beta, o out (bf16), conv ring
+# read of 3 tokens x 3 projections and write of the newest token.
+STATE_RW = 2 * D * D * 4
+DEC_UNIT_BYTES = STATE_RW + 3 * D * 2 + D * 4 + 4 + D * 2 + 3 * 3 * D * 2 + 3 * D * 2
+CONV_W_BYTES = 3 * H * D * 4 * 4
+STEP_BYTES = UNITS * DEC_UNIT_BYTES + CONV_W_BYTES
+# the decode kernel alone: state read+write, q,k,v (bf16), g, beta, o (bf16)
+DECODE_KERNEL_UNIT_BYTES = STATE_RW + 3 * D * 2 + D * 4 + 4 + D * 2
+# prefill per token-head: q,k,v bf16 in, g fp32, beta, o bf16 out
+PREFILL_TOKEN_HEAD_BYTES = 3 * D * 2 + D * 4 + 4 + D * 2
+PREFILL_TOKEN_HEAD_FLOPS = 6 * D * D + 5 * PRE["C"] * D
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _src_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_attention_recurrence_02_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel, src_files, units_in_launch):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("src_sha") != _src_sha(*src_files):
+        return None
+    per_unit = rec["dram_bytes"] / rec["units"]
+    return per_unit * units_in_launch
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            args = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.uuid:
+                args.insert(1, f"--id={self.uuid}")
+            self.proc = subprocess.Popen(args, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 7:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[3 + i]
+                          and "Not" not in r[3 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max([num(r[2]) for r in rows if num(r[2]) is not None] or [0])}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- oracle timing
+def _oracle_decode_sample(d, n_seqs, nthreads):
+    """Oracle conv + decode for the first n_seqs sequences; returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    ry, _ = oracle.shortconv_step(d["x"][:n_seqs], d["ring"][:n_seqs], d["w"])
+    oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], d["g"][:n_seqs], d["beta"][:n_seqs], d["s0"][:n_seqs],
+                       nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(d, budget_s=12.0):
+    cores = len(os.sched_getaffinity(0))
+    t1 = _oracle_decode_sample(d, 1, cores)  # calibration: 1 sequence x 96 heads
+    n = int(max(1, min(B, budget_s / 3 / max(t1, 1e-4))))
+    reps, elapsed = 0, 0.0
+    while elapsed < budget_s / 2 or reps == 0:
+        elapsed += _oracle_decode_sample(d, n, cores)
+        reps += 1
+    bytes_done = reps * (n * H * DEC_UNIT_BYTES + CONV_W_BYTES)
+    return {"value": bytes_done / elapsed / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x conv+decode step of {n} of {B} sequences x {H} heads (d={D}), fp64, "
+                      f"{cores} threads over (sequence, head) units, {elapsed:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    d = synth.decode_inputs(DEC["seed"], B, H, D, True)
+    cores = len(os.sched_getaffinity(0))
+    t1 = _oracle_decode_sample(d, 1, cores)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(B, budget / max(t1, 1e-4))))
+    for _ in range(args.warmup):
+        _oracle_decode_sample(d, n, cores)
+    times = [_oracle_decode_sample(d, n, cores) for _ in range(args.steps)]
+    tot = sum(times)
+    value = args.steps * (n * H * DEC_UNIT_BYTES + CONV_W_BYTES) / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"KDA decode step with short conv, B={B} sequences (sample of {n} per step), "
+                               f"H={H}, d_k=d_v={D}, bf16 q/k/v inputs, fp32 state"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"conv+decode step of {n} of {B} sequences x {H} heads per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from linear_attention_recurrence_02_gb300 import build as kbuild
+    from linear_attention_recurrence_02_gb300 import kda
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kbuild.build_library()
+    hbm_peak, tc_peak, tc_sus, peak_src = _peaks()
+
+    d = synth.decode_inputs(DEC["seed"] + 1000 * rank, B, H, D, True)
+    bf = torch.bfloat16
+
+    def up(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev, dt)
+
+    x, ring, w = up(d["x"], bf), up(d["ring"], bf), up(d["w"], torch.float32)
+    g, beta, state = up(d["g"], torch.float32), up(d["beta"], torch.float32), up(d["s0"], torch.float32)
+    y = torch.empty((3, B, H, D), dtype=bf, device=dev)
+    out = torch.empty((B, H, D), dtype=bf, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_a=None, ev_b=None):
+        kda.kda_shortconv_step(x, ring, w, y, stream=stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        kda.kda_decode_step(y[0], y[1], y[2], g, beta, state, out, stream=stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(args.steps):
+            step(ev_a[i], ev_b[i])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    clocks = clk.summary()
+    ms = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    kda.kda_sync_status(stream)
+    ms_per_step = ms / args.steps
+    value = ws * STEP_BYTES / (ms_per_step * 1e-3) / 1e9
+
+    dec_avg_ms = statistics.mean(dec_ms)
+    dec_bytes = UNITS * DECODE_KERNEL_UNIT_BYTES
+    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    traffic = _traffic("decode_step_kernel", ["kda_decode.cu", "kda_common.cuh"], UNITS)
+
+    # end to end through the public API: pinned host inputs in, output back
+    xh = torch.from_numpy(np.ascontiguousarray(d["x"])).to(bf).pin_memory()
+    gh = torch.from_numpy(d["g"]).pin_memory()
+    bh = torch.from_numpy(d["beta"]).pin_memory()
+    oh = torch.empty((B, H, D), dtype=bf).pin_memory()
+    k_e2e = max(1, min(args.steps, 1000))
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        g.copy_(gh, non_blocking=True)
+        beta.copy_(bh, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+
+    for _ in range(min(args.warmup, 20)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(k_e2e):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = s2.elapsed_time(e2) / k_e2e
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = xh.numel() * 2 + gh.numel() * 4 + bh.numel() * 4
+    d2h = oh.numel() * 2
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) q/k/v, g=-softplus(N(0,1)), beta=sigmoid(N(0,1)), "
+                    "state N(0,0.02^2))",
+            "config": {"workload": f"KDA decode step with short conv: B={B} sequences, H={H}, d_k=d_v={D}, "
+                                   f"bf16 q/k/v, fp32 state (384 MiB), 1 layer",
+                       "B": B, "H": H, "d": D, "l2": "state (384 MiB) larger than L2 (129 MB); no flush",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": achieved,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                         "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                         "traffic": traffic, "algorithmic_bytes": dec_bytes,
+                         "avg_launch_us": dec_avg_ms * 1e3},
+            "e2e": {"value": ws * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }
+        if prefill is not None:
+            line["prefill"] = prefill
+        if ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(d)
+        print(json.dumps(line))
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src):
+    """Chunked prefill of one 4096-token sequence, 96 heads, d=128, C=64."""
+    T, C = PRE["T"], PRE["C"]
+    p = synth.prefill_inputs(PRE["seed"], T, H, D, bf16=True)
+    bf = torch.bfloat16
+
+    def up(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev, dt)
+
+    q, k, v = (up(p[n], bf) for n in ("q", "k", "v"))
+    g, beta = up(p["g"], torch.float32), up(p["beta"], torch.float32)
+    out = torch.empty_like(q)
+    sf = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    ws_bytes = kda.kda_chunk_prefill_workspace_bytes(T, 1, H, D, C)
+    wsb = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    try:
+        kda.kda_chunk_prefill(q, k, v, g, beta, out, final_state=sf, chunk_size=C, workspace=wsb, stream=stream)
+    except kda.KdaError as e:
+        return {"unavailable": str(e)}
+    n = max(3, min(args.steps, 200))
+    for _ in range(max(3, min(args.warmup, 10))):
+        kda.kda_chunk_prefill(q, k, v, g, beta, out, final_state=sf, chunk_size=C, workspace=wsb, stream=stream)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        kda.kda_chunk_prefill(q, k, v, g, beta, out, final_state=sf, chunk_size=C, workspace=wsb, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status(stream)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    toks = T * 1.0
+    by = T * H * PREFILL_TOKEN_HEAD_BYTES + H * D * D * 4
+    fl = T * H * PREFILL_TOKEN_HEAD_FLOPS
+    return {"value": ws * toks / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
+            "config": {"workload": f"chunked prefill T={T}, H={H}, d={D}, C={C}, bf16 q/k/v, zero S0, "
+                                   "fp32 final state", "calls": n},
+            "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by},
+            "roofline_tensor": {"achieved": fl / (ms * 1e-3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s",
+                                "frac": fl / (ms * 1e-3) / 1e12 / tc_peak, "algorithmic_flops": fl,
+                                "peak_source": f"{peak_src} bf16_tflops (burst)"}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,158 @@
+/*
+ * kda.h -- C ABI of libkda.so: the Kimi Delta Attention (KDA) gated
+ * delta-rule recurrence on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *  [W] "KV缓存从11.25GB缩到0.21GB: WARP中Kimi Delta Attention线性注意力原理剖析"
+ *      - "KDA 递推公式先衰减再差分": per token and head, decay the state along
+ *        the key axis, S <- Diag(exp(g_t)) S_{t-1} with g in log space, then
+ *        apply the delta rule S_t = S + beta_t k_t (v_t - S^T k_t)^T, then read
+ *        out o_t = S_t^T q_t; q and k are L2-normalised inside the kernel; a
+ *        width-4 causal short convolution with SiLU precedes q/k/v and needs a
+ *        3-token ring per projection at decode, kept as session state.
+ *      - "414MB 的 KDA 状态从哪来": state 128 x 128 fp32 per (layer, head);
+ *        ring 3 projections x 3 tokens x 128 per head.
+ *  [G] "为什么 Kimi K3 敢把 KV Cache 扔掉？一篇讲透 GPT-2 到 K3 的架构进化"
+ *      - section 5: chunked evaluation (attention-like inside a chunk of C
+ *        tokens, state hand-off between chunks, C = 64 or 128 for tensor cores).
+ *      - section 7: the per-channel gate Diag(alpha_t) of Kimi Linear.
+ *
+ * Conventions shared by every call:
+ *  - State S of one (sequence, head) is D x D fp32, row i = key channel,
+ *    column j = value channel, row-major (d_k = d_v = D).
+ *  - Token tensors are token-major and packed: x[t, h, c] at ((t*H)+h)*D + c.
+ *  - q, k are L2-normalised as x / sqrt(sum x^2 + l2_eps); a vector whose
+ *    sum of squares plus l2_eps is zero normalises to zero. v is not
+ *    normalised; q carries no extra 1/sqrt(D) scale.
+ *  - g (log-space gate, per key channel) and beta are always fp32; q, k, v,
+ *    conv inputs/outputs and the outputs o use `dtype`.
+ *  - Every pointer is a DEVICE pointer owned by the caller and must be
+ *    16-byte aligned. Buffers must not alias one another except where a
+ *    call says so. Calls are asynchronous on `stream` (NULL = the legacy
+ *    default stream), launch on the stream's device and allocate nothing.
+ *  - Argument checks are synchronous: a failure returns KDA_ERR_INVALID_ARG
+ *    (or KDA_ERR_UNSUPPORTED) and launches nothing. A failed launch returns
+ *    KDA_ERR_CUDA. kda_last_error_detail() gives the message of the last
+ *    failure on the calling thread.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, short workspace */
+    KDA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+    KDA_ERR_CUDA = 3,        /* CUDA runtime error (launch, device query) */
+    KDA_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
+    KDA_ERR_DEVICE_CHECK = 5 /* a kernel found invalid data (e.g. non-monotone cu_seqlens) */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Static description of a status code. Never NULL. */
+const char *kda_status_string(kda_status s);
+
+/* Message of the last failed call on the calling thread ("" if none). The
+ * pointer stays valid until the next call on this thread. */
+const char *kda_last_error_detail(void);
+
+/* ABI version of this library (increments on incompatible changes). */
+int kda_abi_version(void);
+
+/* Bytes of recurrent state for `layers` x `heads` states of dk x dv fp32
+ * ([W] "414MB 的 KDA 状态从哪来"; 69 x 96 x 128 x 128 x 4 B = 414 MiB). */
+size_t kda_state_bytes(int layers, int heads, int dk, int dv);
+
+/* Bytes of short-conv ring for `layers` x `batch` x `heads`: 3 projections
+ * x 3 cached tokens x d elements of `elem_bytes` each ([W] same table). */
+size_t kda_shortconv_ring_bytes(int layers, int batch, int heads, int d, int elem_bytes);
+
+/*
+ * One decode step of the width-4 causal depthwise short convolution with
+ * SiLU that precedes q, k and v ([W] "KDA 递推公式先衰减再差分", last
+ * paragraph; ring size from "414MB 的 KDA 状态从哪来").
+ *
+ *   x    [B,3,H,D] dtype   current pre-conv projections, p = 0,1,2 = q,k,v
+ *   ring [B,3,H,3,D] dtype in/out: x_{t-3}, x_{t-2}, x_{t-1} (slot 0 oldest);
+ *                          on return holds x_{t-2}, x_{t-1}, x_t
+ *   w    [3,H,D,4] fp32    taps; w[p,h,c,3] multiplies x_t, w[p,h,c,m] for
+ *                          m < 3 multiplies ring slot m
+ *   y    [3,B,H,D] dtype   out: SiLU(w0 r0 + w1 r1 + w2 r2 + w3 x), written
+ *                          projection-major so that y[0], y[1], y[2] are the
+ *                          contiguous [B,H,D] q, k, v of kda_decode_step
+ * Requires B >= 0, H >= 1, D in {16,32,64,128}. y may not alias x or ring.
+ * B = 0 is a no-op.
+ */
+kda_status kda_shortconv_step(const void *x, void *ring, const float *w, void *y,
+                              int B, int H, int D, kda_dtype dtype, kda_stream_t stream);
+
+/*
+ * One KDA decode step for B independent sequences ([W] "KDA 递推公式先衰减再差分";
+ * per-channel gate as in [G] section 7). For each (b, h):
+ *   q^ = L2(q), k^ = L2(k), a = exp(g)
+ *   S' = Diag(a) S;  delta = beta (v - S'^T k^);  S <- S' + k^ delta^T
+ *   o  = S^T q^  (= S'^T q^ + (k^ . q^) delta)
+ * The state is read once and written once.
+ *
+ *   q, k, v [B,H,D] dtype (post-conv);  g [B,H,D] fp32;  beta [B,H] fp32
+ *   state   [B,H,D,D] fp32, in/out (updated in place)
+ *   out     [B,H,D] dtype
+ * Requires B >= 0, H >= 1, D in {16,32,64,128}, l2_eps >= 0. B = 0 is a no-op.
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float *state, void *out, int B, int H, int D,
+                           kda_dtype dtype, float l2_eps, kda_stream_t stream);
+
+/* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
+size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);
+
+/*
+ * Chunked prefill over a packed batch of N sequences ([G] section 5: inside
+ * a chunk of C tokens the work is attention-like, the state is handed from
+ * chunk to chunk; the result equals the token recurrence of
+ * kda_decode_step applied to every token in order).
+ *
+ *   q, k, v [T,H,D] dtype;  g [T,H,D] fp32;  beta [T,H] fp32
+ *   initial_state [N,H,D,D] fp32 or NULL (zeros)
+ *   final_state   [N,H,D,D] fp32 or NULL (not written); may equal
+ *                 initial_state (read before written per (sequence, head))
+ *   out           [T,H,D] dtype
+ *   cu_seqlens    device int64 [N+1], cu_seqlens[0] = 0, non-decreasing,
+ *                 cu_seqlens[N] = T; or NULL for one sequence of T tokens
+ *                 (then N must be 1). Chunks never straddle sequences; a
+ *                 sequence's last chunk may be short; empty sequences pass
+ *                 their initial state through.
+ *   C             chunk size: 1..64 (bf16 with D = 128 and C = 64 takes the
+ *                 tensor-core path; every other combination runs on CUDA cores)
+ *   workspace     device buffer of at least
+ *                 kda_chunk_prefill_workspace_bytes(T, N, H, D, C) bytes
+ *                 (NULL allowed when that is 0); contents are scratch.
+ * Invalid cu_seqlens contents are found on the device: the affected
+ * sequences are skipped and kda_sync_status() reports KDA_ERR_DEVICE_CHECK.
+ */
+kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const float *initial_state, float *final_state,
+                             void *out, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                             int D, int C, kda_dtype dtype, float l2_eps, void *workspace,
+                             size_t workspace_bytes, kda_stream_t stream);
+
+/* Synchronise `stream`, then report (and clear) any device-side error flag
+ * raised by earlier calls on the stream's device: KDA_ERR_DEVICE_CHECK,
+ * KDA_ERR_TIMEOUT, KDA_ERR_CUDA for an asynchronous CUDA error, else KDA_OK. */
+kda_status kda_sync_status(kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

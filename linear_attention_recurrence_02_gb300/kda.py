@@ -1,0 +1,166 @@
+"""Thin ctypes binding of libkda.so (declared in include/kda.h).
+
+Argument marshalling only: shapes and dtypes are read from the torch tensors
+passed in, their device pointers and the current CUDA stream are handed to
+the C ABI, and a non-OK status raises ``KdaError``. Every step of the
+computation runs in the library's CUDA kernels; there is no fallback. If the
+library has not been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE_CHECK = range(6)
+KDA_F32, KDA_BF16 = 0, 1
+
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_ci = ctypes.c_int
+_cf = ctypes.c_float
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "kda_status_string": ([_ci], ctypes.c_char_p),
+    "kda_last_error_detail": ([], ctypes.c_char_p),
+    "kda_abi_version": ([], _ci),
+    "kda_state_bytes": ([_ci, _ci, _ci, _ci], _sz),
+    "kda_shortconv_ring_bytes": ([_ci, _ci, _ci, _ci, _ci], _sz),
+    "kda_shortconv_step": ([_vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _vp], _ci),
+    "kda_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
+    "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
+    "kda_chunk_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
+                           _cf, _vp, _sz, _vp], _ci),
+    "kda_sync_status": ([_vp], _ci),
+}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{_status_string(status)} ({detail})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded CDLL with argument types set (raises if not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            handle = ctypes.CDLL(path)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGNATURES)
+
+
+def _status_string(status: int) -> str:
+    try:
+        return lib().kda_status_string(status).decode()
+    except Exception:  # library unavailable while formatting an error
+        return f"status {status}"
+
+
+def _check(status: int):
+    if status != KDA_OK:
+        raise KdaError(status, lib().kda_last_error_detail().decode())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def state_bytes(layers, heads, dk, dv) -> int:
+    return int(lib().kda_state_bytes(layers, heads, dk, dv))
+
+
+def shortconv_ring_bytes(layers, batch, heads, d, elem_bytes) -> int:
+    return int(lib().kda_shortconv_ring_bytes(layers, batch, heads, d, elem_bytes))
+
+
+def kda_shortconv_step(x, ring, w, y, stream=None):
+    """x [B,3,H,D], ring [B,3,H,3,D] (in/out), w [3,H,D,4] fp32, y [3,B,H,D]."""
+    B, P, H, D = x.shape
+    if P != 3 or tuple(ring.shape) != (B, 3, H, 3, D) or tuple(w.shape) != (3, H, D, 4) \
+            or tuple(y.shape) != (3, B, H, D):
+        raise ValueError("shape mismatch")
+    _check(lib().kda_shortconv_step(_ptr(x), _ptr(ring), _ptr(w), _ptr(y), B, H, D, _dtype_code(x),
+                                    _stream(stream, x.device)))
+
+
+def kda_decode_step(q, k, v, g, beta, state, out, l2_eps=1e-6, stream=None):
+    """q,k,v,out [B,H,D]; g [B,H,D] fp32; beta [B,H] fp32; state [B,H,D,D] fp32 (in/out)."""
+    B, H, D = q.shape
+    if tuple(g.shape) != (B, H, D) or tuple(beta.shape) != (B, H) or tuple(state.shape) != (B, H, D, D) \
+            or tuple(out.shape) != (B, H, D):
+        raise ValueError("shape mismatch")
+    _check(lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
+                                 B, H, D, _dtype_code(q), float(l2_eps), _stream(stream, q.device)))
+
+
+def kda_chunk_prefill_workspace_bytes(total_tokens, num_seqs, H, D, C) -> int:
+    return int(lib().kda_chunk_prefill_workspace_bytes(total_tokens, num_seqs, H, D, C))
+
+
+def kda_chunk_prefill(q, k, v, g, beta, out, initial_state=None, final_state=None, cu_seqlens=None,
+                      chunk_size=64, l2_eps=1e-6, workspace=None, stream=None):
+    """q,k,v,out [T,H,D]; g [T,H,D] fp32; beta [T,H] fp32; states [N,H,D,D] fp32;
+    cu_seqlens int64 [N+1] on the device (or None for one sequence)."""
+    T, H, D = q.shape
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    ws_bytes = kda_chunk_prefill_workspace_bytes(T, N, H, D, chunk_size)
+    if workspace is None and ws_bytes > 0:
+        import torch
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                   _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
+                                   _dtype_code(q), float(l2_eps), _ptr(workspace), wsz,
+                                   _stream(stream, q.device)))
+
+
+def kda_sync_status(stream=None, device=None):
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(lib().kda_sync_status(_stream(stream, dev)))

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU, no compute calls).
+
+The library must load, export every function include/kda.h declares, give
+the memory figures of the WARP write-up ("KV缓存从11.25GB缩到0.21GB: WARP中Kimi
+Delta Attention线性注意力原理剖析", section "414MB 的 KDA 状态从哪来"), and reject
+bad arguments synchronously, before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests._util import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kda():
+    ensure_built()
+    from linear_attention_recurrence_02_gb300 import kda as mod
+    mod.lib()
+    return mod
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(kda):
+    declared = _declared_functions()
+    assert "kda_decode_step" in declared and "kda_chunk_prefill" in declared
+    handle = ctypes.CDLL(kda.library_path())
+    for name in declared:
+        assert hasattr(handle, name), f"{name} declared in kda.h but not exported"
+    assert set(declared) == set(kda.exported_symbols())
+
+
+def test_status_strings(kda):
+    L = kda.lib()
+    for s in range(6):
+        assert L.kda_status_string(s)
+    assert b"unknown" in L.kda_status_string(99)
+    assert L.kda_abi_version() == 1
+
+
+def test_state_bytes_pins_414_mib(kda):
+    # 69 layers x 96 heads x 128 x 128 x 4 B
+    assert kda.state_bytes(69, 96, 128, 128) == 434_110_464
+    assert kda.state_bytes(69, 96, 128, 128) / 2**20 == 414.0
+    assert kda.state_bytes(-1, 96, 128, 128) == 0
+
+
+def test_ring_bytes_pins_about_30_mib(kda):
+    # 69 layers x 96 heads x 3 projections x 3 tokens x 128 x 4 B = 29.1 MiB,
+    # the "~30 MiB" of the 4K memory ledger
+    b = kda.shortconv_ring_bytes(69, 1, 96, 128, 4)
+    assert b == 69 * 96 * 3 * 3 * 128 * 4
+    assert 29.0 < b / 2**20 < 29.2
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+@pytest.mark.parametrize("case,detail", [
+    (dict(D=24), "D must be"),
+    (dict(H=0), "H must be"),
+    (dict(B=-1), "B must be"),
+    (dict(dtype=7), "dtype"),
+    (dict(eps=-1.0), "l2_eps"),
+    (dict(q=None), "q is NULL"),
+    (dict(state=0x10004), "state is not 16-byte aligned"),
+    (dict(out=0x10000), "out must not alias"),
+])
+def test_decode_rejects_bad_arguments(kda, case, detail):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, g=0x40000, beta=0x50000, state=0x60000, out=0x70000,
+             B=2, H=3, D=128, dtype=1, eps=1e-6)
+    a.update(case)
+    L = kda.lib()
+    st = L.kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["state"], a["out"], a["B"], a["H"],
+                           a["D"], a["dtype"], a["eps"], None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    assert detail in L.kda_last_error_detail().decode()
+
+
+@pytest.mark.parametrize("case,detail", [
+    (dict(D=8), "D must be"),
+    (dict(ring=None), "ring is NULL"),
+    (dict(y=0x20000), "y must not alias"),
+    (dict(w=0x30008), "w is not 16-byte aligned"),
+])
+def test_shortconv_rejects_bad_arguments(kda, case, detail):
+    a = dict(x=0x10000, ring=0x20000, w=0x30000, y=0x40000, B=2, H=3, D=128, dtype=1)
+    a.update(case)
+    L = kda.lib()
+    st = L.kda_shortconv_step(a["x"], a["ring"], a["w"], a["y"], a["B"], a["H"], a["D"], a["dtype"], None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    assert detail in L.kda_last_error_detail().decode()
+
+
+def test_zero_batch_is_a_noop_without_cuda(kda):
+    L = kda.lib()
+    assert L.kda_decode_step(None, None, None, None, None, None, None, 0, 3, 128, 1, 1e-6, None) == kda.KDA_OK
+    assert L.kda_shortconv_step(None, None, None, None, 0, 3, 128, 1, None) == kda.KDA_OK
