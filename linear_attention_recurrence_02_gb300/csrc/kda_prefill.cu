@@ -1,13 +1,275 @@
-// kda_prefill.cu -- chunked prefill (placeholder until the kernels land).
+// kda_prefill.cu -- chunked prefill of the KDA recurrence: argument checks,
+// dispatch, and the general CUDA-core kernel (any D in {16,32,64,128}, any
+// chunk size 1..64, fp32 or bf16 token tensors).
+//
+// Chunk algebra ("为什么 Kimi K3 敢把 KV Cache 扔掉？一篇讲透 GPT-2 到 K3 的架构进化",
+// section 5: attention-like work inside a chunk, state handed between chunks;
+// section 6: decay between two positions is the product of the gates in
+// between, here exp of a difference of cumulative log gates). For a chunk of
+// L tokens entering with state S, with G_r = sum_{s<=r} g_s per key channel:
+//   A_rs = beta_r sum_i k_ri k_si exp(G_ri - G_si)     (s < r)
+//   P_rs = sum_i q_ri k_si exp(G_ri - G_si)             (s <= r)
+//   (I + A) U = Diag(beta) (V - Kt S),      Kt_r = exp(G_r) . k_r
+//   O = Qt S + P U,                         Qt_r = exp(G_r) . q_r
+//   S' = Diag(exp(G_L)) S + Kb^T U,         Kb_s = exp(G_L - G_s) . k_s
+// (q, k already L2-normalised). U is found by forward substitution. This is
+// exact algebra of the token recurrence, so any chunk size gives the same
+// result up to rounding.
+//
+// One CTA per (sequence, head, slice of JS value columns) walks the chunks of
+// its sequence in order. The state slice stays in shared memory for the whole
+// sequence. A and P use exact pairwise exponentials, so the kernel is robust
+// to any finite gate; it is the reference-grade fp32 path, not the fast one.
+#include <algorithm>
+#include <string>
+
 #include "kda_common.cuh"
+#include "kda_prefill.cuh"
+
+namespace kda {
+
+constexpr int SIMT_NT = 256;
+constexpr int SIMT_CMAX = 64;
+
+__host__ __device__ constexpr int simt_js(int D) { return D < 64 ? D : 64; }
+
+__host__ __device__ inline size_t simt_smem_floats(int D, int C) {
+    const int LD = D + 1, JS = simt_js(D);
+    return (size_t)3 * C * LD + (size_t)D * JS + (size_t)C * JS + 2 * (size_t)C * C + 2 * (size_t)D + C;
+}
+
+// Validated [start, end) of sequence n, or false (and the error word is set).
+__device__ __forceinline__ bool seq_range(const int64_t *cu, int n, int N, int64_t T, unsigned *err,
+                                          int64_t &start, int64_t &end) {
+    if (cu == nullptr) {
+        start = 0;
+        end = T;
+        return true;
+    }
+    start = cu[n];
+    end = cu[n + 1];
+    bool ok = start >= 0 && start <= end && end <= T && (n != 0 || start == 0) && (n != N - 1 || end == T);
+    if (!ok && err) atomicOr(err, DEVERR_SEQLENS);
+    return ok;
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(SIMT_NT)
+    prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                        const float *__restrict__ g, const float *__restrict__ beta,
+                        const float *s_init, float *s_final, T *__restrict__ out,
+                        const int64_t *__restrict__ cu_seqlens, int N, int64_t Ttot, int H, int C, float eps,
+                        unsigned *err) {
+    constexpr int JS = simt_js(D), LD = D + 1, NS = D / JS, NW = SIMT_NT / 32;
+    extern __shared__ float smem[];
+    float *sQ = smem;                    // [C][LD]  q^, then Qt
+    float *sK = sQ + C * LD;             // [C][LD]  k^, then Kt
+    float *sG = sK + C * LD;             // [C][LD]  G, then Kb
+    float *sS = sG + C * LD;             // [D][JS]  state slice
+    float *sU = sS + D * JS;             // [C][JS]  v, rhs, then U
+    float *sA = sU + C * JS;             // [C][C]
+    float *sP = sA + C * C;              // [C][C]
+    float *sGL = sP + C * C;             // [D]      exp(G_L)
+    float *sGLl = sGL + D;               // [D]      G_L
+    float *sB = sGLl + D;                // [C]      beta
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int slice = blockIdx.x % NS;
+    const int h = (blockIdx.x / NS) % H;
+    const int n = blockIdx.x / (NS * H);
+    const int j0 = slice * JS;
+    int64_t start, end;
+    if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
+
+    const size_t sbase = ((size_t)n * H + h) * D * D;
+    for (int p = tid; p < D * JS; p += SIMT_NT) {
+        const int i = p / JS, j = p % JS;
+        sS[p] = s_init ? s_init[sbase + (size_t)i * D + j0 + j] : 0.f;
+    }
+
+    for (int64_t c0 = start; c0 < end; c0 += C) {
+        const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
+        __syncthreads();
+        // q^, k^ rows (one warp per row), beta, v slice
+        for (int r = warp; r < L; r += NW) {
+            const size_t o = ((size_t)(c0 + r) * H + h) * D;
+            float sq = 0.f, sk = 0.f;
+            for (int i = lane; i < D; i += 32) {
+                const float a = Elem<T>::load(q + o + i), b = Elem<T>::load(k + o + i);
+                sQ[r * LD + i] = a;
+                sK[r * LD + i] = b;
+                sq += a * a;
+                sk += b * b;
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, m);
+                sk += __shfl_xor_sync(0xffffffffu, sk, m);
+            }
+            const float rq = inv_norm(sq, eps), rk = inv_norm(sk, eps);
+            for (int i = lane; i < D; i += 32) {
+                sQ[r * LD + i] *= rq;
+                sK[r * LD + i] *= rk;
+            }
+            if (lane == 0) sB[r] = beta[(size_t)(c0 + r) * H + h];
+        }
+        for (int p = tid; p < L * JS; p += SIMT_NT) {
+            const int r = p / JS, j = p % JS;
+            sU[p] = Elem<T>::load(v + ((size_t)(c0 + r) * H + h) * D + j0 + j);
+        }
+        // cumulative log decay per key channel
+        if (tid < D) {
+            float acc = 0.f;
+            for (int r = 0; r < L; ++r) {
+                acc += g[((size_t)(c0 + r) * H + h) * D + tid];
+                sG[r * LD + tid] = acc;
+            }
+        }
+        __syncthreads();
+        // A and P with exact pairwise decays
+        for (int p = tid; p < L * L; p += SIMT_NT) {
+            const int r = p / L, s = p % L;
+            float a = 0.f, pq = 0.f;
+            if (s <= r) {
+                for (int i = 0; i < D; ++i) {
+                    const float e = expf(sG[r * LD + i] - sG[s * LD + i]);
+                    const float ks = sK[s * LD + i] * e;
+                    a += sK[r * LD + i] * ks;
+                    pq += sQ[r * LD + i] * ks;
+                }
+            }
+            sA[r * C + s] = (s < r) ? sB[r] * a : 0.f;
+            sP[r * C + s] = pq;
+        }
+        if (tid < D) {
+            sGLl[tid] = sG[(L - 1) * LD + tid];
+            sGL[tid] = expf(sGLl[tid]);
+        }
+        __syncthreads();
+        // Qt, Kt, Kb in place
+        for (int p = tid; p < L * D; p += SIMT_NT) {
+            const int r = p / D, i = p % D;
+            const float Gr = sG[r * LD + i], e = expf(Gr);
+            const float kh = sK[r * LD + i];
+            sQ[r * LD + i] *= e;
+            sK[r * LD + i] = kh * e;
+            sG[r * LD + i] = kh * expf(sGLl[i] - Gr);
+        }
+        __syncthreads();
+        // rhs = beta (v - Kt S)
+        for (int p = tid; p < L * JS; p += SIMT_NT) {
+            const int r = p / JS, j = p % JS;
+            float acc = 0.f;
+            for (int i = 0; i < D; ++i) acc += sK[r * LD + i] * sS[i * JS + j];
+            sU[p] = sB[r] * (sU[p] - acc);
+        }
+        __syncthreads();
+        // forward substitution (I + A) U = rhs, one thread per value column
+        if (tid < JS) {
+            for (int r = 1; r < L; ++r) {
+                float acc = sU[r * JS + tid];
+                for (int s = 0; s < r; ++s) acc -= sA[r * C + s] * sU[s * JS + tid];
+                sU[r * JS + tid] = acc;
+            }
+        }
+        __syncthreads();
+        // O = Qt S + P U
+        for (int p = tid; p < L * JS; p += SIMT_NT) {
+            const int r = p / JS, j = p % JS;
+            float acc = 0.f;
+            for (int i = 0; i < D; ++i) acc += sQ[r * LD + i] * sS[i * JS + j];
+            for (int s = 0; s <= r; ++s) acc += sP[r * C + s] * sU[s * JS + j];
+            Elem<T>::store(out + ((size_t)(c0 + r) * H + h) * D + j0 + j, acc);
+        }
+        __syncthreads();
+        // S' = Diag(exp(G_L)) S + Kb^T U
+        for (int p = tid; p < D * JS; p += SIMT_NT) {
+            const int i = p / JS, j = p % JS;
+            float acc = sGL[i] * sS[p];
+            for (int s = 0; s < L; ++s) acc += sG[s * LD + i] * sU[s * JS + j];
+            sS[p] = acc;
+        }
+    }
+    __syncthreads();
+    if (s_final) {
+        for (int p = tid; p < D * JS; p += SIMT_NT) {
+            const int i = p / JS, j = p % JS;
+            s_final[sbase + (size_t)i * D + j0 + j] = sS[p];
+        }
+    }
+}
+
+template <int D, typename T>
+static kda_status launch_simt(const PrefillArgs &a, cudaStream_t s) {
+    const size_t smem = simt_smem_floats(D, a.C) * sizeof(float);
+    auto kern = prefill_simt_kernel<D, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    const unsigned grid = (unsigned)a.N * a.H * (D / simt_js(D));
+    kern<<<grid, SIMT_NT, smem, s>>>(static_cast<const T *>(a.q), static_cast<const T *>(a.k),
+                                     static_cast<const T *>(a.v), a.g, a.beta, a.s_init, a.s_final,
+                                     static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err);
+    return check_launch("prefill_simt_kernel");
+}
+
+template <typename T>
+static kda_status dispatch_simt(const PrefillArgs &a, cudaStream_t s) {
+    switch (a.D) {
+    case 16: return launch_simt<16, T>(a, s);
+    case 32: return launch_simt<32, T>(a, s);
+    case 64: return launch_simt<64, T>(a, s);
+    default: return launch_simt<128, T>(a, s);
+    }
+}
+
+kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s) {
+    return a.bf16 ? dispatch_simt<__nv_bfloat16>(a, s) : dispatch_simt<float>(a, s);
+}
+
+}  // namespace kda
 
 using namespace kda;
 
-extern "C" size_t kda_chunk_prefill_workspace_bytes(int64_t, int, int, int, int) { return 0; }
+extern "C" size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C) {
+    (void)total_tokens;
+    (void)num_seqs;
+    (void)H;
+    (void)D;
+    (void)C;
+    return 0;
+}
 
-extern "C" kda_status kda_chunk_prefill(const void *, const void *, const void *, const float *, const float *,
-                                        const float *, float *, void *, const int64_t *, int, int64_t, int, int,
-                                        int, kda_dtype, float, void *, size_t, kda_stream_t) {
+extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
+                                        const float *beta, const float *initial_state, float *final_state,
+                                        void *out, const int64_t *cu_seqlens, int N, int64_t T, int H, int D,
+                                        int C, kda_dtype dtype, float l2_eps, void *workspace,
+                                        size_t workspace_bytes, kda_stream_t stream) {
     clear_detail();
-    return fail(KDA_ERR_UNSUPPORTED, "chunked prefill not built yet");
+    if (N < 1) return invalid("N must be >= 1");
+    if (T < 0) return invalid("T must be >= 0");
+    if (H < 1) return invalid("H must be >= 1");
+    if (!valid_head_dim(D)) return invalid("D must be one of 16, 32, 64, 128");
+    if (C < 1 || C > SIMT_CMAX) return invalid("C must be in 1..64");
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return invalid("dtype must be KDA_F32 or KDA_BF16");
+    if (!(l2_eps >= 0.f)) return invalid("l2_eps must be >= 0");
+    if (cu_seqlens == nullptr && N != 1) return invalid("cu_seqlens is NULL but N != 1");
+    if ((long long)N * H * 2 > 0x7fffffffLL) return invalid("N*H too large for one launch");
+    const size_t need = kda_chunk_prefill_workspace_bytes(T, N, H, D, C);
+    if (workspace_bytes < need) return invalid("workspace too small");
+    kda_status st;
+    if (T > 0 && ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
+                  (st = check_ptr(g, "g")) || (st = check_ptr(beta, "beta")) || (st = check_ptr(out, "out"))))
+        return st;
+    if (initial_state && (st = check_ptr(initial_state, "initial_state"))) return st;
+    if (final_state && (st = check_ptr(final_state, "final_state"))) return st;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 7u)) return invalid("cu_seqlens is not 8-byte aligned");
+    if (need && (st = check_ptr(workspace, "workspace"))) return st;
+    if (T > 0 && (out == q || out == k || out == v)) return invalid("out must not alias q, k or v");
+    if (T == 0 && final_state == nullptr) return KDA_OK;
+    if ((st = bind_stream_device(stream))) return st;
+    PrefillArgs a{q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C,
+                  dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word()};
+    if (a.err == nullptr) return fail(KDA_ERR_CUDA, "device error word unavailable");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return prefill_simt(a, s);
 }
