@@ -38,21 +38,6 @@ __host__ __device__ inline size_t simt_smem_floats(int D, int C) {
     return (size_t)3 * C * LD + (size_t)D * JS + (size_t)C * JS + 2 * (size_t)C * C + 2 * (size_t)D + C;
 }
 
-// Validated [start, end) of sequence n, or false (and the error word is set).
-__device__ __forceinline__ bool seq_range(const int64_t *cu, int n, int N, int64_t T, unsigned *err,
-                                          int64_t &start, int64_t &end) {
-    if (cu == nullptr) {
-        start = 0;
-        end = T;
-        return true;
-    }
-    start = cu[n];
-    end = cu[n + 1];
-    bool ok = start >= 0 && start <= end && end <= T && (n != 0 || start == 0) && (n != N - 1 || end == T);
-    if (!ok && err) atomicOr(err, DEVERR_SEQLENS);
-    return ok;
-}
-
 template <int D, typename T>
 __global__ void __launch_bounds__(SIMT_NT)
     prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
@@ -271,5 +256,5 @@ extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void
                   dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word()};
     if (a.err == nullptr) return fail(KDA_ERR_CUDA, "device error word unavailable");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return prefill_simt(a, s);
+    return prefill_tc_applicable(a) ? prefill_tc(a, s) : prefill_simt(a, s);
 }

@@ -24,5 +24,23 @@ struct PrefillArgs {
 };
 
 kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s);
+bool prefill_tc_applicable(const PrefillArgs &a);
+kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s);
+
+// Validated [start, end) of sequence n; on invalid cu_seqlens sets the
+// device error word and returns false (the caller skips the sequence).
+__device__ __forceinline__ bool seq_range(const int64_t *cu, int n, int N, int64_t T, unsigned *err,
+                                          int64_t &start, int64_t &end) {
+    if (cu == nullptr) {
+        start = 0;
+        end = T;
+        return true;
+    }
+    start = cu[n];
+    end = cu[n + 1];
+    const bool ok = start >= 0 && start <= end && end <= T && (n != 0 || start == 0) && (n != N - 1 || end == T);
+    if (!ok && err) atomicOr(err, DEVERR_SEQLENS);
+    return ok;
+}
 
 }  // namespace kda
