@@ -43,19 +43,25 @@ using namespace tc;
 
 constexpr int C = 64, D = 128, NT = 256;
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_QRAW = 0;        // q tile (TMA) -> W' tile (MN-major, rows i)
-constexpr uint32_t OFF_KRAW = 16384;    // k tile (TMA) -> U^T tile (K-major, rows j)
-constexpr uint32_t OFF_V = 32768;       // v tile (TMA)
-constexpr uint32_t OFF_G = 49152;       // g fp32 [64][128] (TMA) -> G -> M^-1 (fp32, column-major) + scratch
-constexpr uint32_t OFF_LKQ = 81920;     // [Lk; Lq] 128 rows
-constexpr uint32_t OFF_RK = 114688;     // Rk 64 rows -> A^T fp32 [64][64]
+constexpr uint32_t OFF_QRAW = 0;        // q tile (TMA, prefetched one chunk ahead)
+constexpr uint32_t OFF_KRAW = 16384;    // k tile (TMA, prefetched)
+constexpr uint32_t OFF_V = 32768;       // v tile (TMA, prefetched after G3)
+constexpr uint32_t OFF_G = 49152;       // g fp32 [64][128] (TMA, prefetched) -> cumulative G
+constexpr uint32_t OFF_LKQ = 81920;     // [Lk; Lq] 128 rows -> W' (rows i) + U^T (rows j) -> O staging
+constexpr uint32_t OFF_W = OFF_LKQ;
+constexpr uint32_t OFF_U = OFF_LKQ + 16384;
+constexpr uint32_t OFF_OST = OFF_LKQ;
+constexpr uint32_t OFF_RK = 114688;     // Rk 64 rows -> A (fp32 [64][64], row-major, swizzled)
 constexpr uint32_t OFF_KB = 131072;     // Kb 64 rows
 constexpr uint32_t OFF_SOP = 147456;    // S~^T 128 rows (j) x 128 (i)
 constexpr uint32_t OFF_T = 180224;      // T 64 rows (r) x 64 (s)
 constexpr uint32_t OFF_P = 188416;      // P 64 rows (r) x 64 (s)
-constexpr uint32_t OFF_SMALL = 196608;  // per-row / per-channel vectors, barriers
-constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;
-constexpr uint32_t LOAD_BYTES = 3 * 16384 + 32768;
+constexpr uint32_t OFF_MT = 196608;     // M^-1 fp32 [64][64], column-major, swizzled
+constexpr uint32_t OFF_Y = 212992;      // blocked-inverse scratch (3 KiB) + diagonal block inverses (4 KiB)
+constexpr uint32_t OFF_SMALL = 221184;  // per-row / per-channel vectors, barriers
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + 3072 + 1024;
+constexpr uint32_t QKG_BYTES = 2 * 16384 + 32768;
+constexpr uint32_t V_BYTES = 16384;
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_S = 0, TM_AP = 128, TM_W = 192, TM_U0 = 256, TM_X = 320, TM_O = 384;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
@@ -71,6 +77,10 @@ constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, 0, 1);
 __device__ __forceinline__ uint32_t swz(int row, int cc, int rows) {
     return (uint32_t)((cc >> 3) * rows * 128 + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
 }
+// float index of the 4-float group k4 (0..15) of row r in a 64 x 64 fp32
+// matrix whose 16-byte groups are XOR-swizzled by the row (bank-conflict free
+// for 16-byte accesses by consecutive rows)
+__device__ __forceinline__ int fsw(int r, int k4) { return r * 64 + ((k4 ^ (r & 7)) << 2); }
 
 __device__ __forceinline__ uint4 pack8(const float *f) {
     uint4 u;
@@ -122,28 +132,43 @@ __global__ void __launch_bounds__(NT, 1)
     float *s_c = s_gl + 128;
     float *s_expc = s_c + 128;
     float *s_expgl = s_expc + 128;
-    uint64_t *bar_load = reinterpret_cast<uint64_t *>(s_expgl + 128);
-    uint64_t *bar_mma = bar_load + 1;
-    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bar_mma + 1);
+    uint64_t *bar_qkg = reinterpret_cast<uint64_t *>(s_expgl + 128);
+    uint64_t *bar_v = bar_qkg + 1;
+    uint64_t *bar_mma = bar_qkg + 2;
+    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bar_qkg + 3);
     float *gt = reinterpret_cast<float *>(sm + OFF_G);
-    float *AT = reinterpret_cast<float *>(sm + OFF_RK);  // A^T: AT[s*64 + r] = A[r][s]
-    float *MT = gt;                                      // M^-1 column-major: MT[s*64 + r]
-    float *Yb = gt + 4096;                               // scratch for the blocked inverse
+    float *Am = reinterpret_cast<float *>(sm + OFF_RK);  // A[r][s] at fsw(r, s/4) + s%4
+    float *MT = reinterpret_cast<float *>(sm + OFF_MT);  // M^-1[k][s] at fsw(s, k/4) + k%4
+    float *Yb = reinterpret_cast<float *>(sm + OFF_Y);   // [block][s_local][k_local]
+    float *Dv = Yb + 768;                                // diagonal inverses [block][row][col]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q4 = warp & 3, hh = warp >> 2;
     const int h = blockIdx.x % H, n = blockIdx.x / H;
     int64_t start, end;
     if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
+    const int x0 = h * D;
 
     if (tid == 0) {
-        mbar_init(bar_load, 1);
+        mbar_init(bar_qkg, 1);
+        mbar_init(bar_v, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_g);
+        if (start < end) {
+            mbar_arrive_expect_tx(bar_qkg, QKG_BYTES);
+            tma_load_2d(sm + OFF_QRAW, &tm_q, bar_qkg, x0, (int)start);
+            tma_load_2d(sm + OFF_QRAW + 8192, &tm_q, bar_qkg, x0 + 64, (int)start);
+            tma_load_2d(sm + OFF_KRAW, &tm_k, bar_qkg, x0, (int)start);
+            tma_load_2d(sm + OFF_KRAW + 8192, &tm_k, bar_qkg, x0 + 64, (int)start);
+            tma_load_2d(sm + OFF_G, &tm_g, bar_qkg, x0, (int)start);
+            mbar_arrive_expect_tx(bar_v, V_BYTES);
+            tma_load_2d(sm + OFF_V, &tm_v, bar_v, x0, (int)start);
+            tma_load_2d(sm + OFF_V + 8192, &tm_v, bar_v, x0 + 64, (int)start);
+        }
     }
     if (warp == 0) {
         tmem_alloc(s_taddr, 512);
@@ -168,30 +193,22 @@ __global__ void __launch_bounds__(NT, 1)
     }
     tmem_st_wait();
 
-    uint32_t ph_load = 0, ph_mma = 0;
+    uint32_t ph = 0, ph_mma = 0;
     bool ok = true;
-    for (int64_t c0 = start; c0 < end; c0 += C) {
+    float beta_reg = 0.f;  // beta of the next chunk, loaded one chunk ahead
+    if (tid < C && start + tid < end) beta_reg = beta[(size_t)(start + tid) * H + h];
+    for (int64_t c0 = start; c0 < end; c0 += C, ph ^= 1) {
         const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
-        sync_for_mma();  // previous chunk fully consumed before its buffers are refilled
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_load, LOAD_BYTES);
-            const int x0 = h * D, y0 = (int)c0;
-            tma_load_2d(sm + OFF_QRAW, &tm_q, bar_load, x0, y0);
-            tma_load_2d(sm + OFF_QRAW + 8192, &tm_q, bar_load, x0 + 64, y0);
-            tma_load_2d(sm + OFF_KRAW, &tm_k, bar_load, x0, y0);
-            tma_load_2d(sm + OFF_KRAW + 8192, &tm_k, bar_load, x0 + 64, y0);
-            tma_load_2d(sm + OFF_V, &tm_v, bar_load, x0, y0);
-            tma_load_2d(sm + OFF_V + 8192, &tm_v, bar_load, x0 + 64, y0);
-            tma_load_2d(sm + OFF_G, &tm_g, bar_load, x0, y0);
-        }
-        if (tid < C) s_beta[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
-        bool got = mbar_wait(bar_load, ph_load, WAIT_LIMIT);
+        const bool has_next = c0 + C < end;
+        sync_for_mma();  // previous chunk fully consumed
+        if (tid < C) s_beta[tid] = beta_reg;
+        bool got = mbar_wait(bar_qkg, ph, WAIT_LIMIT) && mbar_wait(bar_v, ph, WAIT_LIMIT);
         if (__syncthreads_or(!got)) {
-            mbar_wait(bar_load, ph_load, WAIT_LIMIT);
+            mbar_wait(bar_qkg, ph, WAIT_LIMIT);
+            mbar_wait(bar_v, ph, WAIT_LIMIT);
             ok = false;
             break;
         }
-        ph_load ^= 1;
 
         // rows past the end of the sequence: zero q, k, v, g (so beta = 0,
         // k = 0 and G stays at G_{L-1}); they then contribute nothing
@@ -209,36 +226,55 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
         }
 
-        // L2 norms of the q and k rows (one warp per row, 8 bytes per lane)
-        for (int rr = warp; rr < 2 * C; rr += NT / 32) {
-            const int r = rr & 63;
-            const uint8_t *tile = sm + (rr < C ? OFF_QRAW : OFF_KRAW);
-            const int kb = lane >> 4, ch = (lane & 15) >> 1, half = lane & 1;
-            const uint2 u = *reinterpret_cast<const uint2 *>(tile + kb * 8192 + r * 128 + ((ch ^ (r & 7)) << 4) +
-                                                             half * 8);
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-            const float f0 = __bfloat162float(a.x), f1 = __bfloat162float(a.y), f2 = __bfloat162float(b.x),
-                        f3 = __bfloat162float(b.y);
-            float ss = f0 * f0 + f1 * f1 + f2 * f2 + f3 * f3;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (lane == 0) (rr < C ? s_rq : s_rk)[r] = inv_norm(ss, eps);
-        }
-        // cumulative log decay G along the chunk (two halves, then fix-up)
+        // L2 norms of the q and k rows: 16 lanes per row, 8 channels per lane
         {
-            const int i = tid & 127, r0 = (tid >> 7) * 32;
-            float acc = 0.f;
-            for (int r = r0; r < r0 + 32; ++r) {
-                acc += gt[r * 128 + i];
-                gt[r * 128 + i] = acc;
+            const int cc = tid & 15, rb = tid >> 4;
+            float sq[4], sk[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t o = swz(rb + 16 * m, cc, 64);
+                float qf[8], kf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + o), qf);
+                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + o), kf);
+                sq[m] = sk[m] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sq[m] += qf[e] * qf[e];
+                    sk[m] += kf[e] * kf[e];
+                }
             }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    sq[m] += __shfl_xor_sync(0xffffffffu, sq[m], o);
+                    sk[m] += __shfl_xor_sync(0xffffffffu, sk[m], o);
+                }
+            if (cc == 0)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    s_rq[rb + 16 * m] = inv_norm(sq[m], eps);
+                    s_rk[rb + 16 * m] = inv_norm(sk[m], eps);
+                }
         }
-        __syncthreads();
-        if (tid >= 128) {
-            const int i = tid - 128;
-            const float base = gt[31 * 128 + i];
-            for (int r = 32; r < 64; ++r) gt[r * 128 + i] += base;
+        // cumulative log decay G along the chunk: each half-block scans 32 rows
+        // in registers, then the second half adds the first half's total
+        {
+            const int i = tid & 127, half = tid >> 7;
+            float gv[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) gv[r] = gt[(32 * half + r) * 128 + i];
+#pragma unroll
+            for (int r = 1; r < 32; ++r) gv[r] += gv[r - 1];
+            if (half == 0)
+#pragma unroll
+                for (int r = 0; r < 32; ++r) gt[r * 128 + i] = gv[r];
+            __syncthreads();
+            if (half == 1) {
+                const float base = gt[31 * 128 + i];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) gt[(32 + r) * 128 + i] = gv[r] + base;
+            }
         }
         __syncthreads();
         // per-channel anchor; a chunk whose decay span exceeds SPAN_MAX takes the exact path
@@ -247,40 +283,56 @@ __global__ void __launch_bounds__(NT, 1)
         const int exact = __syncthreads_or(bad);
         if (tid < 128) {
             const float GL = gt[63 * 128 + tid];
-            const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
             s_gl[tid] = GL;
+            const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
             s_c[tid] = c;
             s_expc[tid] = expf(c);
             s_expgl[tid] = expf(GL);
         }
         __syncthreads();
 
-        // operand tiles Lk, Lq, Rk, Kb (bf16, swizzled) from q^, k^ and G
-        for (int p = tid; p < C * 16; p += NT) {
-            const int r = p >> 4, cc = p & 15;
-            const uint32_t o64 = swz(r, cc, 64);
-            float qf[8], kf[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + o64), qf);
-            unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + o64), kf);
-            const float rq = s_rq[r], rk = s_rk[r];
-            const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
-            const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
-            const float G[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-            float lk[8], lq[8], rkv[8], kbv[8];
+        // operand tiles Lk, Lq, Rk, Kb (bf16, swizzled) from q^, k^ and G;
+        // each thread keeps one 8-channel group and walks 4 rows
+        {
+            const int cc = tid & 15, rb = tid >> 4;
+            float cv[8], egc[8], glv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int i = cc * 8 + e;
-                const float kh = kf[e] * rk, qh = qf[e] * rq;
-                const float e1 = __expf(G[e] - s_c[i]);
-                lk[e] = e1 * kh;
-                lq[e] = e1 * qh;
-                rkv[e] = __expf(s_c[i] - G[e]) * kh;
-                kbv[e] = __expf(s_gl[i] - G[e]) * kh;
+                cv[e] = s_c[cc * 8 + e];
+                glv[e] = s_gl[cc * 8 + e];
+                egc[e] = __expf(glv[e] - cv[e]);
             }
-            *reinterpret_cast<uint4 *>(sm + OFF_LKQ + swz(r, cc, 128)) = pack8(lk);
-            *reinterpret_cast<uint4 *>(sm + OFF_LKQ + swz(r + 64, cc, 128)) = pack8(lq);
-            if (!exact) *reinterpret_cast<uint4 *>(sm + OFF_RK + o64) = pack8(rkv);
-            *reinterpret_cast<uint4 *>(sm + OFF_KB + o64) = pack8(kbv);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = rb + 16 * m;
+                const uint32_t o64 = swz(r, cc, 64);
+                float qf[8], kf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + o64), qf);
+                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + o64), kf);
+                const float rq = s_rq[r], rk = s_rk[r];
+                const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
+                const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
+                const float G[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                float lk[8], lq[8], rkv[8], kbv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float kh = kf[e] * rk, qh = qf[e] * rq;
+                    const float e1 = __expf(G[e] - cv[e]);
+                    lk[e] = e1 * kh;
+                    lq[e] = e1 * qh;
+                    if (!exact) {
+                        const float inv = __expf(cv[e] - G[e]);  // <= e^80
+                        rkv[e] = inv * kh;
+                        kbv[e] = egc[e] * inv * kh;
+                    } else {
+                        kbv[e] = __expf(glv[e] - G[e]) * kh;
+                    }
+                }
+                *reinterpret_cast<uint4 *>(sm + OFF_LKQ + swz(r, cc, 128)) = pack8(lk);
+                *reinterpret_cast<uint4 *>(sm + OFF_LKQ + swz(r + 64, cc, 128)) = pack8(lq);
+                if (!exact) *reinterpret_cast<uint4 *>(sm + OFF_RK + o64) = pack8(rkv);
+                *reinterpret_cast<uint4 *>(sm + OFF_KB + o64) = pack8(kbv);
+            }
         }
 
         // S~^T = S^T Diag(e^c) as a bf16 operand; S^T <- S^T Diag(e^{G_L}) in TMEM
@@ -308,7 +360,7 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_st_wait();
 
         if (exact) {
-            // A^T and P with exact pairwise decays (rare: decay span > e^160)
+            // A and P with exact pairwise decays (rare: decay span > e^160)
             for (int p = tid; p < C * C; p += NT) {
                 const int r = p & 63, s = p >> 6;
                 float a = 0.f, pq = 0.f;
@@ -328,15 +380,26 @@ __global__ void __launch_bounds__(NT, 1)
                         }
                     }
                 }
-                AT[s * 64 + r] = (s < r) ? s_beta[r] * a : 0.f;
+                Am[fsw(r, s >> 2) + (s & 3)] = (s < r) ? s_beta[r] * a : 0.f;
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_P + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) +
                                                    (s & 7) * 2) = __float2bfloat16_rn(pq);
             }
         }
         sync_for_mma();
 
+        if (tid < C) beta_reg = (has_next && c0 + C + tid < end) ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
+        // q, k, g of this chunk are consumed: prefetch the next chunk's.
         // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T   and   G5: O = Lq S~ (as O^T = S~^T Lq^T)
         if (tid == 0) {
+            if (has_next) {
+                const int y1 = (int)(c0 + C);
+                mbar_arrive_expect_tx(bar_qkg, QKG_BYTES);
+                tma_load_2d(sm + OFF_QRAW, &tm_q, bar_qkg, x0, y1);
+                tma_load_2d(sm + OFF_QRAW + 8192, &tm_q, bar_qkg, x0 + 64, y1);
+                tma_load_2d(sm + OFF_KRAW, &tm_k, bar_qkg, x0, y1);
+                tma_load_2d(sm + OFF_KRAW + 8192, &tm_k, bar_qkg, x0 + 64, y1);
+                tma_load_2d(sm + OFF_G, &tm_g, bar_qkg, x0, y1);
+            }
             if (!exact) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -372,7 +435,15 @@ __global__ void __launch_bounds__(NT, 1)
                 const int r = 32 * q4 + lane;
                 const float br = s_beta[r];
 #pragma unroll
-                for (int m = 0; m < 32; ++m) AT[(s0 + m) * 64 + r] = (s0 + m < r) ? br * __uint_as_float(r32[m]) : 0.f;
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    float4 a4;
+                    const int s = s0 + 4 * g4;
+                    a4.x = (s + 0 < r) ? br * __uint_as_float(r32[4 * g4 + 0]) : 0.f;
+                    a4.y = (s + 1 < r) ? br * __uint_as_float(r32[4 * g4 + 1]) : 0.f;
+                    a4.z = (s + 2 < r) ? br * __uint_as_float(r32[4 * g4 + 2]) : 0.f;
+                    a4.w = (s + 3 < r) ? br * __uint_as_float(r32[4 * g4 + 3]) : 0.f;
+                    *reinterpret_cast<float4 *>(Am + fsw(r, s >> 2)) = a4;
+                }
             } else {
                 const int r = 32 * (q4 - 2) + lane;
                 float pv[32];
@@ -387,51 +458,87 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
 
-        // T = (I + A)^-1 Diag(beta): diagonal 16x16 blocks by forward substitution ...
+        // M^-1 = (I + A)^-1, A strictly lower. Diagonal 16 x 16 blocks by
+        // forward substitution (one thread per column) ...
         if (tid < 64) {
-            const int s0 = tid, b0 = (tid >> 4) * 16;
+            const int b = tid >> 4, cl = tid & 15, s0 = tid, b0 = 16 * b;
             float x[16];
 #pragma unroll
             for (int rl = 0; rl < 16; ++rl) {
-                const int r = b0 + rl;
-                float v = (r == s0) ? 1.f : 0.f;
+                float arow[16];
 #pragma unroll
-                for (int kl = 0; kl < 16; ++kl) {
-                    const int k = b0 + kl;
-                    if (kl < rl && k >= s0) v -= AT[k * 64 + r] * x[kl];
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + fsw(b0 + rl, 4 * b + g4));
+                    arow[4 * g4] = a4.x;
+                    arow[4 * g4 + 1] = a4.y;
+                    arow[4 * g4 + 2] = a4.z;
+                    arow[4 * g4 + 3] = a4.w;
                 }
-                x[rl] = v;
+                float v = (rl == cl) ? 1.f : 0.f;
+#pragma unroll
+                for (int kl = 0; kl < rl; ++kl) v -= arow[kl] * x[kl];
+                x[rl] = (rl < cl) ? 0.f : v;
             }
 #pragma unroll
-            for (int rl = 0; rl < 16; ++rl) MT[s0 * 64 + b0 + rl] = x[rl];
-            for (int r = 0; r < b0; ++r) MT[s0 * 64 + r] = 0.f;
+            for (int g4 = 0; g4 < 16; ++g4) {
+                const int gb = g4 >> 2, l = 4 * (g4 & 3);
+                if (gb > b) continue;  // rows below this block are written later
+                const float4 m4 = (gb == b) ? make_float4(x[l], x[l + 1], x[l + 2], x[l + 3])
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(MT + fsw(s0, g4)) = m4;
+            }
+#pragma unroll
+            for (int rl = 0; rl < 16; ++rl) Dv[b * 256 + rl * 16 + cl] = x[rl];
         }
         __syncthreads();
-        // ... then the blocks below the diagonal, one block-diagonal at a time
+        // ... then the blocks below the diagonal, one block-diagonal at a time:
+        // M^-1_RS = -M^-1_RR sum_{K=S}^{R-1} A_RK M^-1_KS
+#pragma unroll
         for (int dl = 1; dl < 4; ++dl) {
             const int nblk = 4 - dl;
-            for (int e = tid; e < nblk * 256; e += NT) {
+#pragma unroll
+            for (int eb = 0; eb < nblk; ++eb) {
+                const int e = tid + NT * eb;
                 const int b = e >> 8, w = e & 255;
                 const int r = 16 * (b + dl) + (w & 15), s = 16 * b + (w >> 4);
-                float acc = 0.f;
-                for (int k = 16 * b; k < 16 * (b + dl); ++k) acc += AT[k * 64 + r] * MT[s * 64 + k];
-                Yb[e] = acc;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int t = 0; t < 4 * dl; ++t) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + fsw(r, 4 * b + t));
+                    const float4 m4 = *reinterpret_cast<const float4 *>(MT + fsw(s, 4 * b + t));
+                    acc[t & 3] += a4.x * m4.x + a4.y * m4.y + a4.z * m4.z + a4.w * m4.w;
+                }
+                Yb[e] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
             __syncthreads();
-            for (int e = tid; e < nblk * 256; e += NT) {
+#pragma unroll
+            for (int eb = 0; eb < nblk; ++eb) {
+                const int e = tid + NT * eb;
                 const int b = e >> 8, w = e & 255;
-                const int rl = w & 15, sl = w >> 4, Rb = 16 * (b + dl);
+                const int rl = w & 15, sl = w >> 4, R = b + dl;
+                const float *drow = Dv + R * 256 + rl * 16;
+                const float *ycol = Yb + b * 256 + sl * 16;
                 float acc = 0.f;
-                for (int kl = 0; kl <= rl; ++kl) acc += MT[(Rb + kl) * 64 + Rb + rl] * Yb[b * 256 + sl * 16 + kl];
-                MT[(16 * b + sl) * 64 + Rb + rl] = -acc;
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(drow + 4 * g4);
+                    const float4 y4 = *reinterpret_cast<const float4 *>(ycol + 4 * g4);
+                    acc += d4.x * y4.x + d4.y * y4.y + d4.z * y4.z + d4.w * y4.w;
+                }
+                const int r = 16 * R + rl, s = 16 * b + sl;
+                MT[fsw(s, r >> 2) + (r & 3)] = -acc;
             }
             __syncthreads();
         }
+        // T = M^-1 Diag(beta) as bf16 rows r
         for (int p = tid; p < C * 8; p += NT) {
             const int r = p & 63, cc = p >> 6;
             float tv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) tv[e] = MT[(cc * 8 + e) * 64 + r] * s_beta[cc * 8 + e];
+            for (int e = 0; e < 8; ++e) {
+                const int s = cc * 8 + e;
+                tv[e] = MT[fsw(s, r >> 2) + (r & 3)] * s_beta[s];
+            }
             *reinterpret_cast<uint4 *>(sm + OFF_T + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(tv);
         }
         sync_for_mma();
@@ -454,6 +561,12 @@ __global__ void __launch_bounds__(NT, 1)
         }
         ph_mma ^= 1;
         tc_fence_after();
+        if (tid == 0 && has_next) {  // v of this chunk is consumed
+            const int y1 = (int)(c0 + C);
+            mbar_arrive_expect_tx(bar_v, V_BYTES);
+            tma_load_2d(sm + OFF_V, &tm_v, bar_v, x0, y1);
+            tma_load_2d(sm + OFF_V + 8192, &tm_v, bar_v, x0 + 64, y1);
+        }
 
         // W'^T (lane i, column r) -> bf16 tile rows i (MN-major operand)
         {
@@ -466,7 +579,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
                 const int cc = 4 * hh + qd;
-                *reinterpret_cast<uint4 *>(sm + OFF_QRAW + jl * 128 + ((cc ^ (jl & 7)) << 4)) = pack8(wv + 8 * qd);
+                *reinterpret_cast<uint4 *>(sm + OFF_W + jl * 128 + ((cc ^ (jl & 7)) << 4)) = pack8(wv + 8 * qd);
             }
         }
         sync_for_mma();
@@ -477,7 +590,7 @@ __global__ void __launch_bounds__(NT, 1)
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
                 mma_bf16(tbase + TM_X, sdesc_sw128(sbase + OFF_SOP + kb * 16384 + ko, 16, 1024),
-                         sdesc_sw128(sbase + OFF_QRAW + ks * 2048, 8192, 1024), ID_KM64, ks > 0);
+                         sdesc_sw128(sbase + OFF_W + ks * 2048, 8192, 1024), ID_KM64, ks > 0);
             }
             mma_commit(bar_mma);
         }
@@ -502,7 +615,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
                 const int cc = 4 * hh + qd;
-                *reinterpret_cast<uint4 *>(sm + OFF_KRAW + jl * 128 + ((cc ^ (jl & 7)) << 4)) = pack8(uv + 8 * qd);
+                *reinterpret_cast<uint4 *>(sm + OFF_U + jl * 128 + ((cc ^ (jl & 7)) << 4)) = pack8(uv + 8 * qd);
             }
         }
         sync_for_mma();
@@ -511,7 +624,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = sdesc_sw128(sbase + OFF_KRAW + ks * 32, 16, 1024);
+                const uint64_t a = sdesc_sw128(sbase + OFF_U + ks * 32, 16, 1024);
                 mma_bf16(tbase + TM_O, a, sdesc_sw128(sbase + OFF_P + ks * 32, 16, 1024), ID_KK64, 1);
                 mma_bf16(tbase + TM_S, a, sdesc_sw128(sbase + OFF_KB + ks * 2048, 8192, 1024), ID_KM128, 1);
             }
@@ -526,16 +639,22 @@ __global__ void __launch_bounds__(NT, 1)
         ph_mma ^= 1;
         tc_fence_after();
 
-        // O^T (lane j, column r) -> out[t, h, j]
+        // O^T (lane j, column r) -> staging [r][j] bf16 -> 16-byte stores of whole rows
         {
             uint32_t o32[32];
             tmem_ld32(tbase + lrow + TM_O + 32 * hh, o32);
             tmem_ld_wait();
+            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST);
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const int r = 32 * hh + m;
-                if (r < L) out[((size_t)(c0 + r) * H + h) * D + jl] = __float2bfloat16_rn(__uint_as_float(o32[m]));
-            }
+            for (int m = 0; m < 32; ++m) ost[(32 * hh + m) * D + jl] = __float2bfloat16_rn(__uint_as_float(o32[m]));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int p = tid + NT * k4, r = p >> 4, c16 = p & 15;
+            if (r < L)
+                *reinterpret_cast<uint4 *>(out + ((size_t)(c0 + r) * H + h) * D + c16 * 8) =
+                    *reinterpret_cast<const uint4 *>(sm + OFF_OST + r * 256 + c16 * 16);
         }
     }
 
