@@ -43,8 +43,6 @@ STATE_RW = 2 * D * D * 4
 DEC_UNIT_BYTES = STATE_RW + 3 * D * 2 + D * 4 + 4 + D * 2 + 3 * 3 * D * 2 + 3 * D * 2
 CONV_W_BYTES = 3 * H * D * 4 * 4
 STEP_BYTES = UNITS * DEC_UNIT_BYTES + CONV_W_BYTES
-# the decode kernel alone: state read+write, q,k,v (bf16), g, beta, o (bf16)
-DECODE_KERNEL_UNIT_BYTES = STATE_RW + 3 * D * 2 + D * 4 + 4 + D * 2
 # prefill per token-head: q,k,v bf16 in, g fp32, beta, o bf16 out
 PREFILL_TOKEN_HEAD_BYTES = 3 * D * 2 + D * 4 + 4 + D * 2
 PREFILL_TOKEN_HEAD_FLOPS = 6 * D * D + 5 * PRE["C"] * D
@@ -227,15 +225,14 @@ def run_ours(args):
 
     x, ring, w = up(d["x"], bf), up(d["ring"], bf), up(d["w"], torch.float32)
     g, beta, state = up(d["g"], torch.float32), up(d["beta"], torch.float32), up(d["s0"], torch.float32)
-    y = torch.empty((3, B, H, D), dtype=bf, device=dev)
     out = torch.empty((B, H, D), dtype=bf, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev_a=None, ev_b=None):
-        kda.kda_shortconv_step(x, ring, w, y, stream=stream)
+        # one launch: short conv + decode (kda_shortconv_decode_step)
         if ev_a is not None:
             ev_a.record(stream)
-        kda.kda_decode_step(y[0], y[1], y[2], g, beta, state, out, stream=stream)
+        kda.kda_shortconv_decode_step(x, ring, w, g, beta, state, out, stream=stream)
         if ev_b is not None:
             ev_b.record(stream)
 
@@ -272,9 +269,9 @@ def run_ours(args):
     value = ws * STEP_BYTES / (ms_per_step * 1e-3) / 1e9
 
     dec_avg_ms = statistics.mean(dec_ms)
-    dec_bytes = UNITS * DECODE_KERNEL_UNIT_BYTES
+    dec_bytes = STEP_BYTES
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = _traffic("decode_step_kernel", ["kda_decode.cu", "kda_common.cuh"], UNITS)
+    traffic = _traffic("fused_decode_kernel", ["kda_fused_decode.cu", "kda_common.cuh"], UNITS)
 
     # end to end through the public API: pinned host inputs in, output back
     xh = torch.from_numpy(np.ascontiguousarray(d["x"])).to(bf).pin_memory()
@@ -320,18 +317,18 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
             "data": "synthetic (seeded N(0,1) q/k/v, g=-softplus(N(0,1)), beta=sigmoid(N(0,1)), "
                     "state N(0,0.02^2))",
-            "config": {"workload": f"KDA decode step with short conv: B={B} sequences, H={H}, d_k=d_v={D}, "
-                                   f"bf16 q/k/v, fp32 state (384 MiB), 1 layer",
+            "config": {"workload": f"KDA decode step with short conv (fused, one launch): B={B} sequences, "
+                                   f"H={H}, d_k=d_v={D}, bf16 q/k/v, fp32 state (384 MiB), 1 layer",
                        "B": B, "H": H, "d": D, "l2": "state (384 MiB) larger than L2 (129 MB); no flush",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": "fused_decode_kernel", "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                          "traffic": traffic, "algorithmic_bytes": dec_bytes,
                          "avg_launch_us": dec_avg_ms * 1e3},
             "e2e": {"value": ws * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": args.steps,
             "clocks": clocks,
         }
         if prefill is not None:

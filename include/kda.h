@@ -113,6 +113,22 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
                            const float *beta, float *state, void *out, int B, int H, int D,
                            kda_dtype dtype, float l2_eps, kda_stream_t stream);
 
+/*
+ * Short conv + decode step in one launch: the same recurrence as
+ * kda_shortconv_step followed by kda_decode_step on its output ([W] "KDA
+ * 递推公式先衰减再差分": conv + SiLU in front of q/k/v, then decay, delta,
+ * readout), except that the post-conv q, k, v stay in fp32 inside the kernel
+ * (never rounded to `dtype` nor written to memory).
+ *
+ *   x [B,3,H,D] dtype, ring [B,3,H,3,D] dtype (in/out), w [3,H,D,4] fp32,
+ *   g [B,H,D] fp32, beta [B,H] fp32, state [B,H,D,D] fp32 (in/out),
+ *   out [B,H,D] dtype
+ * Same requirements and errors as the two calls it replaces.
+ */
+kda_status kda_shortconv_decode_step(const void *x, void *ring, const float *w, const float *g,
+                                     const float *beta, float *state, void *out, int B, int H, int D,
+                                     kda_dtype dtype, float l2_eps, kda_stream_t stream);
+
 /* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
 size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);
 

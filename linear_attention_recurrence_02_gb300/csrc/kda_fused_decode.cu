@@ -1,0 +1,208 @@
+// kda_fused_decode.cu -- short conv + decode step in one launch.
+//
+// Same arithmetic as kda_shortconv_step followed by kda_decode_step
+// ("KV缓存从11.25GB缩到0.21GB: WARP中Kimi Delta Attention线性注意力原理剖析",
+// section "KDA 递推公式先衰减再差分": a width-4 causal conv with SiLU runs in
+// front of q/k/v, then decay, delta correction and readout), except that the
+// post-conv q, k, v stay in fp32 on chip instead of being stored and read back.
+//
+// One CTA per (sequence, head) owns the whole D x D state slice in registers
+// (D=128: 256 threads x 16 rows x one float4) and every ring channel of that
+// head, so the in-place ring shift cannot race with another CTA's read. The
+// state loads are issued first and stay in flight while the conv, the norms
+// and the decay run; column sums of S'^T k^ and S'^T q^ are reduced through
+// shared memory across the row groups; S is written once.
+#include "kda_common.cuh"
+
+namespace kda {
+
+template <int D> struct FusedShape;
+template <> struct FusedShape<16> { static constexpr int NT = 32; };
+template <> struct FusedShape<32> { static constexpr int NT = 64; };
+template <> struct FusedShape<64> { static constexpr int NT = 128; };
+template <> struct FusedShape<128> { static constexpr int NT = 256; };
+
+template <int D, typename T>
+__global__ void __launch_bounds__(FusedShape<D>::NT)
+    fused_decode_kernel(const T *__restrict__ x, T *__restrict__ ring, const float *__restrict__ w,
+                        const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ state,
+                        T *__restrict__ out, int H, float eps) {
+    constexpr int NT = FusedShape<D>::NT;
+    constexpr int C4 = D / 4;     // float4 columns per state row
+    constexpr int RG = NT / C4;   // row groups
+    constexpr int RPT = D / RG;   // rows per thread
+    constexpr int NW = NT / 32;   // warps
+    static_assert(NT % 32 == 0 && RPT * RG == D && C4 <= 32, "bad fused decode shape");
+
+    const int unit = blockIdx.x;  // b*H + h
+    const int b = unit / H, h = unit % H;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int c4 = t % C4, rg = t / C4;
+
+    float *Sp = state + (size_t)unit * D * D + c4 * 4;
+    float4 s[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(reinterpret_cast<const float4 *>(Sp + (size_t)(rg + m * RG) * D));
+
+    __shared__ float s_y[3][D];
+    __shared__ float s_qa[D], s_ka[D], s_kh[D], s_a[D], s_delta[D];
+    __shared__ float s_red[NW][3];
+    __shared__ float s_part[NW][D][2];
+
+    // 1. width-4 causal conv + SiLU for q, k, v; shift the ring
+    for (int idx = t; idx < 3 * D; idx += NT) {
+        const int p = idx / D, c = idx % D;
+        const size_t row = ((size_t)b * 3 + p) * H + h;
+        const size_t xo = row * D + c, ro = row * 3 * D + c;
+        const float xv = Elem<T>::load(x + xo);
+        const float r0 = Elem<T>::load(ring + ro), r1 = Elem<T>::load(ring + ro + D),
+                    r2 = Elem<T>::load(ring + ro + 2 * D);
+        const float4 tap = __ldg(reinterpret_cast<const float4 *>(w) + (((size_t)p * H + h) * D + c));
+        const float z = tap.x * r0 + tap.y * r1 + tap.z * r2 + tap.w * xv;
+        s_y[p][c] = z / (1.0f + expf(-z));
+        Elem<T>::store(ring + ro, r1);
+        Elem<T>::store(ring + ro + D, r2);
+        Elem<T>::store(ring + ro + 2 * D, xv);
+    }
+    const size_t vo = (size_t)unit * D;
+    const float av = t < D ? expf(__ldg(g + vo + t)) : 0.f;
+    __syncthreads();
+
+    // 2. L2 norms of q, k and their dot
+    float qv = 0.f, kv = 0.f;
+    if (t < D) {
+        qv = s_y[0][t];
+        kv = s_y[1][t];
+    }
+    float sqq = qv * qv, skk = kv * kv, sqk = qv * kv;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sqq += __shfl_xor_sync(0xffffffffu, sqq, o);
+        skk += __shfl_xor_sync(0xffffffffu, skk, o);
+        sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
+    }
+    if (lane == 0) {
+        s_red[warp][0] = sqq;
+        s_red[warp][1] = skk;
+        s_red[warp][2] = sqk;
+    }
+    __syncthreads();
+    sqq = skk = sqk = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < NW; ++wi) {
+        sqq += s_red[wi][0];
+        skk += s_red[wi][1];
+        sqk += s_red[wi][2];
+    }
+    const float rq = inv_norm(sqq, eps), rk = inv_norm(skk, eps);
+    const float kq = sqk * rq * rk;
+    if (t < D) {
+        s_qa[t] = qv * rq * av;
+        s_ka[t] = kv * rk * av;
+        s_kh[t] = kv * rk;
+        s_a[t] = av;
+    }
+    __syncthreads();
+
+    // 3. partial column sums over this thread's rows, then across row groups
+    float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int i = rg + m * RG;
+        const float ka = s_ka[i], qa = s_qa[i];
+        pk[0] += ka * s[m].x; pk[1] += ka * s[m].y; pk[2] += ka * s[m].z; pk[3] += ka * s[m].w;
+        pq[0] += qa * s[m].x; pq[1] += qa * s[m].y; pq[2] += qa * s[m].z; pq[3] += qa * s[m].w;
+    }
+#pragma unroll
+    for (int o = C4; o < 32; o <<= 1) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], o);
+            pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], o);
+        }
+    }
+    if (lane < C4) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            s_part[warp][c4 * 4 + c][0] = pk[c];
+            s_part[warp][c4 * 4 + c][1] = pq[c];
+        }
+    }
+    __syncthreads();
+    if (t < D) {
+        float ks = 0.f, qs = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < NW; ++wi) {
+            ks += s_part[wi][t][0];
+            qs += s_part[wi][t][1];
+        }
+        const float d = __ldg(beta + unit) * (s_y[2][t] - ks);
+        s_delta[t] = d;
+        Elem<T>::store(out + vo + t, qs + kq * d);
+    }
+    __syncthreads();
+
+    // 4. S <- Diag(a) S + k^ delta^T, written back once
+    const float d0 = s_delta[c4 * 4 + 0], d1 = s_delta[c4 * 4 + 1], d2 = s_delta[c4 * 4 + 2],
+                d3 = s_delta[c4 * 4 + 3];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int i = rg + m * RG;
+        const float a = s_a[i], kh = s_kh[i];
+        float4 r;
+        r.x = a * s[m].x + kh * d0;
+        r.y = a * s[m].y + kh * d1;
+        r.z = a * s[m].z + kh * d2;
+        r.w = a * s[m].w + kh * d3;
+        __stcs(reinterpret_cast<float4 *>(Sp + (size_t)i * D), r);
+    }
+}
+
+template <int D, typename T>
+static void launch_fused(const void *x, void *ring, const float *w, const float *g, const float *beta,
+                         float *state, void *out, int B, int H, float eps, cudaStream_t s) {
+    fused_decode_kernel<D, T><<<(unsigned)B * H, FusedShape<D>::NT, 0, s>>>(
+        static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps);
+}
+
+template <typename T>
+static void dispatch_fused(int D, const void *x, void *ring, const float *w, const float *g, const float *beta,
+                           float *state, void *out, int B, int H, float eps, cudaStream_t s) {
+    switch (D) {
+    case 16: launch_fused<16, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    case 32: launch_fused<32, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    case 64: launch_fused<64, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    default: launch_fused<128, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    }
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_shortconv_decode_step(const void *x, void *ring, const float *w, const float *g,
+                                                const float *beta, float *state, void *out, int B, int H, int D,
+                                                kda_dtype dtype, float l2_eps, kda_stream_t stream) {
+    clear_detail();
+    if (B < 0) return invalid("B must be >= 0");
+    if (H < 1) return invalid("H must be >= 1");
+    if (!valid_head_dim(D)) return invalid("D must be one of 16, 32, 64, 128");
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return invalid("dtype must be KDA_F32 or KDA_BF16");
+    if (!(l2_eps >= 0.f)) return invalid("l2_eps must be >= 0");
+    if (B == 0) return KDA_OK;
+    if ((long long)B * H > 0x7fffffffLL) return invalid("B*H too large for one launch");
+    kda_status st;
+    if ((st = check_ptr(x, "x")) || (st = check_ptr(ring, "ring")) || (st = check_ptr(w, "w")) ||
+        (st = check_ptr(g, "g")) || (st = check_ptr(beta, "beta")) || (st = check_ptr(state, "state")) ||
+        (st = check_ptr(out, "out")))
+        return st;
+    if (out == x || out == ring || (const void *)out == (const void *)state)
+        return invalid("out must not alias x, ring or state");
+    if ((st = bind_stream_device(stream))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == KDA_BF16)
+        dispatch_fused<__nv_bfloat16>(D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
+    else
+        dispatch_fused<float>(D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
+    return check_launch("fused_decode_kernel");
+}

@@ -82,6 +82,30 @@ __device__ __forceinline__ uint32_t swz(int row, int cc, int rows) {
 // for 16-byte accesses by consecutive rows)
 __device__ __forceinline__ int fsw(int r, int k4) { return r * 64 + ((k4 ^ (r & 7)) << 2); }
 
+constexpr float LOG2E = 1.4426950408889634f;
+// 2^x on the special-function unit (inputs here are within +-128)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// barrier over the first `n` threads of the CTA only (id > 0)
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// warp-level D(16x8) += A(16x8, row) * B(8x8, col) on tf32 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 __device__ __forceinline__ uint4 pack8(const float *f) {
     uint4 u;
     __nv_bfloat162 t;
@@ -226,81 +250,58 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
         }
 
-        // L2 norms of the q and k rows: 16 lanes per row, 8 channels per lane
-        {
-            const int cc = tid & 15, rb = tid >> 4;
-            float sq[4], sk[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t o = swz(rb + 16 * m, cc, 64);
-                float qf[8], kf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + o), qf);
-                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + o), kf);
-                sq[m] = sk[m] = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    sq[m] += qf[e] * qf[e];
-                    sk[m] += kf[e] * kf[e];
-                }
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    sq[m] += __shfl_xor_sync(0xffffffffu, sq[m], o);
-                    sk[m] += __shfl_xor_sync(0xffffffffu, sk[m], o);
-                }
-            if (cc == 0)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    s_rq[rb + 16 * m] = inv_norm(sq[m], eps);
-                    s_rk[rb + 16 * m] = inv_norm(sk[m], eps);
-                }
-        }
-        // cumulative log decay G along the chunk: each half-block scans 32 rows
-        // in registers, then the second half adds the first half's total
-        {
-            const int i = tid & 127, half = tid >> 7;
-            float gv[32];
-#pragma unroll
-            for (int r = 0; r < 32; ++r) gv[r] = gt[(32 * half + r) * 128 + i];
-#pragma unroll
-            for (int r = 1; r < 32; ++r) gv[r] += gv[r - 1];
-            if (half == 0)
-#pragma unroll
-                for (int r = 0; r < 32; ++r) gt[r * 128 + i] = gv[r];
-            __syncthreads();
-            if (half == 1) {
-                const float base = gt[31 * 128 + i];
-#pragma unroll
-                for (int r = 0; r < 32; ++r) gt[(32 + r) * 128 + i] = gv[r] + base;
-            }
-        }
-        __syncthreads();
-        // per-channel anchor; a chunk whose decay span exceeds SPAN_MAX takes the exact path
+        // warps 0-3: L2 norms, one thread per q or k row; warps 4-7: cumulative
+        // log decay G along the chunk, one channel per thread in registers,
+        // stored back in log2 units, and the per-channel anchor
         int bad = 0;
-        if (tid < 128) bad = !(gt[tid] - gt[63 * 128 + tid] <= SPAN_MAX);
-        const int exact = __syncthreads_or(bad);
         if (tid < 128) {
-            const float GL = gt[63 * 128 + tid];
-            s_gl[tid] = GL;
-            const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
-            s_c[tid] = c;
-            s_expc[tid] = expf(c);
-            s_expgl[tid] = expf(GL);
+            const int r = tid & 63;
+            const uint8_t *tile = sm + (tid < 64 ? OFF_QRAW : OFF_KRAW);
+            float ss = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(tile + swz(r, cc, 64)), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss += f[e] * f[e];
+            }
+            (tid < 64 ? s_rq : s_rk)[r] = inv_norm(ss, eps);
+        } else {
+            const int i = tid - 128;
+            float gv[64];
+#pragma unroll
+            for (int r = 0; r < 64; ++r) gv[r] = gt[r * 128 + i];
+#pragma unroll
+            for (int r = 1; r < 64; ++r) gv[r] += gv[r - 1];
+            const float GL = gv[63];
+            bad = !(gv[0] - GL <= SPAN_MAX);
+            const float c = fminf(0.f, GL + ANCHOR);
+#pragma unroll
+            for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
+            s_gl[i] = GL;
+            s_c[i] = c;
+            s_expc[i] = expf(c);
+            s_expgl[i] = expf(GL);
         }
-        __syncthreads();
+        const int exact = __syncthreads_or(bad);
+        if (exact) {  // rare: no anchor, exact pairwise decays below
+            if (tid < 128) {
+                s_c[tid] = 0.f;
+                s_expc[tid] = 1.f;
+            }
+            __syncthreads();
+        }
 
         // operand tiles Lk, Lq, Rk, Kb (bf16, swizzled) from q^, k^ and G;
         // each thread keeps one 8-channel group and walks 4 rows
         {
             const int cc = tid & 15, rb = tid >> 4;
-            float cv[8], egc[8], glv[8];
+            float cv[8], egc[8], glv[8];  // anchor and G_L in log2 units
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                cv[e] = s_c[cc * 8 + e];
-                glv[e] = s_gl[cc * 8 + e];
-                egc[e] = __expf(glv[e] - cv[e]);
+                cv[e] = s_c[cc * 8 + e] * LOG2E;
+                glv[e] = s_gl[cc * 8 + e] * LOG2E;
+                egc[e] = ex2(glv[e] - cv[e]);
             }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -317,15 +318,15 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float kh = kf[e] * rk, qh = qf[e] * rq;
-                    const float e1 = __expf(G[e] - cv[e]);
+                    const float e1 = ex2(G[e] - cv[e]);
                     lk[e] = e1 * kh;
                     lq[e] = e1 * qh;
                     if (!exact) {
-                        const float inv = __expf(cv[e] - G[e]);  // <= e^80
+                        const float inv = ex2(cv[e] - G[e]);  // <= e^ANCHOR
                         rkv[e] = inv * kh;
                         kbv[e] = egc[e] * inv * kh;
                     } else {
-                        kbv[e] = __expf(glv[e] - G[e]) * kh;
+                        kbv[e] = ex2(glv[e] - G[e]) * kh;
                     }
                 }
                 *reinterpret_cast<uint4 *>(sm + OFF_LKQ + swz(r, cc, 128)) = pack8(lk);
@@ -334,30 +335,6 @@ __global__ void __launch_bounds__(NT, 1)
                 *reinterpret_cast<uint4 *>(sm + OFF_KB + o64) = pack8(kbv);
             }
         }
-
-        // S~^T = S^T Diag(e^c) as a bf16 operand; S^T <- S^T Diag(e^{G_L}) in TMEM
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int i0 = 64 * hh + 32 * part;
-            uint32_t r[32];
-            tmem_ld32(tbase + lrow + TM_S + i0, r);
-            tmem_ld_wait();
-            float so[32];
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const float s = __uint_as_float(r[m]);
-                so[m] = s * s_expc[i0 + m];
-                r[m] = __float_as_uint(s * s_expgl[i0 + m]);
-            }
-            tmem_st32(tbase + lrow + TM_S + i0, r);
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                const int cc = part * 4 + qd;
-                *reinterpret_cast<uint4 *>(sm + OFF_SOP + hh * 16384 + jl * 128 + ((cc ^ (jl & 7)) << 4)) =
-                    pack8(so + 8 * qd);
-            }
-        }
-        tmem_st_wait();
 
         if (exact) {
             // A and P with exact pairwise decays (rare: decay span > e^160)
@@ -374,7 +351,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int i = cc * 8 + e;
-                            const float x = ks[e] * rks * __expf(gt[r * 128 + i] - gt[s * 128 + i]);
+                            const float x = ks[e] * rks * ex2(gt[r * 128 + i] - gt[s * 128 + i]);
                             a += kr[e] * rkr * x;
                             pq += qr[e] * rqr * x;
                         }
@@ -389,7 +366,7 @@ __global__ void __launch_bounds__(NT, 1)
 
         if (tid < C) beta_reg = (has_next && c0 + C + tid < end) ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
         // q, k, g of this chunk are consumed: prefetch the next chunk's.
-        // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T   and   G5: O = Lq S~ (as O^T = S~^T Lq^T)
+        // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T
         if (tid == 0) {
             if (has_next) {
                 const int y1 = (int)(c0 + C);
@@ -407,23 +384,19 @@ __global__ void __launch_bounds__(NT, 1)
                     mma_bf16(tbase + TM_AP, sdesc_sw128(sbase + OFF_LKQ + kb * 16384 + ko, 16, 1024),
                              sdesc_sw128(sbase + OFF_RK + kb * 8192 + ko, 16, 1024), ID_KK64, ks > 0);
                 }
+                mma_commit(bar_mma);
             }
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_SOP + kb * 16384 + ko, 16, 1024),
-                         sdesc_sw128(sbase + OFF_LKQ + 8192 + kb * 16384 + ko, 16, 1024), ID_KK64, ks > 0);
+        }
+        if (!exact) {
+            got = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
+            if (__syncthreads_or(!got)) {
+                mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
+                ok = false;
+                break;
             }
-            mma_commit(bar_mma);
+            ph_mma ^= 1;
+            tc_fence_after();
         }
-        got = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-        if (__syncthreads_or(!got)) {
-            mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-            ok = false;
-            break;
-        }
-        ph_mma ^= 1;
-        tc_fence_after();
 
         // read back A (lanes 0-63, masked, times beta) and P (lanes 64-127, masked)
         if (!exact) {
@@ -458,98 +431,152 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
 
-        // M^-1 = (I + A)^-1, A strictly lower. Diagonal 16 x 16 blocks by
-        // forward substitution (one thread per column) ...
-        if (tid < 64) {
-            const int b = tid >> 4, cl = tid & 15, s0 = tid, b0 = 16 * b;
-            float x[16];
+        // warps 0-3 solve for T while warps 4-7 convert the state operand
+        if (warp < 4) {
+            // M^-1 = (I + A)^-1, A strictly lower. Diagonal 16 x 16 blocks by
+            // forward substitution (one thread per column) ...
+            if (tid < 64) {
+                const int b = tid >> 4, cl = tid & 15, s0 = tid, b0 = 16 * b;
+                // column cl of the block inverse; once x[kl] is final, remove
+                // its contribution from every later row (independent FMAs)
+                float x[16];
 #pragma unroll
-            for (int rl = 0; rl < 16; ++rl) {
-                float arow[16];
+                for (int rl = 0; rl < 16; ++rl) x[rl] = (rl == cl) ? 1.f : 0.f;
 #pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + fsw(b0 + rl, 4 * b + g4));
-                    arow[4 * g4] = a4.x;
-                    arow[4 * g4 + 1] = a4.y;
-                    arow[4 * g4 + 2] = a4.z;
-                    arow[4 * g4 + 3] = a4.w;
+                for (int kl = 0; kl < 15; ++kl) {
+#pragma unroll
+                    for (int rl = kl + 1; rl < 16; ++rl)
+                        x[rl] -= Am[fsw(b0 + rl, (b0 + kl) >> 2) + (kl & 3)] * x[kl];
                 }
-                float v = (rl == cl) ? 1.f : 0.f;
 #pragma unroll
-                for (int kl = 0; kl < rl; ++kl) v -= arow[kl] * x[kl];
-                x[rl] = (rl < cl) ? 0.f : v;
-            }
-#pragma unroll
-            for (int g4 = 0; g4 < 16; ++g4) {
-                const int gb = g4 >> 2, l = 4 * (g4 & 3);
-                if (gb > b) continue;  // rows below this block are written later
-                const float4 m4 = (gb == b) ? make_float4(x[l], x[l + 1], x[l + 2], x[l + 3])
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(MT + fsw(s0, g4)) = m4;
-            }
-#pragma unroll
-            for (int rl = 0; rl < 16; ++rl) Dv[b * 256 + rl * 16 + cl] = x[rl];
-        }
-        __syncthreads();
-        // ... then the blocks below the diagonal, one block-diagonal at a time:
-        // M^-1_RS = -M^-1_RR sum_{K=S}^{R-1} A_RK M^-1_KS
-#pragma unroll
-        for (int dl = 1; dl < 4; ++dl) {
-            const int nblk = 4 - dl;
-#pragma unroll
-            for (int eb = 0; eb < nblk; ++eb) {
-                const int e = tid + NT * eb;
-                const int b = e >> 8, w = e & 255;
-                const int r = 16 * (b + dl) + (w & 15), s = 16 * b + (w >> 4);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int t = 0; t < 4 * dl; ++t) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(Am + fsw(r, 4 * b + t));
-                    const float4 m4 = *reinterpret_cast<const float4 *>(MT + fsw(s, 4 * b + t));
-                    acc[t & 3] += a4.x * m4.x + a4.y * m4.y + a4.z * m4.z + a4.w * m4.w;
+                for (int g4 = 0; g4 < 16; ++g4) {
+                    const int gb = g4 >> 2, l = 4 * (g4 & 3);
+                    if (gb > b) continue;  // rows below this block are written later
+                    const float4 m4 = (gb == b) ? make_float4(x[l], x[l + 1], x[l + 2], x[l + 3])
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                    *reinterpret_cast<float4 *>(MT + fsw(s0, g4)) = m4;
                 }
-                Yb[e] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+                for (int rl = 0; rl < 16; ++rl) Dv[b * 256 + rl * 16 + cl] = x[rl];
             }
-            __syncthreads();
+            named_bar_sync(1, 128);
+            // ... then the blocks below the diagonal, one block-diagonal at a time,
+            // one warp per 16 x 16 block on warp-level tf32 MMA tiles:
+            // M^-1_RS = -M^-1_RR sum_{K=S}^{R-1} A_RK M^-1_KS
 #pragma unroll
-            for (int eb = 0; eb < nblk; ++eb) {
-                const int e = tid + NT * eb;
-                const int b = e >> 8, w = e & 255;
-                const int rl = w & 15, sl = w >> 4, R = b + dl;
-                const float *drow = Dv + R * 256 + rl * 16;
-                const float *ycol = Yb + b * 256 + sl * 16;
-                float acc = 0.f;
+            for (int dl = 1; dl < 4; ++dl) {
+                if (warp < 4 - dl) {
+                    const int b = warp, R = b + dl, g = lane >> 2, tg = lane & 3;
+                    float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(drow + 4 * g4);
-                    const float4 y4 = *reinterpret_cast<const float4 *>(ycol + 4 * g4);
-                    acc += d4.x * y4.x + d4.y * y4.y + d4.z * y4.z + d4.w * y4.w;
+                    for (int kk = 0; kk < 2 * dl; ++kk) {
+                        const int k0 = 16 * b + 8 * kk, r0 = 16 * R + g;
+                        const uint32_t af[4] = {to_tf32(Am[fsw(r0, k0 >> 2) + tg]), to_tf32(Am[fsw(r0 + 8, k0 >> 2) + tg]),
+                                                to_tf32(Am[fsw(r0, (k0 >> 2) + 1) + tg]),
+                                                to_tf32(Am[fsw(r0 + 8, (k0 >> 2) + 1) + tg])};
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const int sc = 16 * b + 8 * nt + g;
+                            const uint32_t bf[2] = {to_tf32(MT[fsw(sc, k0 >> 2) + tg]), to_tf32(MT[fsw(sc, (k0 >> 2) + 1) + tg])};
+                            mma_tf32_16x8x8(y[nt], af, bf);
+                        }
+                    }
+                    float *yb = Yb + b * 256;  // Y block, row-major 16 x 16
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        yb[g * 16 + 8 * nt + 2 * tg] = y[nt][0];
+                        yb[g * 16 + 8 * nt + 2 * tg + 1] = y[nt][1];
+                        yb[(g + 8) * 16 + 8 * nt + 2 * tg] = y[nt][2];
+                        yb[(g + 8) * 16 + 8 * nt + 2 * tg + 1] = y[nt][3];
+                    }
+                    __syncwarp();
+                    const float *dr = Dv + R * 256;  // M^-1_RR, row-major 16 x 16
+                    float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int k0 = 8 * kk;
+                        const uint32_t af[4] = {to_tf32(dr[g * 16 + k0 + tg]), to_tf32(dr[(g + 8) * 16 + k0 + tg]),
+                                                to_tf32(dr[g * 16 + k0 + tg + 4]), to_tf32(dr[(g + 8) * 16 + k0 + tg + 4])};
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const uint32_t bf[2] = {to_tf32(yb[(k0 + tg) * 16 + 8 * nt + g]),
+                                                    to_tf32(yb[(k0 + tg + 4) * 16 + 8 * nt + g])};
+                            mma_tf32_16x8x8(z[nt], af, bf);
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int sc = 16 * b + 8 * nt + 2 * tg, r0 = 16 * R + g;
+                        MT[fsw(sc, r0 >> 2) + (r0 & 3)] = -z[nt][0];
+                        MT[fsw(sc + 1, r0 >> 2) + (r0 & 3)] = -z[nt][1];
+                        MT[fsw(sc, (r0 + 8) >> 2) + (r0 & 3)] = -z[nt][2];
+                        MT[fsw(sc + 1, (r0 + 8) >> 2) + (r0 & 3)] = -z[nt][3];
+                    }
                 }
-                const int r = 16 * R + rl, s = 16 * b + sl;
-                MT[fsw(s, r >> 2) + (r & 3)] = -acc;
+                named_bar_sync(1, 128);
             }
-            __syncthreads();
-        }
-        // T = M^-1 Diag(beta) as bf16 rows r
-        for (int p = tid; p < C * 8; p += NT) {
-            const int r = p & 63, cc = p >> 6;
-            float tv[8];
+            // T = M^-1 Diag(beta) as bf16 rows r
+            for (int p = tid; p < C * 8; p += 128) {
+                const int r = p & 63, cc = p >> 6;
+                float tv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = cc * 8 + e;
-                tv[e] = MT[fsw(s, r >> 2) + (r & 3)] * s_beta[s];
+                for (int e = 0; e < 8; ++e) {
+                    const int s = cc * 8 + e;
+                    tv[e] = MT[fsw(s, r >> 2) + (r & 3)] * s_beta[s];
+                }
+                *reinterpret_cast<uint4 *>(sm + OFF_T + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(tv);
             }
-            *reinterpret_cast<uint4 *>(sm + OFF_T + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(tv);
+        } else {
+            // S~^T = S^T Diag(e^c) as a bf16 operand; S^T <- S^T Diag(e^{G_L}) in TMEM.
+            // Two 32-column TMEM loads per wait; per-channel factors as float4.
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                uint32_t r[2][32];
+                tmem_ld32(tbase + lrow + TM_S + 64 * kb, r[0]);
+                tmem_ld32(tbase + lrow + TM_S + 64 * kb + 32, r[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const int i0 = 64 * kb + 32 * part;
+                    float so[32];
+#pragma unroll
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        const float4 fc = *reinterpret_cast<const float4 *>(s_expc + i0 + 4 * g4);
+                        const float4 fl = *reinterpret_cast<const float4 *>(s_expgl + i0 + 4 * g4);
+                        const float fcv[4] = {fc.x, fc.y, fc.z, fc.w}, flv[4] = {fl.x, fl.y, fl.z, fl.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sv = __uint_as_float(r[part][4 * g4 + e]);
+                            so[4 * g4 + e] = sv * fcv[e];
+                            r[part][4 * g4 + e] = __float_as_uint(sv * flv[e]);
+                        }
+                    }
+                    tmem_st32(tbase + lrow + TM_S + i0, r[part]);
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) {
+                        const int cc = part * 4 + qd;
+                        *reinterpret_cast<uint4 *>(sm + OFF_SOP + kb * 16384 + jl * 128 + ((cc ^ (jl & 7)) << 4)) =
+                            pack8(so + 8 * qd);
+                    }
+                }
+            }
+            tmem_st_wait();
         }
         sync_for_mma();
 
-        // G2: W'^T = Lk^T T^T   and   G3: U0^T = V^T T^T
+        // G2: W'^T = Lk^T T^T,  G3: U0^T = V^T T^T,  G5: O^T = S~^T Lq^T
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t b = sdesc_sw128(sbase + OFF_T + ks * 32, 16, 1024);
                 mma_bf16(tbase + TM_W, sdesc_sw128(sbase + OFF_LKQ + ks * 2048, 16384, 1024), b, ID_MK64, ks > 0);
                 mma_bf16(tbase + TM_U0, sdesc_sw128(sbase + OFF_V + ks * 2048, 8192, 1024), b, ID_MK64, ks > 0);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
+                mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_SOP + kb * 16384 + ko, 16, 1024),
+                         sdesc_sw128(sbase + OFF_LKQ + 8192 + kb * 16384 + ko, 16, 1024), ID_KK64, ks > 0);
             }
             mma_commit(bar_mma);
         }

@@ -34,6 +34,7 @@ _SIGNATURES = {
     "kda_shortconv_ring_bytes": ([_ci, _ci, _ci, _ci, _ci], _sz),
     "kda_shortconv_step": ([_vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _vp], _ci),
     "kda_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
+    "kda_shortconv_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
     "kda_chunk_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
                            _cf, _vp, _sz, _vp], _ci),
@@ -137,6 +138,20 @@ def kda_decode_step(q, k, v, g, beta, state, out, l2_eps=1e-6, stream=None):
         raise ValueError("shape mismatch")
     _check(lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
                                  B, H, D, _dtype_code(q), float(l2_eps), _stream(stream, q.device)))
+
+
+def kda_shortconv_decode_step(x, ring, w, g, beta, state, out, l2_eps=1e-6, stream=None):
+    """Fused short conv + decode step. x [B,3,H,D], ring [B,3,H,3,D] (in/out),
+    w [3,H,D,4] fp32, g [B,H,D] fp32, beta [B,H] fp32, state [B,H,D,D] fp32
+    (in/out), out [B,H,D]."""
+    B, P, H, D = x.shape
+    if P != 3 or tuple(ring.shape) != (B, 3, H, 3, D) or tuple(w.shape) != (3, H, D, 4) \
+            or tuple(g.shape) != (B, H, D) or tuple(beta.shape) != (B, H) \
+            or tuple(state.shape) != (B, H, D, D) or tuple(out.shape) != (B, H, D):
+        raise ValueError("shape mismatch")
+    _check(lib().kda_shortconv_decode_step(_ptr(x), _ptr(ring), _ptr(w), _ptr(g), _ptr(beta), _ptr(state),
+                                           _ptr(out), B, H, D, _dtype_code(x), float(l2_eps),
+                                           _stream(stream, x.device)))
 
 
 def kda_chunk_prefill_workspace_bytes(total_tokens, num_seqs, H, D, C) -> int:

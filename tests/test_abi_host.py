@@ -106,3 +106,20 @@ def test_zero_batch_is_a_noop_without_cuda(kda):
     L = kda.lib()
     assert L.kda_decode_step(None, None, None, None, None, None, None, 0, 3, 128, 1, 1e-6, None) == kda.KDA_OK
     assert L.kda_shortconv_step(None, None, None, None, 0, 3, 128, 1, None) == kda.KDA_OK
+
+
+@pytest.mark.parametrize("case,detail", [
+    (dict(D=48), "D must be"),
+    (dict(x=None), "x is NULL"),
+    (dict(out=0x20000), "out must not alias"),
+    (dict(eps=-0.5), "l2_eps"),
+])
+def test_fused_decode_rejects_bad_arguments(kda, case, detail):
+    a = dict(x=0x10000, ring=0x20000, w=0x30000, g=0x40000, beta=0x50000, state=0x60000, out=0x70000,
+             B=2, H=3, D=128, dtype=1, eps=1e-6)
+    a.update(case)
+    L = kda.lib()
+    st = L.kda_shortconv_decode_step(a["x"], a["ring"], a["w"], a["g"], a["beta"], a["state"], a["out"], a["B"],
+                                     a["H"], a["D"], a["dtype"], a["eps"], None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    assert detail in L.kda_last_error_detail().decode()

@@ -179,3 +179,75 @@ def test_shortconv_then_decode_full_size(env):
     assert_close(to_np(out), ro, True, (0, 1), "out")
     assert_close(to_np(ts), rs, True, (0, 1), "state")
     assert np.array_equal(to_np(tr), rring)
+
+
+# ---------------------------------------------------------------- fused short conv + decode
+def _oracle_conv_decode(d, s0=None, ring=None, x=None):
+    ring = d["ring"] if ring is None else ring
+    x = d["x"] if x is None else x
+    ry, rring = oracle.shortconv_step(x, ring, d["w"])
+    ro, rs = oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], d["g"], d["beta"], d["s0"] if s0 is None else s0,
+                                nthreads=NCPU)
+    return ro, rs, rring
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_fused_conv_decode_matches_oracle(env, D, bf16):
+    """kda_shortconv_decode_step keeps the post-conv q, k, v in fp32, so it is
+    compared with the oracle's conv (fp64, unrounded) feeding its recurrence."""
+    torch, kda = env
+    d = synth.decode_inputs(300 + D, 3, 5, D, bf16, s0_std=0.5)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    tx, tr = to_dev(d["x"], dt, torch), to_dev(d["ring"], dt, torch)
+    tw, tg, tb = (to_dev(d[n], torch.float32, torch) for n in ("w", "g", "beta"))
+    ts = to_dev(d["s0"], torch.float32, torch)
+    out = torch.empty((3, 5, D), dtype=dt, device="cuda")
+    kda.kda_shortconv_decode_step(tx, tr, tw, tg, tb, ts, out)
+    torch.cuda.synchronize()
+    ro, rs, rring = _oracle_conv_decode(d)
+    assert_close(to_np(out), ro, bf16, (0, 1), "out")
+    assert_close(to_np(ts), rs, bf16, (0, 1), "state")
+    assert np.max(np.abs(to_np(ts) - rs)) <= 1e-4
+    assert np.array_equal(to_np(tr), rring)
+
+
+def test_fused_conv_decode_consecutive_steps(env):
+    """Four fused steps in a row (ring and state carried) against the oracle
+    run step by step on the same inputs."""
+    torch, kda = env
+    B, H, D = 2, 3, 64
+    d = synth.decode_inputs(77, B, H, D, True, s0_std=0.3, g_scale=0.1)
+    xs = [synth.bf16_round(np.random.default_rng(100 + i).standard_normal(d["x"].shape).astype(np.float32))
+          for i in range(4)]
+    bf = torch.bfloat16
+    tr = to_dev(d["ring"], bf, torch)
+    tw, tg, tb = (to_dev(d[n], torch.float32, torch) for n in ("w", "g", "beta"))
+    ts = to_dev(d["s0"], torch.float32, torch)
+    ring, st = d["ring"], d["s0"]
+    for i in range(4):
+        out = torch.empty((B, H, D), dtype=bf, device="cuda")
+        kda.kda_shortconv_decode_step(to_dev(xs[i], bf, torch), tr, tw, tg, tb, ts, out)
+        ro, st, ring = _oracle_conv_decode(d, s0=st, ring=ring, x=xs[i])
+        torch.cuda.synchronize()
+        assert_close(to_np(out), ro, True, (0, 1), f"out step {i}")
+        assert_close(to_np(ts), st, True, (0, 1), f"state step {i}")
+        assert np.array_equal(to_np(tr), ring)
+
+
+def test_fused_conv_decode_full_size(env):
+    """Decode workload at full size through the fused call: B=64, H=96, d=128."""
+    torch, kda = env
+    c = synth.DECODE
+    d = synth.decode_inputs(c["seed"], c["B"], c["H"], c["D"], True)
+    bf = torch.bfloat16
+    tx, tr = to_dev(d["x"], bf, torch), to_dev(d["ring"], bf, torch)
+    tw, tg, tb = (to_dev(d[n], torch.float32, torch) for n in ("w", "g", "beta"))
+    ts = to_dev(d["s0"], torch.float32, torch)
+    out = torch.empty((c["B"], c["H"], c["D"]), dtype=bf, device="cuda")
+    kda.kda_shortconv_decode_step(tx, tr, tw, tg, tb, ts, out)
+    torch.cuda.synchronize()
+    ro, rs, rring = _oracle_conv_decode(d)
+    assert_close(to_np(out), ro, True, (0, 1), "out")
+    assert_close(to_np(ts), rs, True, (0, 1), "state")
+    assert np.array_equal(to_np(tr), rring)
