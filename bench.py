@@ -375,7 +375,8 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
     toks = T * 1.0
     by = T * H * PREFILL_TOKEN_HEAD_BYTES + H * D * D * 4
     fl = T * H * PREFILL_TOKEN_HEAD_FLOPS
-    return {"value": ws * toks / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
+    varlen = bench_varlen(torch, kda, dev, stream, ws, hbm_peak)
+    return {"value": ws * toks / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "varlen": varlen,
             "config": {"workload": f"chunked prefill T={T}, H={H}, d={D}, C={C}, bf16 q/k/v, zero S0, "
                                    "fp32 final state", "calls": n},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -383,6 +384,48 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
             "roofline_tensor": {"achieved": fl / (ms * 1e-3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s",
                                 "frac": fl / (ms * 1e-3) / 1e12 / tc_peak, "algorithmic_flops": fl,
                                 "peak_source": f"{peak_src} bf16_tflops (burst)"}}
+
+
+def bench_varlen(torch, kda, dev, stream, ws, hbm_peak):
+    """Variable-length prefill with carry-in: 8 sequences of 512..65536 tokens
+    (130,560 in all), H=96, d=128, C=64, bf16. Timing only; inputs drawn on
+    the device by a seeded torch generator with the workload's distributions."""
+    cu = synth.varlen_cu_seqlens()
+    T, N = int(cu[-1]), len(cu) - 1
+    gen = torch.Generator(device=dev).manual_seed(synth.VARLEN["seed"])
+
+    def rnd(shape):
+        return torch.randn(shape, generator=gen, device=dev)
+    q, k, v = (rnd((T, H, D)).to(torch.bfloat16) for _ in range(3))
+    g = -torch.nn.functional.softplus(rnd((T, H, D)))
+    beta = torch.sigmoid(rnd((T, H)))
+    s0 = rnd((N, H, D, D)) * 0.02
+    sf = torch.empty_like(s0)
+    out = torch.empty_like(q)
+    tcu = torch.from_numpy(cu).to(dev)
+    wsb = torch.empty(max(16, kda.kda_chunk_prefill_workspace_bytes(T, N, H, D, 64)), dtype=torch.uint8, device=dev)
+
+    def call():
+        kda.kda_chunk_prefill(q, k, v, g, beta, out, initial_state=s0, final_state=sf, cu_seqlens=tcu,
+                              chunk_size=64, workspace=wsb, stream=stream)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 5
+    a.record(stream)
+    for _ in range(n):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status(stream)
+    ms = a.elapsed_time(b) / n
+    by = T * H * PREFILL_TOKEN_HEAD_BYTES + 2 * N * H * D * D * 4
+    return {"value": ws * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
+            "config": {"workload": "varlen prefill, 8 sequences 512..65536 (130,560 tokens), H=96, d=128, C=64, "
+                                   "bf16, S0 ~ N(0,0.02^2), final states", "calls": n},
+            "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 
 
 def main():

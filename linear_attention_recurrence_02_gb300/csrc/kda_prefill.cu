@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(SIMT_NT)
                         const float *__restrict__ g, const float *__restrict__ beta,
                         const float *s_init, float *s_final, T *__restrict__ out,
                         const int64_t *__restrict__ cu_seqlens, int N, int64_t Ttot, int H, int C, float eps,
-                        unsigned *err) {
+                        unsigned *err, const int *__restrict__ order) {
     constexpr int JS = simt_js(D), LD = D + 1, NS = D / JS, NW = SIMT_NT / 32;
     extern __shared__ float smem[];
     float *sQ = smem;                    // [C][LD]  q^, then Qt
@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(SIMT_NT)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slice = blockIdx.x % NS;
     const int h = (blockIdx.x / NS) % H;
-    const int n = blockIdx.x / (NS * H);
+    const int n = order ? order[blockIdx.x / (NS * H)] : (int)(blockIdx.x / (NS * H));
     const int j0 = slice * JS;
     int64_t start, end;
     if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
@@ -193,7 +193,8 @@ static kda_status launch_simt(const PrefillArgs &a, cudaStream_t s) {
     const unsigned grid = (unsigned)a.N * a.H * (D / simt_js(D));
     kern<<<grid, SIMT_NT, smem, s>>>(static_cast<const T *>(a.q), static_cast<const T *>(a.k),
                                      static_cast<const T *>(a.v), a.g, a.beta, a.s_init, a.s_final,
-                                     static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err);
+                                     static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err,
+                                     a.order);
     return check_launch("prefill_simt_kernel");
 }
 
@@ -211,17 +212,50 @@ kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s) {
     return a.bf16 ? dispatch_simt<__nv_bfloat16>(a, s) : dispatch_simt<float>(a, s);
 }
 
+// Longest sequences first: a sequence's chunks are walked serially by its
+// CTAs, so starting the long chains first shortens the tail of a mixed-length
+// batch (greedy longest-processing-time order). order[rank] = n, where rank
+// counts longer sequences and equal-length sequences with a smaller index.
+__global__ void __launch_bounds__(1024) prefill_order_kernel(const int64_t *__restrict__ cu, int N,
+                                                             int *__restrict__ order) {
+    extern __shared__ int64_t s_len[];
+    for (int n = threadIdx.x; n < N; n += blockDim.x) s_len[n] = cu[n + 1] - cu[n];
+    __syncthreads();
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+        const int64_t ln = s_len[n];
+        int rank = 0;
+        for (int m = 0; m < N; ++m) {
+            const int64_t lm = s_len[m];
+            rank += (lm > ln) || (lm == ln && m < n);
+        }
+        order[rank] = n;
+    }
+}
+
+kda_status launch_prefill_order(const int64_t *cu_seqlens, int N, int *order, cudaStream_t s) {
+    const size_t smem = (size_t)N * sizeof(int64_t);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess)
+            return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    }
+    prefill_order_kernel<<<1, 1024, smem, s>>>(cu_seqlens, N, order);
+    return check_launch("prefill_order_kernel");
+}
+
 }  // namespace kda
 
 using namespace kda;
 
 extern "C" size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C) {
     (void)total_tokens;
-    (void)num_seqs;
     (void)H;
     (void)D;
     (void)C;
-    return 0;
+    // the launch order of a mixed-length batch: int32 per sequence
+    if (num_seqs < 2 || num_seqs > ORDER_MAX_SEQS) return 0;
+    return ((size_t)num_seqs * sizeof(int) + 255) & ~(size_t)255;
 }
 
 extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
@@ -253,8 +287,13 @@ extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void
     if (T == 0 && final_state == nullptr) return KDA_OK;
     if ((st = bind_stream_device(stream))) return st;
     PrefillArgs a{q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C,
-                  dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word()};
+                  dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word(), nullptr};
     if (a.err == nullptr) return fail(KDA_ERR_CUDA, "device error word unavailable");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (need > 0 && cu_seqlens != nullptr) {
+        int *order = static_cast<int *>(workspace);
+        if ((st = launch_prefill_order(cu_seqlens, N, order, s))) return st;
+        a.order = order;
+    }
     return prefill_tc_applicable(a) ? prefill_tc(a, s) : prefill_simt(a, s);
 }

@@ -21,7 +21,14 @@ struct PrefillArgs {
     void *workspace;
     size_t workspace_bytes;
     unsigned *err;
+    const int *order;  // sequences by descending length (device), or NULL = natural order
 };
+
+// Largest batch the length sort handles; bigger batches keep their order.
+constexpr int ORDER_MAX_SEQS = 4096;
+
+// Launch the length sort of the N sequences into `order` (int32 [N], device).
+kda_status launch_prefill_order(const int64_t *cu_seqlens, int N, int *order, cudaStream_t s);
 
 kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_applicable(const PrefillArgs &a);

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(NT, 1)
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                       const float *__restrict__ beta, const float *s_init, float *s_final,
                       __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens, int N,
-                      int64_t Ttot, int H, float eps, unsigned *err) {
+                      int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *s_rq = reinterpret_cast<float *>(sm + OFF_SMALL);
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q4 = warp & 3, hh = warp >> 2;
-    const int h = blockIdx.x % H, n = blockIdx.x / H;
+    const int h = blockIdx.x % H, n = order ? order[blockIdx.x / H] : (int)(blockIdx.x / H);
     int64_t start, end;
     if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
     const int x0 = h * D;
@@ -753,7 +753,7 @@ kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
     prefill_tc_kernel<<<(unsigned)a.N * a.H, NT, SMEM_BYTES, s>>>(
         mq, mk, mv, mg, a.beta, a.s_init, a.s_final, static_cast<__nv_bfloat16 *>(a.out), a.cu_seqlens, a.N, a.T,
-        a.H, a.eps, a.err);
+        a.H, a.eps, a.err, a.order);
     return check_launch("prefill_tc_kernel");
 }
 

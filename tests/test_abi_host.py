@@ -123,3 +123,38 @@ def test_fused_decode_rejects_bad_arguments(kda, case, detail):
                                      a["H"], a["D"], a["dtype"], a["eps"], None)
     assert st == kda.KDA_ERR_INVALID_ARG
     assert detail in L.kda_last_error_detail().decode()
+
+
+def test_prefill_workspace_is_the_launch_order(kda):
+    """Mixed-length batches of 2..4096 sequences take one int32 per sequence
+    (rounded to 256 bytes) for the longest-first launch order; one sequence
+    or very large batches take none."""
+    assert kda.kda_chunk_prefill_workspace_bytes(1000, 1, 96, 128, 64) == 0
+    assert kda.kda_chunk_prefill_workspace_bytes(1000, 8, 96, 128, 64) == 256
+    assert kda.kda_chunk_prefill_workspace_bytes(1000, 100, 96, 128, 64) == 512
+    assert kda.kda_chunk_prefill_workspace_bytes(1000, 5000, 96, 128, 64) == 0
+
+
+def test_prefill_rejects_short_workspace(kda):
+    L = kda.lib()
+    st = L.kda_chunk_prefill(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, None, None, 0x60000, 0x70000, 8, 100,
+                             4, 128, 64, 1, 1e-6, 0x80000, 16, None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    assert "workspace too small" in L.kda_last_error_detail().decode()
+
+
+@pytest.mark.parametrize("case,detail", [
+    (dict(C=65), "C must be in 1..64"),
+    (dict(C=0), "C must be in 1..64"),
+    (dict(N=2, cu=None), "cu_seqlens is NULL but N != 1"),
+    (dict(D=100), "D must be"),
+    (dict(q=None), "q is NULL"),
+])
+def test_prefill_rejects_bad_arguments(kda, case, detail):
+    a = dict(q=0x10000, cu=0x70000, N=1, T=100, H=4, D=128, C=64)
+    a.update(case)
+    L = kda.lib()
+    st = L.kda_chunk_prefill(a["q"], 0x20000, 0x30000, 0x40000, 0x50000, None, None, 0x60000, a["cu"], a["N"],
+                             a["T"], a["H"], a["D"], a["C"], 1, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    assert detail in L.kda_last_error_detail().decode()

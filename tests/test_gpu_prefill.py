@@ -108,6 +108,20 @@ def test_prefill_default_gates_full_head_dim(env, bf16):
     check(o, s, ro, rs, cu, bf16, "default gates")
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+def test_prefill_unsorted_lengths_launch_order(env, bf16):
+    """Sequences in no particular length order (including an empty one and a
+    long one in the middle): the longest-first launch order must not change
+    which outputs and states belong to which sequence."""
+    torch, kda = env
+    lengths = [70, 5, 0, 300, 33, 129, 64, 1]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    d = synth.prefill_inputs(58, int(cu[-1]), 2, 128, bf16, cu_seqlens=cu, s0_std=0.3, g_scale=0.1)
+    o, s = run_prefill(torch, kda, d, bf16, 64)
+    ro, rs = oracle_prefill(d)
+    check(o, s, ro, rs, cu, bf16, "unsorted lengths")
+
+
 def test_prefill_final_state_may_alias_initial(env):
     torch, kda = env
     d = synth.prefill_inputs(51, 200, 2, 64, False, cu_seqlens=VARLEN_SMALL, s0_std=0.3, g_scale=0.1)
