@@ -162,6 +162,35 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
                              int D, int C, kda_dtype dtype, float l2_eps, void *workspace,
                              size_t workspace_bytes, kda_stream_t stream);
 
+/*
+ * kda_chunk_prefill for callers that cannot allocate device memory. The pages
+ * have no counterpart: this is a convenience of the library, not part of the
+ * method.
+ *
+ * kda_chunk_prefill needs a small workspace for a mixed-length batch: the
+ * longest-first launch order, one int32 per sequence. Some callers cannot call
+ * cudaMalloc when they run the prefill. Examples are code inside another
+ * framework's allocator or memory-pool callback, where a nested allocation
+ * would deadlock or fragment the pool, and serving paths whose policy forbids
+ * allocation per request. This entry point takes no workspace. It keeps that
+ * order in a fixed array in device memory that the library owns: 16 KiB per
+ * GPU, held from the first use until the process exits.
+ *
+ * Arguments, layouts and results are those of kda_chunk_prefill.
+ * Limit: N <= 4096 sequences; a larger N returns KDA_ERR_INVALID_ARG (use
+ * kda_chunk_prefill with a workspace instead).
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current), so make that first call before any
+ * stream capture. Every call on a device shares the array, which keeps the
+ * previous call's contents. Nothing in it needs clearing, because each call
+ * rewrites every entry it reads. Calls that may overlap on the GPU (different
+ * streams, no ordering between them) race on the array and must not be issued.
+ */
+kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, const float *initial_state, float *final_state,
+                                     void *out, const int64_t *cu_seqlens, int N, int64_t T, int H, int D,
+                                     int C, kda_dtype dtype, float l2_eps, kda_stream_t stream);
+
 /* Synchronise `stream`, then report (and clear) any device-side error flag
  * raised by earlier calls on the stream's device: KDA_ERR_DEVICE_CHECK,
  * KDA_ERR_TIMEOUT, KDA_ERR_CUDA for an asynchronous CUDA error, else KDA_OK. */

@@ -38,6 +38,8 @@ _SIGNATURES = {
     "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
     "kda_chunk_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
                            _cf, _vp, _sz, _vp], _ci),
+    "kda_chunk_prefill_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci,
+                                   _ci, _cf, _vp], _ci),
     "kda_sync_status": ([_vp], _ci),
 }
 
@@ -173,6 +175,18 @@ def kda_chunk_prefill(q, k, v, g, beta, out, initial_state=None, final_state=Non
                                    _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
                                    _dtype_code(q), float(l2_eps), _ptr(workspace), wsz,
                                    _stream(stream, q.device)))
+
+
+def kda_chunk_prefill_noalloc(q, k, v, g, beta, out, initial_state=None, final_state=None, cu_seqlens=None,
+                              chunk_size=64, l2_eps=1e-6, stream=None):
+    """kda_chunk_prefill without a workspace, for callers that cannot allocate
+    device memory: the launch-order scratch lives in a fixed array owned by
+    the library (at most 4096 sequences). Overlapping calls race on it."""
+    T, H, D = q.shape
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    _check(lib().kda_chunk_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                           _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
+                                           _dtype_code(q), float(l2_eps), _stream(stream, q.device)))
 
 
 def kda_sync_status(stream=None, device=None):
