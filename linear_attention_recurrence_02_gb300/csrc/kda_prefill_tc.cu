@@ -387,52 +387,35 @@ __global__ void __launch_bounds__(NT, 1)
                 mma_commit(bar_mma);
             }
         }
-        if (!exact) {
-            got = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-            if (__syncthreads_or(!got)) {
-                mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-                ok = false;
-                break;
-            }
-            ph_mma ^= 1;
-            tc_fence_after();
-        }
-
-        // read back A (lanes 0-63, masked, times beta) and P (lanes 64-127, masked)
-        if (!exact) {
-            uint32_t r32[32];
-            tmem_ld32(tbase + lrow + TM_AP + 32 * hh, r32);
-            tmem_ld_wait();
-            const int s0 = 32 * hh;
-            if (q4 < 2) {
-                const int r = 32 * q4 + lane;
-                const float br = s_beta[r];
-#pragma unroll
-                for (int g4 = 0; g4 < 8; ++g4) {
-                    float4 a4;
-                    const int s = s0 + 4 * g4;
-                    a4.x = (s + 0 < r) ? br * __uint_as_float(r32[4 * g4 + 0]) : 0.f;
-                    a4.y = (s + 1 < r) ? br * __uint_as_float(r32[4 * g4 + 1]) : 0.f;
-                    a4.z = (s + 2 < r) ? br * __uint_as_float(r32[4 * g4 + 2]) : 0.f;
-                    a4.w = (s + 3 < r) ? br * __uint_as_float(r32[4 * g4 + 3]) : 0.f;
-                    *reinterpret_cast<float4 *>(Am + fsw(r, s >> 2)) = a4;
-                }
-            } else {
-                const int r = 32 * (q4 - 2) + lane;
-                float pv[32];
-#pragma unroll
-                for (int m = 0; m < 32; ++m) pv[m] = (s0 + m <= r) ? __uint_as_float(r32[m]) : 0.f;
-#pragma unroll
-                for (int qd = 0; qd < 4; ++qd) {
-                    const int cc = 4 * hh + qd;
-                    *reinterpret_cast<uint4 *>(sm + OFF_P + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(pv + 8 * qd);
-                }
-            }
-        }
-        __syncthreads();
-
-        // warps 0-3 solve for T while warps 4-7 convert the state operand
+        // Warps 0-3 wait for G1, read back A and solve for T. Meanwhile warps
+        // 4-7 convert the state operand (independent of G1), then read back P.
+        bool got_mma = true;
         if (warp < 4) {
+            if (!exact) {
+                got_mma = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
+                tc_fence_after();
+                if (q4 < 2) {  // A: TMEM lanes 0-63, masked (s < r), times beta
+                    const int r = 32 * q4 + lane;
+                    const float br = s_beta[r];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r32[32];
+                        tmem_ld32(tbase + lrow + TM_AP + 32 * half, r32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int g4 = 0; g4 < 8; ++g4) {
+                            float4 a4;
+                            const int sc = 32 * half + 4 * g4;
+                            a4.x = (sc + 0 < r) ? br * __uint_as_float(r32[4 * g4 + 0]) : 0.f;
+                            a4.y = (sc + 1 < r) ? br * __uint_as_float(r32[4 * g4 + 1]) : 0.f;
+                            a4.z = (sc + 2 < r) ? br * __uint_as_float(r32[4 * g4 + 2]) : 0.f;
+                            a4.w = (sc + 3 < r) ? br * __uint_as_float(r32[4 * g4 + 3]) : 0.f;
+                            *reinterpret_cast<float4 *>(Am + fsw(r, sc >> 2)) = a4;
+                        }
+                    }
+                }
+            }
+            named_bar_sync(1, 128);
             // M^-1 = (I + A)^-1, A strictly lower. Diagonal 16 x 16 blocks by
             // forward substitution (one thread per column) ...
             if (tid < 64) {
@@ -561,8 +544,38 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             tmem_st_wait();
+            if (!exact) {
+                got_mma = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
+                tc_fence_after();
+                if (q4 >= 2) {  // P: TMEM lanes 64-127, masked (s <= r)
+                    const int r = 32 * (q4 - 2) + lane;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r32[32];
+                        tmem_ld32(tbase + lrow + TM_AP + 32 * half, r32);
+                        tmem_ld_wait();
+                        float pv[32];
+#pragma unroll
+                        for (int m = 0; m < 32; ++m) pv[m] = (32 * half + m <= r) ? __uint_as_float(r32[m]) : 0.f;
+#pragma unroll
+                        for (int qd = 0; qd < 4; ++qd) {
+                            const int cc = 4 * half + qd;
+                            *reinterpret_cast<uint4 *>(sm + OFF_P + r * 128 + ((cc ^ (r & 7)) << 4)) =
+                                pack8(pv + 8 * qd);
+                        }
+                    }
+                }
+            }
         }
-        sync_for_mma();
+        fence_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!got_mma)) {
+            mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        if (!exact) ph_mma ^= 1;
 
         // G2: W'^T = Lk^T T^T,  G3: U0^T = V^T T^T,  G5: O^T = S~^T Lq^T
         if (tid == 0) {
