@@ -304,6 +304,9 @@ def run_ours(args):
     prefill = None
     if not args.no_prefill:
         prefill = bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src)
+    stack = None
+    if not args.no_stack:
+        stack = bench_stack(torch, kda, dev, ws, hbm_peak)
 
     if rank == 0:
         line = {
@@ -328,6 +331,8 @@ def run_ours(args):
         }
         if prefill is not None:
             line["prefill"] = prefill
+        if stack is not None:
+            line["stack"] = stack
         if ws == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(d)
         print(json.dumps(line))
@@ -423,6 +428,59 @@ def bench_varlen(torch, kda, dev, stream, ws, hbm_peak):
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 
 
+def bench_stack(torch, kda, dev, ws, hbm_peak, steps_per_graph=16, replays=8):
+    """Full-stack decode: 69 independent layers x 8 sequences x 96 heads
+    (414 MiB of fp32 state per sequence, 3.3 GB in all), one fused conv+decode
+    launch per layer per step in model order, `steps_per_graph` steps captured
+    in one CUDA graph with each step's own inputs. Inputs are drawn on the
+    device by a seeded torch generator with the workload's distributions."""
+    L, Bs = synth.STACK["layers"], synth.STACK["B"]
+    gen = torch.Generator(device=dev).manual_seed(synth.STACK["seed"])
+
+    def rnd(shape):
+        return torch.randn(shape, generator=gen, device=dev)
+    G = steps_per_graph
+    x = [rnd((G, Bs, 3, H, D)).to(torch.bfloat16) for _ in range(L)]
+    g = [-torch.nn.functional.softplus(rnd((G, Bs, H, D))) for _ in range(L)]
+    beta = [torch.sigmoid(rnd((G, Bs, H))) for _ in range(L)]
+    state = [rnd((Bs, H, D, D)) * 0.02 for _ in range(L)]
+    ring = [rnd((Bs, 3, H, 3, D)).to(torch.bfloat16) for _ in range(L)]
+    w = [rnd((3, H, D, 4)) * 0.5 for _ in range(L)]
+    out = [torch.empty((G, Bs, H, D), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+
+    def run_steps():
+        for t in range(G):
+            for li in range(L):
+                kda.kda_shortconv_decode_step(x[li][t], ring[li], w[li], g[li][t], beta[li][t], state[li], out[li][t])
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        run_steps()  # warm-up outside the graph
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run_steps()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status()
+    ms_step = a.elapsed_time(b) / (replays * G)
+    by = L * (Bs * H * DEC_UNIT_BYTES + CONV_W_BYTES)
+    return {"value": ws * by / (ms_step * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_step,
+            "config": {"workload": f"full-stack decode: {L} layers x {Bs} sequences x {H} heads, d={D}, bf16 q/k/v, "
+                                   f"fp32 state 3.3 GB, {L} fused launches per step in a CUDA graph of {G} steps",
+                       "steps_timed": replays * G},
+            "roofline_hbm": {"achieved": by / (ms_step * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": by / (ms_step * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,6 +489,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -29,6 +29,14 @@ kda_status check_ptr(const void *p, const char *name) {
 kda_status bind_stream_device(kda_stream_t stream) {
     int dev = -1;
     if (stream != nullptr) {
+        // A stream being captured into a CUDA graph does not permit
+        // cudaStreamGetDevice; the capturing thread's current device is the
+        // stream's device then, so it is kept as it is.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs) == cudaSuccess &&
+            cs != cudaStreamCaptureStatusNone)
+            return KDA_OK;
+        cudaGetLastError();
         cudaError_t e = cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &dev);
         if (e != cudaSuccess) {
             cudaGetLastError();
