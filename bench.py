@@ -140,6 +140,19 @@ class ClockSampler:
                 "power_w_max": max([num(r[2]) for r in rows if num(r[2]) is not None] or [0])}
 
 
+def max_over_ranks(value, device=None):
+    """Largest value over the ranks of the default process group (the value
+    itself when there is one rank): per-step times are reported as the
+    slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -254,10 +267,8 @@ def run_ours(args):
     ms = start.elapsed_time(end)
     # the timed region holds only this kernel's launches, one per step
     dec_ms = [ms / args.steps]
+    ms = max_over_ranks(ms, dev)
     if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     kda.kda_sync_status(stream)
     ms_per_step = ms / args.steps
@@ -294,10 +305,7 @@ def run_ours(args):
     e2.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = s2.elapsed_time(e2) / k_e2e
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     h2d = xh.numel() * 2 + gh.numel() * 4 + bh.numel() * 4
     d2h = oh.numel() * 2
 
@@ -371,7 +379,7 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
         b.record(stream)
     torch.cuda.synchronize(dev)
     kda.kda_sync_status(stream)
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
     toks = T * 1.0
     by = T * H * PREFILL_TOKEN_HEAD_BYTES + H * D * D * 4
     fl = T * H * PREFILL_TOKEN_HEAD_FLOPS
@@ -419,7 +427,7 @@ def bench_varlen(torch, kda, dev, stream, ws, hbm_peak):
     b.record(stream)
     torch.cuda.synchronize(dev)
     kda.kda_sync_status(stream)
-    ms = a.elapsed_time(b) / n
+    ms = max_over_ranks(a.elapsed_time(b) / n, dev)
     by = T * H * PREFILL_TOKEN_HEAD_BYTES + 2 * N * H * D * D * 4
     return {"value": ws * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
             "config": {"workload": "varlen prefill, 8 sequences 512..65536 (130,560 tokens), H=96, d=128, C=64, "
@@ -471,7 +479,7 @@ def bench_stack(torch, kda, dev, ws, hbm_peak, steps_per_graph=16, replays=8):
     b.record()
     torch.cuda.synchronize(dev)
     kda.kda_sync_status()
-    ms_step = a.elapsed_time(b) / (replays * G)
+    ms_step = max_over_ranks(a.elapsed_time(b) / (replays * G), dev)
     by = L * (Bs * H * DEC_UNIT_BYTES + CONV_W_BYTES)
     return {"value": ws * by / (ms_step * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_step,
             "config": {"workload": f"full-stack decode: {L} layers x {Bs} sequences x {H} heads, d={D}, bf16 q/k/v, "
