@@ -7,24 +7,28 @@
 // cumulative decay as a product of gates; the WY/UT reparameterisation it
 // names is realised here as T = (I + A)^-1 Diag(beta)). With G the
 // cumulative log decay inside the chunk and a per-channel anchor c:
-//   Lk = e^{G-c} k^,  Lq = e^{G-c} q^,  Rk = e^{c-G} k^,  Kb = e^{G_L-G} k^,
-//   S~ = Diag(e^c) S
+//   Lk = e^{G-c} k^,  Lq = e^{G-c} q^,  Rk = e^{c-G} k^,  S~ = Diag(e^c) S
 //   [A_raw; P_raw] = [Lk; Lq] Rk^T            (G1)   A = mask_<(beta A_raw)
 //   T = (I + A)^-1 Diag(beta)                  (CUDA cores, fp32)
 //   W' = T Lk,  U0 = T V                       (G2, G3)
 //   U = U0 - W' S~                             (G4)
 //   O = Lq S~ + P U                            (G5, G6)
-//   S <- Diag(e^{G_L}) S + Kb^T U              (G7)
+//   S <- Diag(e^{G_L}) S + Kb^T U,  Kb = e^{G_L-G} k^ = Diag(e^{G_L-c}) Rk
 // Lk S~ = Diag-folded e^G k^ S, so W' S~ = T Kt S and Lq S~ = Qt S exactly.
-// c = min(0, G_L + 80) keeps every factor inside e^[-80, 80] whenever the
-// chunk's decay span G_0 - G_L is at most 160; a chunk beyond that computes
-// A and P with exact pairwise exponentials on CUDA cores and uses c = 0.
+// The state is held as S = Diag(sigma) S_st with sigma = e^{G_L-c} of the
+// chunk that wrote it, so the update needs no Kb tile:
+//   S_st <- Diag(e^c sigma_old) S_st + Rk^T U  (G7),  S~ = Diag(e^c sigma_old) S_st
+// c = min(0, G_L + 40) keeps every factor and 1/sigma inside e^[-40, 40]
+// whenever the chunk's decay span G_0 - G_L is at most 80; a chunk beyond that
+// computes A and P with exact pairwise exponentials on CUDA cores, uses c = 0
+// and Kb in place of Rk, and resets sigma to 1.
 //
 // Layout: every MMA has M = 128 on a channel axis, so TMEM lane = channel
-// (key channel i or value channel j) throughout, and the fp32 master state
-// S^T (lane j, column i) never leaves TMEM between chunks. Operands are bf16
-// in 128-byte-swizzled shared memory tiles, loaded by TMA (q, k, v, g) or
-// written by the CUDA cores from TMEM read-backs.
+// (key channel i or value channel j) throughout, and the fp32 state S_st^T
+// (lane j, column i) never leaves TMEM between chunks. Operands are bf16 in
+// 128-byte-swizzled shared memory tiles, loaded by TMA (q, k, v, g) or
+// written by the CUDA cores from TMEM read-backs. TMA drops k and q into one
+// 128-row tile that becomes [Lk; Lq] in place.
 //
 // One CTA (256 threads, 2 warpgroups) per (sequence, head) walks the chunks
 // of its sequence; thread 0 issues TMA and MMAs, every wait is bounded.
@@ -43,29 +47,29 @@ using namespace tc;
 
 constexpr int C = 64, D = 128, NT = 256;
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_QRAW = 0;        // q tile (TMA, prefetched one chunk ahead)
-constexpr uint32_t OFF_KRAW = 16384;    // k tile (TMA, prefetched)
+constexpr uint32_t OFF_X = 0;           // k rows 0-63 + q rows 64-127 (TMA) -> [Lk; Lq] in place
 constexpr uint32_t OFF_V = 32768;       // v tile (TMA, prefetched after G3)
-constexpr uint32_t OFF_G = 49152;       // g fp32 [64][128] (TMA, prefetched) -> cumulative G
-constexpr uint32_t OFF_LKQ = 81920;     // [Lk; Lq] 128 rows -> W' (rows i) + U^T (rows j) -> O staging
-constexpr uint32_t OFF_W = OFF_LKQ;
-constexpr uint32_t OFF_U = OFF_LKQ + 16384;
-constexpr uint32_t OFF_OST = OFF_LKQ;
-constexpr uint32_t OFF_RK = 114688;     // Rk 64 rows -> A (fp32 [64][64], row-major, swizzled)
-constexpr uint32_t OFF_KB = 131072;     // Kb 64 rows
-constexpr uint32_t OFF_SOP = 147456;    // S~^T 128 rows (j) x 128 (i)
-constexpr uint32_t OFF_T = 180224;      // T 64 rows (r) x 64 (s)
-constexpr uint32_t OFF_P = 188416;      // P 64 rows (r) x 64 (s)
-constexpr uint32_t OFF_MT = 196608;     // M^-1 fp32 [64][64], column-major, swizzled
-constexpr uint32_t OFF_Y = 212992;      // blocked-inverse scratch (3 KiB) + diagonal block inverses (4 KiB)
-constexpr uint32_t OFF_SMALL = 221184;  // per-row / per-channel vectors, barriers
-constexpr uint32_t SMEM_BYTES = OFF_SMALL + 3072 + 1024;
-constexpr uint32_t QKG_BYTES = 2 * 16384 + 32768;
-constexpr uint32_t V_BYTES = 16384;
+constexpr uint32_t OFF_G = 49152;       // g fp32 [64][128] (TMA, prefetched) -> cumulative G (log2 units)
+constexpr uint32_t OFF_RK = 81920;      // Rk (Kb on the exact path), 64 rows; kept until G7
+constexpr uint32_t OFF_SOP = 98304;     // S~^T 128 rows (j) x 128 (i) -> O staging
+constexpr uint32_t OFF_OST = OFF_SOP;
+constexpr uint32_t OFF_T = 131072;      // T 64 rows (r) x 64 (s)
+constexpr uint32_t OFF_P = 139264;      // P 64 rows (r) x 64 (s)
+constexpr uint32_t OFF_A = 147456;      // A fp32 [64][64] row-major swizzled -> W' (rows i)
+constexpr uint32_t OFF_W = OFF_A;
+constexpr uint32_t OFF_MT = 163840;     // M^-1 fp32 [64][64] column-major swizzled -> U^T (rows j)
+constexpr uint32_t OFF_U = OFF_MT;
+constexpr uint32_t OFF_Y = 180224;      // blocked-inverse scratch (3 KiB) + diagonal block inverses (4 KiB)
+constexpr uint32_t OFF_SMALL = 188416;  // per-row / per-channel vectors, barriers
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;
+constexpr uint32_t QK_BYTES = 2 * 16384, G_BYTES = 32768, V_BYTES = 16384;
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_S = 0, TM_AP = 128, TM_W = 192, TM_U0 = 256, TM_X = 320, TM_O = 384;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
-constexpr float SPAN_MAX = 160.f, ANCHOR = 80.f;
+// Anchored factors stay within e^[-ANCHOR, ANCHOR] when the chunk's decay
+// span is at most SPAN_MAX; the fp32 state kept as S / sigma then stays
+// below e^ANCHOR times |S|.
+constexpr float ANCHOR = 40.f, SPAN_MAX = 2.f * ANCHOR;
 
 constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_MK64 = idesc_bf16(128, 64, 1, 0);
@@ -152,16 +156,18 @@ __global__ void __launch_bounds__(NT, 1)
     float *s_rq = reinterpret_cast<float *>(sm + OFF_SMALL);
     float *s_rk = s_rq + 64;
     float *s_beta = s_rk + 64;
-    float *s_gl = s_beta + 64;
-    float *s_c = s_gl + 128;
-    float *s_expc = s_c + 128;
-    float *s_expgl = s_expc + 128;
-    uint64_t *bar_qkg = reinterpret_cast<uint64_t *>(s_expgl + 128);
-    uint64_t *bar_v = bar_qkg + 1;
-    uint64_t *bar_mma = bar_qkg + 2;
-    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bar_qkg + 3);
+    float *s_gl = s_beta + 64;      // G at the chunk's last row (natural log)
+    float *s_c = s_gl + 128;        // anchor c
+    float *s_sf = s_c + 128;        // S~ factor e^c sigma_old
+    float *s_pf = s_sf + 128;       // rescale of the stored state before G7 accumulates
+    float *s_sigma = s_pf + 128;    // per-channel scale: S = Diag(sigma) S_stored
+    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(s_sigma + 128);
+    uint64_t *bar_g = bar_qk + 1;
+    uint64_t *bar_v = bar_qk + 2;
+    uint64_t *bar_mma = bar_qk + 3;
+    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bar_qk + 4);
     float *gt = reinterpret_cast<float *>(sm + OFF_G);
-    float *Am = reinterpret_cast<float *>(sm + OFF_RK);  // A[r][s] at fsw(r, s/4) + s%4
+    float *Am = reinterpret_cast<float *>(sm + OFF_A);   // A[r][s] at fsw(r, s/4) + s%4
     float *MT = reinterpret_cast<float *>(sm + OFF_MT);  // M^-1[k][s] at fsw(s, k/4) + k%4
     float *Yb = reinterpret_cast<float *>(sm + OFF_Y);   // [block][s_local][k_local]
     float *Dv = Yb + 768;                                // diagonal inverses [block][row][col]
@@ -173,8 +179,27 @@ __global__ void __launch_bounds__(NT, 1)
     if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
     const int x0 = h * D;
 
+    // q, k land in one 128-row tile: k in rows 0-63, q in rows 64-127
+    auto issue_qk = [&](int y) {
+        mbar_arrive_expect_tx(bar_qk, QK_BYTES);
+        tma_load_2d(sm + OFF_X, &tm_k, bar_qk, x0, y);
+        tma_load_2d(sm + OFF_X + 16384, &tm_k, bar_qk, x0 + 64, y);
+        tma_load_2d(sm + OFF_X + 8192, &tm_q, bar_qk, x0, y);
+        tma_load_2d(sm + OFF_X + 24576, &tm_q, bar_qk, x0 + 64, y);
+    };
+    auto issue_g = [&](int y) {
+        mbar_arrive_expect_tx(bar_g, G_BYTES);
+        tma_load_2d(sm + OFF_G, &tm_g, bar_g, x0, y);
+    };
+    auto issue_v = [&](int y) {
+        mbar_arrive_expect_tx(bar_v, V_BYTES);
+        tma_load_2d(sm + OFF_V, &tm_v, bar_v, x0, y);
+        tma_load_2d(sm + OFF_V + 8192, &tm_v, bar_v, x0 + 64, y);
+    };
+
     if (tid == 0) {
-        mbar_init(bar_qkg, 1);
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_g, 1);
         mbar_init(bar_v, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
@@ -183,17 +208,12 @@ __global__ void __launch_bounds__(NT, 1)
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_g);
         if (start < end) {
-            mbar_arrive_expect_tx(bar_qkg, QKG_BYTES);
-            tma_load_2d(sm + OFF_QRAW, &tm_q, bar_qkg, x0, (int)start);
-            tma_load_2d(sm + OFF_QRAW + 8192, &tm_q, bar_qkg, x0 + 64, (int)start);
-            tma_load_2d(sm + OFF_KRAW, &tm_k, bar_qkg, x0, (int)start);
-            tma_load_2d(sm + OFF_KRAW + 8192, &tm_k, bar_qkg, x0 + 64, (int)start);
-            tma_load_2d(sm + OFF_G, &tm_g, bar_qkg, x0, (int)start);
-            mbar_arrive_expect_tx(bar_v, V_BYTES);
-            tma_load_2d(sm + OFF_V, &tm_v, bar_v, x0, (int)start);
-            tma_load_2d(sm + OFF_V + 8192, &tm_v, bar_v, x0 + 64, (int)start);
+            issue_qk((int)start);
+            issue_g((int)start);
+            issue_v((int)start);
         }
     }
+    if (tid < 128) s_sigma[tid] = 1.f;
     if (warp == 0) {
         tmem_alloc(s_taddr, 512);
         tmem_relinquish();
@@ -205,7 +225,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int jl = 32 * q4 + lane;                    // this thread's TMEM lane (channel)
     const size_t soff = ((size_t)n * H + h) * D * D;
 
-    // initial state -> TMEM (S^T: lane j, column i)
+    // initial state -> TMEM (S^T: lane j, column i); sigma = 1
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
         uint32_t r[32];
@@ -219,6 +239,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     uint32_t ph = 0, ph_mma = 0;
     bool ok = true;
+    bool pend_g = false, pend_qkv = false;  // next chunk's loads in flight (phase ph ^ 1)
     float beta_reg = 0.f;  // beta of the next chunk, loaded one chunk ahead
     if (tid < C && start + tid < end) beta_reg = beta[(size_t)(start + tid) * H + h];
     for (int64_t c0 = start; c0 < end; c0 += C, ph ^= 1) {
@@ -226,13 +247,16 @@ __global__ void __launch_bounds__(NT, 1)
         const bool has_next = c0 + C < end;
         sync_for_mma();  // previous chunk fully consumed
         if (tid < C) s_beta[tid] = beta_reg;
-        bool got = mbar_wait(bar_qkg, ph, WAIT_LIMIT) && mbar_wait(bar_v, ph, WAIT_LIMIT);
+        bool got = mbar_wait(bar_qk, ph, WAIT_LIMIT) && mbar_wait(bar_g, ph, WAIT_LIMIT) &&
+                   mbar_wait(bar_v, ph, WAIT_LIMIT);
         if (__syncthreads_or(!got)) {
-            mbar_wait(bar_qkg, ph, WAIT_LIMIT);
+            mbar_wait(bar_qk, ph, WAIT_LIMIT);
+            mbar_wait(bar_g, ph, WAIT_LIMIT);
             mbar_wait(bar_v, ph, WAIT_LIMIT);
             ok = false;
             break;
         }
+        pend_g = pend_qkv = false;
 
         // rows past the end of the sequence: zero q, k, v, g (so beta = 0,
         // k = 0 and G stays at G_{L-1}); they then contribute nothing
@@ -240,10 +264,9 @@ __global__ void __launch_bounds__(NT, 1)
             const uint4 z4 = make_uint4(0, 0, 0, 0);
             for (int p = tid; p < (C - L) * 16; p += NT) {
                 const int r = L + (p >> 4), cc = p & 15;
-                const uint32_t o = swz(r, cc, 64);
-                *reinterpret_cast<uint4 *>(sm + OFF_QRAW + o) = z4;
-                *reinterpret_cast<uint4 *>(sm + OFF_KRAW + o) = z4;
-                *reinterpret_cast<uint4 *>(sm + OFF_V + o) = z4;
+                *reinterpret_cast<uint4 *>(sm + OFF_X + swz(r, cc, 128)) = z4;
+                *reinterpret_cast<uint4 *>(sm + OFF_X + swz(r + 64, cc, 128)) = z4;
+                *reinterpret_cast<uint4 *>(sm + OFF_V + swz(r, cc, 64)) = z4;
             }
             for (int p = tid; p < (C - L) * 32; p += NT)
                 *reinterpret_cast<uint4 *>(sm + OFF_G + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
@@ -252,16 +275,16 @@ __global__ void __launch_bounds__(NT, 1)
 
         // warps 0-3: L2 norms, one thread per q or k row; warps 4-7: cumulative
         // log decay G along the chunk, one channel per thread in registers,
-        // stored back in log2 units, and the per-channel anchor
+        // stored back in log2 units
         int bad = 0;
         if (tid < 128) {
             const int r = tid & 63;
-            const uint8_t *tile = sm + (tid < 64 ? OFF_QRAW : OFF_KRAW);
+            const int row = tid < 64 ? r + 64 : r;  // q rows follow the k rows
             float ss = 0.f;
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc) {
                 float f[8];
-                unpack8(*reinterpret_cast<const uint4 *>(tile + swz(r, cc, 64)), f);
+                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(row, cc, 128)), f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ss += f[e] * f[e];
             }
@@ -275,69 +298,27 @@ __global__ void __launch_bounds__(NT, 1)
             for (int r = 1; r < 64; ++r) gv[r] += gv[r - 1];
             const float GL = gv[63];
             bad = !(gv[0] - GL <= SPAN_MAX);
-            const float c = fminf(0.f, GL + ANCHOR);
 #pragma unroll
             for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
             s_gl[i] = GL;
-            s_c[i] = c;
-            s_expc[i] = expf(c);
-            s_expgl[i] = expf(GL);
         }
         const int exact = __syncthreads_or(bad);
-        if (exact) {  // rare: no anchor, exact pairwise decays below
-            if (tid < 128) {
-                s_c[tid] = 0.f;
-                s_expc[tid] = 1.f;
-            }
-            __syncthreads();
+        // per-channel anchor and state scale: sigma_new = e^{G_L - c} on the
+        // anchored path (then G7 can use Rk as is), 1 on the exact path
+        if (tid < 128) {
+            const float GL = s_gl[tid], so = s_sigma[tid];
+            const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
+            const float ec = expf(c);
+            s_c[tid] = c;
+            s_sf[tid] = ec * so;
+            s_pf[tid] = exact ? expf(GL) * so : ec * so;
+            s_sigma[tid] = exact ? 1.f : expf(GL - c);
         }
-
-        // operand tiles Lk, Lq, Rk, Kb (bf16, swizzled) from q^, k^ and G;
-        // each thread keeps one 8-channel group and walks 4 rows
-        {
-            const int cc = tid & 15, rb = tid >> 4;
-            float cv[8], egc[8], glv[8];  // anchor and G_L in log2 units
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                cv[e] = s_c[cc * 8 + e] * LOG2E;
-                glv[e] = s_gl[cc * 8 + e] * LOG2E;
-                egc[e] = ex2(glv[e] - cv[e]);
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = rb + 16 * m;
-                const uint32_t o64 = swz(r, cc, 64);
-                float qf[8], kf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + o64), qf);
-                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + o64), kf);
-                const float rq = s_rq[r], rk = s_rk[r];
-                const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
-                const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
-                const float G[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                float lk[8], lq[8], rkv[8], kbv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float kh = kf[e] * rk, qh = qf[e] * rq;
-                    const float e1 = ex2(G[e] - cv[e]);
-                    lk[e] = e1 * kh;
-                    lq[e] = e1 * qh;
-                    if (!exact) {
-                        const float inv = ex2(cv[e] - G[e]);  // <= e^ANCHOR
-                        rkv[e] = inv * kh;
-                        kbv[e] = egc[e] * inv * kh;
-                    } else {
-                        kbv[e] = ex2(glv[e] - G[e]) * kh;
-                    }
-                }
-                *reinterpret_cast<uint4 *>(sm + OFF_LKQ + swz(r, cc, 128)) = pack8(lk);
-                *reinterpret_cast<uint4 *>(sm + OFF_LKQ + swz(r + 64, cc, 128)) = pack8(lq);
-                if (!exact) *reinterpret_cast<uint4 *>(sm + OFF_RK + o64) = pack8(rkv);
-                *reinterpret_cast<uint4 *>(sm + OFF_KB + o64) = pack8(kbv);
-            }
-        }
+        __syncthreads();
 
         if (exact) {
-            // A and P with exact pairwise decays (rare: decay span > e^160)
+            // A and P with exact pairwise decays (rare: decay span G_0 - G_L > SPAN_MAX),
+            // from the raw q, k before they are overwritten in place
             for (int p = tid; p < C * C; p += NT) {
                 const int r = p & 63, s = p >> 6;
                 float a = 0.f, pq = 0.f;
@@ -345,9 +326,9 @@ __global__ void __launch_bounds__(NT, 1)
                     const float rkr = s_rk[r], rks = s_rk[s], rqr = s_rq[r];
                     for (int cc = 0; cc < 16; ++cc) {
                         float kr[8], ks[8], qr[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + swz(r, cc, 64)), kr);
-                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_KRAW + swz(s, cc, 64)), ks);
-                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_QRAW + swz(r, cc, 64)), qr);
+                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(r, cc, 128)), kr);
+                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(s, cc, 128)), ks);
+                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(r + 64, cc, 128)), qr);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int i = cc * 8 + e;
@@ -361,32 +342,62 @@ __global__ void __launch_bounds__(NT, 1)
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_P + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) +
                                                    (s & 7) * 2) = __float2bfloat16_rn(pq);
             }
+            __syncthreads();
+        }
+
+        // operand tiles: [Lk; Lq] in place over [k; q], and Rk (Kb on the
+        // exact path); each thread keeps one 8-channel group and walks 4 rows
+        {
+            const int cc = tid & 15, rb = tid >> 4;
+            float cv[8], glv[8];  // anchor and G_L in log2 units
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                cv[e] = s_c[cc * 8 + e] * LOG2E;
+                glv[e] = s_gl[cc * 8 + e] * LOG2E;
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = rb + 16 * m;
+                const uint32_t ok_ = swz(r, cc, 128), oq = swz(r + 64, cc, 128);
+                float qf[8], kf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + oq), qf);
+                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + ok_), kf);
+                const float rq = s_rq[r], rk = s_rk[r];
+                const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
+                const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
+                const float G[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                float lk[8], lq[8], rkv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float kh = kf[e] * rk, qh = qf[e] * rq;
+                    const float e1 = ex2(G[e] - cv[e]);
+                    lk[e] = e1 * kh;
+                    lq[e] = e1 * qh;
+                    rkv[e] = (exact ? ex2(glv[e] - G[e]) : ex2(cv[e] - G[e])) * kh;  // Kb or Rk (<= e^ANCHOR)
+                }
+                *reinterpret_cast<uint4 *>(sm + OFF_X + ok_) = pack8(lk);
+                *reinterpret_cast<uint4 *>(sm + OFF_X + oq) = pack8(lq);
+                *reinterpret_cast<uint4 *>(sm + OFF_RK + swz(r, cc, 64)) = pack8(rkv);
+            }
         }
         sync_for_mma();
 
         if (tid < C) beta_reg = (has_next && c0 + C + tid < end) ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
-        // q, k, g of this chunk are consumed: prefetch the next chunk's.
+        // g of this chunk is consumed: prefetch the next chunk's.
         // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T
         if (tid == 0) {
-            if (has_next) {
-                const int y1 = (int)(c0 + C);
-                mbar_arrive_expect_tx(bar_qkg, QKG_BYTES);
-                tma_load_2d(sm + OFF_QRAW, &tm_q, bar_qkg, x0, y1);
-                tma_load_2d(sm + OFF_QRAW + 8192, &tm_q, bar_qkg, x0 + 64, y1);
-                tma_load_2d(sm + OFF_KRAW, &tm_k, bar_qkg, x0, y1);
-                tma_load_2d(sm + OFF_KRAW + 8192, &tm_k, bar_qkg, x0 + 64, y1);
-                tma_load_2d(sm + OFF_G, &tm_g, bar_qkg, x0, y1);
-            }
+            if (has_next) issue_g((int)(c0 + C));
             if (!exact) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                    mma_bf16(tbase + TM_AP, sdesc_sw128(sbase + OFF_LKQ + kb * 16384 + ko, 16, 1024),
+                    mma_bf16(tbase + TM_AP, sdesc_sw128(sbase + OFF_X + kb * 16384 + ko, 16, 1024),
                              sdesc_sw128(sbase + OFF_RK + kb * 8192 + ko, 16, 1024), ID_KK64, ks > 0);
                 }
                 mma_commit(bar_mma);
             }
         }
+        pend_g = has_next;
         // Warps 0-3 wait for G1, read back A and solve for T. Meanwhile warps
         // 4-7 convert the state operand (independent of G1), then read back P.
         bool got_mma = true;
@@ -510,7 +521,8 @@ __global__ void __launch_bounds__(NT, 1)
                 *reinterpret_cast<uint4 *>(sm + OFF_T + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(tv);
             }
         } else {
-            // S~^T = S^T Diag(e^c) as a bf16 operand; S^T <- S^T Diag(e^{G_L}) in TMEM.
+            // The state is kept as S = Diag(sigma) S_stored. S~^T = S_stored^T Diag(sf)
+            // becomes the bf16 operand; S_stored^T <- S_stored^T Diag(pf) in TMEM.
             // Two 32-column TMEM loads per wait; per-channel factors as float4.
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
@@ -524,8 +536,8 @@ __global__ void __launch_bounds__(NT, 1)
                     float so[32];
 #pragma unroll
                     for (int g4 = 0; g4 < 8; ++g4) {
-                        const float4 fc = *reinterpret_cast<const float4 *>(s_expc + i0 + 4 * g4);
-                        const float4 fl = *reinterpret_cast<const float4 *>(s_expgl + i0 + 4 * g4);
+                        const float4 fc = *reinterpret_cast<const float4 *>(s_sf + i0 + 4 * g4);
+                        const float4 fl = *reinterpret_cast<const float4 *>(s_pf + i0 + 4 * g4);
                         const float fcv[4] = {fc.x, fc.y, fc.z, fc.w}, flv[4] = {fl.x, fl.y, fl.z, fl.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -582,14 +594,14 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t b = sdesc_sw128(sbase + OFF_T + ks * 32, 16, 1024);
-                mma_bf16(tbase + TM_W, sdesc_sw128(sbase + OFF_LKQ + ks * 2048, 16384, 1024), b, ID_MK64, ks > 0);
+                mma_bf16(tbase + TM_W, sdesc_sw128(sbase + OFF_X + ks * 2048, 16384, 1024), b, ID_MK64, ks > 0);
                 mma_bf16(tbase + TM_U0, sdesc_sw128(sbase + OFF_V + ks * 2048, 8192, 1024), b, ID_MK64, ks > 0);
             }
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
                 mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_SOP + kb * 16384 + ko, 16, 1024),
-                         sdesc_sw128(sbase + OFF_LKQ + 8192 + kb * 16384 + ko, 16, 1024), ID_KK64, ks > 0);
+                         sdesc_sw128(sbase + OFF_X + 8192 + kb * 16384 + ko, 16, 1024), ID_KK64, ks > 0);
             }
             mma_commit(bar_mma);
         }
@@ -601,14 +613,13 @@ __global__ void __launch_bounds__(NT, 1)
         }
         ph_mma ^= 1;
         tc_fence_after();
-        if (tid == 0 && has_next) {  // v of this chunk is consumed
-            const int y1 = (int)(c0 + C);
-            mbar_arrive_expect_tx(bar_v, V_BYTES);
-            tma_load_2d(sm + OFF_V, &tm_v, bar_v, x0, y1);
-            tma_load_2d(sm + OFF_V + 8192, &tm_v, bar_v, x0 + 64, y1);
+        if (tid == 0 && has_next) {  // q, k and v of this chunk are consumed
+            issue_qk((int)(c0 + C));
+            issue_v((int)(c0 + C));
         }
+        pend_qkv = has_next;
 
-        // W'^T (lane i, column r) -> bf16 tile rows i (MN-major operand)
+        // W'^T (lane i, column r) -> bf16 tile rows i (MN-major operand), over A
         {
             uint32_t r32[32];
             tmem_ld32(tbase + lrow + TM_W + 32 * hh, r32);
@@ -643,7 +654,7 @@ __global__ void __launch_bounds__(NT, 1)
         ph_mma ^= 1;
         tc_fence_after();
 
-        // U^T = U0^T - X^T -> bf16 tile rows j (K-major operand)
+        // U^T = U0^T - X^T -> bf16 tile rows j (K-major operand), over M^-1
         {
             uint32_t u0[32], x[32];
             tmem_ld32(tbase + lrow + TM_U0 + 32 * hh, u0);
@@ -660,13 +671,13 @@ __global__ void __launch_bounds__(NT, 1)
         }
         sync_for_mma();
 
-        // G6: O^T += U^T P^T   and   G7: S^T += U^T Kb
+        // G6: O^T += U^T P^T   and   G7: S_stored^T += U^T Rk (Kb on the exact path)
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t a = sdesc_sw128(sbase + OFF_U + ks * 32, 16, 1024);
                 mma_bf16(tbase + TM_O, a, sdesc_sw128(sbase + OFF_P + ks * 32, 16, 1024), ID_KK64, 1);
-                mma_bf16(tbase + TM_S, a, sdesc_sw128(sbase + OFF_KB + ks * 2048, 8192, 1024), ID_KM128, 1);
+                mma_bf16(tbase + TM_S, a, sdesc_sw128(sbase + OFF_RK + ks * 2048, 8192, 1024), ID_KM128, 1);
             }
             mma_commit(bar_mma);
         }
@@ -699,7 +710,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
 
     sync_tc();
-    if (ok && s_final) {
+    if (ok && s_final) {  // S = Diag(sigma) S_stored
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             const int i0 = 64 * hh + 32 * part;
@@ -707,10 +718,18 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_ld32(tbase + lrow + TM_S + i0, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int m = 0; m < 32; ++m) s_final[soff + (size_t)(i0 + m) * D + jl] = __uint_as_float(r[m]);
+            for (int m = 0; m < 32; ++m)
+                s_final[soff + (size_t)(i0 + m) * D + jl] = __uint_as_float(r[m]) * s_sigma[i0 + m];
         }
     }
-    if (!ok && tid == 0) atomicOr(err, DEVERR_TIMEOUT);
+    if (!ok) {  // let this CTA's own copies land before its shared memory goes away
+        if (pend_g) mbar_wait(bar_g, ph ^ 1, WAIT_LIMIT);
+        if (pend_qkv) {
+            mbar_wait(bar_qk, ph ^ 1, WAIT_LIMIT);
+            mbar_wait(bar_v, ph ^ 1, WAIT_LIMIT);
+        }
+        if (tid == 0) atomicOr(err, DEVERR_TIMEOUT);
+    }
     sync_tc();
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
