@@ -57,9 +57,9 @@ constexpr uint32_t OFF_T = 131072;      // T 64 rows (r) x 64 (s)
 constexpr uint32_t OFF_P = 139264;      // P 64 rows (r) x 64 (s)
 constexpr uint32_t OFF_A = 147456;      // A fp32 [64][64] row-major swizzled -> W' (rows i)
 constexpr uint32_t OFF_W = OFF_A;
-constexpr uint32_t OFF_MT = 163840;     // M^-1 fp32 [64][64] column-major swizzled -> U^T (rows j)
-constexpr uint32_t OFF_U = OFF_MT;
-constexpr uint32_t OFF_Y = 180224;      // blocked-inverse scratch (3 KiB) + diagonal block inverses (4 KiB)
+constexpr uint32_t OFF_U = 163840;      // U^T 128 rows (j) x 64 (r)
+constexpr uint32_t OFF_Y = 180224;      // solve scratch: six 16 x 16 fp32 blocks (7.5 KiB)
+constexpr int LDB = 20, BLK = 16 * LDB;  // block row stride (bank-conflict free A fragments), block size
 constexpr uint32_t OFF_SMALL = 188416;  // per-row / per-channel vectors, barriers
 constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;
 constexpr uint32_t QK_BYTES = 2 * 16384, G_BYTES = 32768, V_BYTES = 16384;
@@ -97,17 +97,34 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// fp32 -> tf32 operand: round to nearest (ties away from zero) on the 10-bit
+// mantissa by adding half an ulp of tf32 to the bit pattern and truncating
+__device__ __forceinline__ uint32_t to_tf32(float x) { return (__float_as_uint(x) + 0x1000u) & 0xffffe000u; }
 // warp-level D(16x8) += A(16x8, row) * B(8x8, col) on tf32 inputs, fp32 accumulate
 __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
                  "{%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// C fragments c[nt] of a 16 x 16 tile (rows g, g+8; columns 8nt + 2tg, +1) ->
+// tf32 B fragments b[kk][nt] (rows 8kk + tg, 8kk + tg + 4; column 8nt + g)
+__device__ __forceinline__ void c_to_b(const float (&c)[2][4], uint32_t (&b)[2][2][2], int lane) {
+    const int g = lane >> 2, tg = lane & 3;
+    const int src0 = 4 * tg + (g >> 1), src1 = src0 + 16;
+    const bool odd = g & 1;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float e0 = __shfl_sync(0xffffffffu, c[nt][2 * kk], src0);
+            const float o0 = __shfl_sync(0xffffffffu, c[nt][2 * kk + 1], src0);
+            const float e1 = __shfl_sync(0xffffffffu, c[nt][2 * kk], src1);
+            const float o1 = __shfl_sync(0xffffffffu, c[nt][2 * kk + 1], src1);
+            b[kk][nt][0] = to_tf32(odd ? o0 : e0);
+            b[kk][nt][1] = to_tf32(odd ? o1 : e1);
+        }
 }
 
 __device__ __forceinline__ uint4 pack8(const float *f) {
@@ -168,9 +185,10 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bar_qk + 4);
     float *gt = reinterpret_cast<float *>(sm + OFF_G);
     float *Am = reinterpret_cast<float *>(sm + OFF_A);   // A[r][s] at fsw(r, s/4) + s%4
-    float *MT = reinterpret_cast<float *>(sm + OFF_MT);  // M^-1[k][s] at fsw(s, k/4) + k%4
-    float *Yb = reinterpret_cast<float *>(sm + OFF_Y);   // [block][s_local][k_local]
-    float *Dv = Yb + 768;                                // diagonal inverses [block][row][col]
+    // solve scratch: 16 x 16 fp32 blocks, row stride LDB: D_0..D_3, M_10, M_32 in
+    // Dv; Y_20, Y_21, Y_30, Y_31 in Yv (over the U tile, which is dead then)
+    float *Dv = reinterpret_cast<float *>(sm + OFF_Y);
+    float *Yv = reinterpret_cast<float *>(sm + OFF_U);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q4 = warp & 3, hh = warp >> 2;
@@ -427,98 +445,173 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             named_bar_sync(1, 128);
-            // M^-1 = (I + A)^-1, A strictly lower. Diagonal 16 x 16 blocks by
-            // forward substitution (one thread per column) ...
-            if (tid < 64) {
-                const int b = tid >> 4, cl = tid & 15, s0 = tid, b0 = 16 * b;
-                // column cl of the block inverse; once x[kl] is final, remove
-                // its contribution from every later row (independent FMAs)
+            // M^-1 = (I + A)^-1 with A strictly lower, by 16 x 16 blocks.
+            // Step 1: warp S inverts the diagonal block, D_S = (I + A_SS)^-1, by
+            // forward substitution (lane = column; lanes 16-31 repeat 0-15).
+            {
+                const int S = warp, b0 = 16 * S, cl = lane & 15;
                 float x[16];
 #pragma unroll
                 for (int rl = 0; rl < 16; ++rl) x[rl] = (rl == cl) ? 1.f : 0.f;
 #pragma unroll
-                for (int kl = 0; kl < 15; ++kl) {
+                for (int j = 0; j < 4; ++j) {
+                    float4 a4[16];
 #pragma unroll
-                    for (int rl = kl + 1; rl < 16; ++rl)
-                        x[rl] -= Am[fsw(b0 + rl, (b0 + kl) >> 2) + (kl & 3)] * x[kl];
-                }
+                    for (int rl = 4 * j + 1; rl < 16; ++rl)
+                        a4[rl] = *reinterpret_cast<const float4 *>(Am + fsw(b0 + rl, 4 * S + j));
 #pragma unroll
-                for (int g4 = 0; g4 < 16; ++g4) {
-                    const int gb = g4 >> 2, l = 4 * (g4 & 3);
-                    if (gb > b) continue;  // rows below this block are written later
-                    const float4 m4 = (gb == b) ? make_float4(x[l], x[l + 1], x[l + 2], x[l + 3])
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                    *reinterpret_cast<float4 *>(MT + fsw(s0, g4)) = m4;
-                }
+                    for (int e = 0; e < 4; ++e) {
+                        const int kl = 4 * j + e;
 #pragma unroll
-                for (int rl = 0; rl < 16; ++rl) Dv[b * 256 + rl * 16 + cl] = x[rl];
-            }
-            named_bar_sync(1, 128);
-            // ... then the blocks below the diagonal, one block-diagonal at a time,
-            // one warp per 16 x 16 block on warp-level tf32 MMA tiles:
-            // M^-1_RS = -M^-1_RR sum_{K=S}^{R-1} A_RK M^-1_KS
-#pragma unroll
-            for (int dl = 1; dl < 4; ++dl) {
-                if (warp < 4 - dl) {
-                    const int b = warp, R = b + dl, g = lane >> 2, tg = lane & 3;
-                    float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int kk = 0; kk < 2 * dl; ++kk) {
-                        const int k0 = 16 * b + 8 * kk, r0 = 16 * R + g;
-                        const uint32_t af[4] = {to_tf32(Am[fsw(r0, k0 >> 2) + tg]), to_tf32(Am[fsw(r0 + 8, k0 >> 2) + tg]),
-                                                to_tf32(Am[fsw(r0, (k0 >> 2) + 1) + tg]),
-                                                to_tf32(Am[fsw(r0 + 8, (k0 >> 2) + 1) + tg])};
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            const int sc = 16 * b + 8 * nt + g;
-                            const uint32_t bf[2] = {to_tf32(MT[fsw(sc, k0 >> 2) + tg]), to_tf32(MT[fsw(sc, (k0 >> 2) + 1) + tg])};
-                            mma_tf32_16x8x8(y[nt], af, bf);
+                        for (int rl = kl + 1; rl < 16; ++rl) {
+                            const float a = e == 0 ? a4[rl].x : e == 1 ? a4[rl].y : e == 2 ? a4[rl].z : a4[rl].w;
+                            x[rl] = fmaf(-a, x[kl], x[rl]);
                         }
                     }
-                    float *yb = Yb + b * 256;  // Y block, row-major 16 x 16
+                }
+                if (lane < 16) {
+                    const int s = b0 + cl;
+                    const float bs = s_beta[s];
+                    __nv_bfloat16 *tcol = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_T) + (s & 7);
+#pragma unroll
+                    for (int rl = 0; rl < 16; ++rl) {
+                        const int r = b0 + rl;
+                        Dv[S * BLK + rl * LDB + cl] = x[rl];
+                        tcol[r * 64 + (((s >> 3) ^ (r & 7)) << 3)] = __float2bfloat16_rn(x[rl] * bs);
+                    }
+                }
+                const uint4 z4 = make_uint4(0, 0, 0, 0);
+                for (int R = 0; R < S; ++R) {  // T blocks above the diagonal are zero
+                    const int r = 16 * R + (lane >> 1), cc = 2 * S + (lane & 1);
+                    *reinterpret_cast<uint4 *>(sm + OFF_T + r * 128 + ((cc ^ (r & 7)) << 4)) = z4;
+                }
+            }
+            named_bar_sync(1, 128);
+            // Step 2, by doubling: M_10 = -D_1 A_10 D_0 and M_32 = -D_3 A_32 D_2
+            // (warps 0, 1) while warps 2, 3 start Y_RS = sum_K A_RK M_KS for the
+            // lower-left 32 x 32 block (R = 2, 3) with the parts that need no M_10.
+            // Step 3 adds A_R1 M_10; step 4: M_2S = -D_2 Y_2S, M_3S = -(M_32 Y_2S + D_3 Y_3S).
+            {
+                const int g = lane >> 2, tg = lane & 3;
+                // 16 x 16 block products on m16n8k8 tf32 tiles; X row-major with row stride LDB
+                auto a_blk = [&](const float *X, int kk, uint32_t (&a)[4]) {
+                    a[0] = to_tf32(X[g * LDB + 8 * kk + tg]);
+                    a[1] = to_tf32(X[(g + 8) * LDB + 8 * kk + tg]);
+                    a[2] = to_tf32(X[g * LDB + 8 * kk + tg + 4]);
+                    a[3] = to_tf32(X[(g + 8) * LDB + 8 * kk + tg + 4]);
+                };
+                auto a_am = [&](int R, int K, int kk, uint32_t (&a)[4]) {
+                    const int k4 = 4 * K + 2 * kk, r0 = 16 * R + g;
+                    a[0] = to_tf32(Am[fsw(r0, k4) + tg]);
+                    a[1] = to_tf32(Am[fsw(r0 + 8, k4) + tg]);
+                    a[2] = to_tf32(Am[fsw(r0, k4 + 1) + tg]);
+                    a[3] = to_tf32(Am[fsw(r0 + 8, k4 + 1) + tg]);
+                };
+                auto b_blk = [&](const float *X, int kk, int nt, uint32_t (&b)[2]) {
+                    b[0] = to_tf32(X[(8 * kk + tg) * LDB + 8 * nt + g]);
+                    b[1] = to_tf32(X[(8 * kk + tg + 4) * LDB + 8 * nt + g]);
+                };
+                // acc += A_RK (from Am) * X
+                auto mm_am = [&](float (&acc)[2][4], int R, int K, const float *X) {
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        uint32_t a[4];
+                        a_am(R, K, kk, a);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            uint32_t b[2];
+                            b_blk(X, kk, nt, b);
+                            mma_tf32_16x8x8(acc[nt], a, b);
+                        }
+                    }
+                };
+                // acc += Xa * Xb (both row-major blocks)
+                auto mm_blk = [&](float (&acc)[2][4], const float *Xa, const float *Xb) {
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        uint32_t a[4];
+                        a_blk(Xa, kk, a);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            uint32_t b[2];
+                            b_blk(Xb, kk, nt, b);
+                            mma_tf32_16x8x8(acc[nt], a, b);
+                        }
+                    }
+                };
+                auto st_blk = [&](float *X, const float (&c)[2][4]) {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        yb[g * 16 + 8 * nt + 2 * tg] = y[nt][0];
-                        yb[g * 16 + 8 * nt + 2 * tg + 1] = y[nt][1];
-                        yb[(g + 8) * 16 + 8 * nt + 2 * tg] = y[nt][2];
-                        yb[(g + 8) * 16 + 8 * nt + 2 * tg + 1] = y[nt][3];
+                        *reinterpret_cast<float2 *>(X + g * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][0], c[nt][1]);
+                        *reinterpret_cast<float2 *>(X + (g + 8) * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][2], c[nt][3]);
                     }
-                    __syncwarp();
-                    const float *dr = Dv + R * 256;  // M^-1_RR, row-major 16 x 16
+                };
+                // T_RS = -c Diag(beta_S) as bf16 pairs
+                auto st_t = [&](int R, int S, const float (&c)[2][4]) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int s = 16 * S + 8 * nt + 2 * tg;
+                        const float b0s = -s_beta[s], b1s = -s_beta[s + 1];
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const int r = 16 * R + g + 8 * hf;
+                            *reinterpret_cast<__nv_bfloat162 *>(sm + OFF_T + r * 128 + (((s >> 3) ^ (r & 7)) << 4) +
+                                                                (s & 7) * 2) =
+                                __floats2bfloat162_rn(c[nt][2 * hf] * b0s, c[nt][2 * hf + 1] * b1s);
+                        }
+                    }
+                };
+                const float *D0 = Dv, *D1 = Dv + BLK, *D2 = Dv + 2 * BLK, *D3 = Dv + 3 * BLK;
+                float *M10 = Dv + 4 * BLK, *M32 = Dv + 5 * BLK;
+                float *Y20 = Yv, *Y21 = Yv + BLK, *Y30 = Yv + 2 * BLK, *Y31 = Yv + 3 * BLK;
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float y1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (warp < 2) {
+                    const int R = warp == 0 ? 1 : 3;  // block (R, R-1)
+                    mm_am(acc, R, R - 1, warp == 0 ? D0 : D2);
+                    uint32_t yb[2][2][2];
+                    c_to_b(acc, yb, lane);
+                    const float *dr = warp == 0 ? D1 : D3;
                     float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const int k0 = 8 * kk;
-                        const uint32_t af[4] = {to_tf32(dr[g * 16 + k0 + tg]), to_tf32(dr[(g + 8) * 16 + k0 + tg]),
-                                                to_tf32(dr[g * 16 + k0 + tg + 4]), to_tf32(dr[(g + 8) * 16 + k0 + tg + 4])};
+                        uint32_t a[4];
+                        a_blk(dr, kk, a);
 #pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            const uint32_t bf[2] = {to_tf32(yb[(k0 + tg) * 16 + 8 * nt + g]),
-                                                    to_tf32(yb[(k0 + tg + 4) * 16 + 8 * nt + g])};
-                            mma_tf32_16x8x8(z[nt], af, bf);
-                        }
+                        for (int nt = 0; nt < 2; ++nt) mma_tf32_16x8x8(z[nt], a, yb[kk][nt]);
                     }
+                    st_t(R, R - 1, z);  // T = -z Diag(beta)
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int sc = 16 * b + 8 * nt + 2 * tg, r0 = 16 * R + g;
-                        MT[fsw(sc, r0 >> 2) + (r0 & 3)] = -z[nt][0];
-                        MT[fsw(sc + 1, r0 >> 2) + (r0 & 3)] = -z[nt][1];
-                        MT[fsw(sc, (r0 + 8) >> 2) + (r0 & 3)] = -z[nt][2];
-                        MT[fsw(sc + 1, (r0 + 8) >> 2) + (r0 & 3)] = -z[nt][3];
-                    }
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) z[nt][e] = -z[nt][e];
+                    st_blk(warp == 0 ? M10 : M32, z);
+                } else {
+                    const int R = warp;  // 2 or 3
+                    mm_am(acc, R, 1, D1);              // Y_R1 = A_R1 D_1 (final)
+                    st_blk(R == 2 ? Y21 : Y31, acc);
+                    mm_am(y1, R, 0, D0);               // Y_R0 partial: A_R0 D_0
                 }
                 named_bar_sync(1, 128);
-            }
-            // T = M^-1 Diag(beta) as bf16 rows r
-            for (int p = tid; p < C * 8; p += 128) {
-                const int r = p & 63, cc = p >> 6;
-                float tv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int s = cc * 8 + e;
-                    tv[e] = MT[fsw(s, r >> 2) + (r & 3)] * s_beta[s];
+                if (warp >= 2) {
+                    const int R = warp;
+                    mm_am(y1, R, 1, M10);              // Y_R0 += A_R1 M_10
+                    st_blk(R == 2 ? Y20 : Y30, y1);
                 }
-                *reinterpret_cast<uint4 *>(sm + OFF_T + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(tv);
+                named_bar_sync(1, 128);
+                {
+                    // warp 0: (2,0), 1: (2,1), 2: (3,0), 3: (3,1)
+                    const int R = 2 + (warp >> 1), S = warp & 1;
+                    const float *y2 = S == 0 ? Y20 : Y21;
+                    float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    if (R == 2) {
+                        mm_blk(z, D2, y2);
+                    } else {
+                        mm_blk(z, M32, y2);
+                        mm_blk(z, D3, S == 0 ? Y30 : Y31);
+                    }
+                    st_t(R, S, z);
+                }
             }
         } else {
             // The state is kept as S = Diag(sigma) S_stored. S~^T = S_stored^T Diag(sf)
