@@ -51,20 +51,21 @@ constexpr uint32_t OFF_X = 0;           // k rows 0-63 + q rows 64-127 (TMA) -> 
 constexpr uint32_t OFF_V = 32768;       // v tile (TMA, prefetched after G3)
 constexpr uint32_t OFF_G = 49152;       // g fp32 [64][128] (TMA, prefetched) -> cumulative G (log2 units)
 constexpr uint32_t OFF_RK = 81920;      // Rk (Kb on the exact path), 64 rows; kept until G7
-constexpr uint32_t OFF_SOP = 98304;     // S~^T 128 rows (j) x 128 (i) -> O staging
-constexpr uint32_t OFF_OST = OFF_SOP;
+constexpr uint32_t OFF_OST = OFF_RK;    // O staging [64][128] bf16 once G7 has read Rk
 constexpr uint32_t OFF_T = 131072;      // T 64 rows (r) x 64 (s)
 constexpr uint32_t OFF_P = 139264;      // P 64 rows (r) x 64 (s)
 constexpr uint32_t OFF_A = 147456;      // A fp32 [64][64] row-major swizzled -> W' (rows i)
 constexpr uint32_t OFF_W = OFF_A;
-constexpr uint32_t OFF_U = 163840;      // U^T 128 rows (j) x 64 (r)
+constexpr uint32_t OFF_U = 163840;      // solve scratch: Y blocks (5 KiB); bytes 98304-131071 are unused
 constexpr uint32_t OFF_Y = 180224;      // solve scratch: six 16 x 16 fp32 blocks (7.5 KiB)
 constexpr int LDB = 20, BLK = 16 * LDB;  // block row stride (bank-conflict free A fragments), block size
 constexpr uint32_t OFF_SMALL = 188416;  // per-row / per-channel vectors, barriers
 constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;
 constexpr uint32_t QK_BYTES = 2 * 16384, G_BYTES = 32768, V_BYTES = 16384;
 // TMEM columns (512 allocated)
-constexpr uint32_t TM_S = 0, TM_AP = 128, TM_W = 192, TM_U0 = 256, TM_X = 320, TM_O = 384;
+constexpr uint32_t TM_S = 0, TM_AP = 128, TM_W = 192, TM_U0 = 256, TM_X = 320, TM_O = 384, TM_SB = 448;
+// TM_SB: S~^T as bf16 pairs (A operand of G4, G5); U^T as bf16 pairs goes to
+// TM_W once W' has been read back (A operand of G6, G7)
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 // Anchored factors stay within e^[-ANCHOR, ANCHOR] when the chunk's decay
 // span is at most SPAN_MAX; the fp32 state kept as S / sigma then stays
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(NT, 1)
     float *gt = reinterpret_cast<float *>(sm + OFF_G);
     float *Am = reinterpret_cast<float *>(sm + OFF_A);   // A[r][s] at fsw(r, s/4) + s%4
     // solve scratch: 16 x 16 fp32 blocks, row stride LDB: D_0..D_3, M_10, M_32 in
-    // Dv; Y_20, Y_21, Y_30, Y_31 in Yv (over the U tile, which is dead then)
+    // Dv; Y_20, Y_21, Y_30, Y_31 in Yv
     float *Dv = reinterpret_cast<float *>(sm + OFF_Y);
     float *Yv = reinterpret_cast<float *>(sm + OFF_U);
 
@@ -614,39 +615,37 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         } else {
-            // The state is kept as S = Diag(sigma) S_stored. S~^T = S_stored^T Diag(sf)
-            // becomes the bf16 operand; S_stored^T <- S_stored^T Diag(pf) in TMEM.
-            // Two 32-column TMEM loads per wait; per-channel factors as float4.
+            // The state is kept as S = Diag(sigma) S_st. S~^T = S_st^T Diag(sf) goes to
+            // TMEM as bf16 pairs (i, i+1); S_st^T <- S_st^T Diag(pf) in place.
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-                uint32_t r[2][32];
+                uint32_t r[2][32], pk[32];
                 tmem_ld32(tbase + lrow + TM_S + 64 * kb, r[0]);
                 tmem_ld32(tbase + lrow + TM_S + 64 * kb + 32, r[1]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
                     const int i0 = 64 * kb + 32 * part;
-                    float so[32];
 #pragma unroll
                     for (int g4 = 0; g4 < 8; ++g4) {
                         const float4 fc = *reinterpret_cast<const float4 *>(s_sf + i0 + 4 * g4);
                         const float4 fl = *reinterpret_cast<const float4 *>(s_pf + i0 + 4 * g4);
                         const float fcv[4] = {fc.x, fc.y, fc.z, fc.w}, flv[4] = {fl.x, fl.y, fl.z, fl.w};
+                        float so[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float sv = __uint_as_float(r[part][4 * g4 + e]);
-                            so[4 * g4 + e] = sv * fcv[e];
+                            so[e] = sv * fcv[e];
                             r[part][4 * g4 + e] = __float_as_uint(sv * flv[e]);
                         }
+                        __nv_bfloat162 t0 = __floats2bfloat162_rn(so[0], so[1]);
+                        __nv_bfloat162 t1 = __floats2bfloat162_rn(so[2], so[3]);
+                        pk[16 * part + 2 * g4] = *reinterpret_cast<uint32_t *>(&t0);
+                        pk[16 * part + 2 * g4 + 1] = *reinterpret_cast<uint32_t *>(&t1);
                     }
                     tmem_st32(tbase + lrow + TM_S + i0, r[part]);
-#pragma unroll
-                    for (int qd = 0; qd < 4; ++qd) {
-                        const int cc = part * 4 + qd;
-                        *reinterpret_cast<uint4 *>(sm + OFF_SOP + kb * 16384 + jl * 128 + ((cc ^ (jl & 7)) << 4)) =
-                            pack8(so + 8 * qd);
-                    }
                 }
+                tmem_st32(tbase + lrow + TM_SB + 32 * kb, pk);
             }
             tmem_st_wait();
             if (!exact) {
@@ -693,8 +692,8 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_SOP + kb * 16384 + ko, 16, 1024),
-                         sdesc_sw128(sbase + OFF_X + 8192 + kb * 16384 + ko, 16, 1024), ID_KK64, ks > 0);
+                mma_bf16_ts(tbase + TM_O, tbase + TM_SB + 8 * ks,
+                            sdesc_sw128(sbase + OFF_X + 8192 + kb * 16384 + ko, 16, 1024), ID_KK64, ks > 0);
             }
             mma_commit(bar_mma);
         }
@@ -731,11 +730,9 @@ __global__ void __launch_bounds__(NT, 1)
         // G4: X^T = S~^T W'^T
         if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                mma_bf16(tbase + TM_X, sdesc_sw128(sbase + OFF_SOP + kb * 16384 + ko, 16, 1024),
-                         sdesc_sw128(sbase + OFF_W + ks * 2048, 8192, 1024), ID_KM64, ks > 0);
-            }
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ts(tbase + TM_X, tbase + TM_SB + 8 * ks, sdesc_sw128(sbase + OFF_W + ks * 2048, 8192, 1024),
+                            ID_KM64, ks > 0);
             mma_commit(bar_mma);
         }
         got = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
@@ -747,30 +744,30 @@ __global__ void __launch_bounds__(NT, 1)
         ph_mma ^= 1;
         tc_fence_after();
 
-        // U^T = U0^T - X^T -> bf16 tile rows j (K-major operand), over M^-1
+        // U^T = U0^T - X^T -> bf16 pairs (r, r+1) in TMEM over W'
         {
-            uint32_t u0[32], x[32];
+            uint32_t u0[32], x[32], pk[16];
             tmem_ld32(tbase + lrow + TM_U0 + 32 * hh, u0);
             tmem_ld32(tbase + lrow + TM_X + 32 * hh, x);
             tmem_ld_wait();
-            float uv[32];
 #pragma unroll
-            for (int m = 0; m < 32; ++m) uv[m] = __uint_as_float(u0[m]) - __uint_as_float(x[m]);
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                const int cc = 4 * hh + qd;
-                *reinterpret_cast<uint4 *>(sm + OFF_U + jl * 128 + ((cc ^ (jl & 7)) << 4)) = pack8(uv + 8 * qd);
+            for (int m = 0; m < 16; ++m) {
+                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(u0[2 * m]) - __uint_as_float(x[2 * m]),
+                                                         __uint_as_float(u0[2 * m + 1]) - __uint_as_float(x[2 * m + 1]));
+                pk[m] = *reinterpret_cast<uint32_t *>(&t);
             }
+            tmem_st16(tbase + lrow + TM_W + 16 * hh, pk);
+            tmem_st_wait();
         }
-        sync_for_mma();
+        sync_tc();
 
         // G6: O^T += U^T P^T   and   G7: S_stored^T += U^T Rk (Kb on the exact path)
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = sdesc_sw128(sbase + OFF_U + ks * 32, 16, 1024);
-                mma_bf16(tbase + TM_O, a, sdesc_sw128(sbase + OFF_P + ks * 32, 16, 1024), ID_KK64, 1);
-                mma_bf16(tbase + TM_S, a, sdesc_sw128(sbase + OFF_RK + ks * 2048, 8192, 1024), ID_KM128, 1);
+                const uint32_t a = tbase + TM_W + 8 * ks;
+                mma_bf16_ts(tbase + TM_O, a, sdesc_sw128(sbase + OFF_P + ks * 32, 16, 1024), ID_KK64, 1);
+                mma_bf16_ts(tbase + TM_S, a, sdesc_sw128(sbase + OFF_RK + ks * 2048, 8192, 1024), ID_KM128, 1);
             }
             mma_commit(bar_mma);
         }
