@@ -51,6 +51,8 @@ def _load():
             i64p = ctypes.POINTER(ctypes.c_int64)
             ci, cd = ctypes.c_int, ctypes.c_double
             lib.oracle_shortconv_step.argtypes = [dp, dp, dp, dp, ci, ci, ci]
+            lib.oracle_shortconv_seq.argtypes = [dp, dp, dp, dp, dp, ctypes.c_void_p, ci,
+                                                 ctypes.c_int64, ci, ci]
             lib.oracle_shortconv_step.restype = None
             lib.oracle_recurrence.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
                                               i64p, ci, ci, ci, cd, ci]
@@ -92,6 +94,29 @@ def shortconv_step(x, ring, w):
     y = np.empty_like(x)
     _load().oracle_shortconv_step(_ptr(x), _ptr(ring), _ptr(w), _ptr(y), B, H, D)
     return y, ring
+
+
+def shortconv_seq(x, w, ring_in=None, cu_seqlens=None):
+    """Short conv over packed sequences. Returns (y [3,T,H,D], ring_out [N,3,H,3,D]).
+
+    x [T,3,H,D]; w [3,H,D,4]; ring_in [N,3,H,3,D] or None (zero history);
+    cu_seqlens [N+1] or None (one sequence of T tokens).
+    """
+    x = _f64(x)
+    w = _f64(w)
+    T, P, H, D = x.shape
+    assert P == 3 and w.shape == (3, H, D, 4)
+    cu = _seqlens(cu_seqlens, T)
+    N = len(cu) - 1
+    rin = None
+    if ring_in is not None:
+        rin = _f64(ring_in)
+        assert rin.shape == (N, 3, H, 3, D)
+    y = np.empty((3, T, H, D))
+    rout = np.empty((N, 3, H, 3, D))
+    _load().oracle_shortconv_seq(_ptr(x), _ptr(rin) if rin is not None else None, _ptr(w), _ptr(y),
+                                 _ptr(rout), cu.ctypes.data_as(ctypes.c_void_p), N, T, H, D)
+    return y, rout
 
 
 def _seqlens(cu_seqlens, T):

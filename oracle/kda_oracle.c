@@ -100,6 +100,48 @@ void oracle_shortconv_step(const double *x, double *ring, const double *w,
 }
 
 /*
+ * The same short convolution over a packed batch of sequences, as a prefill
+ * would run it ([W] "KDA 递推公式先衰减再差分": conv + SiLU in front of q/k/v,
+ * with the 3-token ring that decode carries on). Sequence n covers tokens
+ * [cu_seqlens[n], cu_seqlens[n+1]); its history before the first token is
+ * ring_in[n] (zeros if ring_in is NULL). Each token is one application of
+ * the step above to a batch of one; ring_out[n] (if not NULL) receives the
+ * ring after the sequence's last token, so an empty sequence passes ring_in
+ * through unchanged.
+ *   x        [T,3,H,D]     pre-conv projections
+ *   ring_in  [N,3,H,3,D]   or NULL
+ *   y        [3,T,H,D]     post-conv q, k, v (projection-major)
+ *   ring_out [N,3,H,3,D]   or NULL
+ */
+void oracle_shortconv_seq(const double *x, const double *ring_in, const double *w, double *y,
+                          double *ring_out, const int64_t *cu_seqlens, int N, int64_t T, int H, int D)
+{
+    const size_t row = (size_t)3 * H * D;       /* one token of x */
+    const size_t rsz = (size_t)3 * H * 3 * D;   /* one sequence's ring */
+    double *ring = malloc(rsz * sizeof(double));
+    double *yt = malloc(row * sizeof(double));
+    if (!ring || !yt) {
+        free(ring);
+        free(yt);
+        return;
+    }
+    for (int n = 0; n < N; ++n) {
+        for (size_t e = 0; e < rsz; ++e) ring[e] = ring_in ? ring_in[(size_t)n * rsz + e] : 0.0;
+        for (int64_t t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
+            oracle_shortconv_step(x + (size_t)t * row, ring, w, yt, 1, H, D);
+            for (int p = 0; p < 3; ++p)
+                for (int h = 0; h < H; ++h)
+                    for (int c = 0; c < D; ++c)
+                        y[(((size_t)p * T + t) * H + h) * D + c] = yt[((size_t)p * H + h) * D + c];
+        }
+        if (ring_out)
+            for (size_t e = 0; e < rsz; ++e) ring_out[(size_t)n * rsz + e] = ring[e];
+    }
+    free(ring);
+    free(yt);
+}
+
+/*
  * The KDA recurrence, token by token ([W] "KDA 递推公式先衰减再差分").
  *
  * Packed variable-length layout: tokens of all sequences are concatenated;

@@ -369,3 +369,81 @@ def test_shortconv_silu_special_values():
     y, _ = oracle.shortconv_step(x, np.zeros((1, 3, 1, 3, 2)), w)
     assert np.all(y[..., 1] == 0.0)           # SiLU(0) = 0
     np.testing.assert_allclose(y[..., 0], 40.0, rtol=1e-15)  # SiLU(z) -> z for large z
+
+
+# ------------------------------------------------ short conv over sequences
+def _conv_ref(hist, w):
+    """SiLU of the causal width-4 convolution of one channel whose first
+    three entries are the history: out[t] = silu(sum_m w[m] hist[t + m])."""
+    T = len(hist) - 3
+    return _silu(np.array([np.dot(w, hist[t:t + 4]) for t in range(T)]))
+
+
+def test_shortconv_seq_matches_library_convolution():
+    """One sequence from zero history equals numpy.convolve per channel,
+    with y written projection-major."""
+    rng = np.random.default_rng(21)
+    T, H, D = 23, 2, 3
+    x = rng.standard_normal((T, 3, H, D))
+    w = rng.standard_normal((3, H, D, 4))
+    y, ring = oracle.shortconv_seq(x, w)
+    assert y.shape == (3, T, H, D) and ring.shape == (1, 3, H, 3, D)
+    for p in range(3):
+        for h in range(H):
+            for c in range(D):
+                ref = _silu(np.convolve(x[:, p, h, c], w[p, h, c, ::-1])[:T])
+                np.testing.assert_allclose(y[p, :, h, c], ref, atol=1e-13, rtol=0)
+    np.testing.assert_array_equal(ring[0], np.moveaxis(x[T - 3:], 0, 2))
+
+
+def test_shortconv_seq_varlen_history_and_ring_out():
+    """Sequences of 0, 1, 2, 3 and 9 tokens with a given history: each output
+    is the convolution of [history, tokens]; the ring after the sequence is
+    its last three entries, so an empty sequence passes its ring through."""
+    rng = np.random.default_rng(22)
+    lens = [2, 0, 9, 1, 3]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, H, D, N = int(cu[-1]), 2, 3, len(lens)
+    x = rng.standard_normal((T, 3, H, D))
+    w = rng.standard_normal((3, H, D, 4))
+    rin = rng.standard_normal((N, 3, H, 3, D))
+    y, rout = oracle.shortconv_seq(x, w, ring_in=rin, cu_seqlens=cu)
+    for n in range(N):
+        a, b = cu[n], cu[n + 1]
+        for p in range(3):
+            for h in range(H):
+                for c in range(D):
+                    hist = np.concatenate([rin[n, p, h, :, c], x[a:b, p, h, c]])
+                    if b > a:
+                        np.testing.assert_allclose(y[p, a:b, h, c], _conv_ref(hist, w[p, h, c]),
+                                                   atol=1e-13, rtol=0)
+                    np.testing.assert_array_equal(rout[n, p, h, :, c], hist[-3:])
+
+
+def test_shortconv_seq_split_hand_off():
+    """Two calls with the ring handed on equal one call over the whole
+    sequence, outputs and final ring."""
+    rng = np.random.default_rng(23)
+    T1, T2, H, D = 7, 2, 1, 4
+    x = rng.standard_normal((T1 + T2, 3, H, D))
+    w = rng.standard_normal((3, H, D, 4))
+    rin = rng.standard_normal((1, 3, H, 3, D))
+    y, r = oracle.shortconv_seq(x, w, ring_in=rin)
+    y1, r1 = oracle.shortconv_seq(x[:T1], w, ring_in=rin)
+    y2, r2 = oracle.shortconv_seq(x[T1:], w, ring_in=r1)
+    np.testing.assert_array_equal(np.concatenate([y1, y2], axis=1), y)
+    np.testing.assert_array_equal(r2, r)
+
+
+def test_shortconv_seq_then_decode_step():
+    """A prefill conv over T tokens followed by one decode step on its ring
+    equals a prefill conv over T + 1 tokens."""
+    rng = np.random.default_rng(24)
+    T, H, D = 6, 2, 2
+    x = rng.standard_normal((T + 1, 3, H, D))
+    w = rng.standard_normal((3, H, D, 4))
+    y_all, r_all = oracle.shortconv_seq(x, w)
+    _, r = oracle.shortconv_seq(x[:T], w)
+    y_step, r_step = oracle.shortconv_step(x[T][None], r, w)
+    np.testing.assert_array_equal(y_step[0], y_all[:, T])
+    np.testing.assert_array_equal(r_step, r_all)
