@@ -97,6 +97,35 @@ kda_status kda_shortconv_step(const void *x, void *ring, const float *w, void *y
                               int B, int H, int D, kda_dtype dtype, kda_stream_t stream);
 
 /*
+ * The same short convolution over a packed batch of prompts, as prefill runs
+ * it ([W] "KDA 递推公式先衰减再差分": conv + SiLU in front of q/k/v, with the
+ * 3-token ring that decode carries on). For each sequence n, tokens
+ * [cu_seqlens[n], cu_seqlens[n+1]) are convolved as if kda_shortconv_step
+ * had been called once per token, starting from ring_in[n]; ring_out[n]
+ * receives the ring after the last token, ready for kda_shortconv_step or
+ * kda_shortconv_decode_step on the same sequences.
+ *
+ *   x        [T,3,H,D] dtype    pre-conv projections, p = 0,1,2 = q,k,v
+ *   ring_in  [N,3,H,3,D] dtype  history before each sequence (slot 0
+ *                               oldest), or NULL for zeros
+ *   w        [3,H,D,4] fp32     taps, as in kda_shortconv_step
+ *   y        [3,T,H,D] dtype    out: post-conv, projection-major, so y[0],
+ *                               y[1], y[2] are the [T,H,D] q, k, v of
+ *                               kda_chunk_prefill
+ *   ring_out [N,3,H,3,D] dtype  out, or NULL; a sequence with no tokens
+ *                               gets ring_in[n] (or zeros)
+ *   cu_seqlens device int64 [N+1], or NULL for one sequence of T tokens
+ * SiLU is evaluated with the fast exponential and division intrinsics.
+ * Requires N >= 1, T >= 0, H >= 1, D in {16,32,64,128}; y may not alias x
+ * or a ring, and ring_out may not alias ring_in or x. Invalid cu_seqlens
+ * (not 0 .. T, or decreasing) set the device error word reported by
+ * kda_sync_status; the affected tiles write nothing.
+ */
+kda_status kda_shortconv_prefill(const void *x, const void *ring_in, const float *w, void *y,
+                                 void *ring_out, const int64_t *cu_seqlens, int N, int64_t T,
+                                 int H, int D, kda_dtype dtype, kda_stream_t stream);
+
+/*
  * One KDA decode step for B independent sequences ([W] "KDA 递推公式先衰减再差分";
  * per-channel gate as in [G] section 7). For each (b, h):
  *   q^ = L2(q), k^ = L2(k), a = exp(g)

@@ -8,6 +8,13 @@
 // loads, the 4 taps per channel as float4, writes y and the shifted ring.
 // y is written projection-major, [3,B,H,D], so that y[0], y[1], y[2] are the
 // contiguous q, k, v operands of the decode step.
+//
+// The prefill form runs the same convolution over packed sequences: each
+// thread owns one 16-byte channel vector of one (projection, head) and walks
+// a tile of 64 tokens with the 3-token window in registers. A tile's history
+// comes from the tokens before it, or from the sequence's ring where the
+// sequence starts, so tiles are independent; the thread that processes a
+// sequence's last token writes its ring for the decode hand-off.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -69,6 +76,129 @@ __global__ void __launch_bounds__(256) shortconv_step_kernel(const T *__restrict
     store16(ring + roff + 2 * (size_t)D, xv);
 }
 
+constexpr int CONV_TILE = 64;  // tokens per prefill tile
+
+template <typename T>
+__device__ __forceinline__ void zero16(float (&out)[Vec16<T>::N]) {
+#pragma unroll
+    for (int i = 0; i < Vec16<T>::N; ++i) out[i] = 0.f;
+}
+
+// grid: x = token tiles, y = groups of 256 channel vectors of one token row
+template <typename T>
+__global__ void __launch_bounds__(256, 2) shortconv_prefill_kernel(
+    const T *__restrict__ x, const T *__restrict__ ring_in, const float *__restrict__ w, T *__restrict__ y,
+    T *__restrict__ ring_out, const int64_t *__restrict__ cu, int N, int64_t Ttot, int H, int D, unsigned *err) {
+    constexpr int V = Vec16<T>::N;
+    const int nvec = D / V;
+    const int vi = blockIdx.y * blockDim.x + threadIdx.x;
+    if (vi >= 3 * H * nvec) return;
+    const int cv = vi % nvec, ph = vi / nvec;  // ph = p * H + h
+    const int h = ph % H, p = ph / H;
+    const size_t row = (size_t)3 * H * D;      // x elements per token
+    const size_t rsz = (size_t)9 * H * D;      // ring elements per sequence
+    const size_t xo = (size_t)ph * D + (size_t)cv * V;
+    const size_t ro = (size_t)ph * 3 * D + (size_t)cv * V;
+    T *yb = y + (size_t)p * Ttot * H * D + (size_t)h * D + (size_t)cv * V;  // + t * H * D
+    const size_t ystride = (size_t)H * D;
+
+    // Sequences with no tokens pass their ring through (first tile only).
+    if (blockIdx.x == 0 && ring_out) {
+        for (int n = 0; n < N; ++n) {
+            if ((cu ? cu[n + 1] - cu[n] : Ttot) != 0) continue;
+            float r[V];
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                if (ring_in) load16(ring_in + n * rsz + ro + (size_t)m * D, r);
+                else zero16<T>(r);
+                store16(ring_out + n * rsz + ro + (size_t)m * D, r);
+            }
+        }
+    }
+    const int64_t t0 = (int64_t)blockIdx.x * CONV_TILE;
+    const int64_t t1 = t0 + CONV_TILE < Ttot ? t0 + CONV_TILE : Ttot;
+    if (t0 >= t1) return;
+
+    // the sequence holding t0: the last n with cu[n] <= t0
+    int n = 0;
+    int64_t sn = 0, en = Ttot;
+    if (cu) {
+        if (cu[0] != 0 || cu[N] != Ttot) {
+            if (err) atomicOr(err, DEVERR_SEQLENS);
+            return;
+        }
+        int lo = 0, hi = N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cu[mid] <= t0) lo = mid;
+            else hi = mid - 1;
+        }
+        n = lo;
+        sn = cu[n];
+        en = cu[n + 1];
+        if (!(0 <= sn && sn <= t0 && t0 < en && en <= Ttot)) {
+            if (err) atomicOr(err, DEVERR_SEQLENS);
+            return;
+        }
+    }
+    float4 tap[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) tap[i] = __ldg(reinterpret_cast<const float4 *>(w + ((size_t)ph * D + (size_t)cv * V) * 4) + i);
+
+    // window x_{t-3}, x_{t-2}, x_{t-1}: a token of this sequence, else a ring slot
+    float r0[V], r1[V], r2[V];
+    auto hist = [&](int64_t j, float (&out)[V]) {
+        if (j >= sn) load16(x + (size_t)j * row + xo, out);
+        else if (ring_in) load16(ring_in + (size_t)n * rsz + ro + (size_t)(j - sn + 3) * D, out);
+        else zero16<T>(out);
+    };
+    hist(t0 - 3, r0);
+    hist(t0 - 2, r1);
+    hist(t0 - 1, r2);
+    int64_t t = t0;
+    while (t < t1) {
+        const int64_t te = en < t1 ? en : t1;
+#pragma unroll 4
+        for (; t < te; ++t) {
+            float xv[V], yv[V];
+            load16(x + (size_t)t * row + xo, xv);
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const float z = tap[i].x * r0[i] + tap[i].y * r1[i] + tap[i].z * r2[i] + tap[i].w * xv[i];
+                yv[i] = __fdividef(z, 1.0f + __expf(-z));
+                r0[i] = r1[i];
+                r1[i] = r2[i];
+                r2[i] = xv[i];
+            }
+            store16(yb + (size_t)t * ystride, yv);
+        }
+        if (t < en) break;  // tile ends inside the sequence
+        if (ring_out) {
+            store16(ring_out + (size_t)n * rsz + ro, r0);
+            store16(ring_out + (size_t)n * rsz + ro + D, r1);
+            store16(ring_out + (size_t)n * rsz + ro + 2 * (size_t)D, r2);
+        }
+        if (t >= t1) break;
+        // next sequence with tokens; it must start here
+        do {
+            if (n + 1 >= N) {
+                if (err) atomicOr(err, DEVERR_SEQLENS);
+                return;
+            }
+            ++n;
+            sn = cu[n];
+            en = cu[n + 1];
+        } while (en == sn && sn == t);
+        if (sn != t || en < sn || en > Ttot) {
+            if (err) atomicOr(err, DEVERR_SEQLENS);
+            return;
+        }
+        hist(t - 3, r0);
+        hist(t - 2, r1);
+        hist(t - 1, r2);
+    }
+}
+
 }  // namespace kda
 
 using namespace kda;
@@ -100,4 +230,44 @@ extern "C" kda_status kda_shortconv_step(const void *x, void *ring, const float 
                                                             static_cast<float *>(ring), w,
                                                             static_cast<float *>(y), B, H, D);
     return check_launch("shortconv_step_kernel");
+}
+
+extern "C" kda_status kda_shortconv_prefill(const void *x, const void *ring_in, const float *w, void *y,
+                                            void *ring_out, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                                            int D, kda_dtype dtype, kda_stream_t stream) {
+    clear_detail();
+    if (N < 1) return invalid("N must be >= 1");
+    if (T < 0) return invalid("T must be >= 0");
+    if (H < 1) return invalid("H must be >= 1");
+    if (!valid_head_dim(D)) return invalid("D must be one of 16, 32, 64, 128");
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return invalid("dtype must be KDA_F32 or KDA_BF16");
+    if (!cu_seqlens && N != 1) return invalid("cu_seqlens may be NULL only for N = 1");
+    kda_status st;
+    if ((st = check_ptr(w, "w"))) return st;
+    if (T > 0 && ((st = check_ptr(x, "x")) || (st = check_ptr(y, "y")))) return st;
+    if (ring_in && (st = check_ptr(ring_in, "ring_in"))) return st;
+    if (ring_out && (st = check_ptr(ring_out, "ring_out"))) return st;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 7))
+        return invalid("cu_seqlens must be 8-byte aligned");
+    if (y && (y == x || y == ring_in || y == ring_out)) return invalid("y must not alias x or a ring");
+    if (ring_out && (ring_out == ring_in || ring_out == x)) return invalid("ring_out must not alias ring_in or x");
+    if (T == 0 && !ring_out) return KDA_OK;
+    if ((st = bind_stream_device(stream))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int V = dtype == KDA_BF16 ? 8 : 4;
+    const long long vecs = 3LL * H * (D / V);
+    const long long gy = (vecs + 255) / 256;
+    const long long gx = T > 0 ? (T + CONV_TILE - 1) / CONV_TILE : 1;
+    if (gy > 65535 || gx > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "shape too large for one launch");
+    const dim3 grid((unsigned)gx, (unsigned)gy);
+    unsigned *err = device_error_word();
+    if (dtype == KDA_BF16)
+        shortconv_prefill_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(ring_in), w,
+            static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(ring_out), cu_seqlens, N, T, H, D, err);
+    else
+        shortconv_prefill_kernel<float><<<grid, 256, 0, s>>>(
+            static_cast<const float *>(x), static_cast<const float *>(ring_in), w, static_cast<float *>(y),
+            static_cast<float *>(ring_out), cu_seqlens, N, T, H, D, err);
+    return check_launch("shortconv_prefill_kernel");
 }

@@ -33,6 +33,7 @@ _SIGNATURES = {
     "kda_state_bytes": ([_ci, _ci, _ci, _ci], _sz),
     "kda_shortconv_ring_bytes": ([_ci, _ci, _ci, _ci, _ci], _sz),
     "kda_shortconv_step": ([_vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _vp], _ci),
+    "kda_shortconv_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _vp], _ci),
     "kda_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_shortconv_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
@@ -130,6 +131,20 @@ def kda_shortconv_step(x, ring, w, y, stream=None):
         raise ValueError("shape mismatch")
     _check(lib().kda_shortconv_step(_ptr(x), _ptr(ring), _ptr(w), _ptr(y), B, H, D, _dtype_code(x),
                                     _stream(stream, x.device)))
+
+
+def kda_shortconv_prefill(x, w, y, ring_in=None, ring_out=None, cu_seqlens=None, stream=None):
+    """x [T,3,H,D]; w [3,H,D,4] fp32; y [3,T,H,D]; rings [N,3,H,3,D] or None;
+    cu_seqlens int64 [N+1] on the device (or None for one sequence)."""
+    T, P, H, D = x.shape
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    if P != 3 or tuple(w.shape) != (3, H, D, 4) or tuple(y.shape) != (3, T, H, D):
+        raise ValueError("shape mismatch")
+    for r in (ring_in, ring_out):
+        if r is not None and tuple(r.shape) != (N, 3, H, 3, D):
+            raise ValueError("ring shape mismatch")
+    _check(lib().kda_shortconv_prefill(_ptr(x), _ptr(ring_in), _ptr(w), _ptr(y), _ptr(ring_out),
+                                       _ptr(cu_seqlens), N, T, H, D, _dtype_code(x), _stream(stream, x.device)))
 
 
 def kda_decode_step(q, k, v, g, beta, state, out, l2_eps=1e-6, stream=None):

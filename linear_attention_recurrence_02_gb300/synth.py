@@ -135,6 +135,24 @@ def decode_inputs(seed: int, B: int, H: int, D: int, bf16: bool,
                 q=qkv[0], k=qkv[1], v=qkv[2])
 
 
+def conv_prefill_inputs(seed: int, T: int, H: int, D: int, N: int, bf16: bool, heads=None):
+    """Pre-conv projections of a packed prompt batch: x [T,3,H,D] ~ N(0,1),
+    ring_in [N,3,H,3,D] ~ N(0,1) (history before each sequence), w [3,H,D,4]
+    ~ N(0, 0.5^2). With `heads`, only those heads are drawn (each head from
+    its own stream, so a subset equals the same heads of the full draw)."""
+    heads = list(range(H)) if heads is None else list(heads)
+    x = np.empty((T, 3, len(heads), D), np.float32)
+    ring = np.empty((N, 3, len(heads), 3, D), np.float32)
+    w = np.empty((3, len(heads), D, 4), np.float32)
+    for a, h in enumerate(heads):
+        x[:, :, a] = _normal(_rng(seed, _TOK, 3, h), (T, 3, D))
+        ring[:, :, a] = _normal(_rng(seed, _RING, 3, h), (N, 3, 3, D))
+        w[:, a] = _normal(_rng(seed, _CONVW, 3, h), (3, D, 4), 0.5)
+    if bf16:
+        x, ring = bf16_round(x), bf16_round(ring)
+    return dict(x=x, ring=ring, w=w)
+
+
 def stack_unit(seed: int, layer: int, b: int, h: int, steps: int, D: int,
                bf16: bool = True, s0_std=0.02):
     """Inputs of one (layer, sequence, head) unit of a multi-layer decode

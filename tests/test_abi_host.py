@@ -158,3 +158,29 @@ def test_prefill_rejects_bad_arguments(kda, case, detail):
                              a["T"], a["H"], a["D"], a["C"], 1, 1e-6, None, 0, None)
     assert st == kda.KDA_ERR_INVALID_ARG
     assert detail in L.kda_last_error_detail().decode()
+
+
+@pytest.mark.parametrize("case,detail", [
+    (dict(N=0), "N must be"),
+    (dict(T=-1), "T must be"),
+    (dict(D=40), "D must be"),
+    (dict(N=3, cu=None), "cu_seqlens may be NULL only"),
+    (dict(x=None), "x is NULL"),
+    (dict(ring_out=0x50000, ring_in=0x50000), "ring_out must not alias"),
+    (dict(y=0x10000), "y must not alias"),
+    (dict(cu=0x70004), "cu_seqlens must be 8-byte aligned"),
+])
+def test_conv_prefill_rejects_bad_arguments(kda, case, detail):
+    a = dict(x=0x10000, ring_in=0x20000, w=0x30000, y=0x40000, ring_out=0x60000, cu=0x70000, N=1, T=100,
+             H=4, D=128)
+    a.update(case)
+    L = kda.lib()
+    st = L.kda_shortconv_prefill(a["x"], a["ring_in"], a["w"], a["y"], a["ring_out"], a["cu"], a["N"], a["T"],
+                                 a["H"], a["D"], 1, None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    assert detail in L.kda_last_error_detail().decode()
+
+
+def test_conv_prefill_empty_without_ring_is_a_noop(kda):
+    L = kda.lib()
+    assert L.kda_shortconv_prefill(None, None, 0x30000, None, None, None, 1, 0, 4, 128, 1, None) == kda.KDA_OK
