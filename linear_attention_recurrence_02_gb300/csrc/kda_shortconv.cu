@@ -10,11 +10,13 @@
 // contiguous q, k, v operands of the decode step.
 //
 // The prefill form runs the same convolution over packed sequences: each
-// thread owns one 16-byte channel vector of one (projection, head) and walks
+// thread owns four channels of one (projection, head) and walks
 // a tile of 64 tokens with the 3-token window in registers. A tile's history
 // comes from the tokens before it, or from the sequence's ring where the
 // sequence starts, so tiles are independent; the thread that processes a
 // sequence's last token writes its ring for the decode hand-off.
+#include <string>
+
 #include "kda_common.cuh"
 
 namespace kda {
@@ -84,84 +86,107 @@ __device__ __forceinline__ void zero16(float (&out)[Vec16<T>::N]) {
     for (int i = 0; i < Vec16<T>::N; ++i) out[i] = 0.f;
 }
 
-// grid: x = token tiles, y = groups of 256 channel vectors of one token row
+// 4 channels per thread in the prefill form: 8-byte bf16 or 16-byte fp32 vectors
+template <typename T> struct Vec4;
+template <> struct Vec4<float> { using Raw = uint4; };
+template <> struct Vec4<__nv_bfloat16> { using Raw = uint2; };
+
 template <typename T>
-__global__ void __launch_bounds__(256, 2) shortconv_prefill_kernel(
+__device__ __forceinline__ void unpack4(typename Vec4<T>::Raw raw, float (&out)[4]) {
+    const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = Elem<T>::load(e + i);
+}
+template <typename T>
+__device__ __forceinline__ void load4(const T *p, float (&out)[4]) {
+    unpack4<T>(__ldcs(reinterpret_cast<const typename Vec4<T>::Raw *>(p)), out);
+}
+template <typename T>
+__device__ __forceinline__ void store4(T *p, const float (&in)[4]) {
+    typename Vec4<T>::Raw raw;
+    T *e = reinterpret_cast<T *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Elem<T>::store(e + i, in[i]);
+    __stcs(reinterpret_cast<typename Vec4<T>::Raw *>(p), raw);
+}
+
+// One work item = (token tile, group of 256 four-channel vectors of a token
+// row); a persistent grid walks the items, tile-major.
+template <typename T>
+__global__ void __launch_bounds__(256, 3) shortconv_prefill_kernel(
     const T *__restrict__ x, const T *__restrict__ ring_in, const float *__restrict__ w, T *__restrict__ y,
-    T *__restrict__ ring_out, const int64_t *__restrict__ cu, int N, int64_t Ttot, int H, int D, unsigned *err) {
-    constexpr int V = Vec16<T>::N;
+    T *__restrict__ ring_out, const int64_t *__restrict__ cu, int N, int64_t Ttot, int H, int D, unsigned *err,
+    long long ntiles, int ngroups) {
+    constexpr int V = 4;
+    using Raw = typename Vec4<T>::Raw;
+    constexpr int BATCH = sizeof(Raw) == 8 ? 16 : 4;  // token loads in flight per thread
     const int nvec = D / V;
-    const int vi = blockIdx.y * blockDim.x + threadIdx.x;
-    if (vi >= 3 * H * nvec) return;
-    const int cv = vi % nvec, ph = vi / nvec;  // ph = p * H + h
-    const int h = ph % H, p = ph / H;
     const size_t row = (size_t)3 * H * D;      // x elements per token
     const size_t rsz = (size_t)9 * H * D;      // ring elements per sequence
-    const size_t xo = (size_t)ph * D + (size_t)cv * V;
-    const size_t ro = (size_t)ph * 3 * D + (size_t)cv * V;
-    T *yb = y + (size_t)p * Ttot * H * D + (size_t)h * D + (size_t)cv * V;  // + t * H * D
     const size_t ystride = (size_t)H * D;
+    for (long long item = blockIdx.x; item < ntiles * ngroups; item += gridDim.x) {
+        const long long tile = item / ngroups;
+        const int vi = (int)(item % ngroups) * blockDim.x + threadIdx.x;
+        if (vi >= 3 * H * nvec) continue;
+        const int cv = vi % nvec, ph = vi / nvec;  // ph = p * H + h
+        const int h = ph % H, p = ph / H;
+        const size_t xo = (size_t)ph * D + (size_t)cv * V;
+        const size_t ro = (size_t)ph * 3 * D + (size_t)cv * V;
+        T *yb = y + (size_t)p * Ttot * H * D + (size_t)h * D + (size_t)cv * V;  // + t * ystride
 
-    // Sequences with no tokens pass their ring through (first tile only).
-    if (blockIdx.x == 0 && ring_out) {
-        for (int n = 0; n < N; ++n) {
-            if ((cu ? cu[n + 1] - cu[n] : Ttot) != 0) continue;
-            float r[V];
+        // Sequences with no tokens pass their ring through (first tile only).
+        if (tile == 0 && ring_out) {
+            for (int n = 0; n < N; ++n) {
+                if ((cu ? cu[n + 1] - cu[n] : Ttot) != 0) continue;
+                float r[V];
 #pragma unroll
-            for (int m = 0; m < 3; ++m) {
-                if (ring_in) load16(ring_in + n * rsz + ro + (size_t)m * D, r);
-                else zero16<T>(r);
-                store16(ring_out + n * rsz + ro + (size_t)m * D, r);
+                for (int m = 0; m < 3; ++m) {
+                    if (ring_in) load4(ring_in + n * rsz + ro + (size_t)m * D, r);
+                    else r[0] = r[1] = r[2] = r[3] = 0.f;
+                    store4(ring_out + n * rsz + ro + (size_t)m * D, r);
+                }
             }
         }
-    }
-    const int64_t t0 = (int64_t)blockIdx.x * CONV_TILE;
-    const int64_t t1 = t0 + CONV_TILE < Ttot ? t0 + CONV_TILE : Ttot;
-    if (t0 >= t1) return;
+        const int64_t t0 = tile * CONV_TILE;
+        const int64_t t1 = t0 + CONV_TILE < Ttot ? t0 + CONV_TILE : Ttot;
+        if (t0 >= t1) continue;
 
-    // the sequence holding t0: the last n with cu[n] <= t0
-    int n = 0;
-    int64_t sn = 0, en = Ttot;
-    if (cu) {
-        if (cu[0] != 0 || cu[N] != Ttot) {
-            if (err) atomicOr(err, DEVERR_SEQLENS);
-            return;
+        // the sequence holding t0: the last n with cu[n] <= t0
+        int n = 0;
+        int64_t sn = 0, en = Ttot;
+        if (cu) {
+            if (cu[0] != 0 || cu[N] != Ttot) {
+                if (err) atomicOr(err, DEVERR_SEQLENS);
+                continue;
+            }
+            int lo = 0, hi = N - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (cu[mid] <= t0) lo = mid;
+                else hi = mid - 1;
+            }
+            n = lo;
+            sn = cu[n];
+            en = cu[n + 1];
+            if (!(0 <= sn && sn <= t0 && t0 < en && en <= Ttot)) {
+                if (err) atomicOr(err, DEVERR_SEQLENS);
+                continue;
+            }
         }
-        int lo = 0, hi = N - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (cu[mid] <= t0) lo = mid;
-            else hi = mid - 1;
-        }
-        n = lo;
-        sn = cu[n];
-        en = cu[n + 1];
-        if (!(0 <= sn && sn <= t0 && t0 < en && en <= Ttot)) {
-            if (err) atomicOr(err, DEVERR_SEQLENS);
-            return;
-        }
-    }
-    float4 tap[V];
+        float4 tap[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) tap[i] = __ldg(reinterpret_cast<const float4 *>(w + ((size_t)ph * D + (size_t)cv * V) * 4) + i);
+        for (int i = 0; i < V; ++i)
+            tap[i] = __ldg(reinterpret_cast<const float4 *>(w + ((size_t)ph * D + (size_t)cv * V) * 4) + i);
 
-    // window x_{t-3}, x_{t-2}, x_{t-1}: a token of this sequence, else a ring slot
-    float r0[V], r1[V], r2[V];
-    auto hist = [&](int64_t j, float (&out)[V]) {
-        if (j >= sn) load16(x + (size_t)j * row + xo, out);
-        else if (ring_in) load16(ring_in + (size_t)n * rsz + ro + (size_t)(j - sn + 3) * D, out);
-        else zero16<T>(out);
-    };
-    hist(t0 - 3, r0);
-    hist(t0 - 2, r1);
-    hist(t0 - 1, r2);
-    int64_t t = t0;
-    while (t < t1) {
-        const int64_t te = en < t1 ? en : t1;
-#pragma unroll 4
-        for (; t < te; ++t) {
-            float xv[V], yv[V];
-            load16(x + (size_t)t * row + xo, xv);
+        // window x_{t-3}, x_{t-2}, x_{t-1}: a token of this sequence, else a ring slot
+        float r0[V], r1[V], r2[V];
+        auto hist = [&](int64_t j, float (&out)[V]) {
+            if (j >= sn) load4(x + (size_t)j * row + xo, out);
+            else if (ring_in) load4(ring_in + (size_t)n * rsz + ro + (size_t)(j - sn + 3) * D, out);
+            else out[0] = out[1] = out[2] = out[3] = 0.f;
+        };
+        auto step = [&](const float (&xv)[V], int64_t t) {
+            float yv[V];
 #pragma unroll
             for (int i = 0; i < V; ++i) {
                 const float z = tap[i].x * r0[i] + tap[i].y * r1[i] + tap[i].z * r2[i] + tap[i].w * xv[i];
@@ -170,32 +195,57 @@ __global__ void __launch_bounds__(256, 2) shortconv_prefill_kernel(
                 r1[i] = r2[i];
                 r2[i] = xv[i];
             }
-            store16(yb + (size_t)t * ystride, yv);
-        }
-        if (t < en) break;  // tile ends inside the sequence
-        if (ring_out) {
-            store16(ring_out + (size_t)n * rsz + ro, r0);
-            store16(ring_out + (size_t)n * rsz + ro + D, r1);
-            store16(ring_out + (size_t)n * rsz + ro + 2 * (size_t)D, r2);
-        }
-        if (t >= t1) break;
-        // next sequence with tokens; it must start here
-        do {
-            if (n + 1 >= N) {
-                if (err) atomicOr(err, DEVERR_SEQLENS);
-                return;
+            store4(yb + (size_t)t * ystride, yv);
+        };
+        hist(t0 - 3, r0);
+        hist(t0 - 2, r1);
+        hist(t0 - 1, r2);
+        int64_t t = t0;
+        bool bad = false;
+        while (t < t1) {
+            const int64_t te = en < t1 ? en : t1;
+            for (; t + BATCH <= te; t += BATCH) {
+                Raw raw[BATCH];
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) raw[u] = __ldcs(reinterpret_cast<const Raw *>(x + (size_t)(t + u) * row + xo));
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    float xv[V];
+                    unpack4<T>(raw[u], xv);
+                    step(xv, t + u);
+                }
             }
-            ++n;
-            sn = cu[n];
-            en = cu[n + 1];
-        } while (en == sn && sn == t);
-        if (sn != t || en < sn || en > Ttot) {
-            if (err) atomicOr(err, DEVERR_SEQLENS);
-            return;
+            for (; t < te; ++t) {
+                float xv[V];
+                load4(x + (size_t)t * row + xo, xv);
+                step(xv, t);
+            }
+            if (t < en) break;  // tile ends inside the sequence
+            if (ring_out) {
+                store4(ring_out + (size_t)n * rsz + ro, r0);
+                store4(ring_out + (size_t)n * rsz + ro + D, r1);
+                store4(ring_out + (size_t)n * rsz + ro + 2 * (size_t)D, r2);
+            }
+            if (t >= t1) break;
+            // next sequence with tokens; it must start here
+            do {
+                if (n + 1 >= N) {
+                    bad = true;
+                    break;
+                }
+                ++n;
+                sn = cu[n];
+                en = cu[n + 1];
+            } while (en == sn && sn == t);
+            if (bad || sn != t || en < sn || en > Ttot) {
+                bad = true;
+                break;
+            }
+            hist(t - 3, r0);
+            hist(t - 2, r1);
+            hist(t - 1, r2);
         }
-        hist(t - 3, r0);
-        hist(t - 2, r1);
-        hist(t - 1, r2);
+        if (bad && err) atomicOr(err, DEVERR_SEQLENS);
     }
 }
 
@@ -254,20 +304,33 @@ extern "C" kda_status kda_shortconv_prefill(const void *x, const void *ring_in, 
     if (T == 0 && !ring_out) return KDA_OK;
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int V = dtype == KDA_BF16 ? 8 : 4;
-    const long long vecs = 3LL * H * (D / V);
-    const long long gy = (vecs + 255) / 256;
-    const long long gx = T > 0 ? (T + CONV_TILE - 1) / CONV_TILE : 1;
-    if (gy > 65535 || gx > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "shape too large for one launch");
-    const dim3 grid((unsigned)gx, (unsigned)gy);
+    const long long vecs = 3LL * H * (D / 4);
+    const long long groups = (vecs + 255) / 256;
+    const long long tiles = T > 0 ? (T + CONV_TILE - 1) / CONV_TILE : 1;
+    if (groups > 0x7fffffffLL || tiles > (1LL << 40)) return fail(KDA_ERR_UNSUPPORTED, "shape too large");
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = dtype == KDA_BF16
+                ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, shortconv_prefill_kernel<__nv_bfloat16>, 256, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, shortconv_prefill_kernel<float>, 256, 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(KDA_ERR_CUDA, std::string("occupancy query: ") + cudaGetErrorString(e));
+    }
+    const long long items = tiles * groups;
+    const long long resident = (long long)sms * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = (unsigned)(items < resident ? items : resident);
     unsigned *err = device_error_word();
     if (dtype == KDA_BF16)
         shortconv_prefill_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(ring_in), w,
-            static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(ring_out), cu_seqlens, N, T, H, D, err);
+            static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(ring_out), cu_seqlens, N, T, H, D, err,
+            tiles, (int)groups);
     else
         shortconv_prefill_kernel<float><<<grid, 256, 0, s>>>(
             static_cast<const float *>(x), static_cast<const float *>(ring_in), w, static_cast<float *>(y),
-            static_cast<float *>(ring_out), cu_seqlens, N, T, H, D, err);
+            static_cast<float *>(ring_out), cu_seqlens, N, T, H, D, err, tiles, (int)groups);
     return check_launch("shortconv_prefill_kernel");
 }
