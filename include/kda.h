@@ -59,6 +59,15 @@ typedef enum {
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
+/* Form of the decay gate ("为什么 Kimi K3 敢把 KV Cache 扔掉？一篇讲透 GPT-2 到 K3
+ * 的架构进化", section 7: Kimi Delta Attention decays every key channel by its
+ * own factor, Gated DeltaNet by one factor per head; the plain delta rule of
+ * section 4 has no decay). g is always in log space, alpha = exp(g).
+ *   KDA_GATE_CHANNEL  g [..., H, D]: one log-gate per key channel (KDA)
+ *   KDA_GATE_HEAD     g [..., H]:    one log-gate per head (Gated DeltaNet)
+ *   KDA_GATE_NONE     g unused, may be NULL: alpha = 1 (DeltaNet)          */
+typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_HEAD = 1, KDA_GATE_NONE = 2 } kda_gate;
+
 /* Static description of a status code. Never NULL. */
 const char *kda_status_string(kda_status s);
 
@@ -143,6 +152,15 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
                            kda_dtype dtype, float l2_eps, kda_stream_t stream);
 
 /*
+ * kda_decode_step with the gate form chosen by `gate`: g is [B,H,D] for
+ * KDA_GATE_CHANNEL, [B,H] for KDA_GATE_HEAD, and unused (may be NULL) for
+ * KDA_GATE_NONE. kda_decode_step is this call with KDA_GATE_CHANNEL.
+ */
+kda_status kda_decode_step_gated(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, float *state, void *out, int B, int H, int D,
+                                 kda_dtype dtype, kda_gate gate, float l2_eps, kda_stream_t stream);
+
+/*
  * Short conv + decode step in one launch: the same recurrence as
  * kda_shortconv_step followed by kda_decode_step on its output ([W] "KDA
  * 递推公式先衰减再差分": conv + SiLU in front of q/k/v, then decay, delta,
@@ -157,6 +175,16 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
 kda_status kda_shortconv_decode_step(const void *x, void *ring, const float *w, const float *g,
                                      const float *beta, float *state, void *out, int B, int H, int D,
                                      kda_dtype dtype, float l2_eps, kda_stream_t stream);
+
+/*
+ * kda_shortconv_decode_step with the gate form chosen by `gate` (g as in
+ * kda_decode_step_gated). kda_shortconv_decode_step is this call with
+ * KDA_GATE_CHANNEL.
+ */
+kda_status kda_shortconv_decode_step_gated(const void *x, void *ring, const float *w, const float *g,
+                                           const float *beta, float *state, void *out, int B, int H,
+                                           int D, kda_dtype dtype, kda_gate gate, float l2_eps,
+                                           kda_stream_t stream);
 
 /* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
 size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);
@@ -190,6 +218,20 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
                              void *out, const int64_t *cu_seqlens, int N, int64_t T, int H,
                              int D, int C, kda_dtype dtype, float l2_eps, void *workspace,
                              size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_chunk_prefill with the gate form chosen by `gate`: g is [T,H,D] for
+ * KDA_GATE_CHANNEL, [T,H] for KDA_GATE_HEAD, and unused (may be NULL) for
+ * KDA_GATE_NONE. kda_chunk_prefill is this call with KDA_GATE_CHANNEL. The
+ * tensor-core path specialises on the gate form: a per-head gate is read as
+ * one float per token-head and scanned once per chunk, and no gate skips
+ * the decay factors altogether.
+ */
+kda_status kda_chunk_prefill_gated(const void *q, const void *k, const void *v, const float *g,
+                                   const float *beta, const float *initial_state, float *final_state,
+                                   void *out, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                                   int D, int C, kda_dtype dtype, kda_gate gate, float l2_eps,
+                                   void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
 /*
  * kda_chunk_prefill for callers that cannot allocate device memory. The pages

@@ -15,6 +15,10 @@
 // JS*4 = 128 contiguous bytes, so every warp load touches whole 128 B lines.
 // Column sums are reduced with warp shuffles over the row groups of a warp
 // and through shared memory across warps.
+//
+// The gate form is a template parameter: one log-gate per key channel (KDA),
+// one per head (Gated DeltaNet, the same factor on every row of S), or none
+// (the plain delta rule: no decay multiply at all).
 #include "kda_common.cuh"
 
 namespace kda {
@@ -26,7 +30,7 @@ template <> struct DecodeShape<32> { static constexpr int JS = 32, NT = 64; };
 template <> struct DecodeShape<64> { static constexpr int JS = 32, NT = 128; };
 template <> struct DecodeShape<128> { static constexpr int JS = 32, NT = 256; };
 
-template <int D, typename T>
+template <int D, typename T, int GM>
 __global__ void __launch_bounds__(DecodeShape<D>::NT)
     decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                        const float *__restrict__ g, const float *__restrict__ beta,
@@ -62,7 +66,9 @@ __global__ void __launch_bounds__(DecodeShape<D>::NT)
     if (t < D) {
         qv = Elem<T>::load(q + vo + t);
         kv = Elem<T>::load(k + vo + t);
-        av = expf(__ldg(g + vo + t));
+        if constexpr (GM == KDA_GATE_CHANNEL) av = expf(__ldg(g + vo + t));
+        else if constexpr (GM == KDA_GATE_HEAD) av = expf(__ldg(g + unit));
+        else av = 1.f;
     }
     float sqq = qv * qv, skk = kv * kv, sqk = qv * kv;
 #pragma unroll
@@ -150,34 +156,44 @@ __global__ void __launch_bounds__(DecodeShape<D>::NT)
     }
 }
 
-template <int D, typename T>
+template <int D, typename T, int GM>
 static void launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
                           float *state, void *out, int BH, float eps, cudaStream_t s) {
     constexpr int NSLICE = D / DecodeShape<D>::JS;
-    decode_step_kernel<D, T><<<(unsigned)BH * NSLICE, DecodeShape<D>::NT, 0, s>>>(
+    decode_step_kernel<D, T, GM><<<(unsigned)BH * NSLICE, DecodeShape<D>::NT, 0, s>>>(
         static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v), g, beta, state,
         static_cast<T *>(out), eps);
 }
 
-template <typename T>
+template <typename T, int GM>
 static void dispatch_decode(int D, const void *q, const void *k, const void *v, const float *g,
                             const float *beta, float *state, void *out, int BH, float eps, cudaStream_t s) {
     switch (D) {
-    case 16: launch_decode<16, T>(q, k, v, g, beta, state, out, BH, eps, s); break;
-    case 32: launch_decode<32, T>(q, k, v, g, beta, state, out, BH, eps, s); break;
-    case 64: launch_decode<64, T>(q, k, v, g, beta, state, out, BH, eps, s); break;
-    default: launch_decode<128, T>(q, k, v, g, beta, state, out, BH, eps, s); break;
+    case 16: launch_decode<16, T, GM>(q, k, v, g, beta, state, out, BH, eps, s); break;
+    case 32: launch_decode<32, T, GM>(q, k, v, g, beta, state, out, BH, eps, s); break;
+    case 64: launch_decode<64, T, GM>(q, k, v, g, beta, state, out, BH, eps, s); break;
+    default: launch_decode<128, T, GM>(q, k, v, g, beta, state, out, BH, eps, s); break;
     }
+}
+
+template <typename T>
+static void dispatch_gate(kda_gate gate, int D, const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float *state, void *out, int BH, float eps, cudaStream_t s) {
+    if (gate == KDA_GATE_HEAD) dispatch_decode<T, KDA_GATE_HEAD>(D, q, k, v, g, beta, state, out, BH, eps, s);
+    else if (gate == KDA_GATE_NONE) dispatch_decode<T, KDA_GATE_NONE>(D, q, k, v, g, beta, state, out, BH, eps, s);
+    else dispatch_decode<T, KDA_GATE_CHANNEL>(D, q, k, v, g, beta, state, out, BH, eps, s);
 }
 
 }  // namespace kda
 
 using namespace kda;
 
-extern "C" kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
-                                      const float *beta, float *state, void *out, int B, int H, int D,
-                                      kda_dtype dtype, float l2_eps, kda_stream_t stream) {
+extern "C" kda_status kda_decode_step_gated(const void *q, const void *k, const void *v, const float *g,
+                                            const float *beta, float *state, void *out, int B, int H, int D,
+                                            kda_dtype dtype, kda_gate gate, float l2_eps, kda_stream_t stream) {
     clear_detail();
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE)
+        return invalid("gate must be KDA_GATE_CHANNEL, KDA_GATE_HEAD or KDA_GATE_NONE");
     if (B < 0) return invalid("B must be >= 0");
     if (H < 1) return invalid("H must be >= 1");
     if (!valid_head_dim(D)) return invalid("D must be one of 16, 32, 64, 128");
@@ -187,7 +203,8 @@ extern "C" kda_status kda_decode_step(const void *q, const void *k, const void *
     if ((long long)B * H * (D / 16) > 0x7fffffffLL) return invalid("B*H too large for one launch");
     kda_status st;
     if ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
-        (st = check_ptr(g, "g")) || (st = check_ptr(beta, "beta")) || (st = check_ptr(state, "state")) ||
+        (gate != KDA_GATE_NONE && (st = check_ptr(g, "g"))) || (st = check_ptr(beta, "beta")) ||
+        (st = check_ptr(state, "state")) ||
         (st = check_ptr(out, "out")))
         return st;
     if (out == q || out == k || out == v || (const void *)out == (const void *)state)
@@ -195,8 +212,14 @@ extern "C" kda_status kda_decode_step(const void *q, const void *k, const void *
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == KDA_BF16)
-        dispatch_decode<__nv_bfloat16>(D, q, k, v, g, beta, state, out, B * H, l2_eps, s);
+        dispatch_gate<__nv_bfloat16>(gate, D, q, k, v, g, beta, state, out, B * H, l2_eps, s);
     else
-        dispatch_decode<float>(D, q, k, v, g, beta, state, out, B * H, l2_eps, s);
+        dispatch_gate<float>(gate, D, q, k, v, g, beta, state, out, B * H, l2_eps, s);
     return check_launch("decode_step_kernel");
+}
+
+extern "C" kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
+                                      const float *beta, float *state, void *out, int B, int H, int D,
+                                      kda_dtype dtype, float l2_eps, kda_stream_t stream) {
+    return kda_decode_step_gated(q, k, v, g, beta, state, out, B, H, D, dtype, KDA_GATE_CHANNEL, l2_eps, stream);
 }

@@ -11,7 +11,8 @@
 // head, so the in-place ring shift cannot race with another CTA's read. The
 // state loads are issued first and stay in flight while the conv, the norms
 // and the decay run; column sums of S'^T k^ and S'^T q^ are reduced through
-// shared memory across the row groups; S is written once.
+// shared memory across the row groups; S is written once. The gate form
+// (per channel, per head, none) is a template parameter as in kda_decode.cu.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -22,7 +23,7 @@ template <> struct FusedShape<32> { static constexpr int NT = 64; };
 template <> struct FusedShape<64> { static constexpr int NT = 128; };
 template <> struct FusedShape<128> { static constexpr int NT = 256; };
 
-template <int D, typename T>
+template <int D, typename T, int GM>
 __global__ void __launch_bounds__(FusedShape<D>::NT)
     fused_decode_kernel(const T *__restrict__ x, T *__restrict__ ring, const float *__restrict__ w,
                         const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ state,
@@ -65,7 +66,12 @@ __global__ void __launch_bounds__(FusedShape<D>::NT)
         Elem<T>::store(ring + ro + 2 * D, xv);
     }
     const size_t vo = (size_t)unit * D;
-    const float av = t < D ? expf(__ldg(g + vo + t)) : 0.f;
+    float av = 0.f;
+    if (t < D) {
+        if constexpr (GM == KDA_GATE_CHANNEL) av = expf(__ldg(g + vo + t));
+        else if constexpr (GM == KDA_GATE_HEAD) av = expf(__ldg(g + unit));
+        else av = 1.f;
+    }
     __syncthreads();
 
     // 2. L2 norms of q, k and their dot
@@ -158,32 +164,45 @@ __global__ void __launch_bounds__(FusedShape<D>::NT)
     }
 }
 
-template <int D, typename T>
+template <int D, typename T, int GM>
 static void launch_fused(const void *x, void *ring, const float *w, const float *g, const float *beta,
                          float *state, void *out, int B, int H, float eps, cudaStream_t s) {
-    fused_decode_kernel<D, T><<<(unsigned)B * H, FusedShape<D>::NT, 0, s>>>(
+    fused_decode_kernel<D, T, GM><<<(unsigned)B * H, FusedShape<D>::NT, 0, s>>>(
         static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps);
 }
 
-template <typename T>
+template <typename T, int GM>
 static void dispatch_fused(int D, const void *x, void *ring, const float *w, const float *g, const float *beta,
                            float *state, void *out, int B, int H, float eps, cudaStream_t s) {
     switch (D) {
-    case 16: launch_fused<16, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
-    case 32: launch_fused<32, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
-    case 64: launch_fused<64, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
-    default: launch_fused<128, T>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    case 16: launch_fused<16, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    case 32: launch_fused<32, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    case 64: launch_fused<64, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    default: launch_fused<128, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
     }
+}
+
+template <typename T>
+static void dispatch_fused_gate(kda_gate gate, int D, const void *x, void *ring, const float *w, const float *g,
+                                const float *beta, float *state, void *out, int B, int H, float eps,
+                                cudaStream_t s) {
+    if (gate == KDA_GATE_HEAD) dispatch_fused<T, KDA_GATE_HEAD>(D, x, ring, w, g, beta, state, out, B, H, eps, s);
+    else if (gate == KDA_GATE_NONE)
+        dispatch_fused<T, KDA_GATE_NONE>(D, x, ring, w, g, beta, state, out, B, H, eps, s);
+    else dispatch_fused<T, KDA_GATE_CHANNEL>(D, x, ring, w, g, beta, state, out, B, H, eps, s);
 }
 
 }  // namespace kda
 
 using namespace kda;
 
-extern "C" kda_status kda_shortconv_decode_step(const void *x, void *ring, const float *w, const float *g,
-                                                const float *beta, float *state, void *out, int B, int H, int D,
-                                                kda_dtype dtype, float l2_eps, kda_stream_t stream) {
+extern "C" kda_status kda_shortconv_decode_step_gated(const void *x, void *ring, const float *w, const float *g,
+                                                      const float *beta, float *state, void *out, int B, int H,
+                                                      int D, kda_dtype dtype, kda_gate gate, float l2_eps,
+                                                      kda_stream_t stream) {
     clear_detail();
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE)
+        return invalid("gate must be KDA_GATE_CHANNEL, KDA_GATE_HEAD or KDA_GATE_NONE");
     if (B < 0) return invalid("B must be >= 0");
     if (H < 1) return invalid("H must be >= 1");
     if (!valid_head_dim(D)) return invalid("D must be one of 16, 32, 64, 128");
@@ -193,16 +212,23 @@ extern "C" kda_status kda_shortconv_decode_step(const void *x, void *ring, const
     if ((long long)B * H > 0x7fffffffLL) return invalid("B*H too large for one launch");
     kda_status st;
     if ((st = check_ptr(x, "x")) || (st = check_ptr(ring, "ring")) || (st = check_ptr(w, "w")) ||
-        (st = check_ptr(g, "g")) || (st = check_ptr(beta, "beta")) || (st = check_ptr(state, "state")) ||
-        (st = check_ptr(out, "out")))
+        (gate != KDA_GATE_NONE && (st = check_ptr(g, "g"))) || (st = check_ptr(beta, "beta")) ||
+        (st = check_ptr(state, "state")) || (st = check_ptr(out, "out")))
         return st;
     if (out == x || out == ring || (const void *)out == (const void *)state)
         return invalid("out must not alias x, ring or state");
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == KDA_BF16)
-        dispatch_fused<__nv_bfloat16>(D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
+        dispatch_fused_gate<__nv_bfloat16>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
     else
-        dispatch_fused<float>(D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
+        dispatch_fused_gate<float>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
     return check_launch("fused_decode_kernel");
+}
+
+extern "C" kda_status kda_shortconv_decode_step(const void *x, void *ring, const float *w, const float *g,
+                                                const float *beta, float *state, void *out, int B, int H, int D,
+                                                kda_dtype dtype, float l2_eps, kda_stream_t stream) {
+    return kda_shortconv_decode_step_gated(x, ring, w, g, beta, state, out, B, H, D, dtype, KDA_GATE_CHANNEL,
+                                           l2_eps, stream);
 }

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(SIMT_NT)
                         const float *__restrict__ g, const float *__restrict__ beta,
                         const float *s_init, float *s_final, T *__restrict__ out,
                         const int64_t *__restrict__ cu_seqlens, int N, int64_t Ttot, int H, int C, float eps,
-                        unsigned *err, const int *__restrict__ order) {
+                        unsigned *err, const int *__restrict__ order, int gate) {
     constexpr int JS = simt_js(D), LD = D + 1, NS = D / JS, NW = SIMT_NT / 32;
     extern __shared__ float smem[];
     float *sQ = smem;                    // [C][LD]  q^, then Qt
@@ -106,7 +106,9 @@ __global__ void __launch_bounds__(SIMT_NT)
         if (tid < D) {
             float acc = 0.f;
             for (int r = 0; r < L; ++r) {
-                acc += g[((size_t)(c0 + r) * H + h) * D + tid];
+                acc += gate == KDA_GATE_CHANNEL ? g[((size_t)(c0 + r) * H + h) * D + tid]
+                       : gate == KDA_GATE_HEAD  ? g[(size_t)(c0 + r) * H + h]
+                                                : 0.f;
                 sG[r * LD + tid] = acc;
             }
         }
@@ -194,7 +196,7 @@ static kda_status launch_simt(const PrefillArgs &a, cudaStream_t s) {
     kern<<<grid, SIMT_NT, smem, s>>>(static_cast<const T *>(a.q), static_cast<const T *>(a.k),
                                      static_cast<const T *>(a.v), a.g, a.beta, a.s_init, a.s_final,
                                      static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err,
-                                     a.order);
+                                     a.order, a.gate);
     return check_launch("prefill_simt_kernel");
 }
 
@@ -258,12 +260,14 @@ extern "C" size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int nu
     return ((size_t)num_seqs * sizeof(int) + 255) & ~(size_t)255;
 }
 
-extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
-                                        const float *beta, const float *initial_state, float *final_state,
-                                        void *out, const int64_t *cu_seqlens, int N, int64_t T, int H, int D,
-                                        int C, kda_dtype dtype, float l2_eps, void *workspace,
-                                        size_t workspace_bytes, kda_stream_t stream) {
+extern "C" kda_status kda_chunk_prefill_gated(const void *q, const void *k, const void *v, const float *g,
+                                              const float *beta, const float *initial_state, float *final_state,
+                                              void *out, const int64_t *cu_seqlens, int N, int64_t T, int H, int D,
+                                              int C, kda_dtype dtype, kda_gate gate, float l2_eps, void *workspace,
+                                              size_t workspace_bytes, kda_stream_t stream) {
     clear_detail();
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE)
+        return invalid("gate must be KDA_GATE_CHANNEL, KDA_GATE_HEAD or KDA_GATE_NONE");
     if (N < 1) return invalid("N must be >= 1");
     if (T < 0) return invalid("T must be >= 0");
     if (H < 1) return invalid("H must be >= 1");
@@ -277,7 +281,8 @@ extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void
     if (workspace_bytes < need) return invalid("workspace too small");
     kda_status st;
     if (T > 0 && ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
-                  (st = check_ptr(g, "g")) || (st = check_ptr(beta, "beta")) || (st = check_ptr(out, "out"))))
+                  (gate != KDA_GATE_NONE && (st = check_ptr(g, "g"))) || (st = check_ptr(beta, "beta")) ||
+                  (st = check_ptr(out, "out"))))
         return st;
     if (initial_state && (st = check_ptr(initial_state, "initial_state"))) return st;
     if (final_state && (st = check_ptr(final_state, "final_state"))) return st;
@@ -287,7 +292,7 @@ extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void
     if (T == 0 && final_state == nullptr) return KDA_OK;
     if ((st = bind_stream_device(stream))) return st;
     PrefillArgs a{q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C,
-                  dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word(), nullptr};
+                  dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word(), nullptr, (int)gate};
     if (a.err == nullptr) return fail(KDA_ERR_CUDA, "device error word unavailable");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (need > 0 && cu_seqlens != nullptr) {
@@ -296,4 +301,13 @@ extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void
         a.order = order;
     }
     return prefill_tc_applicable(a) ? prefill_tc(a, s) : prefill_simt(a, s);
+}
+
+extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
+                                        const float *beta, const float *initial_state, float *final_state,
+                                        void *out, const int64_t *cu_seqlens, int N, int64_t T, int H, int D,
+                                        int C, kda_dtype dtype, float l2_eps, void *workspace,
+                                        size_t workspace_bytes, kda_stream_t stream) {
+    return kda_chunk_prefill_gated(q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C,
+                                   dtype, KDA_GATE_CHANNEL, l2_eps, workspace, workspace_bytes, stream);
 }

@@ -22,6 +22,7 @@ struct PrefillArgs {
     size_t workspace_bytes;
     unsigned *err;
     const int *order;  // sequences by descending length (device), or NULL = natural order
+    int gate;          // kda_gate: g is [T,H,D], [T,H], or unused
 };
 
 // Largest batch the length sort handles; bigger batches keep their order.

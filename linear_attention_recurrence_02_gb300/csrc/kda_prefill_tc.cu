@@ -34,6 +34,7 @@
 // of its sequence; thread 0 issues TMA and MMAs, every wait is bounded.
 #include <cuda.h>
 
+#include <cstring>
 #include <string>
 
 #include "kda_common.cuh"
@@ -163,12 +164,17 @@ __device__ __forceinline__ void sync_for_mma() {
     sync_tc();
 }
 
+// GM: gate form (kda_gate). Per channel: g arrives as an fp32 TMA tile and is
+// scanned per channel. Per head: one float per token is prefetched like beta
+// and scanned by one warp. None: no decay factors at all (G = 0, c = 0).
+template <int GM>
 __global__ void __launch_bounds__(NT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                      const float *__restrict__ beta, const float *s_init, float *s_final,
-                      __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens, int N,
-                      int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
+                      const float *__restrict__ g_head, const float *__restrict__ beta, const float *s_init,
+                      float *s_final, __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens,
+                      int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
+    constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *s_rq = reinterpret_cast<float *>(sm + OFF_SMALL);
@@ -179,7 +185,8 @@ __global__ void __launch_bounds__(NT, 1)
     float *s_sf = s_c + 128;        // S~ factor e^c sigma_old
     float *s_pf = s_sf + 128;       // rescale of the stored state before G7 accumulates
     float *s_sigma = s_pf + 128;    // per-channel scale: S = Diag(sigma) S_stored
-    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(s_sigma + 128);
+    float *s_g1 = s_sigma + 128;    // per-head gate: g per row, then G per row (log2 units)
+    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(s_g1 + 64);
     uint64_t *bar_g = bar_qk + 1;
     uint64_t *bar_v = bar_qk + 2;
     uint64_t *bar_mma = bar_qk + 3;
@@ -225,10 +232,10 @@ __global__ void __launch_bounds__(NT, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_g);
+        if constexpr (GCH) tma_prefetch_desc(&tm_g);
         if (start < end) {
             issue_qk((int)start);
-            issue_g((int)start);
+            if constexpr (GCH) issue_g((int)start);
             issue_v((int)start);
         }
     }
@@ -260,17 +267,24 @@ __global__ void __launch_bounds__(NT, 1)
     bool ok = true;
     bool pend_g = false, pend_qkv = false;  // next chunk's loads in flight (phase ph ^ 1)
     float beta_reg = 0.f;  // beta of the next chunk, loaded one chunk ahead
-    if (tid < C && start + tid < end) beta_reg = beta[(size_t)(start + tid) * H + h];
+    float gh_reg = 0.f;    // per-head gate of the next chunk, likewise
+    if (tid < C && start + tid < end) {
+        beta_reg = beta[(size_t)(start + tid) * H + h];
+        if constexpr (GHD) gh_reg = g_head[(size_t)(start + tid) * H + h];
+    }
     for (int64_t c0 = start; c0 < end; c0 += C, ph ^= 1) {
         const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
         const bool has_next = c0 + C < end;
         sync_for_mma();  // previous chunk fully consumed
-        if (tid < C) s_beta[tid] = beta_reg;
-        bool got = mbar_wait(bar_qk, ph, WAIT_LIMIT) && mbar_wait(bar_g, ph, WAIT_LIMIT) &&
+        if (tid < C) {
+            s_beta[tid] = beta_reg;
+            if constexpr (GHD) s_g1[tid] = gh_reg;
+        }
+        bool got = mbar_wait(bar_qk, ph, WAIT_LIMIT) && (!GCH || mbar_wait(bar_g, ph, WAIT_LIMIT)) &&
                    mbar_wait(bar_v, ph, WAIT_LIMIT);
         if (__syncthreads_or(!got)) {
             mbar_wait(bar_qk, ph, WAIT_LIMIT);
-            mbar_wait(bar_g, ph, WAIT_LIMIT);
+            if constexpr (GCH) mbar_wait(bar_g, ph, WAIT_LIMIT);
             mbar_wait(bar_v, ph, WAIT_LIMIT);
             ok = false;
             break;
@@ -287,8 +301,9 @@ __global__ void __launch_bounds__(NT, 1)
                 *reinterpret_cast<uint4 *>(sm + OFF_X + swz(r + 64, cc, 128)) = z4;
                 *reinterpret_cast<uint4 *>(sm + OFF_V + swz(r, cc, 64)) = z4;
             }
-            for (int p = tid; p < (C - L) * 32; p += NT)
-                *reinterpret_cast<uint4 *>(sm + OFF_G + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
+            if constexpr (GCH)
+                for (int p = tid; p < (C - L) * 32; p += NT)
+                    *reinterpret_cast<uint4 *>(sm + OFF_G + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
             __syncthreads();
         }
 
@@ -308,7 +323,7 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int e = 0; e < 8; ++e) ss += f[e] * f[e];
             }
             (tid < 64 ? s_rq : s_rk)[r] = inv_norm(ss, eps);
-        } else {
+        } else if constexpr (GCH) {
             const int i = tid - 128;
             float gv[64];
 #pragma unroll
@@ -320,8 +335,31 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
             s_gl[i] = GL;
+        } else if constexpr (GHD) {
+            // one warp: inclusive scan of 64 per-row gates, two rows per lane
+            if (warp == 4) {
+                const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
+                float incl = g0 + g1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const float G1 = incl, G0 = incl - g1;
+                const float GL = __shfl_sync(0xffffffffu, incl, 31);
+                const float Gfirst = __shfl_sync(0xffffffffu, G0, 0);
+                bad = !(Gfirst - GL <= SPAN_MAX);
+                s_g1[2 * lane] = G0 * LOG2E;
+                s_g1[2 * lane + 1] = G1 * LOG2E;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
+            }
+        } else {
+            s_gl[tid - 128] = 0.f;
         }
-        const int exact = __syncthreads_or(bad);
+        int exact = 0;  // never with no gate (no decay span)
+        if constexpr (GNO) __syncthreads();
+        else exact = __syncthreads_or(bad);
         // per-channel anchor and state scale: sigma_new = e^{G_L - c} on the
         // anchored path (then G7 can use Rk as is), 1 on the exact path
         if (tid < 128) {
@@ -351,11 +389,17 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int i = cc * 8 + e;
-                            const float x = ks[e] * rks * ex2(gt[r * 128 + i] - gt[s * 128 + i]);
+                            float x = ks[e] * rks;
+                            if constexpr (GCH) x *= ex2(gt[r * 128 + i] - gt[s * 128 + i]);
                             a += kr[e] * rkr * x;
                             pq += qr[e] * rqr * x;
                         }
                     }
+                }
+                if constexpr (GHD) {  // one decay factor for every channel
+                    const float f = s <= r ? ex2(s_g1[r] - s_g1[s]) : 0.f;
+                    a *= f;
+                    pq *= f;
                 }
                 Am[fsw(r, s >> 2) + (s & 3)] = (s < r) ? s_beta[r] * a : 0.f;
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_P + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) +
@@ -368,11 +412,11 @@ __global__ void __launch_bounds__(NT, 1)
         // exact path); each thread keeps one 8-channel group and walks 4 rows
         {
             const int cc = tid & 15, rb = tid >> 4;
-            float cv[8], glv[8];  // anchor and G_L in log2 units
+            float cv[8], glv[8];  // anchor and G_L in log2 units (one value without a per-channel gate)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                cv[e] = s_c[cc * 8 + e] * LOG2E;
-                glv[e] = s_gl[cc * 8 + e] * LOG2E;
+                cv[e] = s_c[GCH ? cc * 8 + e : 0] * LOG2E;
+                glv[e] = s_gl[GCH ? cc * 8 + e : 0] * LOG2E;
             }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -382,17 +426,31 @@ __global__ void __launch_bounds__(NT, 1)
                 unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + oq), qf);
                 unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + ok_), kf);
                 const float rq = s_rq[r], rk = s_rk[r];
-                const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
-                const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
-                const float G[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                float G[8];
+                if constexpr (GCH) {
+                    const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
+                    const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
+                    G[0] = ga.x; G[1] = ga.y; G[2] = ga.z; G[3] = ga.w;
+                    G[4] = gb.x; G[5] = gb.y; G[6] = gb.z; G[7] = gb.w;
+                } else {
+                    const float gr = GHD ? s_g1[r] : 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) G[e] = gr;
+                }
                 float lk[8], lq[8], rkv[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float kh = kf[e] * rk, qh = qf[e] * rq;
-                    const float e1 = ex2(G[e] - cv[e]);
-                    lk[e] = e1 * kh;
-                    lq[e] = e1 * qh;
-                    rkv[e] = (exact ? ex2(glv[e] - G[e]) : ex2(cv[e] - G[e])) * kh;  // Kb or Rk (<= e^ANCHOR)
+                    if constexpr (GNO) {
+                        lk[e] = kh;
+                        lq[e] = qh;
+                        rkv[e] = kh;
+                    } else {
+                        const float e1 = ex2(G[e] - cv[e]);
+                        lk[e] = e1 * kh;
+                        lq[e] = e1 * qh;
+                        rkv[e] = (exact ? ex2(glv[e] - G[e]) : ex2(cv[e] - G[e])) * kh;  // Kb or Rk (<= e^ANCHOR)
+                    }
                 }
                 *reinterpret_cast<uint4 *>(sm + OFF_X + ok_) = pack8(lk);
                 *reinterpret_cast<uint4 *>(sm + OFF_X + oq) = pack8(lq);
@@ -401,11 +459,16 @@ __global__ void __launch_bounds__(NT, 1)
         }
         sync_for_mma();
 
-        if (tid < C) beta_reg = (has_next && c0 + C + tid < end) ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
+        if (tid < C) {
+            const bool in = has_next && c0 + C + tid < end;
+            beta_reg = in ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
+            if constexpr (GHD) gh_reg = in ? g_head[(size_t)(c0 + C + tid) * H + h] : 0.f;
+        }
         // g of this chunk is consumed: prefetch the next chunk's.
         // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T
         if (tid == 0) {
-            if (has_next) issue_g((int)(c0 + C));
+            if constexpr (GCH)
+                if (has_next) issue_g((int)(c0 + C));
             if (!exact) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -416,7 +479,7 @@ __global__ void __launch_bounds__(NT, 1)
                 mma_commit(bar_mma);
             }
         }
-        pend_g = has_next;
+        pend_g = GCH && has_next;
         // Warps 0-3 wait for G1, read back A and solve for T. Meanwhile warps
         // 4-7 convert the state operand (independent of G1), then read back P.
         bool got_mma = true;
@@ -628,8 +691,10 @@ __global__ void __launch_bounds__(NT, 1)
                     const int i0 = 64 * kb + 32 * part;
 #pragma unroll
                     for (int g4 = 0; g4 < 8; ++g4) {
-                        const float4 fc = *reinterpret_cast<const float4 *>(s_sf + i0 + 4 * g4);
-                        const float4 fl = *reinterpret_cast<const float4 *>(s_pf + i0 + 4 * g4);
+                        const float4 fc = GCH ? *reinterpret_cast<const float4 *>(s_sf + i0 + 4 * g4)
+                                              : make_float4(s_sf[0], s_sf[0], s_sf[0], s_sf[0]);
+                        const float4 fl = GCH ? *reinterpret_cast<const float4 *>(s_pf + i0 + 4 * g4)
+                                              : make_float4(s_pf[0], s_pf[0], s_pf[0], s_pf[0]);
                         const float fcv[4] = {fc.x, fc.y, fc.z, fc.w}, flv[4] = {fl.x, fl.y, fl.z, fl.w};
                         float so[4];
 #pragma unroll
@@ -862,21 +927,33 @@ bool prefill_tc_applicable(const PrefillArgs &a) {
     return a.bf16 && a.D == 128 && a.C == 64 && a.T > 0 && a.T <= 0x7fffffffLL;
 }
 
+template <int GM>
+static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                            const CUtensorMap &mv, const CUtensorMap &mg, cudaStream_t s) {
+    using namespace tcp;
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_tc_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    prefill_tc_kernel<GM><<<(unsigned)a.N * a.H, NT, SMEM_BYTES, s>>>(
+        mq, mk, mv, mg, GM == KDA_GATE_HEAD ? a.g : nullptr, a.beta, a.s_init, a.s_final,
+        static_cast<__nv_bfloat16 *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
+    return check_launch("prefill_tc_kernel");
+}
+
 kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     using namespace tcp;
     CUtensorMap mq, mk, mv, mg;
+    memset(&mg, 0, sizeof(mg));  // not read unless the gate is per channel
     const uint64_t inner = (uint64_t)a.H * D, rows = (uint64_t)a.T;
     if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, inner, rows, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+        (a.gate == KDA_GATE_CHANNEL &&
+         !make_map(&mg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, inner, rows, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
         return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    prefill_tc_kernel<<<(unsigned)a.N * a.H, NT, SMEM_BYTES, s>>>(
-        mq, mk, mv, mg, a.beta, a.s_init, a.s_final, static_cast<__nv_bfloat16 *>(a.out), a.cu_seqlens, a.N, a.T,
-        a.H, a.eps, a.err, a.order);
-    return check_launch("prefill_tc_kernel");
+    if (a.gate == KDA_GATE_HEAD) return launch_tc<KDA_GATE_HEAD>(a, mq, mk, mv, mg, s);
+    if (a.gate == KDA_GATE_NONE) return launch_tc<KDA_GATE_NONE>(a, mq, mk, mv, mg, s);
+    return launch_tc<KDA_GATE_CHANNEL>(a, mq, mk, mv, mg, s);
 }
 
 }  // namespace kda

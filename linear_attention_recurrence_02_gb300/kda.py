@@ -15,6 +15,29 @@ import threading
 from . import build as _build
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE_CHECK = range(6)
+# gate forms: one log-gate per key channel (KDA), per head (Gated DeltaNet), none (DeltaNet)
+KDA_GATE_CHANNEL, KDA_GATE_HEAD, KDA_GATE_NONE = range(3)
+_GATES = {"channel": KDA_GATE_CHANNEL, "head": KDA_GATE_HEAD, "none": KDA_GATE_NONE}
+
+
+def _gate_code(gate):
+    if isinstance(gate, str):
+        return _GATES[gate]
+    return int(gate)
+
+
+def _check_gate(g, gate, lead, H, D):
+    """Shape of g for a gate form: [..., H, D], [..., H], or absent."""
+    code = _gate_code(gate)
+    if code == KDA_GATE_CHANNEL:
+        ok = g is not None and tuple(g.shape) == (*lead, H, D)
+    elif code == KDA_GATE_HEAD:
+        ok = g is not None and tuple(g.shape) == (*lead, H)
+    else:
+        ok = True
+    if not ok:
+        raise ValueError("g shape does not match the gate form")
+    return code
 KDA_F32, KDA_BF16 = 0, 1
 
 _lib = None
@@ -35,6 +58,11 @@ _SIGNATURES = {
     "kda_shortconv_step": ([_vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _vp], _ci),
     "kda_shortconv_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _vp], _ci),
     "kda_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
+    "kda_decode_step_gated": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
+    "kda_shortconv_decode_step_gated": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _vp],
+                                        _ci),
+    "kda_chunk_prefill_gated": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci, _ci,
+                                 _cf, _vp, _sz, _vp], _ci),
     "kda_shortconv_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
     "kda_chunk_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
@@ -157,6 +185,28 @@ def kda_decode_step(q, k, v, g, beta, state, out, l2_eps=1e-6, stream=None):
                                  B, H, D, _dtype_code(q), float(l2_eps), _stream(stream, q.device)))
 
 
+def kda_decode_step_gated(q, k, v, g, beta, state, out, gate="channel", l2_eps=1e-6, stream=None):
+    """kda_decode_step with gate "channel" (g [B,H,D]), "head" (g [B,H]) or "none" (g unused)."""
+    B, H, D = q.shape
+    code = _check_gate(g, gate, (B,), H, D)
+    if tuple(beta.shape) != (B, H) or tuple(state.shape) != (B, H, D, D) or tuple(out.shape) != (B, H, D):
+        raise ValueError("shape mismatch")
+    _check(lib().kda_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
+                                       B, H, D, _dtype_code(q), code, float(l2_eps), _stream(stream, q.device)))
+
+
+def kda_shortconv_decode_step_gated(x, ring, w, g, beta, state, out, gate="channel", l2_eps=1e-6, stream=None):
+    """kda_shortconv_decode_step with a gate form as in kda_decode_step_gated."""
+    B, P, H, D = x.shape
+    code = _check_gate(g, gate, (B,), H, D)
+    if P != 3 or tuple(ring.shape) != (B, 3, H, 3, D) or tuple(w.shape) != (3, H, D, 4) \
+            or tuple(beta.shape) != (B, H) or tuple(state.shape) != (B, H, D, D) or tuple(out.shape) != (B, H, D):
+        raise ValueError("shape mismatch")
+    _check(lib().kda_shortconv_decode_step_gated(_ptr(x), _ptr(ring), _ptr(w), _ptr(g), _ptr(beta), _ptr(state),
+                                                 _ptr(out), B, H, D, _dtype_code(x), code, float(l2_eps),
+                                                 _stream(stream, x.device)))
+
+
 def kda_shortconv_decode_step(x, ring, w, g, beta, state, out, l2_eps=1e-6, stream=None):
     """Fused short conv + decode step. x [B,3,H,D], ring [B,3,H,3,D] (in/out),
     w [3,H,D,4] fp32, g [B,H,D] fp32, beta [B,H] fp32, state [B,H,D,D] fp32
@@ -190,6 +240,23 @@ def kda_chunk_prefill(q, k, v, g, beta, out, initial_state=None, final_state=Non
                                    _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
                                    _dtype_code(q), float(l2_eps), _ptr(workspace), wsz,
                                    _stream(stream, q.device)))
+
+
+def kda_chunk_prefill_gated(q, k, v, g, beta, out, gate="channel", initial_state=None, final_state=None,
+                            cu_seqlens=None, chunk_size=64, l2_eps=1e-6, workspace=None, stream=None):
+    """kda_chunk_prefill with gate "channel" (g [T,H,D]), "head" (g [T,H]) or "none" (g unused)."""
+    T, H, D = q.shape
+    code = _check_gate(g, gate, (T,), H, D)
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    ws_bytes = kda_chunk_prefill_workspace_bytes(T, N, H, D, chunk_size)
+    if workspace is None and ws_bytes > 0:
+        import torch
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kda_chunk_prefill_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                         _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
+                                         _dtype_code(q), code, float(l2_eps), _ptr(workspace), wsz,
+                                         _stream(stream, q.device)))
 
 
 def kda_chunk_prefill_noalloc(q, k, v, g, beta, out, initial_state=None, final_state=None, cu_seqlens=None,

@@ -184,3 +184,31 @@ def test_conv_prefill_rejects_bad_arguments(kda, case, detail):
 def test_conv_prefill_empty_without_ring_is_a_noop(kda):
     L = kda.lib()
     assert L.kda_shortconv_prefill(None, None, 0x30000, None, None, None, 1, 0, 4, 128, 1, None) == kda.KDA_OK
+
+
+def test_gated_calls_reject_unknown_gate(kda):
+    L = kda.lib()
+    st = L.kda_decode_step_gated(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000, 2, 3, 128, 1, 7,
+                                 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "gate must be" in L.kda_last_error_detail().decode()
+    st = L.kda_shortconv_decode_step_gated(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000, 2, 3,
+                                           128, 1, -1, 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "gate must be" in L.kda_last_error_detail().decode()
+    st = L.kda_chunk_prefill_gated(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, None, None, 0x60000, None, 1, 100,
+                                   4, 128, 64, 1, 3, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "gate must be" in L.kda_last_error_detail().decode()
+
+
+def test_gate_none_needs_no_g_but_others_do(kda):
+    """With no gate, g may be NULL (the argument checks pass on to the next
+    pointer); with a per-head gate a NULL g is rejected."""
+    L = kda.lib()
+    st = L.kda_decode_step_gated(0x10000, 0x20000, 0x30000, None, None, 0x60000, 0x70000, 2, 3, 128, 1,
+                                 kda.KDA_GATE_NONE, 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "beta is NULL" in L.kda_last_error_detail().decode()
+    st = L.kda_decode_step_gated(0x10000, 0x20000, 0x30000, None, 0x50000, 0x60000, 0x70000, 2, 3, 128, 1,
+                                 kda.KDA_GATE_HEAD, 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "g is NULL" in L.kda_last_error_detail().decode()
+    st = L.kda_chunk_prefill_gated(0x10000, 0x20000, 0x30000, None, None, None, None, 0x60000, None, 1, 100,
+                                   4, 128, 64, 1, kda.KDA_GATE_NONE, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "beta is NULL" in L.kda_last_error_detail().decode()
