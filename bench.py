@@ -385,8 +385,29 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
     fl = T * H * PREFILL_TOKEN_HEAD_FLOPS
     varlen = bench_varlen(torch, kda, dev, stream, ws, hbm_peak)
     conv = bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak)
+    # the same workload with a per-head gate (Gated DeltaNet) and with none (DeltaNet)
+    gates = {}
+    gh = g[..., 0].contiguous()
+    for name, gg, gbytes in (("head", gh, 4), ("none", None, 0)):
+        def gcall():
+            kda.kda_chunk_prefill_gated(q, k, v, gg, beta, out, gate=name, final_state=sf, chunk_size=C,
+                                        workspace=wsb, stream=stream)
+        for _ in range(3):
+            gcall()
+        torch.cuda.synchronize(dev)
+        ge = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a0, b0 in ge:
+            a0.record(stream)
+            gcall()
+            b0.record(stream)
+        torch.cuda.synchronize(dev)
+        gms = max_over_ranks(statistics.mean(a0.elapsed_time(b0) for a0, b0 in ge), dev)
+        gby = T * H * (PREFILL_TOKEN_HEAD_BYTES - 512 + gbytes) + H * D * D * 4
+        gates[name] = {"value": ws * toks / (gms * 1e-3), "unit": "tokens/s", "ms_per_call": gms,
+                       "roofline_hbm": {"achieved": gby / (gms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                                        "frac": gby / (gms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": gby}}
     return {"value": ws * toks / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "varlen": varlen,
-            "conv": conv,
+            "conv": conv, "gates": gates,
             "config": {"workload": f"chunked prefill T={T}, H={H}, d={D}, C={C}, bf16 q/k/v, zero S0, "
                                    "fp32 final state", "calls": n},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
