@@ -889,6 +889,833 @@ __global__ void __launch_bounds__(NT, 1)
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// ------------------------------------------------- pipelined variant
+// Warps 0-7 ("prep") run the state-independent part of chunk c + 1 (loads,
+// norms, cumulative decay, operand build, G1, solve, G2/G3, W' read-back)
+// while warps 8-11 ("chain") run the state chain of chunk c (S~ conversion,
+// G4/G5, U, G6/G7, output). The hand-offs are mbarriers in shared memory:
+//   ready[b]  prep -> chain: chunk of parity b fully prepared
+//   c45[b]    G4/G5 of chunk parity b done (tcgen05.commit): its [W'; Lq]
+//             tile may be reloaded; the chain itself then issues the q/k
+//             loads of the chunk two ahead into it
+//   ofree[b]  chain -> prep: chunk parity b finished (U0[b], Rk[b], P[b],
+//             the per-chunk factors and the O staging may be reused)
+namespace pipe {
+constexpr int NTP = 384;
+constexpr uint32_t X0 = 0;              // [k; q] -> [Lk; Lq], chunk parity 0 (32 KB); parity 1 at X0 + 32768
+constexpr uint32_t V_ = 65536;          // v tile per parity (16 KB each)
+constexpr uint32_t G_ = 98304;          // g fp32 [64][128] -> G (log2 units) (32 KB)
+constexpr uint32_t RK0 = 131072;        // Rk (Kb on the exact path) per parity (16 KB each); O staging after G7
+constexpr uint32_t P0 = 163840;         // P per parity (8 KB each)
+constexpr uint32_t T_ = 180224;         // T (8 KB)
+constexpr uint32_t A_ = 188416;         // A fp32 (16 KB)
+constexpr uint32_t DV = 204800;         // solve scratch: D_0..D_3, M_10, M_32 (7.5 KB)
+constexpr uint32_t YV = 212992;         // solve scratch: Y blocks (5 KB)
+constexpr uint32_t SMALL = 218112;      // per-row / per-channel vectors, barriers, counters (6 KB)
+constexpr uint32_t SMEM = SMALL + 6144 + 1024;
+constexpr uint32_t ID_KK128 = idesc_bf16(128, 128, 0, 0);
+// TMEM columns
+constexpr uint32_t T_S = 0, T_SB = 128, T_X = 192, T_O = 256, T_U0 = 320, T_AP = 448;  // U0 parity b at 320 + 64 b
+// X and O are adjacent: G4 and G5 are one MMA group with N = 128 (B = [W'; Lq])
+}  // namespace pipe
+
+// Bounded wait that also gives up once the other warp group has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > WAIT_LIMIT) {
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+    return true;
+}
+// OR of `pred` over the `n` threads of named barrier `id` (also a barrier).
+__device__ __forceinline__ bool group_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+template <int GM>
+__global__ void __launch_bounds__(pipe::NTP, 1)
+    prefill_tc_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                           const float *__restrict__ g_head, const float *__restrict__ beta, const float *s_init,
+                           float *s_final, __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens,
+                           int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
+    using namespace pipe;
+    constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
+    constexpr int BAR_PREP = 1, BAR_SOLVE = 3, BAR_CHAIN = 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *s_rq = reinterpret_cast<float *>(sm + SMALL);
+    float *s_rk = s_rq + 64;
+    float *s_beta = s_rk + 64;
+    float *s_gl = s_beta + 64;      // G at the chunk's last row (natural log)
+    float *s_c = s_gl + 128;        // anchor c
+    float *s_g1 = s_c + 128;        // per-head gate: g per row, then G per row (log2 units)
+    float *s_sigp = s_g1 + 64;      // sigma of the chunk prep finished last
+    float *s_sf = s_sigp + 128;     // [2][128] S~ factor e^c sigma_old, per chunk parity
+    float *s_pf = s_sf + 256;       // [2][128] rescale of the stored state before G7
+    float *s_sig = s_pf + 256;      // [2][128] sigma after the chunk
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_sig + 256);
+    uint64_t *bar_qk = bars;        // [2]
+    uint64_t *bar_g = bars + 2;
+    uint64_t *bar_v = bars + 3;     // [2]
+    uint64_t *bar_mp = bars + 5;    // prep MMA commits
+    uint64_t *bar_c45 = bars + 6;   // [2]
+    uint64_t *bar_c67 = bars + 8;
+    uint64_t *bar_ready = bars + 9; // [2]
+    uint64_t *bar_ofree = bars + 11;// [2]
+    volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(bars + 13);
+    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + 14);
+    // TMA barriers qk0, qk1, g, v0, v1: phases armed and phases waited for, so
+    // that an aborted launch can let every copy in flight land before exiting
+    uint32_t *s_armed = reinterpret_cast<uint32_t *>(bars + 15);
+    uint32_t *s_waited = s_armed + 5;
+    float *gt = reinterpret_cast<float *>(sm + G_);
+    float *Am = reinterpret_cast<float *>(sm + A_);
+    float *Dv = reinterpret_cast<float *>(sm + DV);
+    float *Yv = reinterpret_cast<float *>(sm + YV);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q4 = warp & 3, hh = (warp >> 2) & 1;
+    const bool is_prep = tid < 256;
+    const int h = blockIdx.x % H, n = order ? order[blockIdx.x / H] : (int)(blockIdx.x / H);
+    int64_t start, end;
+    if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
+    const int x0 = h * D;
+    const int nchunks = (int)((end - start + C - 1) / C);
+
+    auto issue_qk = [&](int y, int b) {
+        uint8_t *xb = sm + X0 + 32768 * b;
+        s_armed[b] += 1;
+        mbar_arrive_expect_tx(bar_qk + b, QK_BYTES);
+        tma_load_2d(xb, &tm_k, bar_qk + b, x0, y);
+        tma_load_2d(xb + 16384, &tm_k, bar_qk + b, x0 + 64, y);
+        tma_load_2d(xb + 8192, &tm_q, bar_qk + b, x0, y);
+        tma_load_2d(xb + 24576, &tm_q, bar_qk + b, x0 + 64, y);
+    };
+    auto issue_g = [&](int y) {
+        s_armed[2] += 1;
+        mbar_arrive_expect_tx(bar_g, G_BYTES);
+        tma_load_2d(sm + G_, &tm_g, bar_g, x0, y);
+    };
+    auto issue_v = [&](int y, int b) {
+        s_armed[3 + b] += 1;
+        mbar_arrive_expect_tx(bar_v + b, V_BYTES);
+        tma_load_2d(sm + V_ + 16384 * b, &tm_v, bar_v + b, x0, y);
+        tma_load_2d(sm + V_ + 16384 * b + 8192, &tm_v, bar_v + b, x0 + 64, y);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < 13; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < 10; ++i) s_armed[i] = 0u;
+        *s_abort = 0u;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        if constexpr (GCH) tma_prefetch_desc(&tm_g);
+        if (nchunks > 0) {
+            issue_qk((int)start, 0);
+            if constexpr (GCH) issue_g((int)start);
+            issue_v((int)start, 0);
+        }
+        if (nchunks > 1) issue_qk((int)(start + C), 1);
+    }
+    if (tid < 128) s_sigp[tid] = 1.f;
+    if (warp == 0) {
+        tmem_alloc(s_taddr, 512);
+        tmem_relinquish();
+    }
+    sync_tc();
+    const uint32_t tbase = *s_taddr;
+    const uint32_t lrow = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
+    const uint32_t sbase = smem_u32(sm);
+    const int jl = 32 * q4 + lane;                    // this thread's TMEM lane (channel)
+    const size_t soff = ((size_t)n * H + h) * D * D;
+    bool ok = true;
+
+    if (is_prep) {
+        // ============================ prep: warps 0-7 ============================
+        uint32_t ph_mp = 0;
+        bool pend_mp = false;
+        float beta_reg = 0.f, gh_reg = 0.f;  // next chunk's beta / per-head gate, loaded one chunk ahead
+        if (tid < C && start + tid < end) {
+            beta_reg = beta[(size_t)(start + tid) * H + h];
+            if constexpr (GHD) gh_reg = g_head[(size_t)(start + tid) * H + h];
+        }
+        for (int ci = 0; ci < nchunks; ++ci) {
+            const int b = ci & 1;
+            const int64_t c0 = start + (int64_t)ci * C;
+            const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
+            const bool has_next = ci + 1 < nchunks;
+            uint8_t *xb = sm + X0 + 32768 * b;
+            const uint32_t xs = sbase + X0 + 32768 * b;
+            bool got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
+                       (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
+                       wait_or_abort(bar_v + b, (ci >> 1) & 1, s_abort) &&
+                       (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
+            if (group_or(BAR_PREP, 256, !got)) {
+                ok = false;
+                break;
+            }
+            if (tid == 0) {
+                s_waited[b] += 1;
+                if constexpr (GCH) s_waited[2] += 1;
+                s_waited[3 + b] += 1;
+                // V of the other parity was last read by G3 of chunk ci - 1, which has completed
+                if (has_next) issue_v((int)(c0 + C), b ^ 1);
+            }
+            if (tid < C) {
+                s_beta[tid] = beta_reg;
+                if constexpr (GHD) s_g1[tid] = gh_reg;
+            }
+            if (L < C) {  // rows past the end of the sequence contribute nothing
+                const uint4 z4 = make_uint4(0, 0, 0, 0);
+                for (int p = tid; p < (C - L) * 16; p += 256) {
+                    const int r = L + (p >> 4), cc = p & 15;
+                    *reinterpret_cast<uint4 *>(xb + swz(r, cc, 128)) = z4;
+                    *reinterpret_cast<uint4 *>(xb + swz(r + 64, cc, 128)) = z4;
+                    *reinterpret_cast<uint4 *>(sm + V_ + 16384 * b + swz(r, cc, 64)) = z4;
+                }
+                if constexpr (GCH)
+                    for (int p = tid; p < (C - L) * 32; p += 256)
+                        *reinterpret_cast<uint4 *>(sm + G_ + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
+            }
+            named_bar_sync(BAR_PREP, 256);
+
+            // threads 0-127: L2 norms; 128-255: cumulative decay
+            bool bad = false;
+            if (tid < 128) {
+                const int r = tid & 63;
+                const int row = tid < 64 ? r + 64 : r;  // q rows follow the k rows
+                float ss = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 16; ++cc) {
+                    float f[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(xb + swz(row, cc, 128)), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss += f[e] * f[e];
+                }
+                (tid < 64 ? s_rq : s_rk)[r] = inv_norm(ss, eps);
+            } else if constexpr (GCH) {
+                const int i = tid - 128;
+                float gv[64];
+#pragma unroll
+                for (int r = 0; r < 64; ++r) gv[r] = gt[r * 128 + i];
+#pragma unroll
+                for (int r = 1; r < 64; ++r) gv[r] += gv[r - 1];
+                const float GL = gv[63];
+                bad = !(gv[0] - GL <= SPAN_MAX);
+#pragma unroll
+                for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
+                s_gl[i] = GL;
+            } else if constexpr (GHD) {
+                if (warp == 4) {
+                    const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
+                    float incl = g0 + g1;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const float G1v = incl, G0v = incl - g1;
+                    const float GL = __shfl_sync(0xffffffffu, incl, 31);
+                    const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
+                    bad = !(Gfirst - GL <= SPAN_MAX);
+                    s_g1[2 * lane] = G0v * LOG2E;
+                    s_g1[2 * lane + 1] = G1v * LOG2E;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
+                }
+            } else {
+                s_gl[tid - 128] = 0.f;
+            }
+            const bool exact = GNO ? (named_bar_sync(BAR_PREP, 256), false) : group_or(BAR_PREP, 256, bad);
+            // per-channel anchor and state scale (see the sequential kernel)
+            if (tid < 128) {
+                const float GL = s_gl[tid], so = s_sigp[tid];
+                const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
+                const float ec = expf(c);
+                const float sn = exact ? 1.f : expf(GL - c);
+                s_c[tid] = c;
+                s_sf[128 * b + tid] = ec * so;
+                s_pf[128 * b + tid] = exact ? expf(GL) * so : ec * so;
+                s_sig[128 * b + tid] = sn;
+                s_sigp[tid] = sn;
+            }
+            named_bar_sync(BAR_PREP, 256);
+
+            uint8_t *pb = sm + P0 + 8192 * b;
+            if (exact) {  // A and P with exact pairwise decays
+                for (int p = tid; p < C * C; p += 256) {
+                    const int r = p & 63, s = p >> 6;
+                    float a = 0.f, pq = 0.f;
+                    if (s <= r) {
+                        const float rkr = s_rk[r], rks = s_rk[s], rqr = s_rq[r];
+                        for (int cc = 0; cc < 16; ++cc) {
+                            float kr[8], ks[8], qr[8];
+                            unpack8(*reinterpret_cast<const uint4 *>(xb + swz(r, cc, 128)), kr);
+                            unpack8(*reinterpret_cast<const uint4 *>(xb + swz(s, cc, 128)), ks);
+                            unpack8(*reinterpret_cast<const uint4 *>(xb + swz(r + 64, cc, 128)), qr);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int i = cc * 8 + e;
+                                float x = ks[e] * rks;
+                                if constexpr (GCH) x *= ex2(gt[r * 128 + i] - gt[s * 128 + i]);
+                                a += kr[e] * rkr * x;
+                                pq += qr[e] * rqr * x;
+                            }
+                        }
+                    }
+                    if constexpr (GHD) {
+                        const float f = s <= r ? ex2(s_g1[r] - s_g1[s]) : 0.f;
+                        a *= f;
+                        pq *= f;
+                    }
+                    Am[fsw(r, s >> 2) + (s & 3)] = (s < r) ? s_beta[r] * a : 0.f;
+                    *reinterpret_cast<__nv_bfloat16 *>(pb + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) + (s & 7) * 2) =
+                        __float2bfloat16_rn(pq);
+                }
+                named_bar_sync(BAR_PREP, 256);
+            }
+
+            // operand tiles: [Lk; Lq] in place, and Rk (Kb on the exact path)
+            uint8_t *rkb = sm + RK0 + 16384 * b;
+            {
+                const int cc = tid & 15, rb = tid >> 4;
+                float cv[8], glv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    cv[e] = s_c[GCH ? cc * 8 + e : 0] * LOG2E;
+                    glv[e] = s_gl[GCH ? cc * 8 + e : 0] * LOG2E;
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int r = rb + 16 * m;
+                    const uint32_t ok_ = swz(r, cc, 128), oq = swz(r + 64, cc, 128);
+                    float qf[8], kf[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(xb + oq), qf);
+                    unpack8(*reinterpret_cast<const uint4 *>(xb + ok_), kf);
+                    const float rq = s_rq[r], rk = s_rk[r];
+                    float G[8];
+                    if constexpr (GCH) {
+                        const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
+                        const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
+                        G[0] = ga.x; G[1] = ga.y; G[2] = ga.z; G[3] = ga.w;
+                        G[4] = gb.x; G[5] = gb.y; G[6] = gb.z; G[7] = gb.w;
+                    } else {
+                        const float gr = GHD ? s_g1[r] : 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) G[e] = gr;
+                    }
+                    float lk[8], lq[8], rkv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float kh = kf[e] * rk, qh = qf[e] * rq;
+                        if constexpr (GNO) {
+                            lk[e] = kh;
+                            lq[e] = qh;
+                            rkv[e] = kh;
+                        } else {
+                            const float e1 = ex2(G[e] - cv[e]);
+                            lk[e] = e1 * kh;
+                            lq[e] = e1 * qh;
+                            rkv[e] = (exact ? ex2(glv[e] - G[e]) : ex2(cv[e] - G[e])) * kh;
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(xb + ok_) = pack8(lk);
+                    *reinterpret_cast<uint4 *>(xb + oq) = pack8(lq);
+                    *reinterpret_cast<uint4 *>(rkb + swz(r, cc, 64)) = pack8(rkv);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(BAR_PREP, 256);
+            tc_fence_after();
+
+            if (tid < C) {
+                const bool in = has_next && c0 + C + tid < end;
+                beta_reg = in ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
+                if constexpr (GHD) gh_reg = in ? g_head[(size_t)(c0 + C + tid) * H + h] : 0.f;
+            }
+            // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T; g of this chunk is consumed
+            if (tid == 0) {
+                if constexpr (GCH)
+                    if (has_next) issue_g((int)(c0 + C));
+                if (!exact) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
+                        mma_bf16(tbase + T_AP, sdesc_sw128(xs + kb * 16384 + ko, 16, 1024),
+                                 sdesc_sw128(sbase + RK0 + 16384 * b + kb * 8192 + ko, 16, 1024), ID_KK64, ks > 0);
+                    }
+                    mma_commit(bar_mp);
+                }
+            }
+            pend_mp = !exact;
+            // warps 0-3: A read-back and solve; warps 4-7: P read-back
+            got = true;
+            if (!exact) {
+                got = wait_or_abort(bar_mp, ph_mp, s_abort);
+                tc_fence_after();
+            }
+            if (warp < 4) {
+                if (!exact && got && q4 < 2) {  // A: TMEM lanes 0-63, masked (s < r), times beta
+                    const int r = 32 * q4 + lane;
+                    const float br = s_beta[r];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r32[32];
+                        tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int g4 = 0; g4 < 8; ++g4) {
+                            float4 a4;
+                            const int sc = 32 * half + 4 * g4;
+                            a4.x = (sc + 0 < r) ? br * __uint_as_float(r32[4 * g4 + 0]) : 0.f;
+                            a4.y = (sc + 1 < r) ? br * __uint_as_float(r32[4 * g4 + 1]) : 0.f;
+                            a4.z = (sc + 2 < r) ? br * __uint_as_float(r32[4 * g4 + 2]) : 0.f;
+                            a4.w = (sc + 3 < r) ? br * __uint_as_float(r32[4 * g4 + 3]) : 0.f;
+                            *reinterpret_cast<float4 *>(Am + fsw(r, sc >> 2)) = a4;
+                        }
+                    }
+                }
+                named_bar_sync(BAR_SOLVE, 128);
+                // M^-1 = (I + A)^-1 with A strictly lower, by 16 x 16 blocks.
+                // Step 1: warp S inverts the diagonal block, D_S = (I + A_SS)^-1, by
+                // forward substitution (lane = column; lanes 16-31 repeat 0-15).
+                {
+                    const int S = warp, b0 = 16 * S, cl = lane & 15;
+                    float x[16];
+    #pragma unroll
+                    for (int rl = 0; rl < 16; ++rl) x[rl] = (rl == cl) ? 1.f : 0.f;
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float4 a4[16];
+    #pragma unroll
+                        for (int rl = 4 * j + 1; rl < 16; ++rl)
+                            a4[rl] = *reinterpret_cast<const float4 *>(Am + fsw(b0 + rl, 4 * S + j));
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int kl = 4 * j + e;
+    #pragma unroll
+                            for (int rl = kl + 1; rl < 16; ++rl) {
+                                const float a = e == 0 ? a4[rl].x : e == 1 ? a4[rl].y : e == 2 ? a4[rl].z : a4[rl].w;
+                                x[rl] = fmaf(-a, x[kl], x[rl]);
+                            }
+                        }
+                    }
+                    if (lane < 16) {
+                        const int s = b0 + cl;
+                        const float bs = s_beta[s];
+                        __nv_bfloat16 *tcol = reinterpret_cast<__nv_bfloat16 *>(sm + T_) + (s & 7);
+    #pragma unroll
+                        for (int rl = 0; rl < 16; ++rl) {
+                            const int r = b0 + rl;
+                            Dv[S * BLK + rl * LDB + cl] = x[rl];
+                            tcol[r * 64 + (((s >> 3) ^ (r & 7)) << 3)] = __float2bfloat16_rn(x[rl] * bs);
+                        }
+                    }
+                    const uint4 z4 = make_uint4(0, 0, 0, 0);
+                    for (int R = 0; R < S; ++R) {  // T blocks above the diagonal are zero
+                        const int r = 16 * R + (lane >> 1), cc = 2 * S + (lane & 1);
+                        *reinterpret_cast<uint4 *>(sm + T_ + r * 128 + ((cc ^ (r & 7)) << 4)) = z4;
+                    }
+                }
+                named_bar_sync(BAR_SOLVE, 128);
+                // Step 2, by doubling: M_10 = -D_1 A_10 D_0 and M_32 = -D_3 A_32 D_2
+                // (warps 0, 1) while warps 2, 3 start Y_RS = sum_K A_RK M_KS for the
+                // lower-left 32 x 32 block (R = 2, 3) with the parts that need no M_10.
+                // Step 3 adds A_R1 M_10; step 4: M_2S = -D_2 Y_2S, M_3S = -(M_32 Y_2S + D_3 Y_3S).
+                {
+                    const int g = lane >> 2, tg = lane & 3;
+                    // 16 x 16 block products on m16n8k8 tf32 tiles; X row-major with row stride LDB
+                    auto a_blk = [&](const float *X, int kk, uint32_t (&a)[4]) {
+                        a[0] = to_tf32(X[g * LDB + 8 * kk + tg]);
+                        a[1] = to_tf32(X[(g + 8) * LDB + 8 * kk + tg]);
+                        a[2] = to_tf32(X[g * LDB + 8 * kk + tg + 4]);
+                        a[3] = to_tf32(X[(g + 8) * LDB + 8 * kk + tg + 4]);
+                    };
+                    auto a_am = [&](int R, int K, int kk, uint32_t (&a)[4]) {
+                        const int k4 = 4 * K + 2 * kk, r0 = 16 * R + g;
+                        a[0] = to_tf32(Am[fsw(r0, k4) + tg]);
+                        a[1] = to_tf32(Am[fsw(r0 + 8, k4) + tg]);
+                        a[2] = to_tf32(Am[fsw(r0, k4 + 1) + tg]);
+                        a[3] = to_tf32(Am[fsw(r0 + 8, k4 + 1) + tg]);
+                    };
+                    auto b_blk = [&](const float *X, int kk, int nt, uint32_t (&b)[2]) {
+                        b[0] = to_tf32(X[(8 * kk + tg) * LDB + 8 * nt + g]);
+                        b[1] = to_tf32(X[(8 * kk + tg + 4) * LDB + 8 * nt + g]);
+                    };
+                    // acc += A_RK (from Am) * X
+                    auto mm_am = [&](float (&acc)[2][4], int R, int K, const float *X) {
+    #pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            uint32_t a[4];
+                            a_am(R, K, kk, a);
+    #pragma unroll
+                            for (int nt = 0; nt < 2; ++nt) {
+                                uint32_t b[2];
+                                b_blk(X, kk, nt, b);
+                                mma_tf32_16x8x8(acc[nt], a, b);
+                            }
+                        }
+                    };
+                    // acc += Xa * Xb (both row-major blocks)
+                    auto mm_blk = [&](float (&acc)[2][4], const float *Xa, const float *Xb) {
+    #pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            uint32_t a[4];
+                            a_blk(Xa, kk, a);
+    #pragma unroll
+                            for (int nt = 0; nt < 2; ++nt) {
+                                uint32_t b[2];
+                                b_blk(Xb, kk, nt, b);
+                                mma_tf32_16x8x8(acc[nt], a, b);
+                            }
+                        }
+                    };
+                    auto st_blk = [&](float *X, const float (&c)[2][4]) {
+    #pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            *reinterpret_cast<float2 *>(X + g * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][0], c[nt][1]);
+                            *reinterpret_cast<float2 *>(X + (g + 8) * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][2], c[nt][3]);
+                        }
+                    };
+                    // T_RS = -c Diag(beta_S) as bf16 pairs
+                    auto st_t = [&](int R, int S, const float (&c)[2][4]) {
+    #pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const int s = 16 * S + 8 * nt + 2 * tg;
+                            const float b0s = -s_beta[s], b1s = -s_beta[s + 1];
+    #pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const int r = 16 * R + g + 8 * hf;
+                                *reinterpret_cast<__nv_bfloat162 *>(sm + T_ + r * 128 + (((s >> 3) ^ (r & 7)) << 4) +
+                                                                    (s & 7) * 2) =
+                                    __floats2bfloat162_rn(c[nt][2 * hf] * b0s, c[nt][2 * hf + 1] * b1s);
+                            }
+                        }
+                    };
+                    const float *D0 = Dv, *D1 = Dv + BLK, *D2 = Dv + 2 * BLK, *D3 = Dv + 3 * BLK;
+                    float *M10 = Dv + 4 * BLK, *M32 = Dv + 5 * BLK;
+                    float *Y20 = Yv, *Y21 = Yv + BLK, *Y30 = Yv + 2 * BLK, *Y31 = Yv + 3 * BLK;
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    float y1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    if (warp < 2) {
+                        const int R = warp == 0 ? 1 : 3;  // block (R, R-1)
+                        mm_am(acc, R, R - 1, warp == 0 ? D0 : D2);
+                        uint32_t yb[2][2][2];
+                        c_to_b(acc, yb, lane);
+                        const float *dr = warp == 0 ? D1 : D3;
+                        float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    #pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            uint32_t a[4];
+                            a_blk(dr, kk, a);
+    #pragma unroll
+                            for (int nt = 0; nt < 2; ++nt) mma_tf32_16x8x8(z[nt], a, yb[kk][nt]);
+                        }
+                        st_t(R, R - 1, z);  // T = -z Diag(beta)
+    #pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e) z[nt][e] = -z[nt][e];
+                        st_blk(warp == 0 ? M10 : M32, z);
+                    } else {
+                        const int R = warp;  // 2 or 3
+                        mm_am(acc, R, 1, D1);              // Y_R1 = A_R1 D_1 (final)
+                        st_blk(R == 2 ? Y21 : Y31, acc);
+                        mm_am(y1, R, 0, D0);               // Y_R0 partial: A_R0 D_0
+                    }
+                    named_bar_sync(BAR_SOLVE, 128);
+                    if (warp >= 2) {
+                        const int R = warp;
+                        mm_am(y1, R, 1, M10);              // Y_R0 += A_R1 M_10
+                        st_blk(R == 2 ? Y20 : Y30, y1);
+                    }
+                    named_bar_sync(BAR_SOLVE, 128);
+                    {
+                        // warp 0: (2,0), 1: (2,1), 2: (3,0), 3: (3,1)
+                        const int R = 2 + (warp >> 1), S = warp & 1;
+                        const float *y2 = S == 0 ? Y20 : Y21;
+                        float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        if (R == 2) {
+                            mm_blk(z, D2, y2);
+                        } else {
+                            mm_blk(z, M32, y2);
+                            mm_blk(z, D3, S == 0 ? Y30 : Y31);
+                        }
+                        st_t(R, S, z);
+                    }
+                }
+            } else if (!exact && got && q4 >= 2) {  // P: TMEM lanes 64-127, masked (s <= r)
+                const int r = 32 * (q4 - 2) + lane;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
+                    tmem_ld_wait();
+                    float pv[32];
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) pv[m] = (32 * half + m <= r) ? __uint_as_float(r32[m]) : 0.f;
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) {
+                        const int cc = 4 * half + qd;
+                        *reinterpret_cast<uint4 *>(pb + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(pv + 8 * qd);
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            if (group_or(BAR_PREP, 256, !got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (!exact) {
+                ph_mp ^= 1;
+                pend_mp = false;
+            }
+
+            // G2: W'^T = Lk^T T^T (over A/P in TMEM),  G3: U0^T = V^T T^T
+            if (tid == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bd = sdesc_sw128(sbase + T_ + ks * 32, 16, 1024);
+                    mma_bf16(tbase + T_AP, sdesc_sw128(xs + ks * 2048, 16384, 1024), bd, ID_MK64, ks > 0);
+                    mma_bf16(tbase + T_U0 + 64 * b, sdesc_sw128(sbase + V_ + 16384 * b + ks * 2048, 8192, 1024), bd,
+                             ID_MK64, ks > 0);
+                }
+                mma_commit(bar_mp);
+            }
+            pend_mp = true;
+            got = wait_or_abort(bar_mp, ph_mp, s_abort);
+            tc_fence_after();
+            if (group_or(BAR_PREP, 256, !got)) {
+                ok = false;
+                break;
+            }
+            ph_mp ^= 1;
+            pend_mp = false;
+            // W'^T (lane i, column r) -> W' rows r over the Lk rows of this chunk's
+            // tile (dead after G2), so that [W'; Lq] is one K-major operand of G4/G5
+            {
+                uint32_t r32[32];
+                tmem_ld32(tbase + lrow + T_AP + 32 * hh, r32);
+                tmem_ld_wait();
+                const int i = jl;
+                __nv_bfloat16 *wcol = reinterpret_cast<__nv_bfloat16 *>(xb + (i >> 6) * 16384) + (i & 7);
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int r = 32 * hh + m;
+                    wcol[r * 64 + (((((i & 63) >> 3)) ^ (r & 7)) << 3)] = __float2bfloat16_rn(__uint_as_float(r32[m]));
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(BAR_PREP, 256);
+            if (tid == 0) mbar_arrive(bar_ready + b);
+        }
+        if (!ok) {  // let this group's own MMAs land before shared memory goes away
+            *s_abort = 1u;
+            if (pend_mp) mbar_wait(bar_mp, ph_mp, WAIT_LIMIT);
+        }
+    } else {
+        // ============================ chain: warps 8-11 ===========================
+        const int ct = tid - 256;  // 0..127
+        // initial state -> TMEM (S^T: lane j, column i); sigma = 1
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            uint32_t r[32];
+#pragma unroll
+            for (int m = 0; m < 32; ++m)
+                r[m] = s_init ? __float_as_uint(s_init[soff + (size_t)(32 * part + m) * D + jl]) : 0u;
+            tmem_st32(tbase + lrow + T_S + 32 * part, r);
+        }
+        tmem_st_wait();
+        uint32_t ph67 = 0;
+        bool pend67 = false;
+        int pend45 = -1;  // chunk whose G4/G5 are issued but not yet waited for
+        int last_b = -1;
+        for (int ci = 0; ci < nchunks; ++ci) {
+            const int b = ci & 1;
+            const int64_t c0 = start + (int64_t)ci * C;
+            const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
+            bool got = wait_or_abort(bar_ready + b, (ci >> 1) & 1, s_abort);
+            if (group_or(BAR_CHAIN, 128, !got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // S = Diag(sigma) S_st. S~^T = S_st^T Diag(sf) -> TMEM bf16 pairs; S_st^T <- S_st^T Diag(pf)
+            const float *sf = s_sf + 128 * b, *pf = s_pf + 128 * b;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                uint32_t r[2][32], pk[32];
+                tmem_ld32(tbase + lrow + T_S + 64 * kb, r[0]);
+                tmem_ld32(tbase + lrow + T_S + 64 * kb + 32, r[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const int i0 = 64 * kb + 32 * part;
+#pragma unroll
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        const float4 fc = GCH ? *reinterpret_cast<const float4 *>(sf + i0 + 4 * g4)
+                                              : make_float4(sf[0], sf[0], sf[0], sf[0]);
+                        const float4 fl = GCH ? *reinterpret_cast<const float4 *>(pf + i0 + 4 * g4)
+                                              : make_float4(pf[0], pf[0], pf[0], pf[0]);
+                        const float fcv[4] = {fc.x, fc.y, fc.z, fc.w}, flv[4] = {fl.x, fl.y, fl.z, fl.w};
+                        float so[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sv = __uint_as_float(r[part][4 * g4 + e]);
+                            so[e] = sv * fcv[e];
+                            r[part][4 * g4 + e] = __float_as_uint(sv * flv[e]);
+                        }
+                        __nv_bfloat162 t0 = __floats2bfloat162_rn(so[0], so[1]);
+                        __nv_bfloat162 t1 = __floats2bfloat162_rn(so[2], so[3]);
+                        pk[16 * part + 2 * g4] = *reinterpret_cast<uint32_t *>(&t0);
+                        pk[16 * part + 2 * g4 + 1] = *reinterpret_cast<uint32_t *>(&t1);
+                    }
+                    tmem_st32(tbase + lrow + T_S + i0, r[part]);
+                }
+                tmem_st32(tbase + lrow + T_SB + 32 * kb, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            named_bar_sync(BAR_CHAIN, 128);
+            tc_fence_after();
+            // G4 + G5 in one group: [X^T | O^T] = S~^T [W'; Lq]^T
+            if (ct == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
+                    mma_bf16_ts(tbase + T_X, tbase + T_SB + 8 * ks,
+                                sdesc_sw128(sbase + X0 + 32768 * b + kb * 16384 + ko, 16, 1024), ID_KK128, ks > 0);
+                }
+                mma_commit(bar_c45 + b);
+            }
+            pend45 = ci;
+            got = wait_or_abort(bar_c45 + b, (ci >> 1) & 1, s_abort);
+            if (group_or(BAR_CHAIN, 128, !got)) {
+                ok = false;
+                break;
+            }
+            pend45 = -1;
+            tc_fence_after();
+            // this chunk's [W'; Lq] tile is consumed: load the chunk two ahead into it
+            if (ct == 0 && ci + 2 < nchunks) issue_qk((int)(c0 + 2 * C), b);
+            // U^T = U0^T - X^T -> bf16 pairs in TMEM over S~ (dead after G4/G5)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t u0[32], x[32], pk[16];
+                tmem_ld32(tbase + lrow + T_U0 + 64 * b + 32 * half, u0);
+                tmem_ld32(tbase + lrow + T_X + 32 * half, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(u0[2 * m]) - __uint_as_float(x[2 * m]),
+                                                             __uint_as_float(u0[2 * m + 1]) - __uint_as_float(x[2 * m + 1]));
+                    pk[m] = *reinterpret_cast<uint32_t *>(&t);
+                }
+                tmem_st16(tbase + lrow + T_SB + 16 * half, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            named_bar_sync(BAR_CHAIN, 128);
+            tc_fence_after();
+            // G6: O^T += U^T P^T,  G7: S_st^T += U^T Rk (Kb on the exact path)
+            if (ct == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t a = tbase + T_SB + 8 * ks;
+                    mma_bf16_ts(tbase + T_O, a, sdesc_sw128(sbase + P0 + 8192 * b + ks * 32, 16, 1024), ID_KK64, 1);
+                    mma_bf16_ts(tbase + T_S, a, sdesc_sw128(sbase + RK0 + 16384 * b + ks * 2048, 8192, 1024),
+                                ID_KM128, 1);
+                }
+                mma_commit(bar_c67);
+            }
+            pend67 = true;
+            got = wait_or_abort(bar_c67, ph67, s_abort);
+            if (group_or(BAR_CHAIN, 128, !got)) {
+                ok = false;
+                break;
+            }
+            ph67 ^= 1;
+            pend67 = false;
+            tc_fence_after();
+            // O^T (lane j, column r) -> staging [r][j] bf16 over Rk -> 16-byte stores of whole rows
+            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + RK0 + 16384 * b);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t o32[32];
+                tmem_ld32(tbase + lrow + T_O + 32 * half, o32);
+                tmem_ld_wait();
+#pragma unroll
+                for (int m = 0; m < 32; ++m)
+                    ost[(32 * half + m) * D + jl] = __float2bfloat16_rn(__uint_as_float(o32[m]));
+            }
+            tc_fence_before();
+            named_bar_sync(BAR_CHAIN, 128);
+            // staging -> registers, release the chunk's buffers, then the global stores
+            // (an arrive after the stores would wait for them: it has release semantics)
+            uint4 orow[8];
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+                const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
+                orow[k8] = *reinterpret_cast<const uint4 *>(sm + RK0 + 16384 * b + r * 256 + c16 * 16);
+            }
+            named_bar_sync(BAR_CHAIN, 128);
+            if (ct == 0) mbar_arrive(bar_ofree + b);
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+                const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
+                if (r < L) *reinterpret_cast<uint4 *>(out + ((size_t)(c0 + r) * H + h) * D + c16 * 8) = orow[k8];
+            }
+            last_b = b;
+        }
+        if (ok && s_final) {  // S = Diag(sigma) S_st
+            const float *sg = last_b >= 0 ? s_sig + 128 * last_b : nullptr;
+#pragma unroll
+            for (int part = 0; part < 4; ++part) {
+                uint32_t r[32];
+                tmem_ld32(tbase + lrow + T_S + 32 * part, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int m = 0; m < 32; ++m)
+                    s_final[soff + (size_t)(32 * part + m) * D + jl] =
+                        __uint_as_float(r[m]) * (sg ? sg[32 * part + m] : 1.f);
+            }
+        }
+        if (!ok) {
+            *s_abort = 1u;
+            if (pend45 >= 0) mbar_wait(bar_c45 + (pend45 & 1), (pend45 >> 1) & 1, WAIT_LIMIT);
+            if (pend67) mbar_wait(bar_c67, ph67, WAIT_LIMIT);
+        }
+    }
+    if (!ok && (tid == 0 || tid == 256)) atomicOr(err, DEVERR_TIMEOUT);
+    sync_tc();
+    // after an abort: every copy still in flight must land before exit
+    if (tid == 0 && *s_abort) {
+        uint64_t *tb[5] = {bar_qk, bar_qk + 1, bar_g, bar_v, bar_v + 1};
+        for (int i = 0; i < 5; ++i)
+            for (uint32_t w = s_waited[i]; w < s_armed[i]; ++w)
+                if (!mbar_wait(tb[i], w & 1, WAIT_LIMIT)) break;
+    }
+    sync_tc();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -927,17 +1754,32 @@ bool prefill_tc_applicable(const PrefillArgs &a) {
     return a.bf16 && a.D == 128 && a.C == 64 && a.T > 0 && a.T <= 0x7fffffffLL;
 }
 
+// Which kernel runs each gate form, by measurement on the 4K workload. The
+// pipelined kernel wins where the state-independent work is light (per-head
+// gate: 0.382 vs 0.472 ms; no gate: 0.353 vs 0.400 ms). With a per-channel
+// gate its prep warps (per-channel scan, g tile) become the bottleneck and the
+// sequential kernel is faster (0.473 vs 0.496 ms).
 template <int GM>
 static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
                             const CUtensorMap &mv, const CUtensorMap &mg, cudaStream_t s) {
     using namespace tcp;
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_tc_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    prefill_tc_kernel<GM><<<(unsigned)a.N * a.H, NT, SMEM_BYTES, s>>>(
-        mq, mk, mv, mg, GM == KDA_GATE_HEAD ? a.g : nullptr, a.beta, a.s_init, a.s_final,
-        static_cast<__nv_bfloat16 *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
-    return check_launch("prefill_tc_kernel");
+    const float *gh = GM == KDA_GATE_HEAD ? a.g : nullptr;
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out);
+    if constexpr (GM != KDA_GATE_CHANNEL) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_pipe_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)pipe::SMEM);
+        if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+        prefill_tc_pipe_kernel<GM><<<(unsigned)a.N * a.H, pipe::NTP, pipe::SMEM, s>>>(
+            mq, mk, mv, mg, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
+        return check_launch("prefill_tc_pipe_kernel");
+    } else {
+        cudaError_t e =
+            cudaFuncSetAttribute(prefill_tc_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+        prefill_tc_kernel<GM><<<(unsigned)a.N * a.H, NT, SMEM_BYTES, s>>>(
+            mq, mk, mv, mg, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
+        return check_launch("prefill_tc_kernel");
+    }
 }
 
 kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s) {
