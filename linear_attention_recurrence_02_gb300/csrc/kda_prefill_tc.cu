@@ -946,6 +946,7 @@ template <int GM>
 __global__ void __launch_bounds__(pipe::NTP, 1)
     prefill_tc_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                           const __grid_constant__ CUtensorMap tm_o,
                            const float *__restrict__ g_head, const float *__restrict__ beta, const float *s_init,
                            float *s_final, __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens,
                            int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
@@ -1545,6 +1546,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
         tmem_st_wait();
         uint32_t ph67 = 0;
         bool pend67 = false;
+        int ofree_due = -1;  // chunk whose buffers wait for its bulk output store to finish reading them
         int pend45 = -1;  // chunk whose G4/G5 are issued but not yet waited for
         int last_b = -1;
         for (int ci = 0; ci < nchunks; ++ci) {
@@ -1557,6 +1559,15 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 break;
             }
             tc_fence_after();
+            // the previous chunk's bulk output store has had a whole prep phase to
+            // read its staging: release that chunk's buffers now
+            if (ofree_due >= 0) {
+                if (ct == 0) {
+                    bulk_wait_read();
+                    mbar_arrive(bar_ofree + (ofree_due & 1));
+                }
+                ofree_due = -1;
+            }
             // S = Diag(sigma) S_st. S~^T = S_st^T Diag(sf) -> TMEM bf16 pairs; S_st^T <- S_st^T Diag(pf)
             const float *sf = s_sf + 128 * b, *pf = s_pf + 128 * b;
 #pragma unroll
@@ -1654,35 +1665,54 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             ph67 ^= 1;
             pend67 = false;
             tc_fence_after();
-            // O^T (lane j, column r) -> staging [r][j] bf16 over Rk -> 16-byte stores of whole rows
-            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + RK0 + 16384 * b);
+            // O^T (lane j, column r) -> staging over Rk: two [64 rows][64 channels] bf16 boxes
+            uint8_t *ost = sm + RK0 + 16384 * b;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t o32[32];
                 tmem_ld32(tbase + lrow + T_O + 32 * half, o32);
                 tmem_ld_wait();
+                __nv_bfloat16 *col = reinterpret_cast<__nv_bfloat16 *>(ost + (jl >> 6) * 8192) + (jl & 63);
 #pragma unroll
-                for (int m = 0; m < 32; ++m)
-                    ost[(32 * half + m) * D + jl] = __float2bfloat16_rn(__uint_as_float(o32[m]));
+                for (int m = 0; m < 32; ++m) col[(32 * half + m) * 64] = __float2bfloat16_rn(__uint_as_float(o32[m]));
             }
+            fence_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_CHAIN, 128);
-            // staging -> registers, release the chunk's buffers, then the global stores
-            // (an arrive after the stores would wait for them: it has release semantics)
-            uint4 orow[8];
+            if (L == C) {
+                // a whole chunk: one bulk store per 64-channel box; the buffers are
+                // released once the copy engine has read the staging (next chunk)
+                if (ct == 0) {
+                    tma_store_2d(&tm_o, ost, x0, (int)c0);
+                    tma_store_2d(&tm_o, ost + 8192, x0 + 64, (int)c0);
+                    bulk_commit();
+                }
+                ofree_due = ci;
+            } else {
+                // a sequence's short last chunk: plain stores of its rows only (the rows
+                // after it belong to the next sequence)
+                uint4 orow[8];
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-                const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
-                orow[k8] = *reinterpret_cast<const uint4 *>(sm + RK0 + 16384 * b + r * 256 + c16 * 16);
-            }
-            named_bar_sync(BAR_CHAIN, 128);
-            if (ct == 0) mbar_arrive(bar_ofree + b);
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
+                    orow[k8] = *reinterpret_cast<const uint4 *>(ost + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16);
+                }
+                named_bar_sync(BAR_CHAIN, 128);
+                if (ct == 0) mbar_arrive(bar_ofree + b);
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-                const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
-                if (r < L) *reinterpret_cast<uint4 *>(out + ((size_t)(c0 + r) * H + h) * D + c16 * 8) = orow[k8];
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
+                    if (r < L) *reinterpret_cast<uint4 *>(out + ((size_t)(c0 + r) * H + h) * D + c16 * 8) = orow[k8];
+                }
             }
             last_b = b;
+        }
+        if (ct == 0) {
+            if (ofree_due >= 0) {
+                bulk_wait_read();
+                mbar_arrive(bar_ofree + (ofree_due & 1));
+            }
+            bulk_wait_all();  // output copies complete before the CTA's shared memory goes away
         }
         if (ok && s_final) {  // S = Diag(sigma) S_st
             const float *sg = last_b >= 0 ? s_sig + 128 * last_b : nullptr;
@@ -1766,11 +1796,16 @@ static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const C
     const float *gh = GM == KDA_GATE_HEAD ? a.g : nullptr;
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out);
     if constexpr (GM != KDA_GATE_CHANNEL) {
+        // the pipelined kernel stores whole output chunks through this map
+        CUtensorMap mo;
+        if (!make_map(&mo, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.H * D, (uint64_t)a.T, 64, 64,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+            return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_pipe_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)pipe::SMEM);
         if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
         prefill_tc_pipe_kernel<GM><<<(unsigned)a.N * a.H, pipe::NTP, pipe::SMEM, s>>>(
-            mq, mk, mv, mg, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
+            mq, mk, mv, mg, mo, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
         return check_launch("prefill_tc_pipe_kernel");
     } else {
         cudaError_t e =
