@@ -4,6 +4,8 @@
 #include <cstdio>
 #include <string>
 
+#include <atomic>
+
 #include "kda_common.cuh"
 
 namespace kda {
@@ -65,11 +67,22 @@ kda_status check_launch(const char *what) {
 __device__ unsigned g_device_error_word;
 
 unsigned *device_error_word() {
+    // looked up once per device (the calling thread's current device)
+    static std::atomic<unsigned *> cache[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        unsigned *c = cache[dev].load(std::memory_order_acquire);
+        if (c) return c;
+    } else {
+        cudaGetLastError();
+        dev = -1;
+    }
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
+    if (dev >= 0) cache[dev].store(static_cast<unsigned *>(p), std::memory_order_release);
     return static_cast<unsigned *>(p);
 }
 
