@@ -147,3 +147,35 @@ def test_prefill_gated_full_size_sampled_heads(env, gate):
     ro, rs = oracle.recurrence(sub["q"], sub["k"], sub["v"], go, sub["beta"], nthreads=8)
     assert_close(to_np(out)[:, heads], ro, True, (1,), "out")
     assert_close(to_np(sf)[:, heads], rs, True, (0, 1), "final state")
+
+
+@pytest.mark.parametrize("gate", ["channel", "head", "none"])
+@pytest.mark.parametrize("bf16", [True, False])
+def test_fused_decode_many_heads_sampled(env, gate, bf16):
+    """A launch of many waves (12 sequences x 128 heads, d = 128) takes the
+    register-resident fused kernel (small launches take the shared-memory
+    staged one); eight sampled (sequence, head) units are checked against the
+    oracle, including the rings they shift."""
+    torch, kda = env
+    B, H, D = 12, 128, 128
+    d = synth.decode_inputs(360 + bf16, B, H, D, bf16, s0_std=0.5)
+    gk, go = _gate_inputs(d["g"], gate)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    ring = to_dev(d["ring"], dt, torch)
+    ts = to_dev(d["s0"], torch.float32, torch)
+    out = torch.empty((B, H, D), dtype=dt, device="cuda")
+    kda.kda_shortconv_decode_step_gated(to_dev(d["x"], dt, torch), ring, to_dev(d["w"], torch.float32, torch),
+                                        None if gk is None else to_dev(gk, torch.float32, torch),
+                                        to_dev(d["beta"], torch.float32, torch), ts, out, gate=gate)
+    torch.cuda.synchronize()
+    got_o, got_s, got_r = to_np(out), to_np(ts), to_np(ring)
+    for (bb, hh) in [(0, 0), (0, 127), (5, 64), (11, 1), (11, 126), (3, 33), (7, 99), (9, 77)]:
+        x1 = d["x"][bb:bb + 1, :, hh:hh + 1]
+        r1 = d["ring"][bb:bb + 1, :, hh:hh + 1]
+        w1 = d["w"][:, hh:hh + 1]
+        y, rr = oracle.shortconv_step(x1, r1, w1)
+        ro, rs = oracle.decode_step(y[:, 0], y[:, 1], y[:, 2], go[bb:bb + 1, hh:hh + 1],
+                                    d["beta"][bb:bb + 1, hh:hh + 1], d["s0"][bb:bb + 1, hh:hh + 1])
+        assert_close(got_o[bb:bb + 1, hh:hh + 1], ro, bf16, (0, 1), f"out {(bb, hh)}")
+        assert_close(got_s[bb:bb + 1, hh:hh + 1], rs, bf16, (0, 1), f"state {(bb, hh)}")
+        np.testing.assert_array_equal(got_r[bb, :, hh], rr[0, :, 0])
