@@ -267,6 +267,18 @@ kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v
  * KDA_ERR_TIMEOUT, KDA_ERR_CUDA for an asynchronous CUDA error, else KDA_OK. */
 kda_status kda_sync_status(kda_stream_t stream);
 
+/*
+ * Diagnostic of the failure reporting, not part of the method. Launches one
+ * CTA whose thread 0 waits on a shared-memory mbarrier that nothing ever
+ * completes, with the same clock-bounded wait the tensor-core kernels use,
+ * limited to `limit_cycles` SM clock cycles (1 .. 2e9). The wait gives up,
+ * sets the device error word and the kernel returns, so the next
+ * kda_sync_status on the stream reports KDA_ERR_TIMEOUT and the context
+ * stays usable. Lets a caller check, on its own GPU, that an expired wait
+ * is reported instead of hanging.
+ */
+kda_status kda_selftest_bounded_wait(long long limit_cycles, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -7,6 +7,7 @@
 #include <atomic>
 
 #include "kda_common.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -114,6 +115,29 @@ extern "C" size_t kda_state_bytes(int layers, int heads, int dk, int dv) {
 extern "C" size_t kda_shortconv_ring_bytes(int layers, int batch, int heads, int d, int elem_bytes) {
     if (layers < 0 || batch < 0 || heads < 0 || d < 0 || elem_bytes < 0) return 0;
     return (size_t)layers * (size_t)batch * (size_t)heads * 3u * 3u * (size_t)d * (size_t)elem_bytes;
+}
+
+namespace kda {
+// One mbarrier that nothing completes; thread 0 waits on it with the bounded wait.
+__global__ void selftest_wait_kernel(long long limit, unsigned *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+        if (!tc::mbar_wait(&bar, 0, limit)) atomicOr(err, DEVERR_TIMEOUT);
+    }
+}
+}  // namespace kda
+
+extern "C" kda_status kda_selftest_bounded_wait(long long limit_cycles, kda_stream_t stream) {
+    clear_detail();
+    if (limit_cycles < 1 || limit_cycles > 2000000000LL) return invalid("limit_cycles must be in 1 .. 2e9");
+    kda_status st = bind_stream_device(stream);
+    if (st != KDA_OK) return st;
+    unsigned *err = device_error_word();
+    if (!err) return fail(KDA_ERR_CUDA, "device error word unavailable");
+    selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_cycles, err);
+    return check_launch("selftest_wait_kernel");
 }
 
 extern "C" kda_status kda_sync_status(kda_stream_t stream) {

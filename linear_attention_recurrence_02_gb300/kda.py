@@ -70,6 +70,7 @@ _SIGNATURES = {
     "kda_chunk_prefill_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci,
                                    _ci, _cf, _vp], _ci),
     "kda_sync_status": ([_vp], _ci),
+    "kda_selftest_bounded_wait": ([ctypes.c_longlong, _vp], _ci),
 }
 
 
@@ -269,6 +270,14 @@ def kda_chunk_prefill_noalloc(q, k, v, g, beta, out, initial_state=None, final_s
     _check(lib().kda_chunk_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
                                            _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
                                            _dtype_code(q), float(l2_eps), _stream(stream, q.device)))
+
+
+def kda_selftest_bounded_wait(limit_cycles=2_000_000, stream=None, device=None):
+    """Launch the bounded-wait diagnostic (a wait nothing completes); the next
+    kda_sync_status on the stream then raises with KDA_ERR_TIMEOUT."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(lib().kda_selftest_bounded_wait(int(limit_cycles), _stream(stream, dev)))
 
 
 def kda_sync_status(stream=None, device=None):

@@ -212,3 +212,10 @@ def test_gate_none_needs_no_g_but_others_do(kda):
     st = L.kda_chunk_prefill_gated(0x10000, 0x20000, 0x30000, None, None, None, None, 0x60000, None, 1, 100,
                                    4, 128, 64, 1, kda.KDA_GATE_NONE, 1e-6, None, 0, None)
     assert st == kda.KDA_ERR_INVALID_ARG and "beta is NULL" in L.kda_last_error_detail().decode()
+
+
+def test_selftest_rejects_bad_limit(kda):
+    L = kda.lib()
+    for bad in (0, -5, 3_000_000_000):
+        assert L.kda_selftest_bounded_wait(bad, None) == kda.KDA_ERR_INVALID_ARG
+        assert "limit_cycles" in L.kda_last_error_detail().decode()
