@@ -432,8 +432,35 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
         gates[name] = {"value": ws * toks / (gms * 1e-3), "unit": "tokens/s", "ms_per_call": gms,
                        "roofline_hbm": {"achieved": gby / (gms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                                         "frac": gby / (gms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": gby}}
+    # the same workload in fp32, which runs the CUDA-core (reference-grade) kernel
+    simt = None
+    try:
+        q32, k32, v32 = (t_.float() for t_ in (q, k, v))
+        o32 = torch.empty_like(q32)
+
+        def scall():
+            kda.kda_chunk_prefill(q32, k32, v32, g, beta, o32, final_state=sf, chunk_size=C, workspace=wsb,
+                                  stream=stream)
+        for _ in range(2):
+            scall()
+        torch.cuda.synchronize(dev)
+        se = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+        for a0, b0 in se:
+            a0.record(stream)
+            scall()
+            b0.record(stream)
+        torch.cuda.synchronize(dev)
+        sms = max_over_ranks(statistics.mean(a0.elapsed_time(b0) for a0, b0 in se), dev)
+        sby = T * H * (3 * D * 4 + D * 4 + 4 + D * 4) + H * D * D * 4
+        simt = {"value": ws * toks / (sms * 1e-3), "unit": "tokens/s", "ms_per_call": sms,
+                "kernel": "prefill_simt_kernel (fp32 q/k/v/out)",
+                "roofline_hbm": {"achieved": sby / (sms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                                 "frac": sby / (sms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": sby}}
+        del q32, k32, v32, o32
+    except kda.KdaError as e:
+        simt = {"unavailable": str(e)}
     return {"value": ws * toks / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "varlen": varlen,
-            "conv": conv, "gates": gates,
+            "conv": conv, "gates": gates, "fp32": simt,
             "config": {"workload": f"chunked prefill T={T}, H={H}, d={D}, C={C}, bf16 q/k/v, zero S0, "
                                    "fp32 final state", "calls": n},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
