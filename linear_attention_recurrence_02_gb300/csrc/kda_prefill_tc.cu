@@ -34,6 +34,7 @@
 // of its sequence; thread 0 issues TMA and MMAs, every wait is bounded.
 #include <cuda.h>
 
+#include <atomic>
 #include <cstring>
 #include <string>
 
@@ -902,6 +903,12 @@ __global__ void __launch_bounds__(NT, 1)
 //             the per-chunk factors and the O staging may be reused)
 namespace pipe {
 constexpr int NTP = 384;
+// Register split between the warp groups (setmaxnreg): the prep warpgroups grow
+// to PREP_REGS, the chain warpgroup shrinks to CHAIN_REGS. The shares must add
+// up to exactly what the CTA was launched with, 8 * PREP + 4 * CHAIN = 12 * R
+// (R = registers per thread at launch, 168 for 384 threads), or the grow would
+// wait for registers that never come; the host checks this before launching.
+constexpr int PREP_REGS = 184, CHAIN_REGS = 136;
 constexpr uint32_t X0 = 0;              // [k; q] -> [Lk; Lq], chunk parity 0 (32 KB); parity 1 at X0 + 32768
 constexpr uint32_t V_ = 65536;          // v tile per parity (16 KB each)
 constexpr uint32_t G_ = 98304;          // g fp32 [64][128] -> G (log2 units) (32 KB)
@@ -1045,6 +1052,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     bool ok = true;
 
     if (is_prep) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PREP_REGS));
         // ============================ prep: warps 0-7 ============================
         uint32_t ph_mp = 0;
         bool pend_mp = false;
@@ -1532,6 +1540,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             if (pend_mp) mbar_wait(bar_mp, ph_mp, WAIT_LIMIT);
         }
     } else {
+        // first instruction of the chain warps: hand registers to the prep warps
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CHAIN_REGS));
         // ============================ chain: warps 8-11 ===========================
         const int ct = tid - 256;  // 0..127
         // initial state -> TMEM (S^T: lane j, column i); sigma = 1
@@ -1784,37 +1794,37 @@ bool prefill_tc_applicable(const PrefillArgs &a) {
     return a.bf16 && a.D == 128 && a.C == 64 && a.T > 0 && a.T <= 0x7fffffffLL;
 }
 
-// Which kernel runs each gate form, by measurement on the 4K workload. The
-// pipelined kernel wins where the state-independent work is light (per-head
-// gate: 0.382 vs 0.472 ms; no gate: 0.353 vs 0.400 ms). With a per-channel
-// gate its prep warps (per-channel scan, g tile) become the bottleneck and the
-// sequential kernel is faster (0.473 vs 0.496 ms).
+// The pipelined kernel runs every gate form (4K workload, per-channel gate:
+// 0.420 ms against 0.473 ms for the sequential kernel).
 template <int GM>
 static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
                             const CUtensorMap &mv, const CUtensorMap &mg, cudaStream_t s) {
     using namespace tcp;
     const float *gh = GM == KDA_GATE_HEAD ? a.g : nullptr;
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out);
-    if constexpr (GM != KDA_GATE_CHANNEL) {
-        // the pipelined kernel stores whole output chunks through this map
-        CUtensorMap mo;
-        if (!make_map(&mo, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.H * D, (uint64_t)a.T, 64, 64,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
-            return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_pipe_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)pipe::SMEM);
-        if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-        prefill_tc_pipe_kernel<GM><<<(unsigned)a.N * a.H, pipe::NTP, pipe::SMEM, s>>>(
-            mq, mk, mv, mg, mo, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
-        return check_launch("prefill_tc_pipe_kernel");
-    } else {
-        cudaError_t e =
-            cudaFuncSetAttribute(prefill_tc_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-        prefill_tc_kernel<GM><<<(unsigned)a.N * a.H, NT, SMEM_BYTES, s>>>(
-            mq, mk, mv, mg, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
-        return check_launch("prefill_tc_kernel");
+    // the kernel stores whole output chunks through this map
+    CUtensorMap mo;
+    if (!make_map(&mo, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.H * D, (uint64_t)a.T, 64, 64,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+        return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    // the register split only adds up for the launch register count it was made for
+    static std::atomic<int> regs_ok{0};  // 0 unknown, 1 checked, -1 mismatch
+    if (regs_ok.load(std::memory_order_acquire) == 0) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_pipe_kernel<GM>);
+        if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncGetAttributes: ") + cudaGetErrorString(e));
+        const bool okr = 8 * pipe::PREP_REGS + 4 * pipe::CHAIN_REGS == 12 * fa.numRegs &&
+                         pipe::CHAIN_REGS <= fa.numRegs && fa.numRegs <= pipe::PREP_REGS;
+        regs_ok.store(okr ? 1 : -1, std::memory_order_release);
     }
+    if (regs_ok.load(std::memory_order_acquire) < 0)
+        return fail(KDA_ERR_UNSUPPORTED, "prefill kernel built with a register count its warp split was not made for");
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_pipe_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)pipe::SMEM);
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    prefill_tc_pipe_kernel<GM><<<(unsigned)a.N * a.H, pipe::NTP, pipe::SMEM, s>>>(
+        mq, mk, mv, mg, mo, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
+    return check_launch("prefill_tc_pipe_kernel");
 }
 
 kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s) {
