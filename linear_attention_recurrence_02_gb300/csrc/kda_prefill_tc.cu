@@ -27,11 +27,15 @@
 // (key channel i or value channel j) throughout, and the fp32 state S_st^T
 // (lane j, column i) never leaves TMEM between chunks. Operands are bf16 in
 // 128-byte-swizzled shared memory tiles, loaded by TMA (q, k, v, g) or
-// written by the CUDA cores from TMEM read-backs. TMA drops k and q into one
-// 128-row tile that becomes [Lk; Lq] in place.
+// written by the CUDA cores from TMEM read-backs; S~^T and U^T go back to
+// TMEM as bf16 pairs and feed G4-G7 as the A operand. TMA drops k and q into
+// one 128-row tile that becomes [Lk; Lq] in place; W' is later read back over
+// its dead Lk rows, so G4 and G5 are one MMA group over [W'; Lq].
 //
-// One CTA (256 threads, 2 warpgroups) per (sequence, head) walks the chunks
-// of its sequence; thread 0 issues TMA and MMAs, every wait is bounded.
+// One CTA (384 threads) per (sequence, head) walks the chunks of its
+// sequence with two warp groups: eight "prep" warps run the state-independent
+// work of chunk c + 1 while four "chain" warps run the state chain of chunk c
+// (see the pipelined kernel below). Every wait is bounded.
 #include <cuda.h>
 
 #include <atomic>
@@ -47,27 +51,9 @@ namespace tcp {
 
 using namespace tc;
 
-constexpr int C = 64, D = 128, NT = 256;
-// shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_X = 0;           // k rows 0-63 + q rows 64-127 (TMA) -> [Lk; Lq] in place
-constexpr uint32_t OFF_V = 32768;       // v tile (TMA, prefetched after G3)
-constexpr uint32_t OFF_G = 49152;       // g fp32 [64][128] (TMA, prefetched) -> cumulative G (log2 units)
-constexpr uint32_t OFF_RK = 81920;      // Rk (Kb on the exact path), 64 rows; kept until G7
-constexpr uint32_t OFF_OST = OFF_RK;    // O staging [64][128] bf16 once G7 has read Rk
-constexpr uint32_t OFF_T = 131072;      // T 64 rows (r) x 64 (s)
-constexpr uint32_t OFF_P = 139264;      // P 64 rows (r) x 64 (s)
-constexpr uint32_t OFF_A = 147456;      // A fp32 [64][64] row-major swizzled -> W' (rows i)
-constexpr uint32_t OFF_W = OFF_A;
-constexpr uint32_t OFF_U = 163840;      // solve scratch: Y blocks (5 KiB); bytes 98304-131071 are unused
-constexpr uint32_t OFF_Y = 180224;      // solve scratch: six 16 x 16 fp32 blocks (7.5 KiB)
-constexpr int LDB = 20, BLK = 16 * LDB;  // block row stride (bank-conflict free A fragments), block size
-constexpr uint32_t OFF_SMALL = 188416;  // per-row / per-channel vectors, barriers
-constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;
+constexpr int C = 64, D = 128;
+constexpr int LDB = 20, BLK = 16 * LDB;  // solve scratch: block row stride (bank-conflict free A fragments), block size
 constexpr uint32_t QK_BYTES = 2 * 16384, G_BYTES = 32768, V_BYTES = 16384;
-// TMEM columns (512 allocated)
-constexpr uint32_t TM_S = 0, TM_AP = 128, TM_W = 192, TM_U0 = 256, TM_X = 320, TM_O = 384, TM_SB = 448;
-// TM_SB: S~^T as bf16 pairs (A operand of G4, G5); U^T as bf16 pairs goes to
-// TM_W once W' has been read back (A operand of G6, G7)
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 // Anchored factors stay within e^[-ANCHOR, ANCHOR] when the chunk's decay
 // span is at most SPAN_MAX; the fp32 state kept as S / sigma then stays
@@ -76,7 +62,6 @@ constexpr float ANCHOR = 40.f, SPAN_MAX = 2.f * ANCHOR;
 
 constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_MK64 = idesc_bf16(128, 64, 1, 0);
-constexpr uint32_t ID_KM64 = idesc_bf16(128, 64, 0, 1);
 constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, 0, 1);
 
 // byte offset of 16-byte chunk cc (channels 8cc..8cc+7) of `row` in a
@@ -160,737 +145,8 @@ __device__ __forceinline__ void sync_tc() {
     tc_fence_after();
 }
 
-__device__ __forceinline__ void sync_for_mma() {
-    fence_async_smem();
-    sync_tc();
-}
 
-// GM: gate form (kda_gate). Per channel: g arrives as an fp32 TMA tile and is
-// scanned per channel. Per head: one float per token is prefetched like beta
-// and scanned by one warp. None: no decay factors at all (G = 0, c = 0).
-template <int GM>
-__global__ void __launch_bounds__(NT, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                      const float *__restrict__ g_head, const float *__restrict__ beta, const float *s_init,
-                      float *s_final, __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens,
-                      int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
-    constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *s_rq = reinterpret_cast<float *>(sm + OFF_SMALL);
-    float *s_rk = s_rq + 64;
-    float *s_beta = s_rk + 64;
-    float *s_gl = s_beta + 64;      // G at the chunk's last row (natural log)
-    float *s_c = s_gl + 128;        // anchor c
-    float *s_sf = s_c + 128;        // S~ factor e^c sigma_old
-    float *s_pf = s_sf + 128;       // rescale of the stored state before G7 accumulates
-    float *s_sigma = s_pf + 128;    // per-channel scale: S = Diag(sigma) S_stored
-    float *s_g1 = s_sigma + 128;    // per-head gate: g per row, then G per row (log2 units)
-    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(s_g1 + 64);
-    uint64_t *bar_g = bar_qk + 1;
-    uint64_t *bar_v = bar_qk + 2;
-    uint64_t *bar_mma = bar_qk + 3;
-    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bar_qk + 4);
-    float *gt = reinterpret_cast<float *>(sm + OFF_G);
-    float *Am = reinterpret_cast<float *>(sm + OFF_A);   // A[r][s] at fsw(r, s/4) + s%4
-    // solve scratch: 16 x 16 fp32 blocks, row stride LDB: D_0..D_3, M_10, M_32 in
-    // Dv; Y_20, Y_21, Y_30, Y_31 in Yv
-    float *Dv = reinterpret_cast<float *>(sm + OFF_Y);
-    float *Yv = reinterpret_cast<float *>(sm + OFF_U);
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q4 = warp & 3, hh = warp >> 2;
-    const int h = blockIdx.x % H, n = order ? order[blockIdx.x / H] : (int)(blockIdx.x / H);
-    int64_t start, end;
-    if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
-    const int x0 = h * D;
-
-    // q, k land in one 128-row tile: k in rows 0-63, q in rows 64-127
-    auto issue_qk = [&](int y) {
-        mbar_arrive_expect_tx(bar_qk, QK_BYTES);
-        tma_load_2d(sm + OFF_X, &tm_k, bar_qk, x0, y);
-        tma_load_2d(sm + OFF_X + 16384, &tm_k, bar_qk, x0 + 64, y);
-        tma_load_2d(sm + OFF_X + 8192, &tm_q, bar_qk, x0, y);
-        tma_load_2d(sm + OFF_X + 24576, &tm_q, bar_qk, x0 + 64, y);
-    };
-    auto issue_g = [&](int y) {
-        mbar_arrive_expect_tx(bar_g, G_BYTES);
-        tma_load_2d(sm + OFF_G, &tm_g, bar_g, x0, y);
-    };
-    auto issue_v = [&](int y) {
-        mbar_arrive_expect_tx(bar_v, V_BYTES);
-        tma_load_2d(sm + OFF_V, &tm_v, bar_v, x0, y);
-        tma_load_2d(sm + OFF_V + 8192, &tm_v, bar_v, x0 + 64, y);
-    };
-
-    if (tid == 0) {
-        mbar_init(bar_qk, 1);
-        mbar_init(bar_g, 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_mma, 1);
-        fence_mbar_init();
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        if constexpr (GCH) tma_prefetch_desc(&tm_g);
-        if (start < end) {
-            issue_qk((int)start);
-            if constexpr (GCH) issue_g((int)start);
-            issue_v((int)start);
-        }
-    }
-    if (tid < 128) s_sigma[tid] = 1.f;
-    if (warp == 0) {
-        tmem_alloc(s_taddr, 512);
-        tmem_relinquish();
-    }
-    sync_tc();
-    const uint32_t tbase = *s_taddr;
-    const uint32_t lrow = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
-    const uint32_t sbase = smem_u32(sm);
-    const int jl = 32 * q4 + lane;                    // this thread's TMEM lane (channel)
-    const size_t soff = ((size_t)n * H + h) * D * D;
-
-    // initial state -> TMEM (S^T: lane j, column i); sigma = 1
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-        uint32_t r[32];
-        const int i0 = 64 * hh + 32 * part;
-#pragma unroll
-        for (int m = 0; m < 32; ++m)
-            r[m] = s_init ? __float_as_uint(s_init[soff + (size_t)(i0 + m) * D + jl]) : 0u;
-        tmem_st32(tbase + lrow + TM_S + i0, r);
-    }
-    tmem_st_wait();
-
-    uint32_t ph = 0, ph_mma = 0;
-    bool ok = true;
-    bool pend_g = false, pend_qkv = false;  // next chunk's loads in flight (phase ph ^ 1)
-    float beta_reg = 0.f;  // beta of the next chunk, loaded one chunk ahead
-    float gh_reg = 0.f;    // per-head gate of the next chunk, likewise
-    if (tid < C && start + tid < end) {
-        beta_reg = beta[(size_t)(start + tid) * H + h];
-        if constexpr (GHD) gh_reg = g_head[(size_t)(start + tid) * H + h];
-    }
-    for (int64_t c0 = start; c0 < end; c0 += C, ph ^= 1) {
-        const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
-        const bool has_next = c0 + C < end;
-        sync_for_mma();  // previous chunk fully consumed
-        if (tid < C) {
-            s_beta[tid] = beta_reg;
-            if constexpr (GHD) s_g1[tid] = gh_reg;
-        }
-        bool got = mbar_wait(bar_qk, ph, WAIT_LIMIT) && (!GCH || mbar_wait(bar_g, ph, WAIT_LIMIT)) &&
-                   mbar_wait(bar_v, ph, WAIT_LIMIT);
-        if (__syncthreads_or(!got)) {
-            mbar_wait(bar_qk, ph, WAIT_LIMIT);
-            if constexpr (GCH) mbar_wait(bar_g, ph, WAIT_LIMIT);
-            mbar_wait(bar_v, ph, WAIT_LIMIT);
-            ok = false;
-            break;
-        }
-        pend_g = pend_qkv = false;
-
-        // rows past the end of the sequence: zero q, k, v, g (so beta = 0,
-        // k = 0 and G stays at G_{L-1}); they then contribute nothing
-        if (L < C) {
-            const uint4 z4 = make_uint4(0, 0, 0, 0);
-            for (int p = tid; p < (C - L) * 16; p += NT) {
-                const int r = L + (p >> 4), cc = p & 15;
-                *reinterpret_cast<uint4 *>(sm + OFF_X + swz(r, cc, 128)) = z4;
-                *reinterpret_cast<uint4 *>(sm + OFF_X + swz(r + 64, cc, 128)) = z4;
-                *reinterpret_cast<uint4 *>(sm + OFF_V + swz(r, cc, 64)) = z4;
-            }
-            if constexpr (GCH)
-                for (int p = tid; p < (C - L) * 32; p += NT)
-                    *reinterpret_cast<uint4 *>(sm + OFF_G + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
-            __syncthreads();
-        }
-
-        // warps 0-3: L2 norms, one thread per q or k row; warps 4-7: cumulative
-        // log decay G along the chunk, one channel per thread in registers,
-        // stored back in log2 units
-        int bad = 0;
-        if (tid < 128) {
-            const int r = tid & 63;
-            const int row = tid < 64 ? r + 64 : r;  // q rows follow the k rows
-            float ss = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) {
-                float f[8];
-                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(row, cc, 128)), f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss += f[e] * f[e];
-            }
-            (tid < 64 ? s_rq : s_rk)[r] = inv_norm(ss, eps);
-        } else if constexpr (GCH) {
-            const int i = tid - 128;
-            float gv[64];
-#pragma unroll
-            for (int r = 0; r < 64; ++r) gv[r] = gt[r * 128 + i];
-#pragma unroll
-            for (int r = 1; r < 64; ++r) gv[r] += gv[r - 1];
-            const float GL = gv[63];
-            bad = !(gv[0] - GL <= SPAN_MAX);
-#pragma unroll
-            for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
-            s_gl[i] = GL;
-        } else if constexpr (GHD) {
-            // one warp: inclusive scan of 64 per-row gates, two rows per lane
-            if (warp == 4) {
-                const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
-                float incl = g0 + g1;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const float G1 = incl, G0 = incl - g1;
-                const float GL = __shfl_sync(0xffffffffu, incl, 31);
-                const float Gfirst = __shfl_sync(0xffffffffu, G0, 0);
-                bad = !(Gfirst - GL <= SPAN_MAX);
-                s_g1[2 * lane] = G0 * LOG2E;
-                s_g1[2 * lane + 1] = G1 * LOG2E;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
-            }
-        } else {
-            s_gl[tid - 128] = 0.f;
-        }
-        int exact = 0;  // never with no gate (no decay span)
-        if constexpr (GNO) __syncthreads();
-        else exact = __syncthreads_or(bad);
-        // per-channel anchor and state scale: sigma_new = e^{G_L - c} on the
-        // anchored path (then G7 can use Rk as is), 1 on the exact path
-        if (tid < 128) {
-            const float GL = s_gl[tid], so = s_sigma[tid];
-            const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
-            const float ec = expf(c);
-            s_c[tid] = c;
-            s_sf[tid] = ec * so;
-            s_pf[tid] = exact ? expf(GL) * so : ec * so;
-            s_sigma[tid] = exact ? 1.f : expf(GL - c);
-        }
-        __syncthreads();
-
-        if (exact) {
-            // A and P with exact pairwise decays (rare: decay span G_0 - G_L > SPAN_MAX),
-            // from the raw q, k before they are overwritten in place
-            for (int p = tid; p < C * C; p += NT) {
-                const int r = p & 63, s = p >> 6;
-                float a = 0.f, pq = 0.f;
-                if (s <= r) {
-                    const float rkr = s_rk[r], rks = s_rk[s], rqr = s_rq[r];
-                    for (int cc = 0; cc < 16; ++cc) {
-                        float kr[8], ks[8], qr[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(r, cc, 128)), kr);
-                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(s, cc, 128)), ks);
-                        unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + swz(r + 64, cc, 128)), qr);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = cc * 8 + e;
-                            float x = ks[e] * rks;
-                            if constexpr (GCH) x *= ex2(gt[r * 128 + i] - gt[s * 128 + i]);
-                            a += kr[e] * rkr * x;
-                            pq += qr[e] * rqr * x;
-                        }
-                    }
-                }
-                if constexpr (GHD) {  // one decay factor for every channel
-                    const float f = s <= r ? ex2(s_g1[r] - s_g1[s]) : 0.f;
-                    a *= f;
-                    pq *= f;
-                }
-                Am[fsw(r, s >> 2) + (s & 3)] = (s < r) ? s_beta[r] * a : 0.f;
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_P + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) +
-                                                   (s & 7) * 2) = __float2bfloat16_rn(pq);
-            }
-            __syncthreads();
-        }
-
-        // operand tiles: [Lk; Lq] in place over [k; q], and Rk (Kb on the
-        // exact path); each thread keeps one 8-channel group and walks 4 rows
-        {
-            const int cc = tid & 15, rb = tid >> 4;
-            float cv[8], glv[8];  // anchor and G_L in log2 units (one value without a per-channel gate)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                cv[e] = s_c[GCH ? cc * 8 + e : 0] * LOG2E;
-                glv[e] = s_gl[GCH ? cc * 8 + e : 0] * LOG2E;
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = rb + 16 * m;
-                const uint32_t ok_ = swz(r, cc, 128), oq = swz(r + 64, cc, 128);
-                float qf[8], kf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + oq), qf);
-                unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_X + ok_), kf);
-                const float rq = s_rq[r], rk = s_rk[r];
-                float G[8];
-                if constexpr (GCH) {
-                    const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
-                    const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
-                    G[0] = ga.x; G[1] = ga.y; G[2] = ga.z; G[3] = ga.w;
-                    G[4] = gb.x; G[5] = gb.y; G[6] = gb.z; G[7] = gb.w;
-                } else {
-                    const float gr = GHD ? s_g1[r] : 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) G[e] = gr;
-                }
-                float lk[8], lq[8], rkv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float kh = kf[e] * rk, qh = qf[e] * rq;
-                    if constexpr (GNO) {
-                        lk[e] = kh;
-                        lq[e] = qh;
-                        rkv[e] = kh;
-                    } else {
-                        const float e1 = ex2(G[e] - cv[e]);
-                        lk[e] = e1 * kh;
-                        lq[e] = e1 * qh;
-                        rkv[e] = (exact ? ex2(glv[e] - G[e]) : ex2(cv[e] - G[e])) * kh;  // Kb or Rk (<= e^ANCHOR)
-                    }
-                }
-                *reinterpret_cast<uint4 *>(sm + OFF_X + ok_) = pack8(lk);
-                *reinterpret_cast<uint4 *>(sm + OFF_X + oq) = pack8(lq);
-                *reinterpret_cast<uint4 *>(sm + OFF_RK + swz(r, cc, 64)) = pack8(rkv);
-            }
-        }
-        sync_for_mma();
-
-        if (tid < C) {
-            const bool in = has_next && c0 + C + tid < end;
-            beta_reg = in ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
-            if constexpr (GHD) gh_reg = in ? g_head[(size_t)(c0 + C + tid) * H + h] : 0.f;
-        }
-        // g of this chunk is consumed: prefetch the next chunk's.
-        // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T
-        if (tid == 0) {
-            if constexpr (GCH)
-                if (has_next) issue_g((int)(c0 + C));
-            if (!exact) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                    mma_bf16(tbase + TM_AP, sdesc_sw128(sbase + OFF_X + kb * 16384 + ko, 16, 1024),
-                             sdesc_sw128(sbase + OFF_RK + kb * 8192 + ko, 16, 1024), ID_KK64, ks > 0);
-                }
-                mma_commit(bar_mma);
-            }
-        }
-        pend_g = GCH && has_next;
-        // Warps 0-3 wait for G1, read back A and solve for T. Meanwhile warps
-        // 4-7 convert the state operand (independent of G1), then read back P.
-        bool got_mma = true;
-        if (warp < 4) {
-            if (!exact) {
-                got_mma = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-                tc_fence_after();
-                if (q4 < 2) {  // A: TMEM lanes 0-63, masked (s < r), times beta
-                    const int r = 32 * q4 + lane;
-                    const float br = s_beta[r];
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t r32[32];
-                        tmem_ld32(tbase + lrow + TM_AP + 32 * half, r32);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int g4 = 0; g4 < 8; ++g4) {
-                            float4 a4;
-                            const int sc = 32 * half + 4 * g4;
-                            a4.x = (sc + 0 < r) ? br * __uint_as_float(r32[4 * g4 + 0]) : 0.f;
-                            a4.y = (sc + 1 < r) ? br * __uint_as_float(r32[4 * g4 + 1]) : 0.f;
-                            a4.z = (sc + 2 < r) ? br * __uint_as_float(r32[4 * g4 + 2]) : 0.f;
-                            a4.w = (sc + 3 < r) ? br * __uint_as_float(r32[4 * g4 + 3]) : 0.f;
-                            *reinterpret_cast<float4 *>(Am + fsw(r, sc >> 2)) = a4;
-                        }
-                    }
-                }
-            }
-            named_bar_sync(1, 128);
-            // M^-1 = (I + A)^-1 with A strictly lower, by 16 x 16 blocks.
-            // Step 1: warp S inverts the diagonal block, D_S = (I + A_SS)^-1, by
-            // forward substitution (lane = column; lanes 16-31 repeat 0-15).
-            {
-                const int S = warp, b0 = 16 * S, cl = lane & 15;
-                float x[16];
-#pragma unroll
-                for (int rl = 0; rl < 16; ++rl) x[rl] = (rl == cl) ? 1.f : 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float4 a4[16];
-#pragma unroll
-                    for (int rl = 4 * j + 1; rl < 16; ++rl)
-                        a4[rl] = *reinterpret_cast<const float4 *>(Am + fsw(b0 + rl, 4 * S + j));
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int kl = 4 * j + e;
-#pragma unroll
-                        for (int rl = kl + 1; rl < 16; ++rl) {
-                            const float a = e == 0 ? a4[rl].x : e == 1 ? a4[rl].y : e == 2 ? a4[rl].z : a4[rl].w;
-                            x[rl] = fmaf(-a, x[kl], x[rl]);
-                        }
-                    }
-                }
-                if (lane < 16) {
-                    const int s = b0 + cl;
-                    const float bs = s_beta[s];
-                    __nv_bfloat16 *tcol = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_T) + (s & 7);
-#pragma unroll
-                    for (int rl = 0; rl < 16; ++rl) {
-                        const int r = b0 + rl;
-                        Dv[S * BLK + rl * LDB + cl] = x[rl];
-                        tcol[r * 64 + (((s >> 3) ^ (r & 7)) << 3)] = __float2bfloat16_rn(x[rl] * bs);
-                    }
-                }
-                const uint4 z4 = make_uint4(0, 0, 0, 0);
-                for (int R = 0; R < S; ++R) {  // T blocks above the diagonal are zero
-                    const int r = 16 * R + (lane >> 1), cc = 2 * S + (lane & 1);
-                    *reinterpret_cast<uint4 *>(sm + OFF_T + r * 128 + ((cc ^ (r & 7)) << 4)) = z4;
-                }
-            }
-            named_bar_sync(1, 128);
-            // Step 2, by doubling: M_10 = -D_1 A_10 D_0 and M_32 = -D_3 A_32 D_2
-            // (warps 0, 1) while warps 2, 3 start Y_RS = sum_K A_RK M_KS for the
-            // lower-left 32 x 32 block (R = 2, 3) with the parts that need no M_10.
-            // Step 3 adds A_R1 M_10; step 4: M_2S = -D_2 Y_2S, M_3S = -(M_32 Y_2S + D_3 Y_3S).
-            {
-                const int g = lane >> 2, tg = lane & 3;
-                // 16 x 16 block products on m16n8k8 tf32 tiles; X row-major with row stride LDB
-                auto a_blk = [&](const float *X, int kk, uint32_t (&a)[4]) {
-                    a[0] = to_tf32(X[g * LDB + 8 * kk + tg]);
-                    a[1] = to_tf32(X[(g + 8) * LDB + 8 * kk + tg]);
-                    a[2] = to_tf32(X[g * LDB + 8 * kk + tg + 4]);
-                    a[3] = to_tf32(X[(g + 8) * LDB + 8 * kk + tg + 4]);
-                };
-                auto a_am = [&](int R, int K, int kk, uint32_t (&a)[4]) {
-                    const int k4 = 4 * K + 2 * kk, r0 = 16 * R + g;
-                    a[0] = to_tf32(Am[fsw(r0, k4) + tg]);
-                    a[1] = to_tf32(Am[fsw(r0 + 8, k4) + tg]);
-                    a[2] = to_tf32(Am[fsw(r0, k4 + 1) + tg]);
-                    a[3] = to_tf32(Am[fsw(r0 + 8, k4 + 1) + tg]);
-                };
-                auto b_blk = [&](const float *X, int kk, int nt, uint32_t (&b)[2]) {
-                    b[0] = to_tf32(X[(8 * kk + tg) * LDB + 8 * nt + g]);
-                    b[1] = to_tf32(X[(8 * kk + tg + 4) * LDB + 8 * nt + g]);
-                };
-                // acc += A_RK (from Am) * X
-                auto mm_am = [&](float (&acc)[2][4], int R, int K, const float *X) {
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        uint32_t a[4];
-                        a_am(R, K, kk, a);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t b[2];
-                            b_blk(X, kk, nt, b);
-                            mma_tf32_16x8x8(acc[nt], a, b);
-                        }
-                    }
-                };
-                // acc += Xa * Xb (both row-major blocks)
-                auto mm_blk = [&](float (&acc)[2][4], const float *Xa, const float *Xb) {
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        uint32_t a[4];
-                        a_blk(Xa, kk, a);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t b[2];
-                            b_blk(Xb, kk, nt, b);
-                            mma_tf32_16x8x8(acc[nt], a, b);
-                        }
-                    }
-                };
-                auto st_blk = [&](float *X, const float (&c)[2][4]) {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        *reinterpret_cast<float2 *>(X + g * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][0], c[nt][1]);
-                        *reinterpret_cast<float2 *>(X + (g + 8) * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][2], c[nt][3]);
-                    }
-                };
-                // T_RS = -c Diag(beta_S) as bf16 pairs
-                auto st_t = [&](int R, int S, const float (&c)[2][4]) {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int s = 16 * S + 8 * nt + 2 * tg;
-                        const float b0s = -s_beta[s], b1s = -s_beta[s + 1];
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const int r = 16 * R + g + 8 * hf;
-                            *reinterpret_cast<__nv_bfloat162 *>(sm + OFF_T + r * 128 + (((s >> 3) ^ (r & 7)) << 4) +
-                                                                (s & 7) * 2) =
-                                __floats2bfloat162_rn(c[nt][2 * hf] * b0s, c[nt][2 * hf + 1] * b1s);
-                        }
-                    }
-                };
-                const float *D0 = Dv, *D1 = Dv + BLK, *D2 = Dv + 2 * BLK, *D3 = Dv + 3 * BLK;
-                float *M10 = Dv + 4 * BLK, *M32 = Dv + 5 * BLK;
-                float *Y20 = Yv, *Y21 = Yv + BLK, *Y30 = Yv + 2 * BLK, *Y31 = Yv + 3 * BLK;
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                float y1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                if (warp < 2) {
-                    const int R = warp == 0 ? 1 : 3;  // block (R, R-1)
-                    mm_am(acc, R, R - 1, warp == 0 ? D0 : D2);
-                    uint32_t yb[2][2][2];
-                    c_to_b(acc, yb, lane);
-                    const float *dr = warp == 0 ? D1 : D3;
-                    float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        uint32_t a[4];
-                        a_blk(dr, kk, a);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) mma_tf32_16x8x8(z[nt], a, yb[kk][nt]);
-                    }
-                    st_t(R, R - 1, z);  // T = -z Diag(beta)
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) z[nt][e] = -z[nt][e];
-                    st_blk(warp == 0 ? M10 : M32, z);
-                } else {
-                    const int R = warp;  // 2 or 3
-                    mm_am(acc, R, 1, D1);              // Y_R1 = A_R1 D_1 (final)
-                    st_blk(R == 2 ? Y21 : Y31, acc);
-                    mm_am(y1, R, 0, D0);               // Y_R0 partial: A_R0 D_0
-                }
-                named_bar_sync(1, 128);
-                if (warp >= 2) {
-                    const int R = warp;
-                    mm_am(y1, R, 1, M10);              // Y_R0 += A_R1 M_10
-                    st_blk(R == 2 ? Y20 : Y30, y1);
-                }
-                named_bar_sync(1, 128);
-                {
-                    // warp 0: (2,0), 1: (2,1), 2: (3,0), 3: (3,1)
-                    const int R = 2 + (warp >> 1), S = warp & 1;
-                    const float *y2 = S == 0 ? Y20 : Y21;
-                    float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    if (R == 2) {
-                        mm_blk(z, D2, y2);
-                    } else {
-                        mm_blk(z, M32, y2);
-                        mm_blk(z, D3, S == 0 ? Y30 : Y31);
-                    }
-                    st_t(R, S, z);
-                }
-            }
-        } else {
-            // The state is kept as S = Diag(sigma) S_st. S~^T = S_st^T Diag(sf) goes to
-            // TMEM as bf16 pairs (i, i+1); S_st^T <- S_st^T Diag(pf) in place.
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                uint32_t r[2][32], pk[32];
-                tmem_ld32(tbase + lrow + TM_S + 64 * kb, r[0]);
-                tmem_ld32(tbase + lrow + TM_S + 64 * kb + 32, r[1]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const int i0 = 64 * kb + 32 * part;
-#pragma unroll
-                    for (int g4 = 0; g4 < 8; ++g4) {
-                        const float4 fc = GCH ? *reinterpret_cast<const float4 *>(s_sf + i0 + 4 * g4)
-                                              : make_float4(s_sf[0], s_sf[0], s_sf[0], s_sf[0]);
-                        const float4 fl = GCH ? *reinterpret_cast<const float4 *>(s_pf + i0 + 4 * g4)
-                                              : make_float4(s_pf[0], s_pf[0], s_pf[0], s_pf[0]);
-                        const float fcv[4] = {fc.x, fc.y, fc.z, fc.w}, flv[4] = {fl.x, fl.y, fl.z, fl.w};
-                        float so[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float sv = __uint_as_float(r[part][4 * g4 + e]);
-                            so[e] = sv * fcv[e];
-                            r[part][4 * g4 + e] = __float_as_uint(sv * flv[e]);
-                        }
-                        __nv_bfloat162 t0 = __floats2bfloat162_rn(so[0], so[1]);
-                        __nv_bfloat162 t1 = __floats2bfloat162_rn(so[2], so[3]);
-                        pk[16 * part + 2 * g4] = *reinterpret_cast<uint32_t *>(&t0);
-                        pk[16 * part + 2 * g4 + 1] = *reinterpret_cast<uint32_t *>(&t1);
-                    }
-                    tmem_st32(tbase + lrow + TM_S + i0, r[part]);
-                }
-                tmem_st32(tbase + lrow + TM_SB + 32 * kb, pk);
-            }
-            tmem_st_wait();
-            if (!exact) {
-                got_mma = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-                tc_fence_after();
-                if (q4 >= 2) {  // P: TMEM lanes 64-127, masked (s <= r)
-                    const int r = 32 * (q4 - 2) + lane;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t r32[32];
-                        tmem_ld32(tbase + lrow + TM_AP + 32 * half, r32);
-                        tmem_ld_wait();
-                        float pv[32];
-#pragma unroll
-                        for (int m = 0; m < 32; ++m) pv[m] = (32 * half + m <= r) ? __uint_as_float(r32[m]) : 0.f;
-#pragma unroll
-                        for (int qd = 0; qd < 4; ++qd) {
-                            const int cc = 4 * half + qd;
-                            *reinterpret_cast<uint4 *>(sm + OFF_P + r * 128 + ((cc ^ (r & 7)) << 4)) =
-                                pack8(pv + 8 * qd);
-                        }
-                    }
-                }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!got_mma)) {
-            mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        if (!exact) ph_mma ^= 1;
-
-        // G2: W'^T = Lk^T T^T,  G3: U0^T = V^T T^T,  G5: O^T = S~^T Lq^T
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t b = sdesc_sw128(sbase + OFF_T + ks * 32, 16, 1024);
-                mma_bf16(tbase + TM_W, sdesc_sw128(sbase + OFF_X + ks * 2048, 16384, 1024), b, ID_MK64, ks > 0);
-                mma_bf16(tbase + TM_U0, sdesc_sw128(sbase + OFF_V + ks * 2048, 8192, 1024), b, ID_MK64, ks > 0);
-            }
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                mma_bf16_ts(tbase + TM_O, tbase + TM_SB + 8 * ks,
-                            sdesc_sw128(sbase + OFF_X + 8192 + kb * 16384 + ko, 16, 1024), ID_KK64, ks > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        got = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-        if (__syncthreads_or(!got)) {
-            mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-            ok = false;
-            break;
-        }
-        ph_mma ^= 1;
-        tc_fence_after();
-        if (tid == 0 && has_next) {  // q, k and v of this chunk are consumed
-            issue_qk((int)(c0 + C));
-            issue_v((int)(c0 + C));
-        }
-        pend_qkv = has_next;
-
-        // W'^T (lane i, column r) -> bf16 tile rows i (MN-major operand), over A
-        {
-            uint32_t r32[32];
-            tmem_ld32(tbase + lrow + TM_W + 32 * hh, r32);
-            tmem_ld_wait();
-            float wv[32];
-#pragma unroll
-            for (int m = 0; m < 32; ++m) wv[m] = __uint_as_float(r32[m]);
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                const int cc = 4 * hh + qd;
-                *reinterpret_cast<uint4 *>(sm + OFF_W + jl * 128 + ((cc ^ (jl & 7)) << 4)) = pack8(wv + 8 * qd);
-            }
-        }
-        sync_for_mma();
-
-        // G4: X^T = S~^T W'^T
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_ts(tbase + TM_X, tbase + TM_SB + 8 * ks, sdesc_sw128(sbase + OFF_W + ks * 2048, 8192, 1024),
-                            ID_KM64, ks > 0);
-            mma_commit(bar_mma);
-        }
-        got = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-        if (__syncthreads_or(!got)) {
-            mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-            ok = false;
-            break;
-        }
-        ph_mma ^= 1;
-        tc_fence_after();
-
-        // U^T = U0^T - X^T -> bf16 pairs (r, r+1) in TMEM over W'
-        {
-            uint32_t u0[32], x[32], pk[16];
-            tmem_ld32(tbase + lrow + TM_U0 + 32 * hh, u0);
-            tmem_ld32(tbase + lrow + TM_X + 32 * hh, x);
-            tmem_ld_wait();
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(u0[2 * m]) - __uint_as_float(x[2 * m]),
-                                                         __uint_as_float(u0[2 * m + 1]) - __uint_as_float(x[2 * m + 1]));
-                pk[m] = *reinterpret_cast<uint32_t *>(&t);
-            }
-            tmem_st16(tbase + lrow + TM_W + 16 * hh, pk);
-            tmem_st_wait();
-        }
-        sync_tc();
-
-        // G6: O^T += U^T P^T   and   G7: S_stored^T += U^T Rk (Kb on the exact path)
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t a = tbase + TM_W + 8 * ks;
-                mma_bf16_ts(tbase + TM_O, a, sdesc_sw128(sbase + OFF_P + ks * 32, 16, 1024), ID_KK64, 1);
-                mma_bf16_ts(tbase + TM_S, a, sdesc_sw128(sbase + OFF_RK + ks * 2048, 8192, 1024), ID_KM128, 1);
-            }
-            mma_commit(bar_mma);
-        }
-        got = mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-        if (__syncthreads_or(!got)) {
-            mbar_wait(bar_mma, ph_mma, WAIT_LIMIT);
-            ok = false;
-            break;
-        }
-        ph_mma ^= 1;
-        tc_fence_after();
-
-        // O^T (lane j, column r) -> staging [r][j] bf16 -> 16-byte stores of whole rows
-        {
-            uint32_t o32[32];
-            tmem_ld32(tbase + lrow + TM_O + 32 * hh, o32);
-            tmem_ld_wait();
-            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST);
-#pragma unroll
-            for (int m = 0; m < 32; ++m) ost[(32 * hh + m) * D + jl] = __float2bfloat16_rn(__uint_as_float(o32[m]));
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const int p = tid + NT * k4, r = p >> 4, c16 = p & 15;
-            if (r < L)
-                *reinterpret_cast<uint4 *>(out + ((size_t)(c0 + r) * H + h) * D + c16 * 8) =
-                    *reinterpret_cast<const uint4 *>(sm + OFF_OST + r * 256 + c16 * 16);
-        }
-    }
-
-    sync_tc();
-    if (ok && s_final) {  // S = Diag(sigma) S_stored
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int i0 = 64 * hh + 32 * part;
-            uint32_t r[32];
-            tmem_ld32(tbase + lrow + TM_S + i0, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int m = 0; m < 32; ++m)
-                s_final[soff + (size_t)(i0 + m) * D + jl] = __uint_as_float(r[m]) * s_sigma[i0 + m];
-        }
-    }
-    if (!ok) {  // let this CTA's own copies land before its shared memory goes away
-        if (pend_g) mbar_wait(bar_g, ph ^ 1, WAIT_LIMIT);
-        if (pend_qkv) {
-            mbar_wait(bar_qk, ph ^ 1, WAIT_LIMIT);
-            mbar_wait(bar_v, ph ^ 1, WAIT_LIMIT);
-        }
-        if (tid == 0) atomicOr(err, DEVERR_TIMEOUT);
-    }
-    sync_tc();
-    if (warp == 0) tmem_dealloc(tbase, 512);
-}
-
-// ------------------------------------------------- pipelined variant
+// ------------------------------------------------- the kernel
 // Warps 0-7 ("prep") run the state-independent part of chunk c + 1 (loads,
 // norms, cumulative decay, operand build, G1, solve, G2/G3, W' read-back)
 // while warps 8-11 ("chain") run the state chain of chunk c (S~ conversion,
