@@ -147,19 +147,25 @@ __device__ __forceinline__ void sync_tc() {
 
 
 // ------------------------------------------------- the kernel
-// Warps 0-7 ("prep") run the state-independent part of chunk c + 1 (loads,
-// norms, cumulative decay, operand build, G1, solve, G2/G3, W' read-back)
-// while warps 8-11 ("chain") run the state chain of chunk c (S~ conversion,
-// G4/G5, U, G6/G7, output). The hand-offs are mbarriers in shared memory:
-//   ready[b]  prep -> chain: chunk of parity b fully prepared
+// Three warp groups work on three consecutive chunks at once:
+//   front, warps 4-7: chunk c + 2's norms, cumulative decay, anchors and the
+//     operand tiles [Lk; Lq] and Rk (everything that needs no MMA);
+//   back, warps 0-3: chunk c + 1's G1, A/P read-back, the solve for T, G2/G3
+//     and the W' read-back;
+//   chain, warps 8-11: the state chain of chunk c (S~ conversion, G4/G5, U,
+//     G6/G7, output).
+// The hand-offs are mbarriers in shared memory:
+//   fr[b]     front -> back: operand tiles of chunk parity b built
+//   ready[b]  back -> chain: chunk of parity b fully prepared
 //   c45[b]    G4/G5 of chunk parity b done (tcgen05.commit): its [W'; Lq]
 //             tile may be reloaded; the chain itself then issues the q/k
 //             loads of the chunk two ahead into it
-//   ofree[b]  chain -> prep: chunk parity b finished (U0[b], Rk[b], P[b],
-//             the per-chunk factors and the O staging may be reused)
+//   ofree[b]  chain -> front: chunk parity b finished (U0[b], Rk[b], P[b],
+//             the per-chunk factors and the O staging may be reused; the
+//             back warps, which reach them only through fr[b], are done too)
 namespace pipe {
 constexpr int NTP = 384;
-// Register split between the warp groups (setmaxnreg): the prep warpgroups grow
+// Register split between the warp groups (setmaxnreg): the front and back warps grow
 // to PREP_REGS, the chain warpgroup shrinks to CHAIN_REGS. The shares must add
 // up to exactly what the CTA was launched with, 8 * PREP + 4 * CHAIN = 12 * R
 // (R = registers per thread at launch, 168 for 384 threads), or the grow would
@@ -215,13 +221,13 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                            int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
     using namespace pipe;
     constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
-    constexpr int BAR_PREP = 1, BAR_SOLVE = 3, BAR_CHAIN = 2;
+    constexpr int BAR_CHAIN = 2, BAR_BACK = 3, BAR_FRONT = 4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *s_rq = reinterpret_cast<float *>(sm + SMALL);
     float *s_rk = s_rq + 64;
     float *s_beta = s_rk + 64;
-    float *s_gl = s_beta + 64;      // G at the chunk's last row (natural log)
+    float *s_gl = s_beta + 128;     // G at the chunk's last row (natural log)
     float *s_c = s_gl + 128;        // anchor c
     float *s_g1 = s_c + 128;        // per-head gate: g per row, then G per row (log2 units)
     float *s_sigp = s_g1 + 64;      // sigma of the chunk prep finished last
@@ -237,19 +243,21 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     uint64_t *bar_c67 = bars + 8;
     uint64_t *bar_ready = bars + 9; // [2]
     uint64_t *bar_ofree = bars + 11;// [2]
-    volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(bars + 13);
-    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + 14);
+    uint64_t *bar_fr = bars + 13;   // [2] front -> back: operand tiles of chunk parity b built
+    volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(bars + 15);
+    uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + 16);
     // TMA barriers qk0, qk1, g, v0, v1: phases armed and phases waited for, so
     // that an aborted launch can let every copy in flight land before exiting
-    uint32_t *s_armed = reinterpret_cast<uint32_t *>(bars + 15);
+    uint32_t *s_armed = reinterpret_cast<uint32_t *>(bars + 17);
     uint32_t *s_waited = s_armed + 5;
+    uint32_t *s_exact = reinterpret_cast<uint32_t *>(bars + 22);  // [2] chunk parity b takes the exact path
     float *gt = reinterpret_cast<float *>(sm + G_);
     float *Am = reinterpret_cast<float *>(sm + A_);
     float *Dv = reinterpret_cast<float *>(sm + DV);
     float *Yv = reinterpret_cast<float *>(sm + YV);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q4 = warp & 3, hh = (warp >> 2) & 1;
+    const int q4 = warp & 3;
     const bool is_prep = tid < 256;
     const int h = blockIdx.x % H, n = order ? order[blockIdx.x / H] : (int)(blockIdx.x / H);
     int64_t start, end;
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 13; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < 15; ++i) mbar_init(bars + i, 1);
         for (int i = 0; i < 10; ++i) s_armed[i] = 0u;
         *s_abort = 0u;
         fence_mbar_init();
@@ -292,7 +300,10 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             if constexpr (GCH) issue_g((int)start);
             issue_v((int)start, 0);
         }
-        if (nchunks > 1) issue_qk((int)(start + C), 1);
+        if (nchunks > 1) {
+            issue_qk((int)(start + C), 1);
+            issue_v((int)(start + C), 1);
+        }
     }
     if (tid < 128) s_sigp[tid] = 1.f;
     if (warp == 0) {
@@ -309,214 +320,247 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
 
     if (is_prep) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PREP_REGS));
-        // ============================ prep: warps 0-7 ============================
-        uint32_t ph_mp = 0;
-        bool pend_mp = false;
-        float beta_reg = 0.f, gh_reg = 0.f;  // next chunk's beta / per-head gate, loaded one chunk ahead
-        if (tid < C && start + tid < end) {
-            beta_reg = beta[(size_t)(start + tid) * H + h];
-            if constexpr (GHD) gh_reg = g_head[(size_t)(start + tid) * H + h];
-        }
-        for (int ci = 0; ci < nchunks; ++ci) {
-            const int b = ci & 1;
-            const int64_t c0 = start + (int64_t)ci * C;
-            const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
-            const bool has_next = ci + 1 < nchunks;
-            uint8_t *xb = sm + X0 + 32768 * b;
-            const uint32_t xs = sbase + X0 + 32768 * b;
-            bool got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
-                       (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
-                       wait_or_abort(bar_v + b, (ci >> 1) & 1, s_abort) &&
-                       (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
-            if (group_or(BAR_PREP, 256, !got)) {
-                ok = false;
-                break;
+        if (tid >= 128) {
+            // ======================= front: warps 4-7 =======================
+            // Chunk c: waits for its q/k (and g) tiles, norms, cumulative decay,
+            // anchors and the operand tiles [Lk; Lq] and Rk, one chunk ahead of
+            // the back warps; fr[c & 1] hands the chunk over.
+            const int ft = tid - 128;
+            float beta_reg = 0.f, gh_reg = 0.f;  // next chunk's beta / per-head gate, loaded one chunk ahead
+            if (ft < C && start + ft < end) {
+                beta_reg = beta[(size_t)(start + ft) * H + h];
+                if constexpr (GHD) gh_reg = g_head[(size_t)(start + ft) * H + h];
             }
-            if (tid == 0) {
-                s_waited[b] += 1;
-                if constexpr (GCH) s_waited[2] += 1;
-                s_waited[3 + b] += 1;
-                // V of the other parity was last read by G3 of chunk ci - 1, which has completed
-                if (has_next) issue_v((int)(c0 + C), b ^ 1);
-            }
-            if (tid < C) {
-                s_beta[tid] = beta_reg;
-                if constexpr (GHD) s_g1[tid] = gh_reg;
-            }
-            if (L < C) {  // rows past the end of the sequence contribute nothing
-                const uint4 z4 = make_uint4(0, 0, 0, 0);
-                for (int p = tid; p < (C - L) * 16; p += 256) {
-                    const int r = L + (p >> 4), cc = p & 15;
-                    *reinterpret_cast<uint4 *>(xb + swz(r, cc, 128)) = z4;
-                    *reinterpret_cast<uint4 *>(xb + swz(r + 64, cc, 128)) = z4;
-                    *reinterpret_cast<uint4 *>(sm + V_ + 16384 * b + swz(r, cc, 64)) = z4;
+            for (int ci = 0; ci < nchunks; ++ci) {
+                const int b = ci & 1;
+                const int64_t c0 = start + (int64_t)ci * C;
+                const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
+                const bool has_next = ci + 1 < nchunks;
+                uint8_t *xb = sm + X0 + 32768 * b;
+                // ofree[b]: the chain is done with chunk ci - 2, hence the back warps too
+                bool got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
+                           (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
+                           (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
+                if (group_or(BAR_FRONT, 128, !got)) {
+                    ok = false;
+                    break;
                 }
-                if constexpr (GCH)
-                    for (int p = tid; p < (C - L) * 32; p += 256)
-                        *reinterpret_cast<uint4 *>(sm + G_ + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
-            }
-            named_bar_sync(BAR_PREP, 256);
-
-            // threads 0-127: L2 norms; 128-255: cumulative decay
-            bool bad = false;
-            if (tid < 128) {
-                const int r = tid & 63;
-                const int row = tid < 64 ? r + 64 : r;  // q rows follow the k rows
-                float ss = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < 16; ++cc) {
-                    float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(xb + swz(row, cc, 128)), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ss += f[e] * f[e];
+                if (ft == 0) {
+                    s_waited[b] += 1;
+                    if constexpr (GCH) s_waited[2] += 1;
                 }
-                (tid < 64 ? s_rq : s_rk)[r] = inv_norm(ss, eps);
-            } else if constexpr (GCH) {
-                const int i = tid - 128;
-                float gv[64];
-#pragma unroll
-                for (int r = 0; r < 64; ++r) gv[r] = gt[r * 128 + i];
-#pragma unroll
-                for (int r = 1; r < 64; ++r) gv[r] += gv[r - 1];
-                const float GL = gv[63];
-                bad = !(gv[0] - GL <= SPAN_MAX);
-#pragma unroll
-                for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
-                s_gl[i] = GL;
-            } else if constexpr (GHD) {
-                if (warp == 4) {
-                    const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
-                    float incl = g0 + g1;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += y;
+                float *sb = s_beta + 64 * b;
+                if (ft < C) {
+                    sb[ft] = beta_reg;
+                    if constexpr (GHD) s_g1[ft] = gh_reg;
+                }
+                if (L < C) {  // rows past the end of the sequence contribute nothing
+                    const uint4 z4 = make_uint4(0, 0, 0, 0);
+                    for (int p = ft; p < (C - L) * 16; p += 128) {
+                        const int r = L + (p >> 4), cc = p & 15;
+                        *reinterpret_cast<uint4 *>(xb + swz(r, cc, 128)) = z4;
+                        *reinterpret_cast<uint4 *>(xb + swz(r + 64, cc, 128)) = z4;
                     }
-                    const float G1v = incl, G0v = incl - g1;
-                    const float GL = __shfl_sync(0xffffffffu, incl, 31);
-                    const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
-                    bad = !(Gfirst - GL <= SPAN_MAX);
-                    s_g1[2 * lane] = G0v * LOG2E;
-                    s_g1[2 * lane + 1] = G1v * LOG2E;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
+                    if constexpr (GCH)
+                        for (int p = ft; p < (C - L) * 32; p += 128)
+                            *reinterpret_cast<uint4 *>(sm + G_ + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
                 }
-            } else {
-                s_gl[tid - 128] = 0.f;
-            }
-            const bool exact = GNO ? (named_bar_sync(BAR_PREP, 256), false) : group_or(BAR_PREP, 256, bad);
-            // per-channel anchor and state scale (see the sequential kernel)
-            if (tid < 128) {
-                const float GL = s_gl[tid], so = s_sigp[tid];
-                const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
-                const float ec = expf(c);
-                const float sn = exact ? 1.f : expf(GL - c);
-                s_c[tid] = c;
-                s_sf[128 * b + tid] = ec * so;
-                s_pf[128 * b + tid] = exact ? expf(GL) * so : ec * so;
-                s_sig[128 * b + tid] = sn;
-                s_sigp[tid] = sn;
-            }
-            named_bar_sync(BAR_PREP, 256);
+                named_bar_sync(BAR_FRONT, 128);
 
-            uint8_t *pb = sm + P0 + 8192 * b;
-            if (exact) {  // A and P with exact pairwise decays
-                for (int p = tid; p < C * C; p += 256) {
-                    const int r = p & 63, s = p >> 6;
-                    float a = 0.f, pq = 0.f;
-                    if (s <= r) {
-                        const float rkr = s_rk[r], rks = s_rk[s], rqr = s_rq[r];
-                        for (int cc = 0; cc < 16; ++cc) {
-                            float kr[8], ks[8], qr[8];
-                            unpack8(*reinterpret_cast<const uint4 *>(xb + swz(r, cc, 128)), kr);
-                            unpack8(*reinterpret_cast<const uint4 *>(xb + swz(s, cc, 128)), ks);
-                            unpack8(*reinterpret_cast<const uint4 *>(xb + swz(r + 64, cc, 128)), qr);
+                // L2 norm of one row (q rows for ft < 64, k rows after), then the
+                // cumulative decay of one key channel
+                bool bad = false;
+                {
+                    const int r = ft & 63;
+                    const int row = ft < 64 ? r + 64 : r;  // q rows follow the k rows
+                    float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int i = cc * 8 + e;
-                                float x = ks[e] * rks;
-                                if constexpr (GCH) x *= ex2(gt[r * 128 + i] - gt[s * 128 + i]);
-                                a += kr[e] * rkr * x;
-                                pq += qr[e] * rqr * x;
+                    for (int cc = 0; cc < 16; ++cc) {
+                        float f[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(xb + swz(row, cc, 128)), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
+                    }
+                    (ft < 64 ? s_rq : s_rk)[r] = inv_norm((ss[0] + ss[1]) + (ss[2] + ss[3]), eps);
+                }
+                if constexpr (GCH) {
+                    const int i = ft;
+                    float gv[64];
+#pragma unroll
+                    for (int r = 0; r < 64; ++r) gv[r] = gt[r * 128 + i];
+#pragma unroll
+                    for (int r = 1; r < 64; ++r) gv[r] += gv[r - 1];
+                    const float GL = gv[63];
+                    bad = !(gv[0] - GL <= SPAN_MAX);
+#pragma unroll
+                    for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
+                    s_gl[i] = GL;
+                } else if constexpr (GHD) {
+                    if (warp == 4) {
+                        const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
+                        float incl = g0 + g1;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += y;
+                        }
+                        const float G1v = incl, G0v = incl - g1;
+                        const float GL = __shfl_sync(0xffffffffu, incl, 31);
+                        const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
+                        bad = !(Gfirst - GL <= SPAN_MAX);
+                        s_g1[2 * lane] = G0v * LOG2E;
+                        s_g1[2 * lane + 1] = G1v * LOG2E;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
+                    }
+                } else {
+                    s_gl[ft] = 0.f;
+                }
+                const bool exact = GNO ? (named_bar_sync(BAR_FRONT, 128), false) : group_or(BAR_FRONT, 128, bad);
+                // per-channel anchor c and state scale sigma
+                {
+                    const float GL = s_gl[ft], so = s_sigp[ft];
+                    const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
+                    const float ec = expf(c);
+                    const float sn = exact ? 1.f : expf(GL - c);
+                    s_c[ft] = c;
+                    s_sf[128 * b + ft] = ec * so;
+                    s_pf[128 * b + ft] = exact ? expf(GL) * so : ec * so;
+                    s_sig[128 * b + ft] = sn;
+                    s_sigp[ft] = sn;
+                }
+                if (ft == 0) s_exact[b] = exact ? 1u : 0u;
+                named_bar_sync(BAR_FRONT, 128);
+
+                uint8_t *pb = sm + P0 + 8192 * b;
+                if (exact) {  // A and P with exact pairwise decays
+                    // A goes to the back warps' solve buffer: wait until they are done with chunk ci - 1
+                    if (ci > 0) {
+                        got = wait_or_abort(bar_ready + (b ^ 1), ((ci - 1) >> 1) & 1, s_abort);
+                        if (group_or(BAR_FRONT, 128, !got)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    for (int p = ft; p < C * C; p += 128) {
+                        const int r = p & 63, s = p >> 6;
+                        float a = 0.f, pq = 0.f;
+                        if (s <= r) {
+                            const float rkr = s_rk[r], rks = s_rk[s], rqr = s_rq[r];
+                            for (int cc = 0; cc < 16; ++cc) {
+                                float kr[8], ks[8], qr[8];
+                                unpack8(*reinterpret_cast<const uint4 *>(xb + swz(r, cc, 128)), kr);
+                                unpack8(*reinterpret_cast<const uint4 *>(xb + swz(s, cc, 128)), ks);
+                                unpack8(*reinterpret_cast<const uint4 *>(xb + swz(r + 64, cc, 128)), qr);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const int i = cc * 8 + e;
+                                    float x = ks[e] * rks;
+                                    if constexpr (GCH) x *= ex2(gt[r * 128 + i] - gt[s * 128 + i]);
+                                    a += kr[e] * rkr * x;
+                                    pq += qr[e] * rqr * x;
+                                }
                             }
                         }
+                        if constexpr (GHD) {
+                            const float f = s <= r ? ex2(s_g1[r] - s_g1[s]) : 0.f;
+                            a *= f;
+                            pq *= f;
+                        }
+                        Am[fsw(r, s >> 2) + (s & 3)] = (s < r) ? sb[r] * a : 0.f;
+                        *reinterpret_cast<__nv_bfloat16 *>(pb + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) + (s & 7) * 2) =
+                            __float2bfloat16_rn(pq);
                     }
-                    if constexpr (GHD) {
-                        const float f = s <= r ? ex2(s_g1[r] - s_g1[s]) : 0.f;
-                        a *= f;
-                        pq *= f;
-                    }
-                    Am[fsw(r, s >> 2) + (s & 3)] = (s < r) ? s_beta[r] * a : 0.f;
-                    *reinterpret_cast<__nv_bfloat16 *>(pb + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) + (s & 7) * 2) =
-                        __float2bfloat16_rn(pq);
+                    named_bar_sync(BAR_FRONT, 128);
                 }
-                named_bar_sync(BAR_PREP, 256);
-            }
 
-            // operand tiles: [Lk; Lq] in place, and Rk (Kb on the exact path)
-            uint8_t *rkb = sm + RK0 + 16384 * b;
-            {
-                const int cc = tid & 15, rb = tid >> 4;
-                float cv[8], glv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    cv[e] = s_c[GCH ? cc * 8 + e : 0] * LOG2E;
-                    glv[e] = s_gl[GCH ? cc * 8 + e : 0] * LOG2E;
-                }
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = rb + 16 * m;
-                    const uint32_t ok_ = swz(r, cc, 128), oq = swz(r + 64, cc, 128);
-                    float qf[8], kf[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(xb + oq), qf);
-                    unpack8(*reinterpret_cast<const uint4 *>(xb + ok_), kf);
-                    const float rq = s_rq[r], rk = s_rk[r];
-                    float G[8];
-                    if constexpr (GCH) {
-                        const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
-                        const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
-                        G[0] = ga.x; G[1] = ga.y; G[2] = ga.z; G[3] = ga.w;
-                        G[4] = gb.x; G[5] = gb.y; G[6] = gb.z; G[7] = gb.w;
-                    } else {
-                        const float gr = GHD ? s_g1[r] : 0.f;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) G[e] = gr;
-                    }
-                    float lk[8], lq[8], rkv[8];
+                // operand tiles: [Lk; Lq] in place, and Rk (Kb on the exact path)
+                uint8_t *rkb = sm + RK0 + 16384 * b;
+                {
+                    const int cc = ft & 15, rb = ft >> 4;
+                    float cv[8], glv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float kh = kf[e] * rk, qh = qf[e] * rq;
-                        if constexpr (GNO) {
-                            lk[e] = kh;
-                            lq[e] = qh;
-                            rkv[e] = kh;
-                        } else {
-                            const float e1 = ex2(G[e] - cv[e]);
-                            lk[e] = e1 * kh;
-                            lq[e] = e1 * qh;
-                            rkv[e] = (exact ? ex2(glv[e] - G[e]) : ex2(cv[e] - G[e])) * kh;
-                        }
+                        cv[e] = s_c[GCH ? cc * 8 + e : 0] * LOG2E;
+                        glv[e] = s_gl[GCH ? cc * 8 + e : 0] * LOG2E;
                     }
-                    *reinterpret_cast<uint4 *>(xb + ok_) = pack8(lk);
-                    *reinterpret_cast<uint4 *>(xb + oq) = pack8(lq);
-                    *reinterpret_cast<uint4 *>(rkb + swz(r, cc, 64)) = pack8(rkv);
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const int r = rb + 8 * m;
+                        const uint32_t ok_ = swz(r, cc, 128), oq = swz(r + 64, cc, 128);
+                        float qf[8], kf[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(xb + oq), qf);
+                        unpack8(*reinterpret_cast<const uint4 *>(xb + ok_), kf);
+                        const float rq = s_rq[r], rk = s_rk[r];
+                        float G[8];
+                        if constexpr (GCH) {
+                            const float4 ga = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8);
+                            const float4 gb = *reinterpret_cast<const float4 *>(gt + r * 128 + cc * 8 + 4);
+                            G[0] = ga.x; G[1] = ga.y; G[2] = ga.z; G[3] = ga.w;
+                            G[4] = gb.x; G[5] = gb.y; G[6] = gb.z; G[7] = gb.w;
+                        } else {
+                            const float gr = GHD ? s_g1[r] : 0.f;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) G[e] = gr;
+                        }
+                        float lk[8], lq[8], rkv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float kh = kf[e] * rk, qh = qf[e] * rq;
+                            if constexpr (GNO) {
+                                lk[e] = kh;
+                                lq[e] = qh;
+                                rkv[e] = kh;
+                            } else {
+                                const float e1 = ex2(G[e] - cv[e]);
+                                lk[e] = e1 * kh;
+                                lq[e] = e1 * qh;
+                                rkv[e] = (exact ? ex2(glv[e] - G[e]) : ex2(cv[e] - G[e])) * kh;
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(xb + ok_) = pack8(lk);
+                        *reinterpret_cast<uint4 *>(xb + oq) = pack8(lq);
+                        *reinterpret_cast<uint4 *>(rkb + swz(r, cc, 64)) = pack8(rkv);
+                    }
+                }
+                fence_async_smem();
+                named_bar_sync(BAR_FRONT, 128);
+                if (ft == 0) {
+                    mbar_arrive(bar_fr + b);
+                    // g of this chunk is consumed
+                    if constexpr (GCH)
+                        if (has_next) issue_g((int)(c0 + C));
+                }
+                if (ft < C) {
+                    const bool in = has_next && c0 + C + ft < end;
+                    beta_reg = in ? beta[(size_t)(c0 + C + ft) * H + h] : 0.f;
+                    if constexpr (GHD) gh_reg = in ? g_head[(size_t)(c0 + C + ft) * H + h] : 0.f;
                 }
             }
-            fence_async_smem();
-            tc_fence_before();
-            named_bar_sync(BAR_PREP, 256);
-            tc_fence_after();
-
-            if (tid < C) {
-                const bool in = has_next && c0 + C + tid < end;
-                beta_reg = in ? beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
-                if constexpr (GHD) gh_reg = in ? g_head[(size_t)(c0 + C + tid) * H + h] : 0.f;
-            }
-            // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T; g of this chunk is consumed
-            if (tid == 0) {
-                if constexpr (GCH)
-                    if (has_next) issue_g((int)(c0 + C));
-                if (!exact) {
+            if (!ok) *s_abort = 1u;
+        } else {
+            // ======================= back: warps 0-3 ========================
+            // Chunk c: G1, A/P read-back, the solve for T, G2/G3 and the W'
+            // read-back; ready[c & 1] hands the chunk to the chain.
+            uint32_t ph_mp = 0;
+            bool pend_mp = false;
+            for (int ci = 0; ci < nchunks; ++ci) {
+                const int b = ci & 1;
+                const int64_t c0 = start + (int64_t)ci * C;
+                const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
+                uint8_t *xb = sm + X0 + 32768 * b;
+                const uint32_t xs = sbase + X0 + 32768 * b;
+                bool got = wait_or_abort(bar_fr + b, (ci >> 1) & 1, s_abort);
+                if (group_or(BAR_BACK, 128, !got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const bool exact = s_exact[b] != 0u;
+                const float *sb = s_beta + 64 * b;
+                uint8_t *pb = sm + P0 + 8192 * b;
+                // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T
+                if (tid == 0 && !exact) {
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
@@ -525,18 +569,16 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     }
                     mma_commit(bar_mp);
                 }
-            }
-            pend_mp = !exact;
-            // warps 0-3: A read-back and solve; warps 4-7: P read-back
-            got = true;
-            if (!exact) {
-                got = wait_or_abort(bar_mp, ph_mp, s_abort);
-                tc_fence_after();
-            }
-            if (warp < 4) {
+                pend_mp = !exact;
+                // warps 0, 1: A read-back; warps 2, 3: P read-back; then the solve
+                got = true;
+                if (!exact) {
+                    got = wait_or_abort(bar_mp, ph_mp, s_abort);
+                    tc_fence_after();
+                }
                 if (!exact && got && q4 < 2) {  // A: TMEM lanes 0-63, masked (s < r), times beta
                     const int r = 32 * q4 + lane;
-                    const float br = s_beta[r];
+                    const float br = sb[r];
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t r32[32];
@@ -554,7 +596,24 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         }
                     }
                 }
-                named_bar_sync(BAR_SOLVE, 128);
+                if (!exact && got && q4 >= 2) {  // P: TMEM lanes 64-127, masked (s <= r)
+                    const int r = 32 * (q4 - 2) + lane;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r32[32];
+                        tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
+                        tmem_ld_wait();
+                        float pv[32];
+#pragma unroll
+                        for (int m = 0; m < 32; ++m) pv[m] = (32 * half + m <= r) ? __uint_as_float(r32[m]) : 0.f;
+#pragma unroll
+                        for (int qd = 0; qd < 4; ++qd) {
+                            const int cc = 4 * half + qd;
+                            *reinterpret_cast<uint4 *>(pb + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(pv + 8 * qd);
+                        }
+                    }
+                }
+                named_bar_sync(BAR_BACK, 128);
                 // M^-1 = (I + A)^-1 with A strictly lower, by 16 x 16 blocks.
                 // Step 1: warp S inverts the diagonal block, D_S = (I + A_SS)^-1, by
                 // forward substitution (lane = column; lanes 16-31 repeat 0-15).
@@ -581,7 +640,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     }
                     if (lane < 16) {
                         const int s = b0 + cl;
-                        const float bs = s_beta[s];
+                        const float bs = sb[s];
                         __nv_bfloat16 *tcol = reinterpret_cast<__nv_bfloat16 *>(sm + T_) + (s & 7);
     #pragma unroll
                         for (int rl = 0; rl < 16; ++rl) {
@@ -596,7 +655,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         *reinterpret_cast<uint4 *>(sm + T_ + r * 128 + ((cc ^ (r & 7)) << 4)) = z4;
                     }
                 }
-                named_bar_sync(BAR_SOLVE, 128);
+                named_bar_sync(BAR_BACK, 128);
                 // Step 2, by doubling: M_10 = -D_1 A_10 D_0 and M_32 = -D_3 A_32 D_2
                 // (warps 0, 1) while warps 2, 3 start Y_RS = sum_K A_RK M_KS for the
                 // lower-left 32 x 32 block (R = 2, 3) with the parts that need no M_10.
@@ -661,7 +720,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             const int s = 16 * S + 8 * nt + 2 * tg;
-                            const float b0s = -s_beta[s], b1s = -s_beta[s + 1];
+                            const float b0s = -sb[s], b1s = -sb[s + 1];
     #pragma unroll
                             for (int hf = 0; hf < 2; ++hf) {
                                 const int r = 16 * R + g + 8 * hf;
@@ -702,13 +761,13 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         st_blk(R == 2 ? Y21 : Y31, acc);
                         mm_am(y1, R, 0, D0);               // Y_R0 partial: A_R0 D_0
                     }
-                    named_bar_sync(BAR_SOLVE, 128);
+                    named_bar_sync(BAR_BACK, 128);
                     if (warp >= 2) {
                         const int R = warp;
                         mm_am(y1, R, 1, M10);              // Y_R0 += A_R1 M_10
                         st_blk(R == 2 ? Y20 : Y30, y1);
                     }
-                    named_bar_sync(BAR_SOLVE, 128);
+                    named_bar_sync(BAR_BACK, 128);
                     {
                         // warp 0: (2,0), 1: (2,1), 2: (3,0), 3: (3,1)
                         const int R = 2 + (warp >> 1), S = warp & 1;
@@ -723,77 +782,74 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         st_t(R, S, z);
                     }
                 }
-            } else if (!exact && got && q4 >= 2) {  // P: TMEM lanes 64-127, masked (s <= r)
-                const int r = 32 * (q4 - 2) + lane;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t r32[32];
-                    tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
-                    tmem_ld_wait();
-                    float pv[32];
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) pv[m] = (32 * half + m <= r) ? __uint_as_float(r32[m]) : 0.f;
-#pragma unroll
-                    for (int qd = 0; qd < 4; ++qd) {
-                        const int cc = 4 * half + qd;
-                        *reinterpret_cast<uint4 *>(pb + r * 128 + ((cc ^ (r & 7)) << 4)) = pack8(pv + 8 * qd);
+                // the v tile is needed from G3 on (the chain reloads it once the
+                // output store of chunk ci - 2 has read it)
+                got = got && wait_or_abort(bar_v + b, (ci >> 1) & 1, s_abort);
+                if (tid == 0 && got) s_waited[3 + b] += 1;
+                if (L < C && got) {  // v rows past the end of the sequence contribute nothing
+                    const uint4 z4 = make_uint4(0, 0, 0, 0);
+                    for (int p = tid; p < (C - L) * 16; p += 128) {
+                        const int r = L + (p >> 4), cc = p & 15;
+                        *reinterpret_cast<uint4 *>(sm + V_ + 16384 * b + swz(r, cc, 64)) = z4;
                     }
                 }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            if (group_or(BAR_PREP, 256, !got)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (!exact) {
+                fence_async_smem();
+                tc_fence_before();
+                if (group_or(BAR_BACK, 128, !got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (!exact) {
+                    ph_mp ^= 1;
+                    pend_mp = false;
+                }
+
+                // G2: W'^T = Lk^T T^T (over A/P in TMEM),  G3: U0^T = V^T T^T
+                if (tid == 0) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t bd = sdesc_sw128(sbase + T_ + ks * 32, 16, 1024);
+                        mma_bf16(tbase + T_AP, sdesc_sw128(xs + ks * 2048, 16384, 1024), bd, ID_MK64, ks > 0);
+                        mma_bf16(tbase + T_U0 + 64 * b, sdesc_sw128(sbase + V_ + 16384 * b + ks * 2048, 8192, 1024), bd,
+                                 ID_MK64, ks > 0);
+                    }
+                    mma_commit(bar_mp);
+                }
+                pend_mp = true;
+                got = wait_or_abort(bar_mp, ph_mp, s_abort);
+                tc_fence_after();
+                if (group_or(BAR_BACK, 128, !got)) {
+                    ok = false;
+                    break;
+                }
                 ph_mp ^= 1;
                 pend_mp = false;
-            }
-
-            // G2: W'^T = Lk^T T^T (over A/P in TMEM),  G3: U0^T = V^T T^T
-            if (tid == 0) {
+                // W'^T (lane i, column r) -> W' rows r over the Lk rows of this chunk's
+                // tile (dead after G2), so that [W'; Lq] is one K-major operand of G4/G5
+                {
+                    uint32_t r32[2][32];
+                    tmem_ld32(tbase + lrow + T_AP, r32[0]);
+                    tmem_ld32(tbase + lrow + T_AP + 32, r32[1]);
+                    tmem_ld_wait();
+                    const int i = jl;
+                    __nv_bfloat16 *wcol = reinterpret_cast<__nv_bfloat16 *>(xb + (i >> 6) * 16384) + (i & 7);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bd = sdesc_sw128(sbase + T_ + ks * 32, 16, 1024);
-                    mma_bf16(tbase + T_AP, sdesc_sw128(xs + ks * 2048, 16384, 1024), bd, ID_MK64, ks > 0);
-                    mma_bf16(tbase + T_U0 + 64 * b, sdesc_sw128(sbase + V_ + 16384 * b + ks * 2048, 8192, 1024), bd,
-                             ID_MK64, ks > 0);
+                    for (int m = 0; m < 64; ++m) {
+                        const int r = m;
+                        wcol[r * 64 + (((((i & 63) >> 3)) ^ (r & 7)) << 3)] =
+                            __float2bfloat16_rn(__uint_as_float(r32[m >> 5][m & 31]));
+                    }
                 }
-                mma_commit(bar_mp);
+                fence_async_smem();
+                tc_fence_before();
+                named_bar_sync(BAR_BACK, 128);
+                if (tid == 0) mbar_arrive(bar_ready + b);
             }
-            pend_mp = true;
-            got = wait_or_abort(bar_mp, ph_mp, s_abort);
-            tc_fence_after();
-            if (group_or(BAR_PREP, 256, !got)) {
-                ok = false;
-                break;
+            if (!ok) {  // let this group's own MMAs land before shared memory goes away
+                *s_abort = 1u;
+                if (pend_mp) mbar_wait(bar_mp, ph_mp, WAIT_LIMIT);
             }
-            ph_mp ^= 1;
-            pend_mp = false;
-            // W'^T (lane i, column r) -> W' rows r over the Lk rows of this chunk's
-            // tile (dead after G2), so that [W'; Lq] is one K-major operand of G4/G5
-            {
-                uint32_t r32[32];
-                tmem_ld32(tbase + lrow + T_AP + 32 * hh, r32);
-                tmem_ld_wait();
-                const int i = jl;
-                __nv_bfloat16 *wcol = reinterpret_cast<__nv_bfloat16 *>(xb + (i >> 6) * 16384) + (i & 7);
-#pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int r = 32 * hh + m;
-                    wcol[r * 64 + (((((i & 63) >> 3)) ^ (r & 7)) << 3)] = __float2bfloat16_rn(__uint_as_float(r32[m]));
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            named_bar_sync(BAR_PREP, 256);
-            if (tid == 0) mbar_arrive(bar_ready + b);
-        }
-        if (!ok) {  // let this group's own MMAs land before shared memory goes away
-            *s_abort = 1u;
-            if (pend_mp) mbar_wait(bar_mp, ph_mp, WAIT_LIMIT);
         }
     } else {
         // first instruction of the chain warps: hand registers to the prep warps
@@ -812,7 +868,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
         tmem_st_wait();
         uint32_t ph67 = 0;
         bool pend67 = false;
-        int ofree_due = -1;  // chunk whose buffers wait for its bulk output store to finish reading them
+        int v_due = -1;  // chunk whose v tile holds its output staging until the bulk store has read it
         int pend45 = -1;  // chunk whose G4/G5 are issued but not yet waited for
         int last_b = -1;
         for (int ci = 0; ci < nchunks; ++ci) {
@@ -825,14 +881,14 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 break;
             }
             tc_fence_after();
-            // the previous chunk's bulk output store has had a whole prep phase to
-            // read its staging: release that chunk's buffers now
-            if (ofree_due >= 0) {
+            // the previous chunk's bulk output store has had a whole back phase to
+            // read its staging (that chunk's v tile): load v of two chunks on into it
+            if (v_due >= 0) {
                 if (ct == 0) {
                     bulk_wait_read();
-                    mbar_arrive(bar_ofree + (ofree_due & 1));
+                    issue_v((int)(start + (int64_t)(v_due + 2) * C), v_due & 1);
                 }
-                ofree_due = -1;
+                v_due = -1;
             }
             // S = Diag(sigma) S_st. S~^T = S_st^T Diag(sf) -> TMEM bf16 pairs; S_st^T <- S_st^T Diag(pf)
             const float *sf = s_sf + 128 * b, *pf = s_pf + 128 * b;
@@ -931,8 +987,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             ph67 ^= 1;
             pend67 = false;
             tc_fence_after();
-            // O^T (lane j, column r) -> staging over Rk: two [64 rows][64 channels] bf16 boxes
-            uint8_t *ost = sm + RK0 + 16384 * b;
+            // U0[b], Rk[b], P[b] and the factors of this parity are consumed
+            if (ct == 0) mbar_arrive(bar_ofree + b);
+            // O^T (lane j, column r) -> staging over this chunk's v tile (consumed by
+            // G3): two [64 rows][64 channels] bf16 boxes
+            uint8_t *ost = sm + V_ + 16384 * b;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t o32[32];
@@ -946,14 +1005,14 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             tc_fence_before();
             named_bar_sync(BAR_CHAIN, 128);
             if (L == C) {
-                // a whole chunk: one bulk store per 64-channel box; the buffers are
-                // released once the copy engine has read the staging (next chunk)
+                // a whole chunk: one bulk store per 64-channel box; the v tile is
+                // reloaded once the copy engine has read the staging (next chunk)
                 if (ct == 0) {
                     tma_store_2d(&tm_o, ost, x0, (int)c0);
                     tma_store_2d(&tm_o, ost + 8192, x0 + 64, (int)c0);
                     bulk_commit();
                 }
-                ofree_due = ci;
+                if (ci + 2 < nchunks) v_due = ci;
             } else {
                 // a sequence's short last chunk: plain stores of its rows only (the rows
                 // after it belong to the next sequence)
@@ -963,8 +1022,6 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
                     orow[k8] = *reinterpret_cast<const uint4 *>(ost + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16);
                 }
-                named_bar_sync(BAR_CHAIN, 128);
-                if (ct == 0) mbar_arrive(bar_ofree + b);
 #pragma unroll
                 for (int k8 = 0; k8 < 8; ++k8) {
                     const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
@@ -973,13 +1030,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             }
             last_b = b;
         }
-        if (ct == 0) {
-            if (ofree_due >= 0) {
-                bulk_wait_read();
-                mbar_arrive(bar_ofree + (ofree_due & 1));
-            }
-            bulk_wait_all();  // output copies complete before the CTA's shared memory goes away
-        }
+        if (ct == 0) bulk_wait_all();  // output copies complete before the CTA's shared memory goes away
         if (ok && s_final) {  // S = Diag(sigma) S_st
             const float *sg = last_b >= 0 ? s_sig + 128 * last_b : nullptr;
 #pragma unroll
