@@ -148,11 +148,11 @@ __device__ __forceinline__ void sync_tc() {
 
 // ------------------------------------------------- the kernel
 // Three warp groups work on three consecutive chunks at once:
-//   front, warps 4-7: chunk c + 2's norms, cumulative decay, anchors and the
+//   front, warps 4-11: chunk c + 2's norms, cumulative decay, anchors and the
 //     operand tiles [Lk; Lq] and Rk (everything that needs no MMA);
 //   back, warps 0-3: chunk c + 1's G1, A/P read-back, the solve for T, G2/G3
 //     and the W' read-back;
-//   chain, warps 8-11: the state chain of chunk c (S~ conversion, G4/G5, U,
+//   chain, warps 12-15: the state chain of chunk c (S~ conversion, G4/G5, U,
 //     G6/G7, output).
 // The hand-offs are mbarriers in shared memory:
 //   fr[b]     front -> back: operand tiles of chunk parity b built
@@ -163,14 +163,26 @@ __device__ __forceinline__ void sync_tc() {
 //   ofree[b]  chain -> front: chunk parity b finished (U0[b], Rk[b], P[b],
 //             the per-chunk factors and the O staging may be reused; the
 //             back warps, which reach them only through fr[b], are done too)
+// Code size: the three groups run three different loop bodies at once, so the
+// outer loops of the read-backs, the conversions and the operand build are
+// kept rolled (`#pragma unroll 1`). Fully unrolled, instruction-fetch stalls
+// grew fourfold once every SM was busy and a 152-head launch ran 30% slower.
 namespace pipe {
-constexpr int NTP = 384;
-// Register split between the warp groups (setmaxnreg): the front and back warps grow
-// to PREP_REGS, the chain warpgroup shrinks to CHAIN_REGS. The shares must add
-// up to exactly what the CTA was launched with, 8 * PREP + 4 * CHAIN = 12 * R
-// (R = registers per thread at launch, 168 for 384 threads), or the grow would
-// wait for registers that never come; the host checks this before launching.
-constexpr int PREP_REGS = 184, CHAIN_REGS = 136;
+constexpr int NTP = 512;
+// Register split between the warp groups (setmaxnreg, one value per warpgroup):
+// the two front warpgroups shrink to FRONT_REGS, the back and chain warpgroups
+// grow to BACK_REGS and CHAIN_REGS. The shares must add up to exactly what the
+// CTA was launched with, 4 BACK + 8 FRONT + 4 CHAIN = 16 R (R = registers per
+// thread at launch, 128 for 512 threads), or a grow would wait for registers
+// that never come; the host checks this before launching. The per-channel
+// gate's chain needs fewer registers than the others' (its S~ factors are
+// vectors read from shared memory), so its back warps get more.
+template <int GM> struct Regs {
+    static constexpr int BACK = GM == KDA_GATE_CHANNEL ? 168 : 160;
+    static constexpr int FRONT = 104;
+    static constexpr int CHAIN = GM == KDA_GATE_CHANNEL ? 136 : 144;
+    static_assert(4 * BACK + 8 * FRONT + 4 * CHAIN == 16 * 128, "register split");
+};
 constexpr uint32_t X0 = 0;              // [k; q] -> [Lk; Lq], chunk parity 0 (32 KB); parity 1 at X0 + 32768
 constexpr uint32_t V_ = 65536;          // v tile per parity (16 KB each)
 constexpr uint32_t G_ = 98304;          // g fp32 [64][128] -> G (log2 units) (32 KB)
@@ -258,7 +270,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q4 = warp & 3;
-    const bool is_prep = tid < 256;
+    const bool is_prep = tid < 384;  // back (warps 0-3) and front (warps 4-11)
     const int h = blockIdx.x % H, n = order ? order[blockIdx.x / H] : (int)(blockIdx.x / H);
     int64_t start, end;
     if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
@@ -319,13 +331,13 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     bool ok = true;
 
     if (is_prep) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PREP_REGS));
         if (tid >= 128) {
-            // ======================= front: warps 4-7 =======================
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<GM>::FRONT));
+            // ======================= front: warps 4-11 ======================
             // Chunk c: waits for its q/k (and g) tiles, norms, cumulative decay,
             // anchors and the operand tiles [Lk; Lq] and Rk, one chunk ahead of
             // the back warps; fr[c & 1] hands the chunk over.
-            const int ft = tid - 128;
+            const int ft = tid - 128;  // 0..255
             float beta_reg = 0.f, gh_reg = 0.f;  // next chunk's beta / per-head gate, loaded one chunk ahead
             if (ft < C && start + ft < end) {
                 beta_reg = beta[(size_t)(start + ft) * H + h];
@@ -341,13 +353,25 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 bool got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
                            (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
                            (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
-                if (group_or(BAR_FRONT, 128, !got)) {
+                if (group_or(BAR_FRONT, 256, !got)) {
                     ok = false;
                     break;
                 }
                 if (ft == 0) {
                     s_waited[b] += 1;
                     if constexpr (GCH) s_waited[2] += 1;
+                    // the loads of chunk ci + 2 are issued one to two chunks from now,
+                    // inside the pipeline's dependency cycle: stage their tiles in L2
+                    if (ci + 2 < nchunks) {
+                        const int y2 = (int)(c0 + 2 * C);
+                        tma_prefetch_l2_2d(&tm_k, x0, y2);
+                        tma_prefetch_l2_2d(&tm_k, x0 + 64, y2);
+                        tma_prefetch_l2_2d(&tm_q, x0, y2);
+                        tma_prefetch_l2_2d(&tm_q, x0 + 64, y2);
+                        tma_prefetch_l2_2d(&tm_v, x0, y2);
+                        tma_prefetch_l2_2d(&tm_v, x0 + 64, y2);
+                        if constexpr (GCH) tma_prefetch_l2_2d(&tm_g, x0, y2);
+                    }
                 }
                 float *sb = s_beta + 64 * b;
                 if (ft < C) {
@@ -356,25 +380,25 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 }
                 if (L < C) {  // rows past the end of the sequence contribute nothing
                     const uint4 z4 = make_uint4(0, 0, 0, 0);
-                    for (int p = ft; p < (C - L) * 16; p += 128) {
+                    for (int p = ft; p < (C - L) * 16; p += 256) {
                         const int r = L + (p >> 4), cc = p & 15;
                         *reinterpret_cast<uint4 *>(xb + swz(r, cc, 128)) = z4;
                         *reinterpret_cast<uint4 *>(xb + swz(r + 64, cc, 128)) = z4;
                     }
                     if constexpr (GCH)
-                        for (int p = ft; p < (C - L) * 32; p += 128)
+                        for (int p = ft; p < (C - L) * 32; p += 256)
                             *reinterpret_cast<uint4 *>(sm + G_ + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
                 }
-                named_bar_sync(BAR_FRONT, 128);
+                named_bar_sync(BAR_FRONT, 256);
 
-                // L2 norm of one row (q rows for ft < 64, k rows after), then the
-                // cumulative decay of one key channel
+                // ft < 128: L2 norm of one row (q rows for ft < 64, k rows after);
+                // ft >= 128: cumulative decay of key channel ft - 128
                 bool bad = false;
-                {
+                if (ft < 128) {
                     const int r = ft & 63;
                     const int row = ft < 64 ? r + 64 : r;  // q rows follow the k rows
                     float ss[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 4
                     for (int cc = 0; cc < 16; ++cc) {
                         float f[8];
                         unpack8(*reinterpret_cast<const uint4 *>(xb + swz(row, cc, 128)), f);
@@ -382,21 +406,29 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
                     }
                     (ft < 64 ? s_rq : s_rk)[r] = inv_norm((ss[0] + ss[1]) + (ss[2] + ss[3]), eps);
-                }
-                if constexpr (GCH) {
-                    const int i = ft;
-                    float gv[64];
+                } else if constexpr (GCH) {
+                    const int i = ft - 128;
+                    // running sum down the 64 rows, 16 rows at a time
+                    float run = 0.f, G0 = 0.f;
+#pragma unroll 1
+                    for (int r0 = 0; r0 < 64; r0 += 16) {
+                        float gv[16];
 #pragma unroll
-                    for (int r = 0; r < 64; ++r) gv[r] = gt[r * 128 + i];
+                        for (int r = 0; r < 16; ++r) gv[r] = gt[(r0 + r) * 128 + i];
 #pragma unroll
-                    for (int r = 1; r < 64; ++r) gv[r] += gv[r - 1];
-                    const float GL = gv[63];
-                    bad = !(gv[0] - GL <= SPAN_MAX);
+                        for (int r = 0; r < 16; ++r) {
+                            run = r0 + r == 0 ? gv[r] : run + gv[r];
+                            gv[r] = run;
+                        }
+                        if (r0 == 0) G0 = gv[0];
 #pragma unroll
-                    for (int r = 0; r < 64; ++r) gt[r * 128 + i] = gv[r] * LOG2E;
+                        for (int r = 0; r < 16; ++r) gt[(r0 + r) * 128 + i] = gv[r] * LOG2E;
+                    }
+                    const float GL = run;
+                    bad = !(G0 - GL <= SPAN_MAX);
                     s_gl[i] = GL;
                 } else if constexpr (GHD) {
-                    if (warp == 4) {
+                    if (warp == 8) {
                         const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
                         float incl = g0 + g1;
 #pragma unroll
@@ -414,11 +446,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
                     }
                 } else {
-                    s_gl[ft] = 0.f;
+                    s_gl[ft - 128] = 0.f;
                 }
-                const bool exact = GNO ? (named_bar_sync(BAR_FRONT, 128), false) : group_or(BAR_FRONT, 128, bad);
+                const bool exact = GNO ? (named_bar_sync(BAR_FRONT, 256), false) : group_or(BAR_FRONT, 256, bad);
                 // per-channel anchor c and state scale sigma
-                {
+                if (ft < 128) {
                     const float GL = s_gl[ft], so = s_sigp[ft];
                     const float c = exact ? 0.f : fminf(0.f, GL + ANCHOR);
                     const float ec = expf(c);
@@ -430,19 +462,19 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     s_sigp[ft] = sn;
                 }
                 if (ft == 0) s_exact[b] = exact ? 1u : 0u;
-                named_bar_sync(BAR_FRONT, 128);
+                named_bar_sync(BAR_FRONT, 256);
 
                 uint8_t *pb = sm + P0 + 8192 * b;
                 if (exact) {  // A and P with exact pairwise decays
                     // A goes to the back warps' solve buffer: wait until they are done with chunk ci - 1
                     if (ci > 0) {
                         got = wait_or_abort(bar_ready + (b ^ 1), ((ci - 1) >> 1) & 1, s_abort);
-                        if (group_or(BAR_FRONT, 128, !got)) {
+                        if (group_or(BAR_FRONT, 256, !got)) {
                             ok = false;
                             break;
                         }
                     }
-                    for (int p = ft; p < C * C; p += 128) {
+                    for (int p = ft; p < C * C; p += 256) {
                         const int r = p & 63, s = p >> 6;
                         float a = 0.f, pq = 0.f;
                         if (s <= r) {
@@ -471,22 +503,22 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         *reinterpret_cast<__nv_bfloat16 *>(pb + r * 128 + ((((s >> 3) ^ (r & 7))) << 4) + (s & 7) * 2) =
                             __float2bfloat16_rn(pq);
                     }
-                    named_bar_sync(BAR_FRONT, 128);
+                    named_bar_sync(BAR_FRONT, 256);
                 }
 
                 // operand tiles: [Lk; Lq] in place, and Rk (Kb on the exact path)
                 uint8_t *rkb = sm + RK0 + 16384 * b;
                 {
-                    const int cc = ft & 15, rb = ft >> 4;
+                    const int cc = ft & 15, rb = ft >> 4;  // rb 0..15
                     float cv[8], glv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         cv[e] = s_c[GCH ? cc * 8 + e : 0] * LOG2E;
                         glv[e] = s_gl[GCH ? cc * 8 + e : 0] * LOG2E;
                     }
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        const int r = rb + 8 * m;
+#pragma unroll 1
+                    for (int m = 0; m < 4; ++m) {
+                        const int r = rb + 16 * m;
                         const uint32_t ok_ = swz(r, cc, 128), oq = swz(r + 64, cc, 128);
                         float qf[8], kf[8];
                         unpack8(*reinterpret_cast<const uint4 *>(xb + oq), qf);
@@ -524,7 +556,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     }
                 }
                 fence_async_smem();
-                named_bar_sync(BAR_FRONT, 128);
+                named_bar_sync(BAR_FRONT, 256);
                 if (ft == 0) {
                     mbar_arrive(bar_fr + b);
                     // g of this chunk is consumed
@@ -539,6 +571,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             }
             if (!ok) *s_abort = 1u;
         } else {
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<GM>::BACK));
             // ======================= back: warps 0-3 ========================
             // Chunk c: G1, A/P read-back, the solve for T, G2/G3 and the W'
             // read-back; ready[c & 1] hands the chunk to the chain.
@@ -579,7 +612,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 if (!exact && got && q4 < 2) {  // A: TMEM lanes 0-63, masked (s < r), times beta
                     const int r = 32 * q4 + lane;
                     const float br = sb[r];
-#pragma unroll
+#pragma unroll 1
                     for (int half = 0; half < 2; ++half) {
                         uint32_t r32[32];
                         tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
@@ -598,7 +631,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 }
                 if (!exact && got && q4 >= 2) {  // P: TMEM lanes 64-127, masked (s <= r)
                     const int r = 32 * (q4 - 2) + lane;
-#pragma unroll
+#pragma unroll 1
                     for (int half = 0; half < 2; ++half) {
                         uint32_t r32[32];
                         tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
@@ -828,17 +861,18 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 // W'^T (lane i, column r) -> W' rows r over the Lk rows of this chunk's
                 // tile (dead after G2), so that [W'; Lq] is one K-major operand of G4/G5
                 {
-                    uint32_t r32[2][32];
-                    tmem_ld32(tbase + lrow + T_AP, r32[0]);
-                    tmem_ld32(tbase + lrow + T_AP + 32, r32[1]);
-                    tmem_ld_wait();
                     const int i = jl;
                     __nv_bfloat16 *wcol = reinterpret_cast<__nv_bfloat16 *>(xb + (i >> 6) * 16384) + (i & 7);
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r32[32];
+                        tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int m = 0; m < 64; ++m) {
-                        const int r = m;
-                        wcol[r * 64 + (((((i & 63) >> 3)) ^ (r & 7)) << 3)] =
-                            __float2bfloat16_rn(__uint_as_float(r32[m >> 5][m & 31]));
+                        for (int m = 0; m < 32; ++m) {
+                            const int r = 32 * half + m;
+                            wcol[r * 64 + ((((i & 63) >> 3) ^ (r & 7)) << 3)] = __float2bfloat16_rn(__uint_as_float(r32[m]));
+                        }
                     }
                 }
                 fence_async_smem();
@@ -852,10 +886,9 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             }
         }
     } else {
-        // first instruction of the chain warps: hand registers to the prep warps
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CHAIN_REGS));
-        // ============================ chain: warps 8-11 ===========================
-        const int ct = tid - 256;  // 0..127
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<GM>::CHAIN));
+        // ============================ chain: warps 12-15 ==========================
+        const int ct = tid - 384;  // 0..127
         // initial state -> TMEM (S^T: lane j, column i); sigma = 1
 #pragma unroll
         for (int part = 0; part < 4; ++part) {
@@ -892,15 +925,13 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             }
             // S = Diag(sigma) S_st. S~^T = S_st^T Diag(sf) -> TMEM bf16 pairs; S_st^T <- S_st^T Diag(pf)
             const float *sf = s_sf + 128 * b, *pf = s_pf + 128 * b;
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                uint32_t r[2][32], pk[32];
-                tmem_ld32(tbase + lrow + T_S + 64 * kb, r[0]);
-                tmem_ld32(tbase + lrow + T_S + 64 * kb + 32, r[1]);
+#pragma unroll 1
+            for (int q32 = 0; q32 < 4; ++q32) {
+                const int i0 = 32 * q32;
+                uint32_t r[32], pk[16];
+                tmem_ld32(tbase + lrow + T_S + i0, r);
                 tmem_ld_wait();
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const int i0 = 64 * kb + 32 * part;
+                {
 #pragma unroll
                     for (int g4 = 0; g4 < 8; ++g4) {
                         const float4 fc = GCH ? *reinterpret_cast<const float4 *>(sf + i0 + 4 * g4)
@@ -911,18 +942,19 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         float so[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float sv = __uint_as_float(r[part][4 * g4 + e]);
+                            const float sv = __uint_as_float(r[4 * g4 + e]);
                             so[e] = sv * fcv[e];
-                            r[part][4 * g4 + e] = __float_as_uint(sv * flv[e]);
+                            r[4 * g4 + e] = __float_as_uint(sv * flv[e]);
                         }
                         __nv_bfloat162 t0 = __floats2bfloat162_rn(so[0], so[1]);
                         __nv_bfloat162 t1 = __floats2bfloat162_rn(so[2], so[3]);
-                        pk[16 * part + 2 * g4] = *reinterpret_cast<uint32_t *>(&t0);
-                        pk[16 * part + 2 * g4 + 1] = *reinterpret_cast<uint32_t *>(&t1);
+                        pk[2 * g4] = *reinterpret_cast<uint32_t *>(&t0);
+                        pk[2 * g4 + 1] = *reinterpret_cast<uint32_t *>(&t1);
                     }
-                    tmem_st32(tbase + lrow + T_S + i0, r[part]);
+                    // without a gate the rescale is by 1: S_st stays as it is
+                    if constexpr (!GNO) tmem_st32(tbase + lrow + T_S + i0, r);
                 }
-                tmem_st32(tbase + lrow + T_SB + 32 * kb, pk);
+                tmem_st16(tbase + lrow + T_SB + 16 * q32, pk);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -949,7 +981,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             // this chunk's [W'; Lq] tile is consumed: load the chunk two ahead into it
             if (ct == 0 && ci + 2 < nchunks) issue_qk((int)(c0 + 2 * C), b);
             // U^T = U0^T - X^T -> bf16 pairs in TMEM over S~ (dead after G4/G5)
-#pragma unroll
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 uint32_t u0[32], x[32], pk[16];
                 tmem_ld32(tbase + lrow + T_U0 + 64 * b + 32 * half, u0);
@@ -992,7 +1024,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             // O^T (lane j, column r) -> staging over this chunk's v tile (consumed by
             // G3): two [64 rows][64 channels] bf16 boxes
             uint8_t *ost = sm + V_ + 16384 * b;
-#pragma unroll
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 uint32_t o32[32];
                 tmem_ld32(tbase + lrow + T_O + 32 * half, o32);
@@ -1050,7 +1082,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             if (pend67) mbar_wait(bar_c67, ph67, WAIT_LIMIT);
         }
     }
-    if (!ok && (tid == 0 || tid == 256)) atomicOr(err, DEVERR_TIMEOUT);
+    if (!ok && (tid == 0 || tid == 384)) atomicOr(err, DEVERR_TIMEOUT);
     sync_tc();
     // after an abort: every copy still in flight must land before exit
     if (tid == 0 && *s_abort) {
@@ -1120,8 +1152,9 @@ static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const C
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_pipe_kernel<GM>);
         if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncGetAttributes: ") + cudaGetErrorString(e));
-        const bool okr = 8 * pipe::PREP_REGS + 4 * pipe::CHAIN_REGS == 12 * fa.numRegs &&
-                         pipe::CHAIN_REGS <= fa.numRegs && fa.numRegs <= pipe::PREP_REGS;
+        using RG = pipe::Regs<GM>;
+        const bool okr = 4 * RG::BACK + 8 * RG::FRONT + 4 * RG::CHAIN == 16 * fa.numRegs &&
+                         RG::FRONT <= fa.numRegs && fa.numRegs <= RG::BACK && fa.numRegs <= RG::CHAIN;
         regs_ok.store(okr ? 1 : -1, std::memory_order_release);
     }
     if (regs_ok.load(std::memory_order_acquire) < 0)
