@@ -186,6 +186,25 @@ kda_status kda_shortconv_decode_step_gated(const void *x, void *ring, const floa
                                            int D, kda_dtype dtype, kda_gate gate, float l2_eps,
                                            kda_stream_t stream);
 
+/* Launch flags of kda_shortconv_decode_step_ex. */
+enum { KDA_DECODE_OVERLAP_PREV = 1 };
+
+/*
+ * kda_shortconv_decode_step_gated with launch flags (same arguments, layouts,
+ * requirements and errors; flags = 0 is that call). With
+ * KDA_DECODE_OVERLAP_PREV the caller promises that the kernel enqueued on
+ * `stream` just before this call does not write this call's `state` (for
+ * instance, it is the decode step of another layer). The launch may then
+ * start while that kernel drains (programmatic dependent launch) and stream
+ * its state meanwhile. It reads x, ring, g and beta, and writes anything,
+ * only after that kernel has completed. Launch shapes that have no tail to
+ * overlap ignore the flag. Unknown flag bits are KDA_ERR_INVALID_ARG.
+ */
+kda_status kda_shortconv_decode_step_ex(const void *x, void *ring, const float *w, const float *g,
+                                        const float *beta, float *state, void *out, int B, int H, int D,
+                                        kda_dtype dtype, kda_gate gate, float l2_eps, unsigned flags,
+                                        kda_stream_t stream);
+
 /* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
 size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);
 

@@ -207,6 +207,14 @@ __global__ void __launch_bounds__(BULK_NT, 3)
         mbar_arrive_expect_tx(&bar, D * D * 4);
         bulk_load(Ss, Sg, D * D * 4, &bar);
     }
+    // Launched as a programmatic dependent (KDA_DECODE_OVERLAP_PREV), the state
+    // copy above overlaps the previous kernel's tail, and this wait holds every
+    // read of x, ring, g and beta (that kernel's possible outputs) until it has
+    // completed. Dependents are released only after the wait, so a kernel two
+    // launches back has always completed before the next one starts its copy.
+    // Launched plainly, both are no-ops.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // 1. width-4 causal conv + SiLU for q, k, v; shift the ring
     for (int idx = t; idx < 3 * D; idx += BULK_NT) {
@@ -351,10 +359,26 @@ static int device_sms() {
 
 template <int D, typename T, int GM>
 static void launch_fused(const void *x, void *ring, const float *w, const float *g, const float *beta,
-                         float *state, void *out, int B, int H, float eps, cudaStream_t s) {
+                         float *state, void *out, int B, int H, float eps, bool overlap, cudaStream_t s) {
     // three waves of the staged kernel or fewer
     if (D == 128 && (long long)B * H <= 9LL * device_sms()) {
         if (smem_attr_once<fused_decode_bulk_kernel<T, GM>>((int)BULK_SMEM) != cudaSuccess) return;  // reported by check_launch
+        if (overlap) {  // programmatic dependent launch: may start while the previous kernel drains
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)B * H);
+            cfg.blockDim = dim3(BULK_NT);
+            cfg.dynamicSmemBytes = BULK_SMEM;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            cudaLaunchKernelEx(&cfg, fused_decode_bulk_kernel<T, GM>, static_cast<const T *>(x),
+                               static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
+                               device_error_word());  // an error is left for check_launch
+            return;
+        }
         fused_decode_bulk_kernel<T, GM><<<(unsigned)B * H, BULK_NT, BULK_SMEM, s>>>(
             static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
             device_error_word());
@@ -366,34 +390,36 @@ static void launch_fused(const void *x, void *ring, const float *w, const float 
 
 template <typename T, int GM>
 static void dispatch_fused(int D, const void *x, void *ring, const float *w, const float *g, const float *beta,
-                           float *state, void *out, int B, int H, float eps, cudaStream_t s) {
+                           float *state, void *out, int B, int H, float eps, bool ov, cudaStream_t s) {
     switch (D) {
-    case 16: launch_fused<16, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
-    case 32: launch_fused<32, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
-    case 64: launch_fused<64, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
-    default: launch_fused<128, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, s); break;
+    case 16: launch_fused<16, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
+    case 32: launch_fused<32, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
+    case 64: launch_fused<64, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
+    default: launch_fused<128, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
     }
 }
 
 template <typename T>
 static void dispatch_fused_gate(kda_gate gate, int D, const void *x, void *ring, const float *w, const float *g,
-                                const float *beta, float *state, void *out, int B, int H, float eps,
+                                const float *beta, float *state, void *out, int B, int H, float eps, bool ov,
                                 cudaStream_t s) {
-    if (gate == KDA_GATE_HEAD) dispatch_fused<T, KDA_GATE_HEAD>(D, x, ring, w, g, beta, state, out, B, H, eps, s);
+    if (gate == KDA_GATE_HEAD)
+        dispatch_fused<T, KDA_GATE_HEAD>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, s);
     else if (gate == KDA_GATE_NONE)
-        dispatch_fused<T, KDA_GATE_NONE>(D, x, ring, w, g, beta, state, out, B, H, eps, s);
-    else dispatch_fused<T, KDA_GATE_CHANNEL>(D, x, ring, w, g, beta, state, out, B, H, eps, s);
+        dispatch_fused<T, KDA_GATE_NONE>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, s);
+    else dispatch_fused<T, KDA_GATE_CHANNEL>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, s);
 }
 
 }  // namespace kda
 
 using namespace kda;
 
-extern "C" kda_status kda_shortconv_decode_step_gated(const void *x, void *ring, const float *w, const float *g,
-                                                      const float *beta, float *state, void *out, int B, int H,
-                                                      int D, kda_dtype dtype, kda_gate gate, float l2_eps,
-                                                      kda_stream_t stream) {
+extern "C" kda_status kda_shortconv_decode_step_ex(const void *x, void *ring, const float *w, const float *g,
+                                                   const float *beta, float *state, void *out, int B, int H, int D,
+                                                   kda_dtype dtype, kda_gate gate, float l2_eps, unsigned flags,
+                                                   kda_stream_t stream) {
     clear_detail();
+    if (flags & ~(unsigned)KDA_DECODE_OVERLAP_PREV) return invalid("flags: unknown bits");
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE)
         return invalid("gate must be KDA_GATE_CHANNEL, KDA_GATE_HEAD or KDA_GATE_NONE");
     if (B < 0) return invalid("B must be >= 0");
@@ -412,11 +438,19 @@ extern "C" kda_status kda_shortconv_decode_step_gated(const void *x, void *ring,
         return invalid("out must not alias x, ring or state");
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool ov = (flags & KDA_DECODE_OVERLAP_PREV) != 0;
     if (dtype == KDA_BF16)
-        dispatch_fused_gate<__nv_bfloat16>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
+        dispatch_fused_gate<__nv_bfloat16>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, ov, s);
     else
-        dispatch_fused_gate<float>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, s);
+        dispatch_fused_gate<float>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, ov, s);
     return check_launch("fused_decode_kernel");
+}
+
+extern "C" kda_status kda_shortconv_decode_step_gated(const void *x, void *ring, const float *w, const float *g,
+                                                      const float *beta, float *state, void *out, int B, int H,
+                                                      int D, kda_dtype dtype, kda_gate gate, float l2_eps,
+                                                      kda_stream_t stream) {
+    return kda_shortconv_decode_step_ex(x, ring, w, g, beta, state, out, B, H, D, dtype, gate, l2_eps, 0u, stream);
 }
 
 extern "C" kda_status kda_shortconv_decode_step(const void *x, void *ring, const float *w, const float *g,

@@ -17,6 +17,7 @@ from . import build as _build
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE_CHECK = range(6)
 # gate forms: one log-gate per key channel (KDA), per head (Gated DeltaNet), none (DeltaNet)
 KDA_GATE_CHANNEL, KDA_GATE_HEAD, KDA_GATE_NONE = range(3)
+KDA_DECODE_OVERLAP_PREV = 1  # launch flag of kda_shortconv_decode_step_ex
 _GATES = {"channel": KDA_GATE_CHANNEL, "head": KDA_GATE_HEAD, "none": KDA_GATE_NONE}
 
 
@@ -64,6 +65,8 @@ _SIGNATURES = {
     "kda_chunk_prefill_gated": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci, _ci,
                                  _cf, _vp, _sz, _vp], _ci),
     "kda_shortconv_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
+    "kda_shortconv_decode_step_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf,
+                                      ctypes.c_uint, _vp], _ci),
     "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
     "kda_chunk_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
                            _cf, _vp, _sz, _vp], _ci),
@@ -206,6 +209,23 @@ def kda_shortconv_decode_step_gated(x, ring, w, g, beta, state, out, gate="chann
     _check(lib().kda_shortconv_decode_step_gated(_ptr(x), _ptr(ring), _ptr(w), _ptr(g), _ptr(beta), _ptr(state),
                                                  _ptr(out), B, H, D, _dtype_code(x), code, float(l2_eps),
                                                  _stream(stream, x.device)))
+
+
+def kda_shortconv_decode_step_ex(x, ring, w, g, beta, state, out, gate="channel", l2_eps=1e-6,
+                                 overlap_prev=False, stream=None):
+    """kda_shortconv_decode_step_gated with launch flags. overlap_prev=True is
+    the caller's promise that the kernel enqueued just before on the stream
+    does not write `state` (e.g. the step of another layer); the launch may
+    then overlap that kernel's tail (KDA_DECODE_OVERLAP_PREV)."""
+    B, P, H, D = x.shape
+    code = _check_gate(g, gate, (B,), H, D)
+    if P != 3 or tuple(ring.shape) != (B, 3, H, 3, D) or tuple(w.shape) != (3, H, D, 4) \
+            or tuple(beta.shape) != (B, H) or tuple(state.shape) != (B, H, D, D) or tuple(out.shape) != (B, H, D):
+        raise ValueError("shape mismatch")
+    flags = KDA_DECODE_OVERLAP_PREV if overlap_prev else 0
+    _check(lib().kda_shortconv_decode_step_ex(_ptr(x), _ptr(ring), _ptr(w), _ptr(g), _ptr(beta), _ptr(state),
+                                              _ptr(out), B, H, D, _dtype_code(x), code, float(l2_eps), flags,
+                                              _stream(stream, x.device)))
 
 
 def kda_shortconv_decode_step(x, ring, w, g, beta, state, out, l2_eps=1e-6, stream=None):

@@ -219,3 +219,16 @@ def test_selftest_rejects_bad_limit(kda):
     for bad in (0, -5, 3_000_000_000):
         assert L.kda_selftest_bounded_wait(bad, None) == kda.KDA_ERR_INVALID_ARG
         assert "limit_cycles" in L.kda_last_error_detail().decode()
+
+
+def test_decode_ex_flags(kda):
+    """kda_shortconv_decode_step_ex: unknown flag bits are rejected before
+    anything else; KDA_DECODE_OVERLAP_PREV passes on to the usual argument
+    checks (here a NULL beta)."""
+    L = kda.lib()
+    st = L.kda_shortconv_decode_step_ex(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000, 2, 3,
+                                        128, 1, kda.KDA_GATE_CHANNEL, 1e-6, 4, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "flags" in L.kda_last_error_detail().decode()
+    st = L.kda_shortconv_decode_step_ex(0x10000, 0x20000, 0x30000, 0x40000, None, 0x60000, 0x70000, 2, 3,
+                                        128, 1, kda.KDA_GATE_CHANNEL, 1e-6, kda.KDA_DECODE_OVERLAP_PREV, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "beta is NULL" in L.kda_last_error_detail().decode()

@@ -25,7 +25,11 @@ SEED = synth.STACK["seed"]
 SAMPLES = [(l, b, h) for l in (0, 34, 68) for b in (0, 7) for h in (0, 95)]
 
 
-def test_full_stack_decode_256_steps():
+@pytest.mark.parametrize("overlap", [False, True])
+def test_full_stack_decode_256_steps(overlap):
+    """overlap=True launches every step with KDA_DECODE_OVERLAP_PREV (each
+    launch follows another layer's), so each layer's state streams in while
+    the previous layer's launch drains; the results must not change."""
     torch = cuda_or_skip()
     ensure_built()
     from linear_attention_recurrence_02_gb300 import kda
@@ -58,7 +62,11 @@ def test_full_stack_decode_256_steps():
 
     for t in range(STEPS):
         for l in range(LAYERS):
-            kda.kda_shortconv_decode_step(x[l][t], ring[l], w[l], g[l][t], beta[l][t], state[l], out[l][t])
+            if overlap:
+                kda.kda_shortconv_decode_step_ex(x[l][t], ring[l], w[l], g[l][t], beta[l][t], state[l], out[l][t],
+                                                 overlap_prev=True)
+            else:
+                kda.kda_shortconv_decode_step(x[l][t], ring[l], w[l], g[l][t], beta[l][t], state[l], out[l][t])
     torch.cuda.synchronize()
     kda.kda_sync_status()
 
