@@ -160,9 +160,11 @@ __device__ __forceinline__ void sync_tc() {
 //   c45[b]    G4/G5 of chunk parity b done (tcgen05.commit): its [W'; Lq]
 //             tile may be reloaded; the chain itself then issues the q/k
 //             loads of the chunk two ahead into it
-//   ofree[b]  chain -> front: chunk parity b finished (U0[b], Rk[b], P[b],
-//             the per-chunk factors and the O staging may be reused; the
-//             back warps, which reach them only through fr[b], are done too)
+//   ofree[b]  chain -> front, right after G6/G7 of chunk parity b: U0[b],
+//             Rk[b], P[b] and the per-chunk factors may be reused (the back
+//             warps, which reach them only through fr[b], are done too). The
+//             output is staged in the chunk's v tile, which G3 has consumed;
+//             the chain reloads that tile once the bulk store has read it.
 // Code size: the three groups run three different loop bodies at once, so the
 // outer loops of the read-backs, the conversions and the operand build are
 // kept rolled (`#pragma unroll 1`). Fully unrolled, instruction-fetch stalls
@@ -184,9 +186,9 @@ template <int GM> struct Regs {
     static_assert(4 * BACK + 8 * FRONT + 4 * CHAIN == 16 * 128, "register split");
 };
 constexpr uint32_t X0 = 0;              // [k; q] -> [Lk; Lq], chunk parity 0 (32 KB); parity 1 at X0 + 32768
-constexpr uint32_t V_ = 65536;          // v tile per parity (16 KB each)
+constexpr uint32_t V_ = 65536;          // v tile per parity (16 KB each); O staging after G3
 constexpr uint32_t G_ = 98304;          // g fp32 [64][128] -> G (log2 units) (32 KB)
-constexpr uint32_t RK0 = 131072;        // Rk (Kb on the exact path) per parity (16 KB each); O staging after G7
+constexpr uint32_t RK0 = 131072;        // Rk (Kb on the exact path) per parity (16 KB each)
 constexpr uint32_t P0 = 163840;         // P per parity (8 KB each)
 constexpr uint32_t T_ = 180224;         // T (8 KB)
 constexpr uint32_t A_ = 188416;         // A fp32 (16 KB)
