@@ -179,3 +179,45 @@ def test_fused_decode_many_heads_sampled(env, gate, bf16):
         assert_close(got_o[bb:bb + 1, hh:hh + 1], ro, bf16, (0, 1), f"out {(bb, hh)}")
         assert_close(got_s[bb:bb + 1, hh:hh + 1], rs, bf16, (0, 1), f"state {(bb, hh)}")
         np.testing.assert_array_equal(got_r[bb, :, hh], rr[0, :, 0])
+
+
+@pytest.mark.parametrize("D,bf16", [(16, False), (128, True)])
+def test_fused_decode_overlap_flag(env, D, bf16):
+    """kda_shortconv_decode_step_ex with KDA_DECODE_OVERLAP_PREV, two layers
+    launched alternately for three steps (each launch follows the other
+    layer's, so the promise holds): D=16 takes the register kernel, D=128 the
+    shared-memory-staged one with a programmatic dependent launch. Every
+    result equals the plain launch bit for bit, and layer 0 matches the fp64
+    oracle over the three steps."""
+    torch, kda = env
+    B, H, steps = 2, 3, 3
+    dt = torch.bfloat16 if bf16 else torch.float32
+    layers = [synth.decode_inputs(700 + 10 * l + D, B, H, D, bf16, s0_std=0.5) for l in range(2)]
+    xs = [[synth.decode_inputs(800 + 10 * l + t, B, H, D, bf16)["x"] for t in range(steps)] for l in range(2)]
+
+    def run(overlap):
+        st = [to_dev(d["s0"], torch.float32, torch) for d in layers]
+        rg = [to_dev(d["ring"], dt, torch) for d in layers]
+        outs = []
+        for t in range(steps):
+            for l, d in enumerate(layers):
+                out = torch.empty((B, H, D), dtype=dt, device="cuda")
+                kda.kda_shortconv_decode_step_ex(to_dev(xs[l][t], dt, torch), rg[l], to_dev(d["w"], torch.float32, torch),
+                                                 to_dev(d["g"], torch.float32, torch),
+                                                 to_dev(d["beta"], torch.float32, torch), st[l], out,
+                                                 overlap_prev=overlap)
+                outs.append(out)
+        torch.cuda.synchronize()
+        return [to_np(o) for o in outs], [to_np(s) for s in st], [to_np(r) for r in rg]
+
+    o1, s1, r1 = run(True)
+    o0, s0, r0 = run(False)
+    for a, b in zip(o1 + s1 + r1, o0 + s0 + r0):
+        np.testing.assert_array_equal(a, b)
+    d = layers[0]
+    S, ring = d["s0"], d["ring"]
+    for t in range(steps):
+        y, ring = oracle.shortconv_step(xs[0][t], ring, d["w"])
+        ro, S = oracle.decode_step(y[:, 0], y[:, 1], y[:, 2], d["g"], d["beta"], S)
+        assert_close(o1[2 * t], ro, bf16, (0, 1), f"out step {t}")
+    assert_close(s1[0], S, bf16, (0, 1), "state")
