@@ -655,18 +655,18 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 {
                     const int S = warp, b0 = 16 * S, cl = lane & 15;
                     float x[16];
-    #pragma unroll
+#pragma unroll
                     for (int rl = 0; rl < 16; ++rl) x[rl] = (rl == cl) ? 1.f : 0.f;
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         float4 a4[16];
-    #pragma unroll
+#pragma unroll
                         for (int rl = 4 * j + 1; rl < 16; ++rl)
                             a4[rl] = *reinterpret_cast<const float4 *>(Am + fsw(b0 + rl, 4 * S + j));
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int kl = 4 * j + e;
-    #pragma unroll
+#pragma unroll
                             for (int rl = kl + 1; rl < 16; ++rl) {
                                 const float a = e == 0 ? a4[rl].x : e == 1 ? a4[rl].y : e == 2 ? a4[rl].z : a4[rl].w;
                                 x[rl] = fmaf(-a, x[kl], x[rl]);
@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         const int s = b0 + cl;
                         const float bs = sb[s];
                         __nv_bfloat16 *tcol = reinterpret_cast<__nv_bfloat16 *>(sm + T_) + (s & 7);
-    #pragma unroll
+#pragma unroll
                         for (int rl = 0; rl < 16; ++rl) {
                             const int r = b0 + rl;
                             Dv[S * BLK + rl * LDB + cl] = x[rl];
@@ -717,11 +717,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     };
                     // acc += A_RK (from Am) * X
                     auto mm_am = [&](float (&acc)[2][4], int R, int K, const float *X) {
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             uint32_t a[4];
                             a_am(R, K, kk, a);
-    #pragma unroll
+#pragma unroll
                             for (int nt = 0; nt < 2; ++nt) {
                                 uint32_t b[2];
                                 b_blk(X, kk, nt, b);
@@ -731,11 +731,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     };
                     // acc += Xa * Xb (both row-major blocks)
                     auto mm_blk = [&](float (&acc)[2][4], const float *Xa, const float *Xb) {
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             uint32_t a[4];
                             a_blk(Xa, kk, a);
-    #pragma unroll
+#pragma unroll
                             for (int nt = 0; nt < 2; ++nt) {
                                 uint32_t b[2];
                                 b_blk(Xb, kk, nt, b);
@@ -744,7 +744,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         }
                     };
                     auto st_blk = [&](float *X, const float (&c)[2][4]) {
-    #pragma unroll
+#pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             *reinterpret_cast<float2 *>(X + g * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][0], c[nt][1]);
                             *reinterpret_cast<float2 *>(X + (g + 8) * LDB + 8 * nt + 2 * tg) = make_float2(c[nt][2], c[nt][3]);
@@ -752,11 +752,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     };
                     // T_RS = -c Diag(beta_S) as bf16 pairs
                     auto st_t = [&](int R, int S, const float (&c)[2][4]) {
-    #pragma unroll
+#pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             const int s = 16 * S + 8 * nt + 2 * tg;
                             const float b0s = -sb[s], b1s = -sb[s + 1];
-    #pragma unroll
+#pragma unroll
                             for (int hf = 0; hf < 2; ++hf) {
                                 const int r = 16 * R + g + 8 * hf;
                                 *reinterpret_cast<__nv_bfloat162 *>(sm + T_ + r * 128 + (((s >> 3) ^ (r & 7)) << 4) +
@@ -777,17 +777,17 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         c_to_b(acc, yb, lane);
                         const float *dr = warp == 0 ? D1 : D3;
                         float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             uint32_t a[4];
                             a_blk(dr, kk, a);
-    #pragma unroll
+#pragma unroll
                             for (int nt = 0; nt < 2; ++nt) mma_tf32_16x8x8(z[nt], a, yb[kk][nt]);
                         }
                         st_t(R, R - 1, z);  // T = -z Diag(beta)
-    #pragma unroll
+#pragma unroll
                         for (int nt = 0; nt < 2; ++nt)
-    #pragma unroll
+#pragma unroll
                             for (int e = 0; e < 4; ++e) z[nt][e] = -z[nt][e];
                         st_blk(warp == 0 ? M10 : M32, z);
                     } else {
