@@ -60,6 +60,8 @@ def _load():
             lib.oracle_chunked.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
                                            i64p, ci, ci, ci, cd, ci, ci]
             lib.oracle_chunked.restype = None
+            lib.oracle_gated_rmsnorm.argtypes = [dp, dp, dp, dp, ctypes.c_int64, ci, cd, ci]
+            lib.oracle_gated_rmsnorm.restype = None
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _lib = lib
@@ -166,3 +168,17 @@ def decode_step(q, k, v, g, beta, state, eps=1e-6, nthreads=1):
     cu = np.arange(B + 1, dtype=np.int64)
     return recurrence(q, k, v, g, beta, s_init=state, cu_seqlens=cu, eps=eps,
                       nthreads=nthreads)
+
+
+def gated_rmsnorm(o, gate, weight, eps=1e-6, act="sigmoid"):
+    """Output epilogue: o, gate [..., D] (one row per token-head), weight [D].
+    Returns y [..., D] = RMSNorm(o) * weight * act(gate), act in
+    {"sigmoid", "silu"}."""
+    o, gate, weight = _f64(o), _f64(gate), _f64(weight)
+    assert o.shape == gate.shape and weight.shape == (o.shape[-1],)
+    D = o.shape[-1]
+    R = o.size // D if D else 0
+    y = np.empty_like(o)
+    _load().oracle_gated_rmsnorm(_ptr(o), _ptr(gate), _ptr(weight), _ptr(y), R, D, float(eps),
+                                 {"sigmoid": 0, "silu": 1}[act])
+    return y

@@ -325,6 +325,35 @@ void oracle_chunked(const double *q, const double *k, const double *v,
     }
 }
 
+/*
+ * Output epilogue of a layer: gated RMSNorm of the attention output, one row
+ * of D value channels per (token, head). [W] section "相关源码与文档导航" lists a
+ * gated RMSNorm among the parts of the KDA kernel, and [G] section 6 (the
+ * Gated DeltaNet architecture figure) says the output passes a gate that
+ * scales its features; neither prints the formula. The reading taken (and
+ * listed in the design notes) is the plainest one:
+ *   y_j = o_j / sqrt(mean_j' o_j'^2 + eps) * weight_j * act(gate_j)
+ * with act the logistic sigmoid (act = 0) or SiLU, z * sigmoid(z) (act = 1).
+ *
+ *   o, gate [R, D] (R = tokens x heads rows), weight [D], y [R, D]
+ */
+void oracle_gated_rmsnorm(const double *o, const double *gate, const double *weight, double *y,
+                          int64_t R, int D, double eps, int act)
+{
+    for (int64_t r = 0; r < R; ++r) {
+        const double *orow = o + r * D, *grow = gate + r * D;
+        double ss = 0.0;
+        for (int j = 0; j < D; ++j)
+            ss += orow[j] * orow[j];
+        const double inv = 1.0 / sqrt(ss / D + eps);
+        for (int j = 0; j < D; ++j) {
+            const double z = grow[j];
+            const double sg = 1.0 / (1.0 + exp(-z));
+            y[r * D + j] = orow[j] * inv * weight[j] * (act == 1 ? z * sg : sg);
+        }
+    }
+}
+
 /* Number of threads the OpenMP runtime would use by default (for reporting). */
 int oracle_max_threads(void)
 {

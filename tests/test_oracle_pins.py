@@ -447,3 +447,72 @@ def test_shortconv_seq_then_decode_step():
     y_step, r_step = oracle.shortconv_step(x[T][None], r, w)
     np.testing.assert_array_equal(y_step[0], y_all[:, T])
     np.testing.assert_array_equal(r_step, r_all)
+
+
+# ---- output epilogue: gated RMSNorm ("WARP中Kimi Delta Attention" section
+# "相关源码与文档导航" names it; "为什么 Kimi K3 ..." section 6: an output gate
+# that scales the features). The pins below hold for RMS normalisation and
+# for the logistic / SiLU gates whatever the implementation.
+
+def _epi_inputs(seed, R=5, D=16):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((R, D)), rng.standard_normal((R, D)), rng.uniform(0.5, 2.0, D)
+
+
+def test_epilogue_open_gate_gives_unit_mean_square():
+    """With the gate fully open (sigmoid(40) = 1 to 1e-17), unit weight and
+    eps = 0, every output row has mean square exactly 1 and points the same
+    way as its input row."""
+    o, _, _ = _epi_inputs(1)
+    y = oracle.gated_rmsnorm(o, np.full_like(o, 40.0), np.ones(o.shape[1]), eps=0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-12)
+    cos = np.sum(y * o, axis=1) / np.linalg.norm(y, axis=1) / np.linalg.norm(o, axis=1)
+    np.testing.assert_allclose(cos, 1.0, rtol=1e-12)
+    # a closed gate (sigmoid(-40) ~ 4e-18) passes nothing
+    z = oracle.gated_rmsnorm(o, np.full_like(o, -40.0), np.ones(o.shape[1]), eps=0.0)
+    assert np.max(np.abs(z)) < 1e-16
+
+
+def test_epilogue_scale_invariance_and_eps():
+    """RMS normalisation ignores a positive scale of the row when eps = 0;
+    with eps > 0 a zero row maps to zero and a tiny row stays tiny."""
+    o, gate, w = _epi_inputs(2)
+    y1 = oracle.gated_rmsnorm(o, gate, w, eps=0.0)
+    y2 = oracle.gated_rmsnorm(37.5 * o, gate, w, eps=0.0)
+    np.testing.assert_allclose(y1, y2, rtol=1e-12)
+    z = oracle.gated_rmsnorm(np.zeros_like(o), gate, w, eps=1e-6)
+    assert np.all(z == 0.0)
+    t = oracle.gated_rmsnorm(1e-6 * o, gate, w, eps=1.0)
+    assert np.max(np.abs(t)) < 1e-5
+
+
+def test_epilogue_sigmoid_symmetry_and_weight():
+    """sigmoid(z) + sigmoid(-z) = 1, so the outputs for gate and -gate add up
+    to the ungated normalised row times the weight; the weight multiplies
+    channel by channel (a transposed or shifted weight fails)."""
+    o, gate, w = _epi_inputs(3)
+    ya = oracle.gated_rmsnorm(o, gate, w, eps=1e-3)
+    yb = oracle.gated_rmsnorm(o, -gate, w, eps=1e-3)
+    full = oracle.gated_rmsnorm(o, np.full_like(o, 40.0), w, eps=1e-3)
+    np.testing.assert_allclose(ya + yb, full, rtol=1e-12, atol=1e-14)
+    y1 = oracle.gated_rmsnorm(o, gate, np.ones_like(w), eps=1e-3)
+    np.testing.assert_allclose(ya, y1 * w[None, :], rtol=1e-12)
+    # gate = 0: sigmoid(0) = 1/2 exactly
+    h = oracle.gated_rmsnorm(o, np.zeros_like(o), w, eps=1e-3)
+    np.testing.assert_allclose(2.0 * h, full, rtol=1e-12, atol=1e-14)
+
+
+def test_epilogue_silu_identity():
+    """SiLU(z) - SiLU(-z) = z: the SiLU-gated outputs for gate and -gate
+    differ by the normalised row times weight times gate; SiLU(0) = 0."""
+    o, gate, w = _epi_inputs(4)
+    ya = oracle.gated_rmsnorm(o, gate, w, eps=1e-3, act="silu")
+    yb = oracle.gated_rmsnorm(o, -gate, w, eps=1e-3, act="silu")
+    full = oracle.gated_rmsnorm(o, np.full_like(o, 40.0), w, eps=1e-3)
+    np.testing.assert_allclose(ya - yb, full * gate, rtol=1e-11, atol=1e-13)
+    z = oracle.gated_rmsnorm(o, np.zeros_like(o), w, eps=1e-3, act="silu")
+    assert np.all(z == 0.0)
+    # far from zero SiLU(z) -> z (a gate written as z * sigmoid(-z) keeps the
+    # odd-part identity above but fails here)
+    big = oracle.gated_rmsnorm(o, np.full_like(o, 40.0), w, eps=1e-3, act="silu")
+    np.testing.assert_allclose(big, 40.0 * full, rtol=1e-12, atol=1e-14)
