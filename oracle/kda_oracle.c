@@ -334,6 +334,7 @@ void oracle_chunked(const double *q, const double *k, const double *v,
  * listed in the design notes) is the plainest one:
  *   y_j = o_j / sqrt(mean_j' o_j'^2 + eps) * weight_j * act(gate_j)
  * with act the logistic sigmoid (act = 0) or SiLU, z * sigmoid(z) (act = 1).
+ * A row whose mean square plus eps is exactly zero maps to zero.
  *
  *   o, gate [R, D] (R = tokens x heads rows), weight [D], y [R, D]
  */
@@ -345,7 +346,10 @@ void oracle_gated_rmsnorm(const double *o, const double *gate, const double *wei
         double ss = 0.0;
         for (int j = 0; j < D; ++j)
             ss += orow[j] * orow[j];
-        const double inv = 1.0 / sqrt(ss / D + eps);
+        /* a row whose mean square plus eps is exactly zero maps to zero, as in
+         * the L2 normalisation above */
+        const double den = ss / D + eps;
+        const double inv = den > 0.0 ? 1.0 / sqrt(den) : 0.0;
         for (int j = 0; j < D; ++j) {
             const double z = grow[j];
             const double sg = 1.0 / (1.0 + exp(-z));

@@ -482,6 +482,8 @@ def test_epilogue_scale_invariance_and_eps():
     np.testing.assert_allclose(y1, y2, rtol=1e-12)
     z = oracle.gated_rmsnorm(np.zeros_like(o), gate, w, eps=1e-6)
     assert np.all(z == 0.0)
+    z0 = oracle.gated_rmsnorm(np.zeros_like(o), gate, w, eps=0.0)  # 0 / 0 read as 0
+    assert np.all(z0 == 0.0)
     t = oracle.gated_rmsnorm(1e-6 * o, gate, w, eps=1.0)
     assert np.max(np.abs(t)) < 1e-5
 
