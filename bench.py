@@ -411,6 +411,7 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
     fl = T * H * PREFILL_TOKEN_HEAD_FLOPS
     varlen = bench_varlen(torch, kda, dev, stream, ws, hbm_peak)
     conv = bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak)
+    epilogue = bench_epilogue(torch, kda, dev, stream, ws, hbm_peak)
     # the same workload with a per-head gate (Gated DeltaNet) and with none (DeltaNet)
     gates = {}
     gh = g[..., 0].contiguous()
@@ -460,7 +461,7 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
     except kda.KdaError as e:
         simt = {"unavailable": str(e)}
     return {"value": ws * toks / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "varlen": varlen,
-            "conv": conv, "gates": gates, "fp32": simt,
+            "conv": conv, "epilogue": epilogue, "gates": gates, "fp32": simt,
             "config": {"workload": f"chunked prefill T={T}, H={H}, d={D}, C={C}, bf16 q/k/v, zero S0, "
                                    "fp32 final state", "calls": n},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -510,6 +511,41 @@ def bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak, n=20):
     return {"value": ws * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
             "config": {"workload": f"short conv + SiLU prefill T={T}, H={H}, d={D}, bf16, ring in and out",
                        "calls": n, "l2": "3 rotating input/output sets (450 MB)"},
+            "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+
+
+def bench_epilogue(torch, kda, dev, stream, ws, hbm_peak, n=20):
+    """Output epilogue (gated RMSNorm, sigmoid gate) over the 4096-token
+    prefill output, 96 heads, d=128, bf16. Timing only; inputs drawn on the
+    device by a seeded torch generator. Two sets of o, gate and y (604 MB in
+    all, above the 129 MB L2) alternate."""
+    T = PRE["T"]
+    gen = torch.Generator(device=dev).manual_seed(PRE["seed"] + 7)
+    bf = torch.bfloat16
+    sets = [(torch.randn((T, H, D), generator=gen, device=dev).to(bf),
+             torch.randn((T, H, D), generator=gen, device=dev).to(bf),
+             torch.empty((T, H, D), dtype=bf, device=dev)) for _ in range(2)]
+    w = torch.rand((D,), generator=gen, device=dev) + 0.5
+
+    def call(i):
+        o, gt, y = sets[i % 2]
+        kda.kda_gated_rmsnorm(o, gt, w, y, stream=stream)
+    for i in range(4):
+        call(i)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        call(i)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status(stream)
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
+    by = 3 * T * H * D * 2 + D * 4
+    return {"value": ws * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
+            "config": {"workload": f"gated RMSNorm output epilogue T={T}, H={H}, d={D}, bf16, sigmoid gate",
+                       "calls": n, "l2": "2 alternating sets (604 MB)"},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 

@@ -68,6 +68,11 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  *   KDA_GATE_NONE     g unused, may be NULL: alpha = 1 (DeltaNet)          */
 typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_HEAD = 1, KDA_GATE_NONE = 2 } kda_gate;
 
+/* Activation of the output gate in kda_gated_rmsnorm:
+ *   KDA_ACT_SIGMOID  act(z) = 1 / (1 + exp(-z))
+ *   KDA_ACT_SILU     act(z) = z / (1 + exp(-z))                           */
+typedef enum { KDA_ACT_SIGMOID = 0, KDA_ACT_SILU = 1 } kda_gate_act;
+
 /* Static description of a status code. Never NULL. */
 const char *kda_status_string(kda_status s);
 
@@ -204,6 +209,26 @@ kda_status kda_shortconv_decode_step_ex(const void *x, void *ring, const float *
                                         const float *beta, float *state, void *out, int B, int H, int D,
                                         kda_dtype dtype, kda_gate gate, float l2_eps, unsigned flags,
                                         kda_stream_t stream);
+
+/*
+ * Output epilogue of a layer: gated RMSNorm of the attention output, per
+ * (token, head) row of D value channels. [W] "相关源码与文档导航" names a
+ * gated RMSNorm among the KDA kernel's parts and [G] section 6 (the Gated
+ * DeltaNet figure) an output gate that scales the features; neither prints a
+ * formula, and this is the plainest reading:
+ *
+ *   y[t,h,j] = o[t,h,j] / sqrt(mean_j' o[t,h,j']^2 + eps) * weight[j]
+ *              * act(gate[t,h,j])
+ *
+ * A row whose mean square plus eps is exactly zero gives zeros.
+ *   o, gate, y [T,H,D] dtype (o: the output of a decode step, T = B, or of a
+ *   prefill); weight [D] fp32, shared by the heads. y may alias o or gate
+ *   (each element is read before it is written by the same thread).
+ * Requires T >= 0, H >= 1, D in {16,32,64,128}, eps >= 0. T = 0 is a no-op.
+ */
+kda_status kda_gated_rmsnorm(const void *o, const void *gate, const float *weight, void *y, int64_t T,
+                             int H, int D, kda_dtype dtype, kda_gate_act act, float eps,
+                             kda_stream_t stream);
 
 /* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
 size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);

@@ -18,6 +18,8 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT,
 # gate forms: one log-gate per key channel (KDA), per head (Gated DeltaNet), none (DeltaNet)
 KDA_GATE_CHANNEL, KDA_GATE_HEAD, KDA_GATE_NONE = range(3)
 KDA_DECODE_OVERLAP_PREV = 1  # launch flag of kda_shortconv_decode_step_ex
+KDA_ACT_SIGMOID, KDA_ACT_SILU = 0, 1  # output-gate activations of kda_gated_rmsnorm
+_ACTS = {"sigmoid": KDA_ACT_SIGMOID, "silu": KDA_ACT_SILU}
 _GATES = {"channel": KDA_GATE_CHANNEL, "head": KDA_GATE_HEAD, "none": KDA_GATE_NONE}
 
 
@@ -72,6 +74,7 @@ _SIGNATURES = {
                            _cf, _vp, _sz, _vp], _ci),
     "kda_chunk_prefill_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci,
                                    _ci, _cf, _vp], _ci),
+    "kda_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i64, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_sync_status": ([_vp], _ci),
     "kda_selftest_bounded_wait": ([ctypes.c_longlong, _vp], _ci),
 }
@@ -240,6 +243,19 @@ def kda_shortconv_decode_step(x, ring, w, g, beta, state, out, l2_eps=1e-6, stre
     _check(lib().kda_shortconv_decode_step(_ptr(x), _ptr(ring), _ptr(w), _ptr(g), _ptr(beta), _ptr(state),
                                            _ptr(out), B, H, D, _dtype_code(x), float(l2_eps),
                                            _stream(stream, x.device)))
+
+
+def kda_gated_rmsnorm(o, gate, weight, y, act="sigmoid", eps=1e-6, stream=None):
+    """Output epilogue: y = RMSNorm(o) * weight * act(gate) per (token, head)
+    row. o, gate, y [T,H,D] (y may be o); weight [D] fp32; act "sigmoid" or
+    "silu"."""
+    T, H, D = o.shape
+    if tuple(gate.shape) != (T, H, D) or tuple(y.shape) != (T, H, D) or tuple(weight.shape) != (D,):
+        raise ValueError("shape mismatch")
+    if act not in _ACTS:
+        raise ValueError(f"act must be one of {sorted(_ACTS)}")
+    _check(lib().kda_gated_rmsnorm(_ptr(o), _ptr(gate), _ptr(weight), _ptr(y), T, H, D, _dtype_code(o),
+                                   _ACTS[act], float(eps), _stream(stream, o.device)))
 
 
 def kda_chunk_prefill_workspace_bytes(total_tokens, num_seqs, H, D, C) -> int:

@@ -183,5 +183,18 @@ VARLEN_LENGTHS = [512, 1024, 2048, 4096, 8192, 16384, 32768, 65536]
 VARLEN = dict(H=96, D=128, C=64, seed=4)
 
 
+def epilogue_inputs(seed: int, T: int, H: int, D: int, bf16: bool):
+    """Inputs of the output epilogue: o [T,H,D] ~ N(0,1) with a per-row scale
+    exp(N(0,1)) (rows of different magnitude), gate [T,H,D] ~ N(0, 2^2),
+    weight [D] ~ U(0.5, 1.5). o and gate rounded to bf16 when bf16."""
+    rng = _rng(seed, 0xE1)
+    o = _normal(rng, (T, H, D)) * np.exp(rng.standard_normal((T, H, 1))).astype(np.float32)
+    gate = _normal(rng, (T, H, D), 2.0)
+    weight = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    if bf16:
+        o, gate = bf16_round(o), bf16_round(gate)
+    return dict(o=o.astype(np.float32), gate=gate, weight=weight)
+
+
 def varlen_cu_seqlens(lengths=VARLEN_LENGTHS):
     return np.concatenate([[0], np.cumsum(np.asarray(lengths, np.int64))]).astype(np.int64)

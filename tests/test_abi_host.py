@@ -232,3 +232,20 @@ def test_decode_ex_flags(kda):
     st = L.kda_shortconv_decode_step_ex(0x10000, 0x20000, 0x30000, 0x40000, None, 0x60000, 0x70000, 2, 3,
                                         128, 1, kda.KDA_GATE_CHANNEL, 1e-6, kda.KDA_DECODE_OVERLAP_PREV, None)
     assert st == kda.KDA_ERR_INVALID_ARG and "beta is NULL" in L.kda_last_error_detail().decode()
+
+
+def test_gated_rmsnorm_argument_checks(kda):
+    """kda_gated_rmsnorm: T = 0 is a no-op before any pointer check; bad
+    activation, eps, head dim and NULL pointers are rejected without a launch."""
+    L = kda.lib()
+    assert L.kda_gated_rmsnorm(None, None, None, None, 0, 4, 128, 1, kda.KDA_ACT_SIGMOID, 1e-6, None) == kda.KDA_OK
+    st = L.kda_gated_rmsnorm(0x10000, 0x20000, 0x30000, 0x40000, 8, 4, 128, 1, 7, 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "act must be" in L.kda_last_error_detail().decode()
+    st = L.kda_gated_rmsnorm(0x10000, 0x20000, 0x30000, 0x40000, 8, 4, 128, 1, kda.KDA_ACT_SILU, -1.0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "eps" in L.kda_last_error_detail().decode()
+    st = L.kda_gated_rmsnorm(0x10000, 0x20000, 0x30000, 0x40000, 8, 4, 48, 1, kda.KDA_ACT_SILU, 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "D must be" in L.kda_last_error_detail().decode()
+    st = L.kda_gated_rmsnorm(0x10000, None, 0x30000, 0x40000, 8, 4, 128, 1, kda.KDA_ACT_SIGMOID, 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "gate is NULL" in L.kda_last_error_detail().decode()
+    st = L.kda_gated_rmsnorm(0x10000, 0x20000, 0x30008, 0x40000, 8, 4, 128, 1, kda.KDA_ACT_SIGMOID, 1e-6, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "weight is not 16-byte aligned" in L.kda_last_error_detail().decode()

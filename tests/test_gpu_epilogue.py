@@ -1,0 +1,73 @@
+"""GPU parity of the output epilogue, kda_gated_rmsnorm (gated RMSNorm of the
+attention output: "KV缓存从11.25GB缩到0.21GB: WARP中Kimi Delta Attention线性注意力
+原理剖析", section "相关源码与文档导航"; "为什么 Kimi K3 敢把 KV Cache 扔掉？一篇讲透
+GPT-2 到 K3 的架构进化", section 6), against the fp64 oracle, one row per
+(token, head)."""
+import numpy as np
+import pytest
+
+import oracle
+from linear_attention_recurrence_02_gb300 import synth
+from tests._util import assert_close, cuda_or_skip, ensure_built, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = cuda_or_skip()
+    ensure_built()
+    from linear_attention_recurrence_02_gb300 import kda
+    return torch, kda
+
+
+@pytest.mark.parametrize("act", ["sigmoid", "silu"])
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_gated_rmsnorm_matches_oracle(env, act, D, bf16):
+    """37 tokens x 3 heads (not a multiple of the rows a warp takes), rows of
+    magnitudes spread over e^+-3, one row all zero."""
+    torch, kda = env
+    T, H = 37, 3
+    d = synth.epilogue_inputs(10 + D, T, H, D, bf16)
+    d["o"][5, 1] = 0.0
+    dt = torch.bfloat16 if bf16 else torch.float32
+    o, gate = to_dev(d["o"], dt, torch), to_dev(d["gate"], dt, torch)
+    y = torch.empty_like(o)
+    kda.kda_gated_rmsnorm(o, gate, to_dev(d["weight"], torch.float32, torch), y, act=act, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.gated_rmsnorm(d["o"], d["gate"], d["weight"], eps=1e-6, act=act)
+    assert_close(to_np(y), ref, bf16, (0, 1), "y")
+    assert np.all(to_np(y)[5, 1] == 0.0)
+
+
+def test_gated_rmsnorm_in_place_and_zero_eps(env):
+    """y may be o; with eps = 0 a zero row still gives zeros."""
+    torch, kda = env
+    T, H, D = 9, 5, 128
+    d = synth.epilogue_inputs(77, T, H, D, False)
+    d["o"][3] = 0.0
+    o = to_dev(d["o"], torch.float32, torch)
+    kda.kda_gated_rmsnorm(o, to_dev(d["gate"], torch.float32, torch), to_dev(d["weight"], torch.float32, torch), o,
+                          act="silu", eps=0.0)
+    torch.cuda.synchronize()
+    ref = oracle.gated_rmsnorm(d["o"], d["gate"], d["weight"], eps=0.0, act="silu")
+    assert_close(to_np(o), ref, False, (0, 1), "y in place")
+    assert np.all(to_np(o)[3] == 0.0)
+
+
+def test_gated_rmsnorm_full_size_sampled_rows(env):
+    """The prefill output size, T=4096, H=96, D=128, bf16: 64 sampled rows
+    against the oracle (each row is independent, so a sample is exact)."""
+    torch, kda = env
+    T, H, D = 4096, 96, 128
+    d = synth.epilogue_inputs(5, T, H, D, True)
+    o, gate = to_dev(d["o"], torch.bfloat16, torch), to_dev(d["gate"], torch.bfloat16, torch)
+    y = torch.empty_like(o)
+    kda.kda_gated_rmsnorm(o, gate, to_dev(d["weight"], torch.float32, torch), y)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    ts, hs = rng.integers(0, T, 64), rng.integers(0, H, 64)
+    got = to_np(y)[ts, hs]
+    ref = oracle.gated_rmsnorm(d["o"][ts, hs], d["gate"][ts, hs], d["weight"])
+    assert_close(got[:, None], ref[:, None], True, (0, 1), "sampled rows")
