@@ -333,6 +333,8 @@ def run_ours(args):
     h2d = nx + ng + nb
     d2h = out.numel() * 2
 
+    dec_unfused = bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d)
+
     prefill = None
     if not args.no_prefill:
         prefill = bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src)
@@ -362,6 +364,7 @@ def run_ours(args):
                               "double-buffered, overlapping the neighbouring steps' launches"},
             "gpu_launches": args.steps,
             "clocks": clocks,
+            "decode_unfused": dec_unfused,
         }
         if prefill is not None:
             line["prefill"] = prefill
@@ -588,6 +591,40 @@ def bench_varlen(torch, kda, dev, stream, ws, hbm_peak):
     return {"value": ws * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
             "config": {"workload": "varlen prefill, 8 sequences 512..65536 (130,560 tokens), H=96, d=128, C=64, "
                                    "bf16, S0 ~ N(0,0.02^2), final states", "calls": n},
+            "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+
+
+def bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d, steps=200):
+    """The decode step alone (kda_decode_step, post-conv q/k/v, no conv) on
+    the headline workload: B=64, H=96, d=128, bf16 q/k/v, its own 384 MiB
+    fp32 state (larger than L2, so no flush)."""
+    bf = torch.bfloat16
+
+    def up(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev, dt)
+    q, k, v = up(d["q"], bf), up(d["k"], bf), up(d["v"], bf)
+    g, beta, state = up(d["g"], torch.float32), up(d["beta"], torch.float32), up(d["s0"], torch.float32)
+    out = torch.empty_like(q)
+
+    def step():
+        kda.kda_decode_step(q, k, v, g, beta, state, out, stream=stream)
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status(stream)
+    ms = max_over_ranks(a.elapsed_time(b) / steps, dev)
+    by = B * H * (2 * D * D * 4 + 3 * D * 2 + D * 4 + 4 + D * 2)
+    return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "kernel": "decode_step_kernel",
+            "config": {"workload": f"decode step without conv (kda_decode_step): B={B}, H={H}, d={D}, bf16 q/k/v, "
+                                   "fp32 state 384 MiB", "steps": steps},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 
