@@ -415,6 +415,7 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
     varlen = bench_varlen(torch, kda, dev, stream, ws, hbm_peak)
     conv = bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak)
     epilogue = bench_epilogue(torch, kda, dev, stream, ws, hbm_peak)
+    long_seq = bench_long_sequence(torch, kda, dev, stream, ws)
     # the same workload with a per-head gate (Gated DeltaNet) and with none (DeltaNet)
     gates = {}
     gh = g[..., 0].contiguous()
@@ -464,7 +465,7 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
     except kda.KdaError as e:
         simt = {"unavailable": str(e)}
     return {"value": ws * toks / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "varlen": varlen,
-            "conv": conv, "epilogue": epilogue, "gates": gates, "fp32": simt,
+            "conv": conv, "epilogue": epilogue, "long_sequence": long_seq, "gates": gates, "fp32": simt,
             "config": {"workload": f"chunked prefill T={T}, H={H}, d={D}, C={C}, bf16 q/k/v, zero S0, "
                                    "fp32 final state", "calls": n},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -551,6 +552,46 @@ def bench_epilogue(torch, kda, dev, stream, ws, hbm_peak, n=20):
                        "calls": n, "l2": "2 alternating sets (604 MB)"},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+
+
+def bench_long_sequence(torch, kda, dev, stream, ws, T=65536, Hs=8, segments=16, n=3):
+    """One 65,536-token sequence with 8 heads, d=128, C=64, bf16, per-channel
+    gate: the serial prefill (one chain of 1024 chunks per head, 8 SMs busy)
+    against kda_chunk_prefill_scan with 16 segments. Timing only; inputs drawn
+    on the device by a seeded torch generator with the workloads'
+    distributions."""
+    gen = torch.Generator(device=dev).manual_seed(PRE["seed"] + 11)
+
+    def rnd(shape):
+        return torch.randn(shape, generator=gen, device=dev)
+    q, k, v = (rnd((T, Hs, D)).to(torch.bfloat16) for _ in range(3))
+    g = -torch.nn.functional.softplus(rnd((T, Hs, D)))
+    beta = torch.sigmoid(rnd((T, Hs)))
+    out = torch.empty_like(q)
+    sf = torch.empty((Hs, D, D), device=dev)
+    wsb = torch.empty(max(16, kda.kda_chunk_prefill_scan_workspace_bytes(T, Hs, D, 64, segments)),
+                      dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(a.elapsed_time(b) / n, dev)
+    ms_serial = timed(lambda: kda.kda_chunk_prefill(q, k, v, g, beta, out, final_state=sf[None], chunk_size=64,
+                                                    stream=stream))
+    ms_scan = timed(lambda: kda.kda_chunk_prefill_scan(q, k, v, g, beta, out, segments, final_state=sf,
+                                                       workspace=wsb, stream=stream))
+    kda.kda_sync_status(stream)
+    return {"value": ws * T / (ms_scan * 1e-3), "unit": "tokens/s", "ms_per_call": ms_scan,
+            "serial_ms_per_call": ms_serial, "speedup": ms_serial / ms_scan,
+            "config": {"workload": f"one sequence of {T} tokens, H={Hs}, d={D}, C=64, bf16, per-channel gate: "
+                                   f"kda_chunk_prefill_scan with {segments} segments vs kda_chunk_prefill",
+                       "calls": n}}
 
 
 def bench_varlen(torch, kda, dev, stream, ws, hbm_peak):

@@ -230,6 +230,34 @@ kda_status kda_gated_rmsnorm(const void *o, const void *gate, const float *weigh
                              int H, int D, kda_dtype dtype, kda_gate_act act, float eps,
                              kda_stream_t stream);
 
+/*
+ * Chunked prefill of ONE sequence of T tokens, split into `segments` runs of
+ * whole chunks that are processed side by side ([G] section 5: each chunk
+ * step is affine in the state, S <- A S + B with A acting on the key axis,
+ * and so is a run of them). Three passes of the ordinary prefill over the
+ * segments (their B from zero states; their A from identity states with v
+ * read as zero; the outputs from the true states) around a serial fp32 scan
+ * S_{p+1} = A_p S_p + B_p. The result equals kda_chunk_prefill_gated on the
+ * whole sequence up to rounding. It pays when the sequence is long and H is
+ * small, so that the serial chunk chain leaves most SMs idle.
+ *
+ *   q, k, v, out [T,H,D] dtype; g [T,H,D] / [T,H] / unused per `gate`;
+ *   beta [T,H] fp32; initial_state [H,D,D] fp32 or NULL (zeros);
+ *   final_state [H,D,D] fp32 or NULL.
+ *   workspace: kda_chunk_prefill_scan_workspace_bytes(T, H, D, C, segments)
+ *   bytes of device memory, 16-byte aligned (four fp32 states per segment
+ *   and head).
+ * segments in 1..4096; segments = 1, T = 0 or T <= C run the ordinary
+ * prefill (no workspace needed). Other requirements and errors as
+ * kda_chunk_prefill_gated.
+ */
+size_t kda_chunk_prefill_scan_workspace_bytes(int64_t T, int H, int D, int C, int segments);
+kda_status kda_chunk_prefill_scan(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, const float *initial_state, float *final_state,
+                                  void *out, int64_t T, int H, int D, int C, kda_dtype dtype, kda_gate gate,
+                                  float l2_eps, int segments, void *workspace, size_t workspace_bytes,
+                                  kda_stream_t stream);
+
 /* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
 size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);
 

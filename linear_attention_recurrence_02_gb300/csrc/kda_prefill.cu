@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(SIMT_NT)
                         const float *__restrict__ g, const float *__restrict__ beta,
                         const float *s_init, float *s_final, T *__restrict__ out,
                         const int64_t *__restrict__ cu_seqlens, int N, int64_t Ttot, int H, int C, float eps,
-                        unsigned *err, const int *__restrict__ order, int gate) {
+                        unsigned *err, const int *__restrict__ order, int gate, int v_zero) {
     constexpr int JS = simt_js(D), LD = D + 1, NS = D / JS, NW = SIMT_NT / 32;
     extern __shared__ float smem[];
     float *sQ = smem;                    // [C][LD]  q^, then Qt
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(SIMT_NT)
         }
         for (int p = tid; p < L * JS; p += SIMT_NT) {
             const int r = p / JS, j = p % JS;
-            sU[p] = Elem<T>::load(v + ((size_t)(c0 + r) * H + h) * D + j0 + j);
+            sU[p] = v_zero ? 0.f : Elem<T>::load(v + ((size_t)(c0 + r) * H + h) * D + j0 + j);
         }
         // cumulative log decay per key channel
         if (tid < D) {
@@ -196,7 +196,7 @@ static kda_status launch_simt(const PrefillArgs &a, cudaStream_t s) {
     kern<<<grid, SIMT_NT, smem, s>>>(static_cast<const T *>(a.q), static_cast<const T *>(a.k),
                                      static_cast<const T *>(a.v), a.g, a.beta, a.s_init, a.s_final,
                                      static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err,
-                                     a.order, a.gate);
+                                     a.order, a.gate, a.v_zero ? 1 : 0);
     return check_launch("prefill_simt_kernel");
 }
 

@@ -23,6 +23,7 @@ struct PrefillArgs {
     unsigned *err;
     const int *order;  // sequences by descending length (device), or NULL = natural order
     int gate;          // kda_gate: g is [T,H,D], [T,H], or unused
+    bool v_zero = false;  // read v as all zeros (v is not loaded)
 };
 
 // Largest batch the length sort handles; bigger batches keep their order.

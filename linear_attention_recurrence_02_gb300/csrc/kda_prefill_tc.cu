@@ -232,7 +232,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                            const __grid_constant__ CUtensorMap tm_o,
                            const float *__restrict__ g_head, const float *__restrict__ beta, const float *s_init,
                            float *s_final, __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens,
-                           int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order) {
+                           int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order,
+                           int v_zero) {
     using namespace pipe;
     constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
     constexpr int BAR_CHAIN = 2, BAR_BACK = 3, BAR_FRONT = 4;
@@ -295,6 +296,10 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     };
     auto issue_v = [&](int y, int b) {
         s_armed[3 + b] += 1;
+        if (v_zero) {  // nothing to load: release the tile; the back warps zero it
+            mbar_arrive(bar_v + b);
+            return;
+        }
         mbar_arrive_expect_tx(bar_v + b, V_BYTES);
         tma_load_2d(sm + V_ + 16384 * b, &tm_v, bar_v + b, x0, y);
         tma_load_2d(sm + V_ + 16384 * b + 8192, &tm_v, bar_v + b, x0 + 64, y);
@@ -821,10 +826,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 // output store of chunk ci - 2 has read it)
                 got = got && wait_or_abort(bar_v + b, (ci >> 1) & 1, s_abort);
                 if (tid == 0 && got) s_waited[3 + b] += 1;
-                if (L < C && got) {  // v rows past the end of the sequence contribute nothing
+                const int z0 = v_zero ? 0 : L;  // v read as zeros: every row
+                if (z0 < C && got) {  // v rows past the end of the sequence contribute nothing
                     const uint4 z4 = make_uint4(0, 0, 0, 0);
-                    for (int p = tid; p < (C - L) * 16; p += 128) {
-                        const int r = L + (p >> 4), cc = p & 15;
+                    for (int p = tid; p < (C - z0) * 16; p += 128) {
+                        const int r = z0 + (p >> 4), cc = p & 15;
                         *reinterpret_cast<uint4 *>(sm + V_ + 16384 * b + swz(r, cc, 64)) = z4;
                     }
                 }
@@ -1165,7 +1171,8 @@ static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const C
                                          (int)pipe::SMEM);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
     prefill_tc_pipe_kernel<GM><<<(unsigned)a.N * a.H, pipe::NTP, pipe::SMEM, s>>>(
-        mq, mk, mv, mg, mo, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order);
+        mq, mk, mv, mg, mo, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order,
+        a.v_zero ? 1 : 0);
     return check_launch("prefill_tc_pipe_kernel");
 }
 

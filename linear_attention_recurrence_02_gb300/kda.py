@@ -75,6 +75,9 @@ _SIGNATURES = {
     "kda_chunk_prefill_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci,
                                    _ci, _cf, _vp], _ci),
     "kda_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i64, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
+    "kda_chunk_prefill_scan_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
+    "kda_chunk_prefill_scan": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _ci, _ci, _ci, _ci, _ci, _cf, _ci,
+                                _vp, _sz, _vp], _ci),
     "kda_sync_status": ([_vp], _ci),
     "kda_selftest_bounded_wait": ([ctypes.c_longlong, _vp], _ci),
 }
@@ -256,6 +259,29 @@ def kda_gated_rmsnorm(o, gate, weight, y, act="sigmoid", eps=1e-6, stream=None):
         raise ValueError(f"act must be one of {sorted(_ACTS)}")
     _check(lib().kda_gated_rmsnorm(_ptr(o), _ptr(gate), _ptr(weight), _ptr(y), T, H, D, _dtype_code(o),
                                    _ACTS[act], float(eps), _stream(stream, o.device)))
+
+
+def kda_chunk_prefill_scan_workspace_bytes(T, H, D, C, segments) -> int:
+    return int(lib().kda_chunk_prefill_scan_workspace_bytes(T, H, D, C, segments))
+
+
+def kda_chunk_prefill_scan(q, k, v, g, beta, out, segments, initial_state=None, final_state=None, gate="channel",
+                           chunk_size=64, l2_eps=1e-6, workspace=None, stream=None):
+    """Prefill of one long sequence split into `segments` runs processed side
+    by side. q,k,v,out [T,H,D]; g per `gate`; beta [T,H]; states [H,D,D] fp32.
+    workspace: a device uint8 tensor of kda_chunk_prefill_scan_workspace_bytes
+    (allocated here when None)."""
+    T, H, D = q.shape
+    code = _check_gate(g, gate, (T,), H, D)
+    need = kda_chunk_prefill_scan_workspace_bytes(T, H, D, chunk_size, segments)
+    if workspace is None and need > 0:
+        import torch
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib().kda_chunk_prefill_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                        _ptr(final_state), _ptr(out), T, H, D, chunk_size, _dtype_code(q), code,
+                                        float(l2_eps), int(segments), _ptr(workspace),
+                                        0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                        _stream(stream, q.device)))
 
 
 def kda_chunk_prefill_workspace_bytes(total_tokens, num_seqs, H, D, C) -> int:

@@ -1,0 +1,100 @@
+"""GPU parity of kda_chunk_prefill_scan, the prefill of one long sequence cut
+into segments that run side by side ("为什么 Kimi K3 敢把 KV Cache 扔掉？一篇讲透
+GPT-2 到 K3 的架构进化", section 5: the chunk steps are affine in the state, so a
+run of them is one affine map), against the fp64 token recurrence. The gates
+are scaled down (slow decay) so that each segment's state still matters to the
+next one: with the workloads' decay a segment forgets its initial state within
+a chunk or two and a wrong scan would go unnoticed."""
+import numpy as np
+import pytest
+
+import oracle
+from linear_attention_recurrence_02_gb300 import synth
+from tests._util import assert_close, cuda_or_skip, ensure_built, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = cuda_or_skip()
+    ensure_built()
+    from linear_attention_recurrence_02_gb300 import kda
+    return torch, kda
+
+
+def _run(torch, kda, p, D, bf16, segments, C, gate="channel", with_s0=True):
+    dt = torch.bfloat16 if bf16 else torch.float32
+    q, k, v = (to_dev(p[n], dt, torch) for n in "qkv")
+    g_all = p["g"]
+    if gate == "head":
+        gk, go = np.ascontiguousarray(g_all[..., 0]), np.repeat(g_all[..., :1], D, axis=-1)
+    elif gate == "none":
+        gk, go = None, np.zeros_like(g_all)
+    else:
+        gk, go = g_all, g_all
+    s0 = p["s0"][0] if with_s0 else None
+    out = torch.empty_like(q)
+    sf = torch.empty((q.shape[1], D, D), device="cuda")
+    kda.kda_chunk_prefill_scan(q, k, v, None if gk is None else to_dev(gk, torch.float32, torch),
+                               to_dev(p["beta"], torch.float32, torch), out, segments,
+                               initial_state=None if s0 is None else to_dev(s0, torch.float32, torch),
+                               final_state=sf, gate=gate, chunk_size=C)
+    torch.cuda.synchronize()
+    kda.kda_sync_status()
+    ro, rs = oracle.recurrence(p["q"], p["k"], p["v"], go, p["beta"],
+                               s_init=None if s0 is None else s0[None])
+    return to_np(out), to_np(sf), ro, rs[0]
+
+
+@pytest.mark.parametrize("segments", [2, 3, 8])
+def test_scan_tensor_core_path(env, segments):
+    """bf16, d=128, C=64 (the tensor-core kernel for all three passes),
+    1061 tokens (a ragged last chunk), carry-in state."""
+    torch, kda = env
+    T, H, D = 1061, 2, 128
+    p = synth.prefill_inputs(31, T, H, D, True, s0_std=0.05, g_scale=0.02)
+    o, s, ro, rs = _run(torch, kda, p, D, True, segments, 64)
+    assert_close(o, ro, True, (1,), "out")
+    assert_close(s, rs, True, (0,), "final state")
+
+
+@pytest.mark.parametrize("gate", ["head", "none"])
+def test_scan_gate_forms(env, gate):
+    """Per-head gate and no gate (the state never decays: every segment's map
+    A is far from zero)."""
+    torch, kda = env
+    T, H, D = 640, 2, 128
+    p = synth.prefill_inputs(32, T, H, D, True, s0_std=0.05, g_scale=0.02)
+    o, s, ro, rs = _run(torch, kda, p, D, True, 4, 64, gate=gate)
+    assert_close(o, ro, True, (1,), "out")
+    assert_close(s, rs, True, (0,), "final state")
+
+
+@pytest.mark.parametrize("with_s0", [False, True])
+def test_scan_fp32_cuda_core_path(env, with_s0):
+    """fp32, d=16, C=16 (the CUDA-core kernel): the fp32 tolerance."""
+    torch, kda = env
+    T, H, D = 300, 3, 16
+    p = synth.prefill_inputs(33, T, H, D, False, s0_std=0.05, g_scale=0.02)
+    o, s, ro, rs = _run(torch, kda, p, D, False, 5, 16, with_s0=with_s0)
+    assert_close(o, ro, False, (1,), "out")
+    assert_close(s, rs, False, (0,), "final state")
+
+
+def test_scan_matches_the_serial_prefill(env):
+    """The workloads' own decay (g_scale 1): the segmented and the serial
+    prefill agree to bf16 tolerance."""
+    torch, kda = env
+    T, H, D = 2048, 4, 128
+    p = synth.prefill_inputs(34, T, H, D, True)
+    bf = torch.bfloat16
+    q, k, v = (to_dev(p[n], bf, torch) for n in "qkv")
+    g, b = to_dev(p["g"], torch.float32, torch), to_dev(p["beta"], torch.float32, torch)
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    s1, s2 = torch.empty((H, D, D), device="cuda"), torch.empty((H, D, D), device="cuda")
+    kda.kda_chunk_prefill(q, k, v, g, b, o1, final_state=s1[None], chunk_size=64)
+    kda.kda_chunk_prefill_scan(q, k, v, g, b, o2, 8, final_state=s2)
+    torch.cuda.synchronize()
+    assert_close(to_np(o2), to_np(o1), True, (1,), "out")
+    assert_close(to_np(s2), to_np(s1), True, (0,), "final state")
