@@ -95,6 +95,61 @@ __global__ void __launch_bounds__(SCAN_NT) segment_scan_kernel(const float *__re
     }
 }
 
+// D = 128: one CTA per (head, 16 value columns), 256 threads, each a 2 x 4
+// register tile of the output; A passes through shared memory transposed, 32
+// k at a time, so that a k step is one 8-byte load of A and one 16-byte load
+// of S for 8 FMAs.
+constexpr int SCAN128_JS = 16;
+__global__ void __launch_bounds__(SCAN_NT) segment_scan128_kernel(const float *__restrict__ A,
+                                                                   const float *__restrict__ B,
+                                                                   const float *__restrict__ S0,
+                                                                   float *__restrict__ Sp, int P, int H) {
+    constexpr int D = 128, JS = SCAN128_JS, NS = D / JS, KT = 32, LDA = D + 2;
+    __shared__ __align__(16) float sS[D][JS];
+    __shared__ __align__(16) float sAT[KT][LDA];
+    const int h = blockIdx.x / NS, j0 = (blockIdx.x % NS) * JS, tid = threadIdx.x;
+    const int i0 = (tid >> 2) * 2, c0 = (tid & 3) * 4;  // rows i0, i0+1; columns c0..c0+3 of the slice
+    const size_t DD = (size_t)D * D;
+    for (int e = tid; e < D * JS; e += SCAN_NT) {
+        const int i = e / JS, j = e % JS;
+        const float v = S0 ? S0[(size_t)h * DD + (size_t)i * D + j0 + j] : 0.f;
+        sS[i][j] = v;
+        Sp[(size_t)h * DD + (size_t)i * D + j0 + j] = v;
+    }
+    for (int p = 1; p < P; ++p) {
+        const float *Ap = A + ((size_t)(p - 1) * H + h) * DD;
+        const float *Bp = B + ((size_t)(p - 1) * H + h) * DD;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int k0 = 0; k0 < D; k0 += KT) {
+            __syncthreads();
+            for (int e = tid; e < D * KT; e += SCAN_NT) {  // row i, k0 + kk: 32 consecutive floats per row
+                const int i = e / KT, kk = e % KT;
+                sAT[kk][i] = Ap[(size_t)i * D + k0 + kk];
+            }
+            __syncthreads();
+#pragma unroll 8
+            for (int kk = 0; kk < KT; ++kk) {
+                const float2 a = *reinterpret_cast<const float2 *>(&sAT[kk][i0]);
+                const float4 sv = *reinterpret_cast<const float4 *>(&sS[k0 + kk][c0]);
+                acc[0][0] = fmaf(a.x, sv.x, acc[0][0]); acc[0][1] = fmaf(a.x, sv.y, acc[0][1]);
+                acc[0][2] = fmaf(a.x, sv.z, acc[0][2]); acc[0][3] = fmaf(a.x, sv.w, acc[0][3]);
+                acc[1][0] = fmaf(a.y, sv.x, acc[1][0]); acc[1][1] = fmaf(a.y, sv.y, acc[1][1]);
+                acc[1][2] = fmaf(a.y, sv.z, acc[1][2]); acc[1][3] = fmaf(a.y, sv.w, acc[1][3]);
+            }
+        }
+        __syncthreads();  // every thread is done reading the old state
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = i0 + r, j = c0 + c;
+                const float v = acc[r][c] + Bp[(size_t)i * D + j0 + j];
+                sS[i][j] = v;
+                Sp[((size_t)p * H + h) * DD + (size_t)i * D + j0 + j] = v;
+            }
+    }
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // segments actually used for P requested over T tokens in chunks of C
@@ -183,7 +238,9 @@ extern "C" kda_status kda_chunk_prefill_scan(const void *q, const void *k, const
     case 16: segment_scan_kernel<16><<<H * ns, SCAN_NT, 0, s>>>(As, Bs, initial_state, Sp, P, H); break;
     case 32: segment_scan_kernel<32><<<H * ns, SCAN_NT, 0, s>>>(As, Bs, initial_state, Sp, P, H); break;
     case 64: segment_scan_kernel<64><<<H * ns, SCAN_NT, 0, s>>>(As, Bs, initial_state, Sp, P, H); break;
-    default: segment_scan_kernel<128><<<H * ns, SCAN_NT, 0, s>>>(As, Bs, initial_state, Sp, P, H); break;
+    default:
+        segment_scan128_kernel<<<H * (128 / SCAN128_JS), SCAN_NT, 0, s>>>(As, Bs, initial_state, Sp, P, H);
+        break;
     }
     if ((st = check_launch("segment_scan_kernel"))) return st;
     // 4. outputs and final states from the true initial states
