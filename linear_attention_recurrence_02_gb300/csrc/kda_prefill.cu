@@ -38,13 +38,13 @@ __host__ __device__ inline size_t simt_smem_floats(int D, int C) {
     return (size_t)3 * C * LD + (size_t)D * JS + (size_t)C * JS + 2 * (size_t)C * C + 2 * (size_t)D + C;
 }
 
-template <int D, typename T>
+template <int D, typename T, bool VZ>  // VZ: v is read as all zeros (not loaded)
 __global__ void __launch_bounds__(SIMT_NT)
     prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                         const float *__restrict__ g, const float *__restrict__ beta,
                         const float *s_init, float *s_final, T *__restrict__ out,
                         const int64_t *__restrict__ cu_seqlens, int N, int64_t Ttot, int H, int C, float eps,
-                        unsigned *err, const int *__restrict__ order, int gate, int v_zero) {
+                        unsigned *err, const int *__restrict__ order, int gate) {
     constexpr int JS = simt_js(D), LD = D + 1, NS = D / JS, NW = SIMT_NT / 32;
     extern __shared__ float smem[];
     float *sQ = smem;                    // [C][LD]  q^, then Qt
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(SIMT_NT)
         }
         for (int p = tid; p < L * JS; p += SIMT_NT) {
             const int r = p / JS, j = p % JS;
-            sU[p] = v_zero ? 0.f : Elem<T>::load(v + ((size_t)(c0 + r) * H + h) * D + j0 + j);
+            sU[p] = VZ ? 0.f : Elem<T>::load(v + ((size_t)(c0 + r) * H + h) * D + j0 + j);
         }
         // cumulative log decay per key channel
         if (tid < D) {
@@ -189,14 +189,14 @@ __global__ void __launch_bounds__(SIMT_NT)
 template <int D, typename T>
 static kda_status launch_simt(const PrefillArgs &a, cudaStream_t s) {
     const size_t smem = simt_smem_floats(D, a.C) * sizeof(float);
-    auto kern = prefill_simt_kernel<D, T>;
+    auto kern = a.v_zero ? prefill_simt_kernel<D, T, true> : prefill_simt_kernel<D, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
     const unsigned grid = (unsigned)a.N * a.H * (D / simt_js(D));
     kern<<<grid, SIMT_NT, smem, s>>>(static_cast<const T *>(a.q), static_cast<const T *>(a.k),
                                      static_cast<const T *>(a.v), a.g, a.beta, a.s_init, a.s_final,
                                      static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err,
-                                     a.order, a.gate, a.v_zero ? 1 : 0);
+                                     a.order, a.gate);
     return check_launch("prefill_simt_kernel");
 }
 
