@@ -415,6 +415,30 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
     varlen = bench_varlen(torch, kda, dev, stream, ws, hbm_peak)
     conv = bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak)
     epilogue = bench_epilogue(torch, kda, dev, stream, ws, hbm_peak)
+    # the prefill and its output epilogue in one call (kda_chunk_prefill_epi)
+    egen = torch.Generator(device=dev).manual_seed(PRE["seed"] + 13)
+    egate = torch.randn((T, H, D), generator=egen, device=dev).to(bf)
+    ew = torch.rand((D,), generator=egen, device=dev) + 0.5
+
+    def ecall():
+        kda.kda_chunk_prefill_epi(q, k, v, g, beta, out, egate, ew, final_state=sf, chunk_size=C, workspace=wsb,
+                                  stream=stream)
+    for _ in range(3):
+        ecall()
+    torch.cuda.synchronize(dev)
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a0, b0 in ee:
+        a0.record(stream)
+        ecall()
+        b0.record(stream)
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status(stream)
+    ems = max_over_ranks(statistics.mean(a0.elapsed_time(b0) for a0, b0 in ee), dev)
+    epilogue["with_prefill"] = {
+        "ms_per_call": ems, "unit": "ms", "prefill_alone_ms": ms,
+        "workload": "kda_chunk_prefill_epi on the 4096-token prefill (sigmoid gate): the prefill, then the "
+                    "epilogue pass in place"}
+    del egate
     long_seq = bench_long_sequence(torch, kda, dev, stream, ws)
     # the same workload with a per-head gate (Gated DeltaNet) and with none (DeltaNet)
     gates = {}

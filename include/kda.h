@@ -258,6 +258,24 @@ kda_status kda_chunk_prefill_scan(const void *q, const void *k, const void *v, c
                                   float l2_eps, int segments, void *workspace, size_t workspace_bytes,
                                   kda_stream_t stream);
 
+/*
+ * kda_chunk_prefill_gated followed by the output epilogue of
+ * kda_gated_rmsnorm on its output, in one call: out receives
+ *   RMSNorm(o) * norm_weight * act(out_gate)
+ * per (token, head) row, o being the attention output: the prefill, then
+ * the epilogue kernel in place over out (run inside the tensor-core prefill
+ * kernel instead, it was slower). out_gate [T,H,D] dtype, norm_weight [D]
+ * fp32 (16-byte aligned);
+ * out_gate may not alias out, q, k or v. Other arguments and errors as
+ * kda_chunk_prefill_gated and kda_gated_rmsnorm.
+ */
+kda_status kda_chunk_prefill_epi(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const float *initial_state, float *final_state,
+                                 void *out, const int64_t *cu_seqlens, int N, int64_t T, int H, int D,
+                                 int C, kda_dtype dtype, kda_gate gate, float l2_eps, const void *out_gate,
+                                 const float *norm_weight, kda_gate_act act, float norm_eps,
+                                 void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
 /* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
 size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);
 

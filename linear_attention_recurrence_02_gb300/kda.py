@@ -76,6 +76,8 @@ _SIGNATURES = {
                                    _ci, _cf, _vp], _ci),
     "kda_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i64, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_chunk_prefill_scan_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
+    "kda_chunk_prefill_epi": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci, _ci,
+                               _cf, _vp, _vp, _ci, _cf, _vp, _sz, _vp], _ci),
     "kda_chunk_prefill_scan": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _ci, _ci, _ci, _ci, _ci, _cf, _ci,
                                 _vp, _sz, _vp], _ci),
     "kda_sync_status": ([_vp], _ci),
@@ -259,6 +261,30 @@ def kda_gated_rmsnorm(o, gate, weight, y, act="sigmoid", eps=1e-6, stream=None):
         raise ValueError(f"act must be one of {sorted(_ACTS)}")
     _check(lib().kda_gated_rmsnorm(_ptr(o), _ptr(gate), _ptr(weight), _ptr(y), T, H, D, _dtype_code(o),
                                    _ACTS[act], float(eps), _stream(stream, o.device)))
+
+
+def kda_chunk_prefill_epi(q, k, v, g, beta, out, out_gate, norm_weight, gate="channel", act="sigmoid",
+                          norm_eps=1e-6, initial_state=None, final_state=None, cu_seqlens=None, chunk_size=64,
+                          l2_eps=1e-6, workspace=None, stream=None):
+    """kda_chunk_prefill_gated whose output goes through the gated RMSNorm
+    epilogue in the same call: out = RMSNorm(o) * norm_weight * act(out_gate).
+    out_gate [T,H,D] like q; norm_weight [D] fp32."""
+    T, H, D = q.shape
+    code = _check_gate(g, gate, (T,), H, D)
+    if tuple(out_gate.shape) != (T, H, D) or tuple(norm_weight.shape) != (D,):
+        raise ValueError("shape mismatch")
+    if act not in _ACTS:
+        raise ValueError(f"act must be one of {sorted(_ACTS)}")
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    ws_bytes = kda_chunk_prefill_workspace_bytes(T, N, H, D, chunk_size)
+    if workspace is None and ws_bytes > 0:
+        import torch
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kda_chunk_prefill_epi(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                       _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
+                                       _dtype_code(q), code, float(l2_eps), _ptr(out_gate), _ptr(norm_weight),
+                                       _ACTS[act], float(norm_eps), _ptr(workspace), wsz, _stream(stream, q.device)))
 
 
 def kda_chunk_prefill_scan_workspace_bytes(T, H, D, C, segments) -> int:

@@ -265,3 +265,17 @@ def test_prefill_scan_argument_checks(kda):
     assert need >= 4 * 4 * 2 * 128 * 128 * 4  # four fp32 states per segment and head
     st = L.kda_chunk_prefill_scan(None, *args[1:], 1, None, 0, None)
     assert st == kda.KDA_ERR_INVALID_ARG and "q is NULL" in L.kda_last_error_detail().decode()
+
+
+def test_prefill_epi_argument_checks(kda):
+    """kda_chunk_prefill_epi: bad activation, NULL weight and an out_gate that
+    aliases out are rejected before any launch."""
+    L = kda.lib()
+    base = (0x10000, 0x20000, 0x30000, 0x40000, 0x50000, None, None, 0x60000, None, 1, 100, 2, 128, 64, 1,
+            kda.KDA_GATE_CHANNEL, 1e-6)
+    st = L.kda_chunk_prefill_epi(*base, 0x70000, 0x80000, 5, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "act must be" in L.kda_last_error_detail().decode()
+    st = L.kda_chunk_prefill_epi(*base, 0x70000, None, kda.KDA_ACT_SIGMOID, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "norm_weight is NULL" in L.kda_last_error_detail().decode()
+    st = L.kda_chunk_prefill_epi(*base, 0x60000, 0x80000, kda.KDA_ACT_SIGMOID, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG and "out_gate must not alias" in L.kda_last_error_detail().decode()

@@ -71,3 +71,69 @@ def test_gated_rmsnorm_full_size_sampled_rows(env):
     got = to_np(y)[ts, hs]
     ref = oracle.gated_rmsnorm(d["o"][ts, hs], d["gate"][ts, hs], d["weight"])
     assert_close(got[:, None], ref[:, None], True, (0, 1), "sampled rows")
+
+
+def _epi_ref(p, d, act, s0=None):
+    ro, rs = oracle.recurrence(p["q"], p["k"], p["v"], p["g"], p["beta"], s_init=s0, cu_seqlens=p["cu_seqlens"])
+    return oracle.gated_rmsnorm(ro, d["gate"], d["weight"], eps=1e-6, act=act), rs
+
+
+@pytest.mark.parametrize("act", ["sigmoid", "silu"])
+def test_prefill_epi_tensor_core(env, act):
+    """kda_chunk_prefill_epi on the tensor-core path (bf16, d=128, C=64). Two
+    sequences of 130 and 77 tokens (short last chunks), carry-in states."""
+    torch, kda = env
+    H, D = 2, 128
+    cu = np.array([0, 130, 207], dtype=np.int64)
+    T = int(cu[-1])
+    p = synth.prefill_inputs(41, T, H, D, True, cu_seqlens=cu, s0_std=0.05)
+    d = synth.epilogue_inputs(42, T, H, D, True)
+    bf = torch.bfloat16
+    q, k, v = (to_dev(p[n], bf, torch) for n in "qkv")
+    out = torch.empty_like(q)
+    sf = torch.empty((2, H, D, D), device="cuda")
+    kda.kda_chunk_prefill_epi(q, k, v, to_dev(p["g"], torch.float32, torch), to_dev(p["beta"], torch.float32, torch),
+                              out, to_dev(d["gate"], bf, torch), to_dev(d["weight"], torch.float32, torch), act=act,
+                              initial_state=to_dev(p["s0"], torch.float32, torch), final_state=sf,
+                              cu_seqlens=torch.from_numpy(cu).cuda())
+    torch.cuda.synchronize()
+    kda.kda_sync_status()
+    ref, rs = _epi_ref(p, d, act, p["s0"])
+    assert_close(to_np(out), ref, True, (1,), "out")
+    assert_close(to_np(sf), rs, True, (0, 1), "final state")
+
+
+def test_prefill_epi_cuda_core(env):
+    """fp32, d=16, C=16: the CUDA-core prefill, then the epilogue pass."""
+    torch, kda = env
+    T, H, D = 90, 3, 16
+    p = synth.prefill_inputs(43, T, H, D, False)
+    d = synth.epilogue_inputs(44, T, H, D, False)
+    q, k, v = (to_dev(p[n], torch.float32, torch) for n in "qkv")
+    out = torch.empty_like(q)
+    kda.kda_chunk_prefill_epi(q, k, v, to_dev(p["g"], torch.float32, torch), to_dev(p["beta"], torch.float32, torch),
+                              out, to_dev(d["gate"], torch.float32, torch), to_dev(d["weight"], torch.float32, torch),
+                              act="silu", chunk_size=16)
+    torch.cuda.synchronize()
+    ref, _ = _epi_ref(p, d, "silu")
+    assert_close(to_np(out), ref, False, (1,), "out")
+
+
+def test_prefill_epi_full_size_matches_separate_pass(env):
+    """The 4K workload (T=4096, H=96): the one-call prefill with epilogue
+    against the prefill followed by kda_gated_rmsnorm, every row."""
+    torch, kda = env
+    T, H, D = 4096, 96, 128
+    p = synth.prefill_inputs(2, T, H, D, True)
+    d = synth.epilogue_inputs(45, T, H, D, True)
+    bf = torch.bfloat16
+    q, k, v = (to_dev(p[n], bf, torch) for n in "qkv")
+    g, b = to_dev(p["g"], torch.float32, torch), to_dev(p["beta"], torch.float32, torch)
+    gate, w = to_dev(d["gate"], bf, torch), to_dev(d["weight"], torch.float32, torch)
+    fused, plain = torch.empty_like(q), torch.empty_like(q)
+    kda.kda_chunk_prefill_epi(q, k, v, g, b, fused, gate, w)
+    kda.kda_chunk_prefill(q, k, v, g, b, plain)
+    sep = torch.empty_like(q)
+    kda.kda_gated_rmsnorm(plain, gate, w, sep)
+    torch.cuda.synchronize()
+    assert_close(to_np(fused), to_np(sep), True, (1,), "fused vs separate")
