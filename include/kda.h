@@ -342,7 +342,9 @@ kda_status kda_chunk_prefill_gated(const void *q, const void *k, const void *v, 
  * kda_chunk_prefill with a workspace instead).
  * The first call on a device looks up the array's device address (once per
  * device, with that device current), so make that first call before any
- * stream capture. Every call on a device shares the array, which keeps the
+ * stream capture. The address is kept with the CUDA context it belongs to: if
+ * the device's primary context is rebuilt (cudaDeviceReset), the next call
+ * looks it up again, so that call too should come before any capture. Every call on a device shares the array, which keeps the
  * previous call's contents. Nothing in it needs clearing, because each call
  * rewrites every entry it reads. Calls that may overlap on the GPU (different
  * streams, no ordering between them) race on the array and must not be issued.

@@ -5,6 +5,7 @@
 #include <string>
 
 #include <atomic>
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
@@ -67,23 +68,58 @@ kda_status check_launch(const char *what) {
 
 __device__ unsigned g_device_error_word;
 
-unsigned *device_error_word() {
-    // looked up once per device (the calling thread's current device)
-    static std::atomic<unsigned *> cache[64];
+// The CUDA context current on the calling thread, through the driver entry
+// point (the library links only the runtime). NULL when none is current.
+static void *current_context() {
+    typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+    static std::atomic<CtxGetCurrentFn> fn{nullptr};
+    CtxGetCurrentFn f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || p == nullptr) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        f = reinterpret_cast<CtxGetCurrentFn>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    CUcontext c = nullptr;
+    return f(&c) == CUDA_SUCCESS ? static_cast<void *>(c) : nullptr;
+}
+
+kda_status symbol_address(const void *symbol, SymbolCache &cache, void **out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
-        unsigned *c = cache[dev].load(std::memory_order_acquire);
-        if (c) return c;
-    } else {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
         cudaGetLastError();
-        dev = -1;
+        return fail(KDA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    }
+    if (dev < 0 || dev >= SymbolCache::MAX_DEV) return fail(KDA_ERR_UNSUPPORTED, "device index above 63");
+    std::lock_guard<std::mutex> lock(cache.mu);
+    void *ctx = current_context();
+    if (cache.addr[dev] != nullptr && ctx != nullptr && ctx == cache.ctx[dev]) {
+        *out = cache.addr[dev];
+        return KDA_OK;
     }
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) {
+    e = cudaGetSymbolAddress(&p, symbol);
+    if (e != cudaSuccess || p == nullptr) {
         cudaGetLastError();
-        return nullptr;
+        return fail(KDA_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
     }
-    if (dev >= 0) cache[dev].store(static_cast<unsigned *>(p), std::memory_order_release);
+    // the lookup makes the device's primary context current if none was
+    cache.addr[dev] = p;
+    cache.ctx[dev] = ctx != nullptr ? ctx : current_context();
+    *out = p;
+    return KDA_OK;
+}
+
+unsigned *device_error_word() {
+    static SymbolCache cache;
+    void *p = nullptr;
+    if (symbol_address(&g_device_error_word, cache, &p) != KDA_OK) return nullptr;
     return static_cast<unsigned *>(p);
 }
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <string>
 
 #include "kda.h"
@@ -32,6 +33,18 @@ kda_status check_ptr(const void *p, const char *name);
 // bit 1 = bounded wait timed out.
 enum : unsigned { DEVERR_SEQLENS = 1u, DEVERR_TIMEOUT = 2u };
 unsigned *device_error_word();  // device address of the word on the current device
+
+// Device address of a file-scope __device__ variable on the current device.
+// The lookup is cached per device and keyed on the CUDA context that was
+// current when it was made: after a cudaDeviceReset the primary context, and
+// with it the variable's address, is new, and the next call looks it up again.
+struct SymbolCache {
+    static constexpr int MAX_DEV = 64;
+    std::mutex mu;
+    void *addr[MAX_DEV] = {};
+    void *ctx[MAX_DEV] = {};
+};
+kda_status symbol_address(const void *symbol, SymbolCache &cache, void **out);
 
 // ---------------------------------------------------------------- device side
 template <typename T> struct Elem;

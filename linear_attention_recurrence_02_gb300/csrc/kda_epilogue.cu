@@ -52,9 +52,12 @@ template <typename Vec> __device__ __forceinline__ void st_stream(Vec *p, const 
 }
 
 template <int D, typename T, int ACT>
-__global__ void __launch_bounds__(128) gated_rmsnorm_kernel(const T *__restrict__ o, const T *__restrict__ gate,
-                                                            const float *__restrict__ weight, T *__restrict__ y,
+__global__ void __launch_bounds__(128) gated_rmsnorm_kernel(const T *o, const T *gate,
+                                                            const float *__restrict__ weight, T *y,
                                                             long long R, float eps) {
+    // y may alias o or gate (the in-place epilogue of a prefill output), so
+    // none of the three is declared restrict; each thread loads every element
+    // it stores before storing it.
     constexpr int LPR = D < 32 ? D : 32;  // lanes per row
     constexpr int V = D / LPR;            // channels per lane
     constexpr int RPW = 32 / LPR;         // rows per warp pass

@@ -12,7 +12,6 @@
 // exits. The entry point below passes the array's device address as the
 // workspace of the ordinary prefill, so the computation is identical to
 // kda_chunk_prefill with a caller-provided workspace.
-#include <mutex>
 #include <string>
 
 #include "kda_common.cuh"
@@ -23,31 +22,14 @@ static __device__ __align__(256) int g_noalloc_order[KDA_NOALLOC_MAX_SEQS];
 
 namespace kda {
 
-// The symbol's device address, looked up once per device with that device
-// current. In host code `g_noalloc_order` is only a host-side stand-in, so
-// the kernel must be given this address, never the name.
+// The symbol's device address on the current device. In host code
+// `g_noalloc_order` is only a host-side stand-in, so the kernel must be given
+// this address, never the name. It is looked up on a device's first call and
+// again whenever the device's context has changed since (a cudaDeviceReset
+// rebuilds the primary context, and the array moves with it).
 static kda_status noalloc_scratch(void **out) {
-    static std::mutex mu;
-    static void *addr[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(KDA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
-    }
-    if (dev < 0 || dev >= 64) return fail(KDA_ERR_UNSUPPORTED, "device index above 63");
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_order);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return fail(KDA_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-        }
-        addr[dev] = p;
-    }
-    *out = addr[dev];
-    return KDA_OK;
+    static SymbolCache cache;
+    return symbol_address(&g_noalloc_order, cache, out);
 }
 
 }  // namespace kda

@@ -32,10 +32,11 @@
 // one 128-row tile that becomes [Lk; Lq] in place; W' is later read back over
 // its dead Lk rows, so G4 and G5 are one MMA group over [W'; Lq].
 //
-// One CTA (384 threads) per (sequence, head) walks the chunks of its
-// sequence with two warp groups: eight "prep" warps run the state-independent
-// work of chunk c + 1 while four "chain" warps run the state chain of chunk c
-// (see the pipelined kernel below). Every wait is bounded.
+// One CTA (512 threads) per (sequence, head) walks the chunks of its
+// sequence with three warp groups: eight "front" warps build the operand
+// tiles of chunk c + 2, four "back" warps run the MMAs and the solve of chunk
+// c + 1, and four "chain" warps run the state chain of chunk c (see the
+// pipelined kernel below). Every wait is bounded.
 #include <cuda.h>
 
 #include <atomic>

@@ -13,6 +13,7 @@ already run.
 import numpy as np
 import pytest
 
+import oracle
 from linear_attention_recurrence_02_gb300 import synth
 from tests._util import BF16_REL, F32_ATOL, cuda_or_skip, ensure_built, to_dev, to_np
 
@@ -27,9 +28,14 @@ def env():
     return torch, kda
 
 
-def _inputs(torch, seed, lengths, bf16, D=128):
+def _draw(seed, lengths, bf16, D=128):
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
-    d = synth.prefill_inputs(seed, int(cu[-1]), 3, D, bf16, cu_seqlens=cu, s0_std=0.1, g_scale=0.2)
+    return synth.prefill_inputs(seed, int(cu[-1]), 3, D, bf16, cu_seqlens=cu, s0_std=0.1, g_scale=0.2)
+
+
+def _inputs(torch, seed, lengths, bf16, D=128):
+    d = _draw(seed, lengths, bf16, D)
+    cu = d["cu_seqlens"]
     dt = torch.bfloat16 if bf16 else torch.float32
     t = {n: to_dev(d[n], dt, torch) for n in ("q", "k", "v")}
     t["g"] = to_dev(d["g"], torch.float32, torch)
@@ -70,6 +76,25 @@ def test_noalloc_prefill_matches_workspace_prefill_twice(env, bf16):
         o_na, s_na = _run(torch, kda, t, n, noalloc=True)
         _close(o_na, o_ref, bf16)
         _close(s_na, s_ref, bf16)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_noalloc_single_sequence_and_oracle(env, bf16):
+    # N = 1 needs no launch order, so the call passes no scratch at all; then a
+    # small mixed batch against the fp64 oracle directly, per (sequence, head)
+    torch, kda = env
+    for seed, lengths in ((903, [150]), (904, [64, 0, 97, 2])):
+        d = _draw(seed, lengths, bf16)
+        t, n = _inputs(torch, seed, lengths, bf16)
+        o_na, s_na = _run(torch, kda, t, n, noalloc=True)
+        ro, rs = oracle.recurrence(d["q"], d["k"], d["v"], d["g"], d["beta"], s_init=d["s0"],
+                                   cu_seqlens=d["cu_seqlens"], eps=1e-6)
+        cu = d["cu_seqlens"]
+        for i in range(n):
+            a, b = cu[i], cu[i + 1]
+            if b > a:
+                _close(o_na[a:b], ro[a:b], bf16)
+            _close(s_na[i], rs[i], bf16)
 
 
 def test_noalloc_rejects_batches_above_its_limit(env):
