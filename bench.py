@@ -334,6 +334,7 @@ def run_ours(args):
     d2h = out.numel() * 2
 
     dec_unfused = bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d)
+    dec_epi = bench_decode_epi(torch, kda, dev, stream, ws, hbm_peak, d, ms_per_step)
 
     prefill = None
     if not args.no_prefill:
@@ -365,6 +366,7 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
             "decode_unfused": dec_unfused,
+            "decode_epilogue": dec_epi,
         }
         if prefill is not None:
             line["prefill"] = prefill
@@ -690,6 +692,43 @@ def bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d, steps=200):
             "kernel": "decode_step_kernel",
             "config": {"workload": f"decode step without conv (kda_decode_step): B={B}, H={H}, d={D}, bf16 q/k/v, "
                                    "fp32 state 384 MiB", "steps": steps},
+            "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+
+
+def bench_decode_epi(torch, kda, dev, stream, ws, hbm_peak, d, fused_ms, steps=200):
+    """The fused conv + decode step with the gated RMSNorm output epilogue in
+    the same launch (kda_shortconv_decode_step_epi) on the headline workload:
+    the step's bytes plus the output gate read (bf16) and the norm weight;
+    the output is the epilogue's y instead of o."""
+    bf = torch.bfloat16
+
+    def up(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev, dt)
+    x, ring, w = up(d["x"], bf), up(d["ring"], bf), up(d["w"], torch.float32)
+    g, beta, state = up(d["g"], torch.float32), up(d["beta"], torch.float32), up(d["s0"], torch.float32)
+    e = synth.epilogue_inputs(DEC["seed"] + 50, B, H, D, True)
+    og, nw = up(e["gate"], bf), up(e["weight"], torch.float32)
+    y = torch.empty((B, H, D), dtype=bf, device=dev)
+
+    def step():
+        kda.kda_shortconv_decode_step_epi(x, ring, w, g, beta, state, og, nw, y, stream=stream)
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status(stream)
+    ms = max_over_ranks(a.elapsed_time(b) / steps, dev)
+    by = STEP_BYTES + B * H * D * 2 + D * 4
+    return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "fused_step_without_epilogue_ms": fused_ms, "kernel": "fused_decode_kernel (output epilogue)",
+            "config": {"workload": f"fused conv + decode step with the gated RMSNorm epilogue (sigmoid gate) in "
+                                   f"one launch: B={B}, H={H}, d={D}, bf16, fp32 state 384 MiB", "steps": steps},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 

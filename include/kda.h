@@ -231,6 +231,34 @@ kda_status kda_gated_rmsnorm(const void *o, const void *gate, const float *weigh
                              kda_stream_t stream);
 
 /*
+ * Fused short conv + decode step with the output epilogue of
+ * kda_gated_rmsnorm applied before the output is stored, in one launch ([W]
+ * "KDA 递推公式先衰减再差分" for the step, [W] "相关源码与文档导航" and [G]
+ * section 6 for the gated RMSNorm; the reading of kda_gated_rmsnorm):
+ *
+ *   y[b,h,j] = o[b,h,j] / sqrt(mean_j' o[b,h,j']^2 + norm_eps)
+ *              * norm_weight[j] * act(out_gate[b,h,j])
+ *
+ * where o is the decode step's attention output, kept in fp32 inside the
+ * kernel (never rounded to `dtype` nor written to memory). The state and
+ * the ring are updated exactly as by kda_shortconv_decode_step_ex.
+ *   x, ring, w, g, beta, state: as kda_shortconv_decode_step_gated
+ *   out_gate [B,H,D] dtype: the output gate's pre-activation for this token
+ *   norm_weight [D] fp32, shared by the heads
+ *   y [B,H,D] dtype: receives the epilogue's result; it may not alias x,
+ *   ring, state or out_gate
+ * flags as kda_shortconv_decode_step_ex (with KDA_DECODE_OVERLAP_PREV the
+ * gate too is read only after the previous kernel has completed).
+ * Requires act KDA_ACT_SIGMOID or KDA_ACT_SILU and norm_eps >= 0; other
+ * requirements and errors as kda_shortconv_decode_step_ex. B = 0 is a no-op.
+ */
+kda_status kda_shortconv_decode_step_epi(const void *x, void *ring, const float *w, const float *g,
+                                         const float *beta, float *state, const void *out_gate,
+                                         const float *norm_weight, void *y, int B, int H, int D,
+                                         kda_dtype dtype, kda_gate gate, kda_gate_act act, float l2_eps,
+                                         float norm_eps, unsigned flags, kda_stream_t stream);
+
+/*
  * Chunked prefill of ONE sequence of T tokens, split into `segments` runs of
  * whole chunks that are processed side by side ([G] section 5: each chunk
  * step is affine in the state, S <- A S + B with A acting on the key axis,

@@ -13,6 +13,17 @@
 // and the decay run; column sums of S'^T k^ and S'^T q^ are reduced through
 // shared memory across the row groups; S is written once. The gate form
 // (per channel, per head, none) is a template parameter as in kda_decode.cu.
+//
+// With an output epilogue (template parameter EP = the gate activation), the
+// head's output vector o never leaves the CTA: it is normalised by its RMS,
+// scaled per channel by the norm weight and multiplied by act(gate) before
+// the one store ("WARP中Kimi Delta Attention线性注意力原理剖析", section
+// "相关源码与文档导航": a gated RMSNorm follows the recurrence; "为什么 Kimi K3
+// 敢把 KV Cache 扔掉？", section 6: an output gate scales the features). The
+// reading is that of kda_gated_rmsnorm, per (sequence, head) row of D value
+// channels: y = o / sqrt(mean(o^2) + eps) * weight * act(gate), a row whose
+// mean square plus eps is zero giving zeros. o is taken in fp32, before any
+// rounding to the storage type.
 #include <atomic>
 #include <string>
 
@@ -27,11 +38,22 @@ template <> struct FusedShape<32> { static constexpr int NT = 64; };
 template <> struct FusedShape<64> { static constexpr int NT = 128; };
 template <> struct FusedShape<128> { static constexpr int NT = 256; };
 
-template <int D, typename T, int GM>
+// Output epilogue selector: no epilogue (o is stored), or the gate
+// activation of the gated RMSNorm (KDA_ACT_SIGMOID, KDA_ACT_SILU).
+constexpr int EP_NONE = -1;
+
+// act(z) of the output gate, fp32 (one element per thread: exact forms)
+template <int EP> __device__ __forceinline__ float gate_act(float z) {
+    const float sg = 1.0f / (1.0f + expf(-z));
+    return EP == KDA_ACT_SILU ? z * sg : sg;
+}
+
+template <int D, typename T, int GM, int EP>
 __global__ void __launch_bounds__(FusedShape<D>::NT)
     fused_decode_kernel(const T *__restrict__ x, T *__restrict__ ring, const float *__restrict__ w,
                         const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ state,
-                        T *__restrict__ out, int H, float eps) {
+                        T *__restrict__ out, int H, float eps, const T *__restrict__ gate_in,
+                        const float *__restrict__ nweight, float neps) {
     constexpr int NT = FusedShape<D>::NT;
     constexpr int C4 = D / 4;     // float4 columns per state row
     constexpr int RG = NT / C4;   // row groups
@@ -70,11 +92,15 @@ __global__ void __launch_bounds__(FusedShape<D>::NT)
         Elem<T>::store(ring + ro + 2 * D, xv);
     }
     const size_t vo = (size_t)unit * D;
-    float av = 0.f;
+    float av = 0.f, gz = 0.f, nw = 0.f;
     if (t < D) {
         if constexpr (GM == KDA_GATE_CHANNEL) av = expf(__ldg(g + vo + t));
         else if constexpr (GM == KDA_GATE_HEAD) av = expf(__ldg(g + unit));
         else av = 1.f;
+        if constexpr (EP != EP_NONE) {
+            gz = Elem<T>::load(gate_in + vo + t);
+            nw = __ldg(nweight + t);
+        }
     }
     __syncthreads();
 
@@ -112,7 +138,7 @@ __global__ void __launch_bounds__(FusedShape<D>::NT)
         s_kh[t] = kv * rk;
         s_a[t] = av;
     }
-    __syncthreads();
+    __syncthreads();  // also: every thread has read s_red, which the epilogue reuses
 
     // 3. partial column sums over this thread's rows, then across row groups
     float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
@@ -139,6 +165,7 @@ __global__ void __launch_bounds__(FusedShape<D>::NT)
         }
     }
     __syncthreads();
+    float ov = 0.f;
     if (t < D) {
         float ks = 0.f, qs = 0.f;
 #pragma unroll
@@ -148,9 +175,26 @@ __global__ void __launch_bounds__(FusedShape<D>::NT)
         }
         const float d = __ldg(beta + unit) * (s_y[2][t] - ks);
         s_delta[t] = d;
-        Elem<T>::store(out + vo + t, qs + kq * d);
+        ov = qs + kq * d;
+        if constexpr (EP == EP_NONE) Elem<T>::store(out + vo + t, ov);
+    }
+    if constexpr (EP != EP_NONE) {  // the sum of o^2 over the head's D channels, per warp
+        float ss = ov * ov;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) s_red[warp][0] = ss;
     }
     __syncthreads();
+    if constexpr (EP != EP_NONE) {  // y = o / rms(o) * weight * act(gate): the only store of the output
+        if (t < D) {
+            float ss = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < NW; ++wi) ss += s_red[wi][0];
+            const float den = ss / (float)D + neps;
+            const float inv = den > 0.f ? 1.0f / sqrtf(den) : 0.f;
+            Elem<T>::store(out + vo + t, ov * inv * nw * gate_act<EP>(gz));
+        }
+    }
 
     // 4. S <- Diag(a) S + k^ delta^T, written back once
     const float d0 = s_delta[c4 * 4 + 0], d1 = s_delta[c4 * 4 + 1], d2 = s_delta[c4 * 4 + 2],
@@ -182,11 +226,12 @@ constexpr int BULK_NT = 256;
 constexpr uint32_t BULK_SMEM = 128 * 128 * 4 + 16;
 constexpr long long WAIT_LIMIT_DECODE = 2000000000LL;  // clock cycles (about 1 s)
 
-template <typename T, int GM>
+template <typename T, int GM, int EP>
 __global__ void __launch_bounds__(BULK_NT, 3)
     fused_decode_bulk_kernel(const T *__restrict__ x, T *__restrict__ ring, const float *__restrict__ w,
                              const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ state,
-                             T *__restrict__ out, int H, float eps, unsigned *err) {
+                             T *__restrict__ out, int H, float eps, unsigned *err, const T *__restrict__ gate_in,
+                             const float *__restrict__ nweight, float neps) {
     using namespace tc;
     constexpr int D = 128, NW = BULK_NT / 32;
     extern __shared__ uint8_t smem_raw[];
@@ -232,11 +277,15 @@ __global__ void __launch_bounds__(BULK_NT, 3)
         Elem<T>::store(ring + ro + 2 * D, xv);
     }
     const size_t vo = (size_t)unit * D;
-    float av = 0.f;
+    float av = 0.f, gz = 0.f, nw = 0.f;
     if (t < D) {
         if constexpr (GM == KDA_GATE_CHANNEL) av = expf(__ldg(g + vo + t));
         else if constexpr (GM == KDA_GATE_HEAD) av = expf(__ldg(g + unit));
         else av = 1.f;
+        if constexpr (EP != EP_NONE) {
+            gz = Elem<T>::load(gate_in + vo + t);
+            nw = __ldg(nweight + t);
+        }
     }
     __syncthreads();
 
@@ -274,7 +323,8 @@ __global__ void __launch_bounds__(BULK_NT, 3)
         s_kh[t] = kv * rk;
         s_a[t] = av;
     }
-    // 3. the state slice has landed (bounded wait)
+    // 3. the state slice has landed (bounded wait); the barrier also orders
+    // every read of s_red above before the epilogue reuses it
     const bool got = mbar_wait(&bar, 0, WAIT_LIMIT_DECODE);
     if (__syncthreads_or(!got)) {
         if (t == 0) {
@@ -306,15 +356,33 @@ __global__ void __launch_bounds__(BULK_NT, 3)
     __syncthreads();
     *reinterpret_cast<float4 *>(&s_part[rg][4 * c4]) = make_float4(pq[0], pq[1], pq[2], pq[3]);
     __syncthreads();
+    float ov = 0.f;
     if (t < D) {
         float qs = 0.f;
 #pragma unroll
         for (int wi = 0; wi < NW; ++wi) qs += s_part[wi][t];
         const float d = __ldg(beta + unit) * (s_y[2][t] - ks);
         s_delta[t] = d;
-        Elem<T>::store(out + vo + t, qs + kq * d);
+        ov = qs + kq * d;
+        if constexpr (EP == EP_NONE) Elem<T>::store(out + vo + t, ov);
+    }
+    if constexpr (EP != EP_NONE) {  // the sum of o^2 over the head's D channels, per warp
+        float ss = ov * ov;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) s_red[warp][0] = ss;
     }
     __syncthreads();
+    if constexpr (EP != EP_NONE) {  // y = o / rms(o) * weight * act(gate): the only store of the output
+        if (t < D) {
+            float ss = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < NW; ++wi) ss += s_red[wi][0];
+            const float den = ss / (float)D + neps;
+            const float inv = den > 0.f ? 1.0f / sqrtf(den) : 0.f;
+            Elem<T>::store(out + vo + t, ov * inv * nw * gate_act<EP>(gz));
+        }
+    }
 
     // 5. S <- Diag(a) S + k^ delta^T, written back once with 16-byte row stores
     const float4 d4 = *reinterpret_cast<const float4 *>(&s_delta[4 * c4]);
@@ -357,12 +425,23 @@ static int device_sms() {
     return n;
 }
 
-template <int D, typename T, int GM>
+// Epilogue operands of one launch: the output gate [B, H, D] (storage dtype),
+// the norm weight [D] and the norm eps; unused when EP == EP_NONE.
+struct EpiArgs {
+    const void *gate = nullptr;
+    const float *weight = nullptr;
+    float eps = 0.f;
+};
+
+template <int D, typename T, int GM, int EP>
 static void launch_fused(const void *x, void *ring, const float *w, const float *g, const float *beta,
-                         float *state, void *out, int B, int H, float eps, bool overlap, cudaStream_t s) {
+                         float *state, void *out, int B, int H, float eps, bool overlap, const EpiArgs &ea,
+                         cudaStream_t s) {
+    const T *gi = static_cast<const T *>(ea.gate);
     // three waves of the staged kernel or fewer
     if (D == 128 && (long long)B * H <= 9LL * device_sms()) {
-        if (smem_attr_once<fused_decode_bulk_kernel<T, GM>>((int)BULK_SMEM) != cudaSuccess) return;  // reported by check_launch
+        if (smem_attr_once<fused_decode_bulk_kernel<T, GM, EP>>((int)BULK_SMEM) != cudaSuccess)
+            return;  // reported by check_launch
         if (overlap) {  // programmatic dependent launch: may start while the previous kernel drains
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)B * H);
@@ -374,51 +453,48 @@ static void launch_fused(const void *x, void *ring, const float *w, const float 
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            cudaLaunchKernelEx(&cfg, fused_decode_bulk_kernel<T, GM>, static_cast<const T *>(x),
+            cudaLaunchKernelEx(&cfg, fused_decode_bulk_kernel<T, GM, EP>, static_cast<const T *>(x),
                                static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
-                               device_error_word());  // an error is left for check_launch
+                               device_error_word(), gi, ea.weight, ea.eps);  // an error is left for check_launch
             return;
         }
-        fused_decode_bulk_kernel<T, GM><<<(unsigned)B * H, BULK_NT, BULK_SMEM, s>>>(
+        fused_decode_bulk_kernel<T, GM, EP><<<(unsigned)B * H, BULK_NT, BULK_SMEM, s>>>(
             static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
-            device_error_word());
+            device_error_word(), gi, ea.weight, ea.eps);
     } else {
-        fused_decode_kernel<D, T, GM><<<(unsigned)B * H, FusedShape<D>::NT, 0, s>>>(
-            static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps);
+        fused_decode_kernel<D, T, GM, EP><<<(unsigned)B * H, FusedShape<D>::NT, 0, s>>>(
+            static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
+            gi, ea.weight, ea.eps);
     }
 }
 
-template <typename T, int GM>
+template <typename T, int GM, int EP>
 static void dispatch_fused(int D, const void *x, void *ring, const float *w, const float *g, const float *beta,
-                           float *state, void *out, int B, int H, float eps, bool ov, cudaStream_t s) {
+                           float *state, void *out, int B, int H, float eps, bool ov, const EpiArgs &ea,
+                           cudaStream_t s) {
     switch (D) {
-    case 16: launch_fused<16, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
-    case 32: launch_fused<32, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
-    case 64: launch_fused<64, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
-    default: launch_fused<128, T, GM>(x, ring, w, g, beta, state, out, B, H, eps, ov, s); break;
+    case 16: launch_fused<16, T, GM, EP>(x, ring, w, g, beta, state, out, B, H, eps, ov, ea, s); break;
+    case 32: launch_fused<32, T, GM, EP>(x, ring, w, g, beta, state, out, B, H, eps, ov, ea, s); break;
+    case 64: launch_fused<64, T, GM, EP>(x, ring, w, g, beta, state, out, B, H, eps, ov, ea, s); break;
+    default: launch_fused<128, T, GM, EP>(x, ring, w, g, beta, state, out, B, H, eps, ov, ea, s); break;
     }
 }
 
-template <typename T>
+template <typename T, int EP>
 static void dispatch_fused_gate(kda_gate gate, int D, const void *x, void *ring, const float *w, const float *g,
                                 const float *beta, float *state, void *out, int B, int H, float eps, bool ov,
-                                cudaStream_t s) {
+                                const EpiArgs &ea, cudaStream_t s) {
     if (gate == KDA_GATE_HEAD)
-        dispatch_fused<T, KDA_GATE_HEAD>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, s);
+        dispatch_fused<T, KDA_GATE_HEAD, EP>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, ea, s);
     else if (gate == KDA_GATE_NONE)
-        dispatch_fused<T, KDA_GATE_NONE>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, s);
-    else dispatch_fused<T, KDA_GATE_CHANNEL>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, s);
+        dispatch_fused<T, KDA_GATE_NONE, EP>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, ea, s);
+    else dispatch_fused<T, KDA_GATE_CHANNEL, EP>(D, x, ring, w, g, beta, state, out, B, H, eps, ov, ea, s);
 }
 
-}  // namespace kda
-
-using namespace kda;
-
-extern "C" kda_status kda_shortconv_decode_step_ex(const void *x, void *ring, const float *w, const float *g,
-                                                   const float *beta, float *state, void *out, int B, int H, int D,
-                                                   kda_dtype dtype, kda_gate gate, float l2_eps, unsigned flags,
-                                                   kda_stream_t stream) {
-    clear_detail();
+// Arguments shared by the fused entry points; KDA_OK when a launch may follow.
+static kda_status check_fused_args(const void *x, void *ring, const float *w, const float *g, const float *beta,
+                                   float *state, void *out, int B, int H, int D, kda_dtype dtype, kda_gate gate,
+                                   float l2_eps, unsigned flags) {
     if (flags & ~(unsigned)KDA_DECODE_OVERLAP_PREV) return invalid("flags: unknown bits");
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE)
         return invalid("gate must be KDA_GATE_CHANNEL, KDA_GATE_HEAD or KDA_GATE_NONE");
@@ -436,14 +512,68 @@ extern "C" kda_status kda_shortconv_decode_step_ex(const void *x, void *ring, co
         return st;
     if (out == x || out == ring || (const void *)out == (const void *)state)
         return invalid("out must not alias x, ring or state");
+    return KDA_OK;
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_shortconv_decode_step_ex(const void *x, void *ring, const float *w, const float *g,
+                                                   const float *beta, float *state, void *out, int B, int H, int D,
+                                                   kda_dtype dtype, kda_gate gate, float l2_eps, unsigned flags,
+                                                   kda_stream_t stream) {
+    clear_detail();
+    kda_status st = check_fused_args(x, ring, w, g, beta, state, out, B, H, D, dtype, gate, l2_eps, flags);
+    if (st != KDA_OK || B == 0) return st;
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool ov = (flags & KDA_DECODE_OVERLAP_PREV) != 0;
+    const EpiArgs none;
     if (dtype == KDA_BF16)
-        dispatch_fused_gate<__nv_bfloat16>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, ov, s);
+        dispatch_fused_gate<__nv_bfloat16, EP_NONE>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, ov, none,
+                                                    s);
     else
-        dispatch_fused_gate<float>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, ov, s);
+        dispatch_fused_gate<float, EP_NONE>(gate, D, x, ring, w, g, beta, state, out, B, H, l2_eps, ov, none, s);
     return check_launch("fused_decode_kernel");
+}
+
+extern "C" kda_status kda_shortconv_decode_step_epi(const void *x, void *ring, const float *w, const float *g,
+                                                    const float *beta, float *state, const void *out_gate,
+                                                    const float *norm_weight, void *y, int B, int H, int D,
+                                                    kda_dtype dtype, kda_gate gate, kda_gate_act act,
+                                                    float l2_eps, float norm_eps, unsigned flags,
+                                                    kda_stream_t stream) {
+    clear_detail();
+    kda_status st = check_fused_args(x, ring, w, g, beta, state, y, B, H, D, dtype, gate, l2_eps, flags);
+    if (st != KDA_OK) return st;
+    if (act != KDA_ACT_SIGMOID && act != KDA_ACT_SILU) return invalid("act must be KDA_ACT_SIGMOID or KDA_ACT_SILU");
+    if (!(norm_eps >= 0.f)) return invalid("norm_eps must be >= 0");
+    if (B == 0) return KDA_OK;
+    if ((st = check_ptr(out_gate, "out_gate")) || (st = check_ptr(norm_weight, "norm_weight"))) return st;
+    if (y == out_gate) return invalid("y must not alias out_gate");
+    if ((st = bind_stream_device(stream))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool ov = (flags & KDA_DECODE_OVERLAP_PREV) != 0;
+    EpiArgs ea;
+    ea.gate = out_gate;
+    ea.weight = norm_weight;
+    ea.eps = norm_eps;
+    if (dtype == KDA_BF16) {
+        if (act == KDA_ACT_SILU)
+            dispatch_fused_gate<__nv_bfloat16, KDA_ACT_SILU>(gate, D, x, ring, w, g, beta, state, y, B, H, l2_eps, ov,
+                                                             ea, s);
+        else
+            dispatch_fused_gate<__nv_bfloat16, KDA_ACT_SIGMOID>(gate, D, x, ring, w, g, beta, state, y, B, H, l2_eps,
+                                                                ov, ea, s);
+    } else {
+        if (act == KDA_ACT_SILU)
+            dispatch_fused_gate<float, KDA_ACT_SILU>(gate, D, x, ring, w, g, beta, state, y, B, H, l2_eps, ov, ea, s);
+        else
+            dispatch_fused_gate<float, KDA_ACT_SIGMOID>(gate, D, x, ring, w, g, beta, state, y, B, H, l2_eps, ov, ea,
+                                                        s);
+    }
+    return check_launch("fused_decode_kernel (output epilogue)");
 }
 
 extern "C" kda_status kda_shortconv_decode_step_gated(const void *x, void *ring, const float *w, const float *g,

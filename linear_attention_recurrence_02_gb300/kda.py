@@ -69,6 +69,8 @@ _SIGNATURES = {
     "kda_shortconv_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_shortconv_decode_step_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf,
                                       ctypes.c_uint, _vp], _ci),
+    "kda_shortconv_decode_step_epi": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci,
+                                       _cf, _cf, ctypes.c_uint, _vp], _ci),
     "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
     "kda_chunk_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
                            _cf, _vp, _sz, _vp], _ci),
@@ -234,6 +236,28 @@ def kda_shortconv_decode_step_ex(x, ring, w, g, beta, state, out, gate="channel"
     _check(lib().kda_shortconv_decode_step_ex(_ptr(x), _ptr(ring), _ptr(w), _ptr(g), _ptr(beta), _ptr(state),
                                               _ptr(out), B, H, D, _dtype_code(x), code, float(l2_eps), flags,
                                               _stream(stream, x.device)))
+
+
+def kda_shortconv_decode_step_epi(x, ring, w, g, beta, state, out_gate, norm_weight, y, gate="channel",
+                                  act="sigmoid", l2_eps=1e-6, norm_eps=1e-6, overlap_prev=False, stream=None):
+    """Fused short conv + decode step whose output goes through the gated
+    RMSNorm epilogue before it is stored: y = RMSNorm(o) * norm_weight *
+    act(out_gate), o the step's output (fp32 inside the kernel). out_gate and
+    y [B,H,D] like x; norm_weight [D] fp32; other arguments as
+    kda_shortconv_decode_step_ex."""
+    B, P, H, D = x.shape
+    code = _check_gate(g, gate, (B,), H, D)
+    if P != 3 or tuple(ring.shape) != (B, 3, H, 3, D) or tuple(w.shape) != (3, H, D, 4) \
+            or tuple(beta.shape) != (B, H) or tuple(state.shape) != (B, H, D, D) or tuple(y.shape) != (B, H, D) \
+            or tuple(out_gate.shape) != (B, H, D) or tuple(norm_weight.shape) != (D,):
+        raise ValueError("shape mismatch")
+    if act not in _ACTS:
+        raise ValueError(f"act must be one of {sorted(_ACTS)}")
+    flags = KDA_DECODE_OVERLAP_PREV if overlap_prev else 0
+    _check(lib().kda_shortconv_decode_step_epi(_ptr(x), _ptr(ring), _ptr(w), _ptr(g), _ptr(beta), _ptr(state),
+                                               _ptr(out_gate), _ptr(norm_weight), _ptr(y), B, H, D, _dtype_code(x),
+                                               code, _ACTS[act], float(l2_eps), float(norm_eps), flags,
+                                               _stream(stream, x.device)))
 
 
 def kda_shortconv_decode_step(x, ring, w, g, beta, state, out, l2_eps=1e-6, stream=None):

@@ -137,3 +137,112 @@ def test_prefill_epi_full_size_matches_separate_pass(env):
     kda.kda_gated_rmsnorm(plain, gate, w, sep)
     torch.cuda.synchronize()
     assert_close(to_np(fused), to_np(sep), True, (1,), "fused vs separate")
+
+
+# ------------------------------------------------------------------------------------------------------------
+# The epilogue fused into the fused conv + decode step (kda_shortconv_decode_step_epi): the oracle's conv
+# (fp64) feeds its recurrence, whose output goes through the oracle's gated RMSNorm.
+NCPU = max(1, len(__import__("os").sched_getaffinity(0)))
+
+
+def _gate_arg(d, gate):
+    """The decode inputs' g in the layout of `gate` (per-head gate: channel 0 of the drawn per-channel gate)."""
+    if gate == "head":
+        gh = np.ascontiguousarray(d["g"][..., 0])
+        return gh, np.repeat(gh[..., None], d["g"].shape[-1], axis=-1)
+    if gate == "none":
+        return None, np.zeros_like(d["g"])
+    return d["g"], d["g"]
+
+
+def _oracle_decode_epi(d, e, act, gate="channel"):
+    ry, rring = oracle.shortconv_step(d["x"], d["ring"], d["w"])
+    _, g_or = _gate_arg(d, gate)
+    ro, rs = oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], g_or, d["beta"], d["s0"], nthreads=NCPU)
+    B, H, D = ro.shape
+    ryo = oracle.gated_rmsnorm(ro.reshape(B, H, D), e["gate"], e["weight"], eps=1e-6, act=act)
+    return ryo, rs, rring
+
+
+def _gpu_decode_epi(torch, kda, d, e, bf16, act, gate="channel", overlap=False):
+    dt = torch.bfloat16 if bf16 else torch.float32
+    B, _, H, D = d["x"].shape
+    tx, tr = to_dev(d["x"], dt, torch), to_dev(d["ring"], dt, torch)
+    tw, tb = to_dev(d["w"], torch.float32, torch), to_dev(d["beta"], torch.float32, torch)
+    g_in, _ = _gate_arg(d, gate)
+    tg = to_dev(g_in, torch.float32, torch) if g_in is not None else None
+    ts = to_dev(d["s0"], torch.float32, torch)
+    og, nw = to_dev(e["gate"], dt, torch), to_dev(e["weight"], torch.float32, torch)
+    y = torch.full((B, H, D), float("nan"), dtype=dt, device="cuda")
+    kda.kda_shortconv_decode_step_epi(tx, tr, tw, tg, tb, ts, og, nw, y, gate=gate, act=act, overlap_prev=overlap)
+    torch.cuda.synchronize()
+    return to_np(y), to_np(ts), to_np(tr)
+
+
+@pytest.mark.parametrize("act", ["sigmoid", "silu"])
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_fused_decode_epilogue_matches_oracle(env, act, D, bf16):
+    """3 sequences x 5 heads (D = 128 takes the shared-memory-staged kernel at this size): y, state and ring."""
+    torch, kda = env
+    d = synth.decode_inputs(500 + D, 3, 5, D, bf16, s0_std=0.5)
+    e = synth.epilogue_inputs(600 + D, 3, 5, D, bf16)
+    y, st, ring = _gpu_decode_epi(torch, kda, d, e, bf16, act)
+    ry, rs, rring = _oracle_decode_epi(d, e, act)
+    assert_close(y, ry, bf16, (0, 1), "y")
+    assert_close(st, rs, bf16, (0, 1), "state")
+    assert np.max(np.abs(st - rs)) <= 1e-4
+    assert np.array_equal(ring, rring)
+
+
+@pytest.mark.parametrize("gate", ["head", "none"])
+@pytest.mark.parametrize("overlap", [False, True])
+def test_fused_decode_epilogue_gate_forms(env, gate, overlap):
+    """Per-head and no gate, plain and programmatic-dependent launches (the staged kernel: B=8, H=12)."""
+    torch, kda = env
+    d = synth.decode_inputs(700, 8, 12, 128, True, s0_std=0.3)
+    e = synth.epilogue_inputs(701, 8, 12, 128, True)
+    y, st, ring = _gpu_decode_epi(torch, kda, d, e, True, "sigmoid", gate=gate, overlap=overlap)
+    ry, rs, rring = _oracle_decode_epi(d, e, "sigmoid", gate=gate)
+    assert_close(y, ry, True, (0, 1), "y")
+    assert_close(st, rs, True, (0, 1), "state")
+    assert np.array_equal(ring, rring)
+
+
+def test_fused_decode_epilogue_zero_output_row(env):
+    """A head whose output is exactly zero (zero state, zero v: o = 0) maps to zeros with norm eps = 0, as the
+    oracle's reading fixes; the other heads are unaffected."""
+    torch, kda = env
+    d = synth.decode_inputs(710, 2, 3, 64, False, s0_std=None)
+    d["x"][0, 2, 1] = 0.0  # v projection of (sequence 0, head 1): conv of zeros plus a zero ring
+    d["ring"][0, 2, 1] = 0.0
+    e = synth.epilogue_inputs(711, 2, 3, 64, False)
+    dt = torch.float32
+    tx, tr = to_dev(d["x"], dt, torch), to_dev(d["ring"], dt, torch)
+    ts = to_dev(d["s0"], dt, torch)
+    y = torch.full((2, 3, 64), float("nan"), dtype=dt, device="cuda")
+    kda.kda_shortconv_decode_step_epi(tx, tr, to_dev(d["w"], dt, torch), to_dev(d["g"], dt, torch),
+                                      to_dev(d["beta"], dt, torch), ts, to_dev(e["gate"], dt, torch),
+                                      to_dev(e["weight"], dt, torch), y, norm_eps=0.0)
+    torch.cuda.synchronize()
+    ry, _ = oracle.shortconv_step(d["x"], d["ring"], d["w"])
+    ro, _ = oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], d["g"], d["beta"], d["s0"])
+    ref = oracle.gated_rmsnorm(ro, e["gate"], e["weight"], eps=0.0)
+    got = to_np(y)
+    assert np.all(got[0, 1] == 0.0) and np.all(ref[0, 1] == 0.0)
+    assert_close(got, ref, False, (0, 1), "y")
+
+
+def test_fused_decode_epilogue_full_size(env):
+    """The decode workload at full size (B=64, H=96, d=128, bf16: the register kernel), every unit against
+    the oracle."""
+    torch, kda = env
+    c = synth.DECODE
+    d = synth.decode_inputs(c["seed"], c["B"], c["H"], c["D"], True)
+    e = synth.epilogue_inputs(c["seed"] + 50, c["B"], c["H"], c["D"], True)
+    y, st, ring = _gpu_decode_epi(torch, kda, d, e, True, "sigmoid")
+    ry, rs, rring = _oracle_decode_epi(d, e, "sigmoid")
+    r = assert_close(y, ry, True, (0, 1), "y")
+    assert_close(st, rs, True, (0, 1), "state")
+    assert np.array_equal(ring, rring)
+    print(f"fused decode + epilogue, full size: worst per-head relative error {r:.3e}")
