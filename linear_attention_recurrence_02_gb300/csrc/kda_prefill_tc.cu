@@ -147,6 +147,120 @@ __device__ __forceinline__ void sync_tc() {
 }
 
 
+// ------------------------------------------------- MMA groups, issued by one elected lane
+// Each helper is called by a whole warp (warp-uniform control flow). One lane,
+// chosen by elect.sync, issues the group's MMAs and commits them to `bar`;
+// the shared-memory descriptors of the later K steps are the first ones plus
+// immediate offsets (the start-address field counts 16-byte units, and every
+// tile here lies below 256 KB, so the additions never carry out of it).
+// Issuing from a divergent `if (tid == 0)` with per-call descriptor
+// arithmetic cost about 100 cycles per MMA on a busy SM; this form about 60.
+
+// 8 MMAs over K = 128 (two 64-channel blocks of four 16-wide steps), A and B
+// K-major in shared memory, blocks ABLK / BBLK bytes apart; the first step
+// accumulates when `acc` is nonzero.
+template <uint32_t ABLK, uint32_t BBLK>
+__device__ __forceinline__ void mma8_ss(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc,
+                                        uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred p, a0, t;\n\t.reg .b64 x1, x2, x3, x4, x5, x6, x7, y1, y2, y3, y4, y5, y6, y7;\n\t"
+        "setp.ne.u32 a0, %4, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
+        "add.s64 x1, %1, 2;\n\tadd.s64 x2, %1, 4;\n\tadd.s64 x3, %1, 6;\n\t"
+        "add.s64 x4, %1, %6;\n\tadd.s64 x5, %1, %7;\n\tadd.s64 x6, %1, %8;\n\tadd.s64 x7, %1, %9;\n\t"
+        "add.s64 y1, %2, 2;\n\tadd.s64 y2, %2, 4;\n\tadd.s64 y3, %2, 6;\n\t"
+        "add.s64 y4, %2, %10;\n\tadd.s64 y5, %2, %11;\n\tadd.s64 y6, %2, %12;\n\tadd.s64 y7, %2, %13;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, a0;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x1, y1, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x2, y2, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x3, y3, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x4, y4, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x5, y5, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x6, y6, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x7, y7, %3, t;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}\n" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(acc), "r"(smem_u32(bar)), "n"(ABLK / 16), "n"(ABLK / 16 + 2),
+        "n"(ABLK / 16 + 4), "n"(ABLK / 16 + 6), "n"(BBLK / 16), "n"(BBLK / 16 + 2), "n"(BBLK / 16 + 4),
+        "n"(BBLK / 16 + 6)
+        : "memory");
+}
+
+// Two interleaved groups of four MMAs over K = 64 sharing the B operand
+// (K-major, steps 32 bytes apart): D1 = A1 B^T, D2 = A2 B^T with A1, A2
+// MN-major, K steps 2048 bytes apart (G2 and G3).
+__device__ __forceinline__ void mma44_ss(uint32_t d1, uint64_t a1, uint32_t d2, uint64_t a2, uint64_t bd,
+                                         uint32_t idesc, uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred p, f, t;\n\t.reg .b64 x1, x2, x3, z1, z2, z3, y1, y2, y3;\n\t"
+        "setp.ne.u32 f, 0, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
+        "add.s64 x1, %1, 128;\n\tadd.s64 x2, %1, 256;\n\tadd.s64 x3, %1, 384;\n\t"
+        "add.s64 z1, %3, 128;\n\tadd.s64 z2, %3, 256;\n\tadd.s64 z3, %3, 384;\n\t"
+        "add.s64 y1, %4, 2;\n\tadd.s64 y2, %4, 4;\n\tadd.s64 y3, %4, 6;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %4, %5, f;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%2], %3, %4, %5, f;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x1, y1, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%2], z1, y1, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x2, y2, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%2], z2, y2, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], x3, y3, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%2], z3, y3, %5, t;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}\n" ::"r"(d1),
+        "l"(a1), "r"(d2), "l"(a2), "l"(bd), "r"(idesc), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 8 MMAs with A in TMEM (bf16 pairs, 8 columns per 16-wide K step) and B
+// K-major in shared memory, two 64-channel blocks BBLK bytes apart (G4 + G5).
+template <uint32_t BBLK>
+__device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t at, uint64_t bd, uint32_t idesc, uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred p, f, t;\n\t.reg .b32 x1, x2, x3, x4, x5, x6, x7;\n\t.reg .b64 y1, y2, y3, y4, y5, y6, y7;\n\t"
+        "setp.ne.u32 f, 0, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
+        "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\tadd.u32 x4, %1, 32;\n\t"
+        "add.u32 x5, %1, 40;\n\tadd.u32 x6, %1, 48;\n\tadd.u32 x7, %1, 56;\n\t"
+        "add.s64 y1, %2, 2;\n\tadd.s64 y2, %2, 4;\n\tadd.s64 y3, %2, 6;\n\t"
+        "add.s64 y4, %2, %5;\n\tadd.s64 y5, %2, %6;\n\tadd.s64 y6, %2, %7;\n\tadd.s64 y7, %2, %8;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], y1, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], y2, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], y3, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x4], y4, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x5], y5, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x6], y6, %3, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x7], y7, %3, t;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}\n" ::"r"(d),
+        "r"(at), "l"(bd), "r"(idesc), "r"(smem_u32(bar)), "n"(BBLK / 16), "n"(BBLK / 16 + 2), "n"(BBLK / 16 + 4),
+        "n"(BBLK / 16 + 6)
+        : "memory");
+}
+
+// Two interleaved groups of four accumulating MMAs over K = 64 with the same
+// A in TMEM (8 columns per K step): D1 += A B1^T with B1 K-major (steps 32
+// bytes apart), D2 += A B2^T with B2 MN-major (steps 2048 bytes apart) (G6, G7).
+__device__ __forceinline__ void mma44_ts(uint32_t d1, uint64_t b1, uint32_t idesc1, uint32_t d2, uint64_t b2,
+                                         uint32_t idesc2, uint32_t at, uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t.reg .b32 x1, x2, x3;\n\t.reg .b64 y1, y2, y3, z1, z2, z3;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "add.u32 x1, %6, 8;\n\tadd.u32 x2, %6, 16;\n\tadd.u32 x3, %6, 24;\n\t"
+        "add.s64 y1, %1, 2;\n\tadd.s64 y2, %1, 4;\n\tadd.s64 y3, %1, 6;\n\t"
+        "add.s64 z1, %4, 128;\n\tadd.s64 z2, %4, 256;\n\tadd.s64 z3, %4, 384;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %1, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [%6], %4, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], y1, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x1], z1, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], y2, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x2], z2, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], y3, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x3], z3, %5, t;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}\n" ::"r"(d1),
+        "l"(b1), "r"(idesc1), "r"(d2), "l"(b2), "r"(idesc2), "r"(at), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------- the kernel
 // Three warp groups work on three consecutive chunks at once:
 //   front, warps 4-11: chunk c + 2's norms, cumulative decay, anchors and the
@@ -187,7 +301,8 @@ template <int GM> struct Regs {
     static_assert(4 * BACK + 8 * FRONT + 4 * CHAIN == 16 * 128, "register split");
 };
 constexpr uint32_t X0 = 0;              // [k; q] -> [Lk; Lq], chunk parity 0 (32 KB); parity 1 at X0 + 32768
-constexpr uint32_t V_ = 65536;          // v tile per parity (16 KB each); O staging after G3
+constexpr uint32_t V_ = 65536;          // v tile (16 KB): loaded for chunk c + 1 once G3 of chunk c is done
+constexpr uint32_t OST = 81920;         // O staging of the chain's bulk output store (16 KB)
 constexpr uint32_t G_ = 98304;          // g fp32 [64][128] -> G (log2 units) (32 KB)
 constexpr uint32_t RK0 = 131072;        // Rk (Kb on the exact path) per parity (16 KB each)
 constexpr uint32_t P0 = 163840;         // P per parity (8 KB each)
@@ -253,7 +368,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(s_sig + 256);
     uint64_t *bar_qk = bars;        // [2]
     uint64_t *bar_g = bars + 2;
-    uint64_t *bar_v = bars + 3;     // [2]
+    uint64_t *bar_v = bars + 3;
     uint64_t *bar_mp = bars + 5;    // prep MMA commits
     uint64_t *bar_c45 = bars + 6;   // [2]
     uint64_t *bar_c67 = bars + 8;
@@ -262,8 +377,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     uint64_t *bar_fr = bars + 13;   // [2] front -> back: operand tiles of chunk parity b built
     volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(bars + 15);
     uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + 16);
-    // TMA barriers qk0, qk1, g, v0, v1: phases armed and phases waited for, so
-    // that an aborted launch can let every copy in flight land before exiting
+    // TMA barriers qk0, qk1, g, v: phases armed and phases waited for, so that
+    // an aborted launch can let every copy in flight land before exiting
     uint32_t *s_armed = reinterpret_cast<uint32_t *>(bars + 17);
     uint32_t *s_waited = s_armed + 5;
     uint32_t *s_exact = reinterpret_cast<uint32_t *>(bars + 22);  // [2] chunk parity b takes the exact path
@@ -295,15 +410,15 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
         mbar_arrive_expect_tx(bar_g, G_BYTES);
         tma_load_2d(sm + G_, &tm_g, bar_g, x0, y);
     };
-    auto issue_v = [&](int y, int b) {
-        s_armed[3 + b] += 1;
+    auto issue_v = [&](int y) {
+        s_armed[3] += 1;
         if (v_zero) {  // nothing to load: release the tile; the back warps zero it
-            mbar_arrive(bar_v + b);
+            mbar_arrive(bar_v);
             return;
         }
-        mbar_arrive_expect_tx(bar_v + b, V_BYTES);
-        tma_load_2d(sm + V_ + 16384 * b, &tm_v, bar_v + b, x0, y);
-        tma_load_2d(sm + V_ + 16384 * b + 8192, &tm_v, bar_v + b, x0 + 64, y);
+        mbar_arrive_expect_tx(bar_v, V_BYTES);
+        tma_load_2d(sm + V_, &tm_v, bar_v, x0, y);
+        tma_load_2d(sm + V_ + 8192, &tm_v, bar_v, x0 + 64, y);
     };
 
     if (tid == 0) {
@@ -318,12 +433,9 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
         if (nchunks > 0) {
             issue_qk((int)start, 0);
             if constexpr (GCH) issue_g((int)start);
-            issue_v((int)start, 0);
+            issue_v((int)start);
         }
-        if (nchunks > 1) {
-            issue_qk((int)(start + C), 1);
-            issue_v((int)(start + C), 1);
-        }
+        if (nchunks > 1) issue_qk((int)(start + C), 1);
     }
     if (tid < 128) s_sigp[tid] = 1.f;
     if (warp == 0) {
@@ -357,10 +469,14 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
                 const bool has_next = ci + 1 < nchunks;
                 uint8_t *xb = sm + X0 + 32768 * b;
-                // ofree[b]: the chain is done with chunk ci - 2, hence the back warps too
-                bool got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
-                           (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
-                           (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
+                // ofree[b]: the chain is done with chunk ci - 2, hence the back warps too.
+                // One warp spins on the barriers; the others wait in the named
+                // barrier, which costs them no issue slots.
+                bool got = true;
+                if (ft < 32)
+                    got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
+                          (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
+                          (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
                 if (group_or(BAR_FRONT, 256, !got)) {
                     ok = false;
                     break;
@@ -476,7 +592,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 if (exact) {  // A and P with exact pairwise decays
                     // A goes to the back warps' solve buffer: wait until they are done with chunk ci - 1
                     if (ci > 0) {
-                        got = wait_or_abort(bar_ready + (b ^ 1), ((ci - 1) >> 1) & 1, s_abort);
+                        if (ft < 32) got = wait_or_abort(bar_ready + (b ^ 1), ((ci - 1) >> 1) & 1, s_abort);
                         if (group_or(BAR_FRONT, 256, !got)) {
                             ok = false;
                             break;
@@ -591,7 +707,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
                 uint8_t *xb = sm + X0 + 32768 * b;
                 const uint32_t xs = sbase + X0 + 32768 * b;
-                bool got = wait_or_abort(bar_fr + b, (ci >> 1) & 1, s_abort);
+                bool got = warp != 0 || wait_or_abort(bar_fr + b, (ci >> 1) & 1, s_abort);
                 if (group_or(BAR_BACK, 128, !got)) {
                     ok = false;
                     break;
@@ -601,20 +717,15 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 const float *sb = s_beta + 64 * b;
                 uint8_t *pb = sm + P0 + 8192 * b;
                 // G1: [A_raw; P_raw] = [Lk; Lq] Rk^T
-                if (tid == 0 && !exact) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                        mma_bf16(tbase + T_AP, sdesc_sw128(xs + kb * 16384 + ko, 16, 1024),
-                                 sdesc_sw128(sbase + RK0 + 16384 * b + kb * 8192 + ko, 16, 1024), ID_KK64, ks > 0);
-                    }
-                    mma_commit(bar_mp);
-                }
+                if (warp == 0 && !exact)
+                    mma8_ss<16384, 8192>(tbase + T_AP, sdesc_sw128(xs, 16, 1024),
+                                         sdesc_sw128(sbase + RK0 + 16384 * b, 16, 1024), ID_KK64, 0u, bar_mp);
                 pend_mp = !exact;
                 // warps 0, 1: A read-back; warps 2, 3: P read-back; then the solve
                 got = true;
                 if (!exact) {
-                    got = wait_or_abort(bar_mp, ph_mp, s_abort);
+                    if (warp == 0) got = wait_or_abort(bar_mp, ph_mp, s_abort);
+                    got = !group_or(BAR_BACK, 128, !got);
                     tc_fence_after();
                 }
                 if (!exact && got && q4 < 2) {  // A: TMEM lanes 0-63, masked (s < r), times beta
@@ -823,16 +934,19 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                         st_t(R, S, z);
                     }
                 }
-                // the v tile is needed from G3 on (the chain reloads it once the
-                // output store of chunk ci - 2 has read it)
-                got = got && wait_or_abort(bar_v + b, (ci >> 1) & 1, s_abort);
-                if (tid == 0 && got) s_waited[3 + b] += 1;
+                // the v tile is needed from G3 on (loaded right after G3 of the
+                // chunk before)
+                if (warp == 0) got = got && wait_or_abort(bar_v, ci & 1, s_abort);
+                if (tid == 0 && got) s_waited[3] += 1;
                 const int z0 = v_zero ? 0 : L;  // v read as zeros: every row
-                if (z0 < C && got) {  // v rows past the end of the sequence contribute nothing
+                // rows past the end of the sequence contribute nothing: zeroed
+                // once every back thread knows the tile has landed
+                if (z0 < C) got = !group_or(BAR_BACK, 128, !got);
+                if (z0 < C && got) {
                     const uint4 z4 = make_uint4(0, 0, 0, 0);
                     for (int p = tid; p < (C - z0) * 16; p += 128) {
                         const int r = z0 + (p >> 4), cc = p & 15;
-                        *reinterpret_cast<uint4 *>(sm + V_ + 16384 * b + swz(r, cc, 64)) = z4;
+                        *reinterpret_cast<uint4 *>(sm + V_ + swz(r, cc, 64)) = z4;
                     }
                 }
                 fence_async_smem();
@@ -848,25 +962,20 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 }
 
                 // G2: W'^T = Lk^T T^T (over A/P in TMEM),  G3: U0^T = V^T T^T
-                if (tid == 0) {
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t bd = sdesc_sw128(sbase + T_ + ks * 32, 16, 1024);
-                        mma_bf16(tbase + T_AP, sdesc_sw128(xs + ks * 2048, 16384, 1024), bd, ID_MK64, ks > 0);
-                        mma_bf16(tbase + T_U0 + 64 * b, sdesc_sw128(sbase + V_ + 16384 * b + ks * 2048, 8192, 1024), bd,
-                                 ID_MK64, ks > 0);
-                    }
-                    mma_commit(bar_mp);
-                }
+                if (warp == 0)
+                    mma44_ss(tbase + T_AP, sdesc_sw128(xs, 16384, 1024), tbase + T_U0 + 64 * b,
+                             sdesc_sw128(sbase + V_, 8192, 1024), sdesc_sw128(sbase + T_, 16, 1024), ID_MK64, bar_mp);
                 pend_mp = true;
-                got = wait_or_abort(bar_mp, ph_mp, s_abort);
-                tc_fence_after();
+                got = warp != 0 || wait_or_abort(bar_mp, ph_mp, s_abort);
                 if (group_or(BAR_BACK, 128, !got)) {
                     ok = false;
                     break;
                 }
+                tc_fence_after();
                 ph_mp ^= 1;
                 pend_mp = false;
+                // G3 has read the v tile: load the next chunk's v into it
+                if (tid == 0 && ci + 1 < nchunks) issue_v((int)(c0 + C));
                 // W'^T (lane i, column r) -> W' rows r over the Lk rows of this chunk's
                 // tile (dead after G2), so that [W'; Lq] is one K-major operand of G4/G5
                 {
@@ -910,28 +1019,22 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
         tmem_st_wait();
         uint32_t ph67 = 0;
         bool pend67 = false;
-        int v_due = -1;  // chunk whose v tile holds its output staging until the bulk store has read it
         int pend45 = -1;  // chunk whose G4/G5 are issued but not yet waited for
         int last_b = -1;
         for (int ci = 0; ci < nchunks; ++ci) {
             const int b = ci & 1;
             const int64_t c0 = start + (int64_t)ci * C;
             const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
-            bool got = wait_or_abort(bar_ready + b, (ci >> 1) & 1, s_abort);
+            bool got = ct >= 32 || wait_or_abort(bar_ready + b, (ci >> 1) & 1, s_abort);
             if (group_or(BAR_CHAIN, 128, !got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             // the previous chunk's bulk output store has had a whole back phase to
-            // read its staging (that chunk's v tile): load v of two chunks on into it
-            if (v_due >= 0) {
-                if (ct == 0) {
-                    bulk_wait_read();
-                    issue_v((int)(start + (int64_t)(v_due + 2) * C), v_due & 1);
-                }
-                v_due = -1;
-            }
+            // read the output staging; the barrier after the S~ conversion
+            // publishes that to the other chain threads before they rewrite it
+            if (ct == 0 && ci > 0) bulk_wait_read();
             // S = Diag(sigma) S_st. S~^T = S_st^T Diag(sf) -> TMEM bf16 pairs; S_st^T <- S_st^T Diag(pf)
             const float *sf = s_sf + 128 * b, *pf = s_pf + 128 * b;
 #pragma unroll 1
@@ -970,17 +1073,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             named_bar_sync(BAR_CHAIN, 128);
             tc_fence_after();
             // G4 + G5 in one group: [X^T | O^T] = S~^T [W'; Lq]^T
-            if (ct == 0) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-                    mma_bf16_ts(tbase + T_X, tbase + T_SB + 8 * ks,
-                                sdesc_sw128(sbase + X0 + 32768 * b + kb * 16384 + ko, 16, 1024), ID_KK128, ks > 0);
-                }
-                mma_commit(bar_c45 + b);
-            }
+            if (ct < 32)
+                mma8_ts<16384>(tbase + T_X, tbase + T_SB, sdesc_sw128(sbase + X0 + 32768 * b, 16, 1024), ID_KK128,
+                               bar_c45 + b);
             pend45 = ci;
-            got = wait_or_abort(bar_c45 + b, (ci >> 1) & 1, s_abort);
+            got = ct >= 32 || wait_or_abort(bar_c45 + b, (ci >> 1) & 1, s_abort);
             if (group_or(BAR_CHAIN, 128, !got)) {
                 ok = false;
                 break;
@@ -1009,18 +1106,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             named_bar_sync(BAR_CHAIN, 128);
             tc_fence_after();
             // G6: O^T += U^T P^T,  G7: S_st^T += U^T Rk (Kb on the exact path)
-            if (ct == 0) {
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t a = tbase + T_SB + 8 * ks;
-                    mma_bf16_ts(tbase + T_O, a, sdesc_sw128(sbase + P0 + 8192 * b + ks * 32, 16, 1024), ID_KK64, 1);
-                    mma_bf16_ts(tbase + T_S, a, sdesc_sw128(sbase + RK0 + 16384 * b + ks * 2048, 8192, 1024),
-                                ID_KM128, 1);
-                }
-                mma_commit(bar_c67);
-            }
+            if (ct < 32)
+                mma44_ts(tbase + T_O, sdesc_sw128(sbase + P0 + 8192 * b, 16, 1024), ID_KK64, tbase + T_S,
+                         sdesc_sw128(sbase + RK0 + 16384 * b, 8192, 1024), ID_KM128, tbase + T_SB, bar_c67);
             pend67 = true;
-            got = wait_or_abort(bar_c67, ph67, s_abort);
+            got = ct >= 32 || wait_or_abort(bar_c67, ph67, s_abort);
             if (group_or(BAR_CHAIN, 128, !got)) {
                 ok = false;
                 break;
@@ -1030,9 +1120,9 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             tc_fence_after();
             // U0[b], Rk[b], P[b] and the factors of this parity are consumed
             if (ct == 0) mbar_arrive(bar_ofree + b);
-            // O^T (lane j, column r) -> staging over this chunk's v tile (consumed by
-            // G3): two [64 rows][64 channels] bf16 boxes
-            uint8_t *ost = sm + V_ + 16384 * b;
+            // O^T (lane j, column r) -> the output staging: two [64 rows][64
+            // channels] bf16 boxes
+            uint8_t *ost = sm + OST;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 uint32_t o32[32];
@@ -1046,14 +1136,13 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             tc_fence_before();
             named_bar_sync(BAR_CHAIN, 128);
             if (L == C) {
-                // a whole chunk: one bulk store per 64-channel box; the v tile is
-                // reloaded once the copy engine has read the staging (next chunk)
+                // a whole chunk: one bulk store per 64-channel box; the staging is
+                // rewritten once the copy engine has read it (next chunk)
                 if (ct == 0) {
                     tma_store_2d(&tm_o, ost, x0, (int)c0);
                     tma_store_2d(&tm_o, ost + 8192, x0 + 64, (int)c0);
                     bulk_commit();
                 }
-                if (ci + 2 < nchunks) v_due = ci;
             } else {
                 // a sequence's short last chunk: plain stores of its rows only (the rows
                 // after it belong to the next sequence)
@@ -1095,8 +1184,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     sync_tc();
     // after an abort: every copy still in flight must land before exit
     if (tid == 0 && *s_abort) {
-        uint64_t *tb[5] = {bar_qk, bar_qk + 1, bar_g, bar_v, bar_v + 1};
-        for (int i = 0; i < 5; ++i)
+        uint64_t *tb[4] = {bar_qk, bar_qk + 1, bar_g, bar_v};
+        for (int i = 0; i < 4; ++i)
             for (uint32_t w = s_waited[i]; w < s_armed[i]; ++w)
                 if (!mbar_wait(tb[i], w & 1, WAIT_LIMIT)) break;
     }
