@@ -65,9 +65,14 @@ def _src_sha(*names):
     return h.hexdigest()[:16]
 
 
+TRAFFIC_NOTE = ("DRAM bytes of one launch from the committed ncu counters, scaled to this launch by the units "
+                "processed; dram_write is a lower bound: dirty lines still in L2 when the kernel ends are not "
+                "counted (algorithmic_write_bytes is what the kernel stores)")
+
+
 def _traffic(kernel, src_files, units_in_launch):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel; else None."""
+    """DRAM read and write bytes per launch from the committed ncu summary,
+    if it was taken on the current source of the kernel; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -75,8 +80,15 @@ def _traffic(kernel, src_files, units_in_launch):
         rec = json.load(f).get(kernel)
     if not rec or rec.get("src_sha") != _src_sha(*src_files):
         return None
-    per_unit = rec["dram_bytes"] / rec["units"]
-    return per_unit * units_in_launch
+    scale = units_in_launch / rec["units"]
+    return {"traffic": rec["dram_bytes"] * scale, "dram_read": rec["dram_read"] * scale,
+            "dram_write": rec["dram_write"] * scale, "dram_write_is_lower_bound": True}
+
+
+def _traffic_fields(tr, algo_write):
+    if tr is None:
+        return {"traffic": None}
+    return dict(tr, algorithmic_write_bytes=algo_write, traffic_note=TRAFFIC_NOTE)
 
 
 class ClockSampler:
@@ -278,6 +290,8 @@ def run_ours(args):
     dec_bytes = STEP_BYTES
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = _traffic("fused_decode_kernel", ["kda_fused_decode.cu", "kda_common.cuh"], UNITS)
+    # state written back, o, the shifted 3-slot ring
+    dec_write = UNITS * (D * D * 4 + D * 2 + 9 * D * 2)
 
     # End to end through the public API, the way a serving loop runs it: every
     # step's inputs (x, g, beta, packed in one pinned host buffer) go host ->
@@ -335,6 +349,7 @@ def run_ours(args):
 
     dec_unfused = bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d)
     dec_epi = bench_decode_epi(torch, kda, dev, stream, ws, hbm_peak, d, ms_per_step)
+    conv_step = bench_shortconv_step(torch, kda, dev, stream, ws, hbm_peak)
 
     prefill = None
     if not args.no_prefill:
@@ -357,7 +372,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": "fused_decode_kernel", "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                         "traffic": traffic, "algorithmic_bytes": dec_bytes,
+                         **_traffic_fields(traffic, dec_write), "algorithmic_bytes": dec_bytes,
                          "avg_launch_us": dec_avg_ms * 1e3},
             "e2e": {"value": ws * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -367,6 +382,7 @@ def run_ours(args):
             "clocks": clocks,
             "decode_unfused": dec_unfused,
             "decode_epilogue": dec_epi,
+            "shortconv_step": conv_step,
         }
         if prefill is not None:
             line["prefill"] = prefill
@@ -495,7 +511,11 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
             "config": {"workload": f"chunked prefill T={T}, H={H}, d={D}, C={C}, bf16 q/k/v, zero S0, "
                                    "fp32 final state", "calls": n},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by},
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by,
+                             **_traffic_fields(_traffic("prefill_tc_pipe_kernel",
+                                                        ["kda_prefill_tc.cu", "kda_tc.cuh", "kda_prefill.cuh",
+                                                         "kda_common.cuh"], T * H),
+                                               T * H * D * 2 + H * D * D * 4)},
             "roofline_tensor": {"achieved": fl / (ms * 1e-3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s",
                                 "frac": fl / (ms * 1e-3) / 1e12 / tc_peak, "algorithmic_flops": fl,
                                 "peak_source": f"{peak_src} bf16_tflops (burst)"}}
@@ -543,6 +563,46 @@ def bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak, n=20):
                        "calls": n, "l2": "3 rotating input/output sets (450 MB)"},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+
+
+def bench_shortconv_step(torch, kda, dev, stream, ws, hbm_peak, n=200, nsets=6):
+    """The standalone short conv decode step (kda_shortconv_step) on the
+    headline batch: B=64, H=96, d=128, bf16, writing y for callers that need
+    the post-conv q, k, v. Timing only; inputs drawn on the device by a seeded
+    torch generator. `nsets` sets of x, ring and y (38 MB each, 226 MB in all,
+    above the 129 MB L2) rotate so that every call misses in L2."""
+    gen = torch.Generator(device=dev).manual_seed(DEC["seed"] + 21)
+    bf = torch.bfloat16
+    sets = [(torch.randn((B, 3, H, D), generator=gen, device=dev).to(bf),
+             torch.randn((B, 3, H, 3, D), generator=gen, device=dev).to(bf),
+             torch.empty((3, B, H, D), dtype=bf, device=dev)) for _ in range(nsets)]
+    w = torch.randn((3, H, D, 4), generator=gen, device=dev) * 0.5
+
+    def call(i):
+        x, ring, y = sets[i % nsets]
+        kda.kda_shortconv_step(x, ring, w, y, stream=stream)
+    for i in range(2 * nsets):
+        call(i)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(n):
+        call(i)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    kda.kda_sync_status(stream)
+    ms = max_over_ranks(a.elapsed_time(b) / n, dev)
+    # per (sequence, head): x read, the 3-slot ring read and rewritten (shifted), y written; plus the taps
+    by = B * H * (3 * D * 2 + 2 * 9 * D * 2 + 3 * D * 2) + 3 * H * D * 16
+    return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "kernel": "shortconv_step_kernel",
+            "config": {"workload": f"short conv decode step alone (kda_shortconv_step): B={B}, H={H}, d={D}, bf16, "
+                                   "y written", "steps": n, "l2": f"{nsets} rotating x/ring/y sets (226 MB)"},
+            "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by,
+                             **_traffic_fields(_traffic("shortconv_step_kernel", ["kda_shortconv.cu",
+                                                                                  "kda_common.cuh"], B * H),
+                                               B * H * 12 * D * 2)}}
 
 
 def bench_epilogue(torch, kda, dev, stream, ws, hbm_peak, n=20):
@@ -688,8 +748,9 @@ def bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d, steps=200):
     kda.kda_sync_status(stream)
     ms = max_over_ranks(a.elapsed_time(b) / steps, dev)
     by = B * H * (2 * D * D * 4 + 3 * D * 2 + D * 4 + 4 + D * 2)
+    tr = _traffic("decode_step_kernel", ["kda_decode.cu", "kda_common.cuh"], B * H)
     return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "kernel": "decode_step_kernel",
+            "kernel": "decode_step_kernel", "dram": _traffic_fields(tr, B * H * (D * D * 4 + D * 2)),
             "config": {"workload": f"decode step without conv (kda_decode_step): B={B}, H={H}, d={D}, bf16 q/k/v, "
                                    "fp32 state 384 MiB", "steps": steps},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -725,7 +786,9 @@ def bench_decode_epi(torch, kda, dev, stream, ws, hbm_peak, d, fused_ms, steps=2
     kda.kda_sync_status(stream)
     ms = max_over_ranks(a.elapsed_time(b) / steps, dev)
     by = STEP_BYTES + B * H * D * 2 + D * 4
+    tr = _traffic("fused_decode_kernel_epilogue", ["kda_fused_decode.cu", "kda_common.cuh"], B * H)
     return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "dram": _traffic_fields(tr, B * H * (D * D * 4 + D * 2 + 9 * D * 2)),
             "fused_step_without_epilogue_ms": fused_ms, "kernel": "fused_decode_kernel (output epilogue)",
             "config": {"workload": f"fused conv + decode step with the gated RMSNorm epilogue (sigmoid gate) in "
                                    f"one launch: B={B}, H={H}, d={D}, bf16, fp32 state 384 MiB", "steps": steps},

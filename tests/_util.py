@@ -52,3 +52,28 @@ def assert_close(got, ref, dtype_is_bf16, unit_axes, what=""):
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     assert err <= F32_ATOL, f"{what}: max abs error {err:.3e} > {F32_ATOL}"
     return float(err)
+
+
+def row_rel_err(got, ref, floor=1e-6):
+    """Per-row relative error of [..., D] arrays: max_j |got - ref| / max(max_j |ref|, floor)
+    for every row (a (token, head) or (sequence, head) output vector)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    num = np.max(np.abs(got - ref), axis=-1)
+    den = np.maximum(np.max(np.abs(ref), axis=-1), floor)
+    return (num / den).ravel()
+
+
+def report_rows(got, ref, what):
+    """Print the 99.9th percentile and the maximum of the per-row relative
+    error (a report beside the per-(sequence, head) gate, not a gate). Rows
+    whose reference is ~0 (below 1e-3 of the largest row) are left out: their
+    relative error measures only rounding of a vanishing value."""
+    ref = np.asarray(ref, np.float64)
+    rmax = np.max(np.abs(ref), axis=-1).ravel()
+    keep = rmax >= 1e-3 * max(float(rmax.max()) if rmax.size else 0.0, 1e-30)
+    r = row_rel_err(got, ref)[keep]
+    if r.size:
+        print(f"{what}: per-row relative error p99.9 {np.percentile(r, 99.9):.3e}, max {r.max():.3e} "
+              f"({r.size} rows)")
+    return r

@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from linear_attention_recurrence_02_gb300 import synth
-from tests._util import assert_close, cuda_or_skip, ensure_built, to_dev, to_np
+from tests._util import assert_close, cuda_or_skip, ensure_built, report_rows, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 NCPU = max(1, len(os.sched_getaffinity(0)))
@@ -251,3 +251,4 @@ def test_fused_conv_decode_full_size(env):
     assert_close(to_np(out), ro, True, (0, 1), "out")
     assert_close(to_np(ts), rs, True, (0, 1), "state")
     assert np.array_equal(to_np(tr), rring)
+    report_rows(to_np(out), ro, "fused decode outputs, full size")

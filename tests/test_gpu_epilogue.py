@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 from linear_attention_recurrence_02_gb300 import synth
-from tests._util import assert_close, cuda_or_skip, ensure_built, to_dev, to_np
+from tests._util import assert_close, cuda_or_skip, ensure_built, report_rows, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -246,3 +246,4 @@ def test_fused_decode_epilogue_full_size(env):
     assert_close(st, rs, True, (0, 1), "state")
     assert np.array_equal(ring, rring)
     print(f"fused decode + epilogue, full size: worst per-head relative error {r:.3e}")
+    report_rows(y, ry, "fused decode + epilogue, full size")

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from linear_attention_recurrence_02_gb300 import synth
-from tests._util import BF16_REL, F32_ATOL, cuda_or_skip, ensure_built, to_dev, to_np
+from tests._util import BF16_REL, F32_ATOL, cuda_or_skip, ensure_built, report_rows, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 NCPU = max(1, len(os.sched_getaffinity(0)))
@@ -223,6 +223,7 @@ def test_prefill_full_size_4k_workload(env):
     o, s = run_prefill(torch, kda, d, True, c["C"])
     ro, rs = oracle_prefill(d, init=False)
     check(o, s, ro, rs, d["cu_seqlens"], True, "4K prefill")
+    report_rows(o, ro, "4K prefill outputs")
 
 
 def test_prefill_full_size_varlen_sampled_heads(env):
@@ -260,3 +261,4 @@ def test_prefill_full_size_varlen_sampled_heads(env):
     got_s = to_np(sf[:, hs])
     ro, rs = oracle_prefill(d)
     check(got_o, got_s, ro, rs, cu, True, "varlen full size")
+    report_rows(got_o, ro, "varlen prefill outputs (sampled heads)")
