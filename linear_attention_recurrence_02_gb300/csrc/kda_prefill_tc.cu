@@ -30,7 +30,8 @@
 // written by the CUDA cores from TMEM read-backs; S~^T and U^T go back to
 // TMEM as bf16 pairs and feed G4-G7 as the A operand. TMA drops k and q into
 // one 128-row tile that becomes [Lk; Lq] in place; W' is later read back over
-// its dead Lk rows, so G4 and G5 are one MMA group over [W'; Lq].
+// its dead Lk rows, transposed: channel-major, so that each thread stores
+// its own 128-byte row, and G4 takes it as an MN-major operand.
 //
 // One CTA (512 threads) per (sequence, head) walks the chunks of its
 // sequence with three warp groups: eight "front" warps build the operand
@@ -64,6 +65,7 @@ constexpr float ANCHOR = 40.f, SPAN_MAX = 2.f * ANCHOR;
 constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_MK64 = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t ID_KM64 = idesc_bf16(128, 64, 0, 1);
 
 // byte offset of 16-byte chunk cc (channels 8cc..8cc+7) of `row` in a
 // 128-byte-swizzled tile whose 64-channel blocks hold `rows` rows each
@@ -210,29 +212,41 @@ __device__ __forceinline__ void mma44_ss(uint32_t d1, uint64_t a1, uint32_t d2, 
         : "memory");
 }
 
-// 8 MMAs with A in TMEM (bf16 pairs, 8 columns per 16-wide K step) and B
-// K-major in shared memory, two 64-channel blocks BBLK bytes apart (G4 + G5).
-template <uint32_t BBLK>
-__device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t at, uint64_t bd, uint32_t idesc, uint64_t *bar) {
+// G4 and G5: two interleaved groups of eight MMAs over K = 128 with the same A
+// in TMEM (8 columns per K step): D1 = A B1^T with B1 MN-major (K rows of 128
+// bytes, 16 per step, 64 rows per piece, pieces 16 KB apart), D2 = A B2^T
+// with B2 K-major (steps 32 bytes apart, 64-channel blocks 16 KB apart).
+__device__ __forceinline__ void mma88_ts(uint32_t d1, uint64_t b1, uint32_t idesc1, uint32_t d2, uint64_t b2,
+                                         uint32_t idesc2, uint32_t at, uint64_t *bar) {
     asm volatile(
-        "{\n\t.reg .pred p, f, t;\n\t.reg .b32 x1, x2, x3, x4, x5, x6, x7;\n\t.reg .b64 y1, y2, y3, y4, y5, y6, y7;\n\t"
+        "{\n\t.reg .pred p, f, t;\n\t.reg .b32 x1, x2, x3, x4, x5, x6, x7;\n\t"
+        ".reg .b64 y1, y2, y3, y4, y5, y6, y7, z1, z2, z3, z4, z5, z6, z7;\n\t"
         "setp.ne.u32 f, 0, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
-        "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\tadd.u32 x4, %1, 32;\n\t"
-        "add.u32 x5, %1, 40;\n\tadd.u32 x6, %1, 48;\n\tadd.u32 x7, %1, 56;\n\t"
-        "add.s64 y1, %2, 2;\n\tadd.s64 y2, %2, 4;\n\tadd.s64 y3, %2, 6;\n\t"
-        "add.s64 y4, %2, %5;\n\tadd.s64 y5, %2, %6;\n\tadd.s64 y6, %2, %7;\n\tadd.s64 y7, %2, %8;\n\t"
+        "add.u32 x1, %6, 8;\n\tadd.u32 x2, %6, 16;\n\tadd.u32 x3, %6, 24;\n\tadd.u32 x4, %6, 32;\n\t"
+        "add.u32 x5, %6, 40;\n\tadd.u32 x6, %6, 48;\n\tadd.u32 x7, %6, 56;\n\t"
+        "add.s64 y1, %1, 128;\n\tadd.s64 y2, %1, 256;\n\tadd.s64 y3, %1, 384;\n\t"
+        "add.s64 y4, %1, 1024;\n\tadd.s64 y5, %1, 1152;\n\tadd.s64 y6, %1, 1280;\n\tadd.s64 y7, %1, 1408;\n\t"
+        "add.s64 z1, %4, 2;\n\tadd.s64 z2, %4, 4;\n\tadd.s64 z3, %4, 6;\n\t"
+        "add.s64 z4, %4, 1024;\n\tadd.s64 z5, %4, 1026;\n\tadd.s64 z6, %4, 1028;\n\tadd.s64 z7, %4, 1030;\n\t"
         "elect.sync _|p, 0xffffffff;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], y1, %3, t;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], y2, %3, t;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], y3, %3, t;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x4], y4, %3, t;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x5], y5, %3, t;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x6], y6, %3, t;\n\t"
-        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x7], y7, %3, t;\n\t"
-        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}\n" ::"r"(d),
-        "r"(at), "l"(bd), "r"(idesc), "r"(smem_u32(bar)), "n"(BBLK / 16), "n"(BBLK / 16 + 2), "n"(BBLK / 16 + 4),
-        "n"(BBLK / 16 + 6)
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %1, %2, f;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [%6], %4, %5, f;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], y1, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x1], z1, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], y2, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x2], z2, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], y3, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x3], z3, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x4], y4, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x4], z4, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x5], y5, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x5], z5, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x6], y6, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x6], z6, %5, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [x7], y7, %2, t;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%3], [x7], z7, %5, t;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}\n" ::"r"(d1),
+        "l"(b1), "r"(idesc1), "r"(d2), "l"(b2), "r"(idesc2), "r"(at), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -272,14 +286,14 @@ __device__ __forceinline__ void mma44_ts(uint32_t d1, uint64_t b1, uint32_t ides
 // The hand-offs are mbarriers in shared memory:
 //   fr[b]     front -> back: operand tiles of chunk parity b built
 //   ready[b]  back -> chain: chunk of parity b fully prepared
-//   c45[b]    G4/G5 of chunk parity b done (tcgen05.commit): its [W'; Lq]
+//   c45[b]    G4/G5 of chunk parity b done (tcgen05.commit): its W' / Lq
 //             tile may be reloaded; the chain itself then issues the q/k
 //             loads of the chunk two ahead into it
 //   ofree[b]  chain -> front, right after G6/G7 of chunk parity b: U0[b],
 //             Rk[b], P[b] and the per-chunk factors may be reused (the back
 //             warps, which reach them only through fr[b], are done too). The
-//             output is staged in the chunk's v tile, which G3 has consumed;
-//             the chain reloads that tile once the bulk store has read it.
+//             output is staged in its own tile, which the chain rewrites
+//             once the bulk store of the chunk before has read it.
 // Code size: the three groups run three different loop bodies at once, so the
 // outer loops of the read-backs, the conversions and the operand build are
 // kept rolled (`#pragma unroll 1`). Fully unrolled, instruction-fetch stalls
@@ -312,10 +326,8 @@ constexpr uint32_t DV = 204800;         // solve scratch: D_0..D_3, M_10, M_32 (
 constexpr uint32_t YV = 212992;         // solve scratch: Y blocks (5 KB)
 constexpr uint32_t SMALL = 218112;      // per-row / per-channel vectors, barriers, counters (6 KB)
 constexpr uint32_t SMEM = SMALL + 6144 + 1024;
-constexpr uint32_t ID_KK128 = idesc_bf16(128, 128, 0, 0);
 // TMEM columns
 constexpr uint32_t T_S = 0, T_SB = 128, T_X = 192, T_O = 256, T_U0 = 320, T_AP = 448;  // U0 parity b at 320 + 64 b
-// X and O are adjacent: G4 and G5 are one MMA group with N = 128 (B = [W'; Lq])
 }  // namespace pipe
 
 // Bounded wait that also gives up once the other warp group has aborted.
@@ -976,20 +988,25 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 pend_mp = false;
                 // G3 has read the v tile: load the next chunk's v into it
                 if (tid == 0 && ci + 1 < nchunks) issue_v((int)(c0 + C));
-                // W'^T (lane i, column r) -> W' rows r over the Lk rows of this chunk's
-                // tile (dead after G2), so that [W'; Lq] is one K-major operand of G4/G5
+                // W'^T (lane i, column r) -> row i of an MN-major W' operand (128 rows of
+                // 64 tokens, 128 bytes each) over the Lk rows of this chunk's tile (dead
+                // after G2): rows 0-63 over block 0's, rows 64-127 over block 1's. Each
+                // thread stores its own row with 16-byte stores.
                 {
                     const int i = jl;
-                    __nv_bfloat16 *wcol = reinterpret_cast<__nv_bfloat16 *>(xb + (i >> 6) * 16384) + (i & 7);
+                    uint8_t *wrow = xb + (i >> 6) * 16384 + (i & 63) * 128;
 #pragma unroll 1
                     for (int half = 0; half < 2; ++half) {
                         uint32_t r32[32];
                         tmem_ld32(tbase + lrow + T_AP + 32 * half, r32);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int m = 0; m < 32; ++m) {
-                            const int r = 32 * half + m;
-                            wcol[r * 64 + ((((i & 63) >> 3) ^ (r & 7)) << 3)] = __float2bfloat16_rn(__uint_as_float(r32[m]));
+                        for (int q = 0; q < 4; ++q) {
+                            const int cc = 4 * half + q;
+                            float f[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r32[8 * q + e]);
+                            *reinterpret_cast<uint4 *>(wrow + ((cc ^ (i & 7)) << 4)) = pack8(f);
                         }
                     }
                 }
@@ -1072,10 +1089,10 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             tc_fence_before();
             named_bar_sync(BAR_CHAIN, 128);
             tc_fence_after();
-            // G4 + G5 in one group: [X^T | O^T] = S~^T [W'; Lq]^T
+            // G4: X^T = S~^T W'^T (W' channel-major), G5: O^T = S~^T Lq^T, one commit
             if (ct < 32)
-                mma8_ts<16384>(tbase + T_X, tbase + T_SB, sdesc_sw128(sbase + X0 + 32768 * b, 16, 1024), ID_KK128,
-                               bar_c45 + b);
+                mma88_ts(tbase + T_X, sdesc_sw128(sbase + X0 + 32768 * b, 8192, 1024), ID_KM64, tbase + T_O,
+                         sdesc_sw128(sbase + X0 + 32768 * b + 8192, 16, 1024), ID_KK64, tbase + T_SB, bar_c45 + b);
             pend45 = ci;
             got = ct >= 32 || wait_or_abort(bar_c45 + b, (ci >> 1) & 1, s_abort);
             if (group_or(BAR_CHAIN, 128, !got)) {
@@ -1084,7 +1101,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             }
             pend45 = -1;
             tc_fence_after();
-            // this chunk's [W'; Lq] tile is consumed: load the chunk two ahead into it
+            // this chunk's W' / Lq tile is consumed: load the chunk two ahead into it
             if (ct == 0 && ci + 2 < nchunks) issue_qk((int)(c0 + 2 * C), b);
             // U^T = U0^T - X^T -> bf16 pairs in TMEM over S~ (dead after G4/G5)
 #pragma unroll 1
