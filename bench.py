@@ -640,12 +640,13 @@ def bench_epilogue(torch, kda, dev, stream, ws, hbm_peak, n=20):
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 
 
-def bench_long_sequence(torch, kda, dev, stream, ws, T=65536, Hs=8, segments=16, n=3):
+def bench_long_sequence(torch, kda, dev, stream, ws, T=65536, Hs=8, segments=0, n=3):
     """One 65,536-token sequence with 8 heads, d=128, C=64, bf16, per-channel
     gate: the serial prefill (one chain of 1024 chunks per head, 8 SMs busy)
-    against kda_chunk_prefill_scan with 16 segments. Timing only; inputs drawn
-    on the device by a seeded torch generator with the workloads'
-    distributions."""
+    against kda_chunk_prefill_scan with the automatic segment count
+    (floor(SMs / H): one pass over the segments fills the GPU once). Timing
+    only; inputs drawn on the device by a seeded torch generator with the
+    workloads' distributions."""
     gen = torch.Generator(device=dev).manual_seed(PRE["seed"] + 11)
 
     def rnd(shape):
@@ -676,7 +677,9 @@ def bench_long_sequence(torch, kda, dev, stream, ws, T=65536, Hs=8, segments=16,
     return {"value": ws * T / (ms_scan * 1e-3), "unit": "tokens/s", "ms_per_call": ms_scan,
             "serial_ms_per_call": ms_serial, "speedup": ms_serial / ms_scan,
             "config": {"workload": f"one sequence of {T} tokens, H={Hs}, d={D}, C=64, bf16, per-channel gate: "
-                                   f"kda_chunk_prefill_scan with {segments} segments vs kda_chunk_prefill",
+                                   "kda_chunk_prefill_scan vs kda_chunk_prefill",
+                       "segments": segments if segments else max(2, torch.cuda.get_device_properties(dev)
+                                                                 .multi_processor_count // Hs),
                        "calls": n}}
 
 

@@ -262,20 +262,26 @@ kda_status kda_shortconv_decode_step_epi(const void *x, void *ring, const float 
  * Chunked prefill of ONE sequence of T tokens, split into `segments` runs of
  * whole chunks that are processed side by side ([G] section 5: each chunk
  * step is affine in the state, S <- A S + B with A acting on the key axis,
- * and so is a run of them). Three passes of the ordinary prefill over the
- * segments (their B from zero states; their A from identity states with v
- * read as zero; the outputs from the true states) around a serial fp32 scan
- * S_{p+1} = A_p S_p + B_p. The result equals kda_chunk_prefill_gated on the
- * whole sequence up to rounding. It pays when the sequence is long and H is
- * small, so that the serial chunk chain leaves most SMs idle.
+ * and so is a run of them, and so is every readout o_t = S_t^T q_t). Two
+ * passes of the ordinary prefill over the segments: from zero states (their
+ * B, and the outputs without the carried state's part) and from identity
+ * states with v read as zero (their A, and the outputs A_t^T q_t that carry
+ * that part); then a serial fp32 scan S_{p+1} = A_p S_p + B_p gives the
+ * state at every segment start and the final state, and one product per
+ * segment and head adds (A_t^T q_t)^T S_p to every output. The result equals
+ * kda_chunk_prefill_gated on the whole sequence up to rounding. It pays when
+ * the sequence is long and H is small, so that the serial chunk chain leaves
+ * most SMs idle. segments = 0 picks floor(SMs / H) (at least 2): one pass
+ * over the segments then fills the GPU once.
  *
  *   q, k, v, out [T,H,D] dtype; g [T,H,D] / [T,H] / unused per `gate`;
  *   beta [T,H] fp32; initial_state [H,D,D] fp32 or NULL (zeros);
  *   final_state [H,D,D] fp32 or NULL.
  *   workspace: kda_chunk_prefill_scan_workspace_bytes(T, H, D, C, segments)
- *   bytes of device memory, 16-byte aligned (four fp32 states per segment
- *   and head).
- * segments in 1..4096; segments = 1, T = 0 or T <= C run the ordinary
+ *   bytes of device memory, 16-byte aligned: four fp32 states per segment and
+ *   head and one [T,H,D] output buffer (sized for fp32; with segments = 0 the
+ *   size is that of the current device's choice).
+ * segments in 0..4096; segments = 1, T = 0 or T <= C run the ordinary
  * prefill (no workspace needed). Other requirements and errors as
  * kda_chunk_prefill_gated.
  */

@@ -2,6 +2,8 @@
 // its kernels (CUDA-core general path, tensor-core bf16 path).
 #pragma once
 
+#include <cuda.h>
+
 #include "kda_common.cuh"
 
 namespace kda {
@@ -35,6 +37,13 @@ kda_status launch_prefill_order(const int64_t *cu_seqlens, int N, int *order, cu
 kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_applicable(const PrefillArgs &a);
 kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s);
+
+namespace tcp {
+// 2-D tiled TMA map over a row-major [rows][inner] tensor of `elem`-byte
+// elements with a box of box_inner x box_rows; false if the encoder fails.
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t elem, uint64_t inner,
+              uint64_t rows, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
+}  // namespace tcp
 
 // Validated [start, end) of sequence n; on invalid cu_seqlens sets the
 // device error word and returns false (the caller skips the sequence).

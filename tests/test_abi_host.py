@@ -253,16 +253,21 @@ def test_gated_rmsnorm_argument_checks(kda):
 
 def test_prefill_scan_argument_checks(kda):
     """kda_chunk_prefill_scan: segments out of range and a short workspace are
-    rejected; one segment falls through to the ordinary prefill's checks."""
+    rejected (segments = 0 is the automatic count); one segment falls through
+    to the ordinary prefill's checks."""
     L = kda.lib()
     args = (0x10000, 0x20000, 0x30000, 0x40000, 0x50000, None, None, 0x60000, 1000, 2, 128, 64, 1,
             kda.KDA_GATE_CHANNEL, 1e-6)
-    st = L.kda_chunk_prefill_scan(*args, 0, None, 0, None)
-    assert st == kda.KDA_ERR_INVALID_ARG and "segments" in L.kda_last_error_detail().decode()
-    st = L.kda_chunk_prefill_scan(*args, 4, None, 0, None)
-    assert st == kda.KDA_ERR_INVALID_ARG and "workspace too small" in L.kda_last_error_detail().decode()
+    for bad in (-1, 4097):
+        st = L.kda_chunk_prefill_scan(*args, bad, None, 0, None)
+        assert st == kda.KDA_ERR_INVALID_ARG and "segments" in L.kda_last_error_detail().decode()
+    for segs in (0, 4):
+        st = L.kda_chunk_prefill_scan(*args, segs, None, 0, None)
+        assert st == kda.KDA_ERR_INVALID_ARG and "workspace too small" in L.kda_last_error_detail().decode()
     need = L.kda_chunk_prefill_scan_workspace_bytes(1000, 2, 128, 64, 4)
-    assert need >= 4 * 4 * 2 * 128 * 128 * 4  # four fp32 states per segment and head
+    # four fp32 states per segment and head, and a [T, H, D] fp32 output buffer
+    assert need >= 4 * 4 * 2 * 128 * 128 * 4 + 1000 * 2 * 128 * 4
+    assert L.kda_chunk_prefill_scan_workspace_bytes(1000, 2, 128, 64, 0) > 0
     st = L.kda_chunk_prefill_scan(None, *args[1:], 1, None, 0, None)
     assert st == kda.KDA_ERR_INVALID_ARG and "q is NULL" in L.kda_last_error_detail().decode()
 

@@ -98,3 +98,26 @@ def test_scan_matches_the_serial_prefill(env):
     torch.cuda.synchronize()
     assert_close(to_np(o2), to_np(o1), True, (1,), "out")
     assert_close(to_np(s2), to_np(s1), True, (0,), "final state")
+
+
+def test_scan_tensor_core_path_no_carry_in(env):
+    """bf16, d=128, no initial state: the outputs of the first segment need no correction; 1500 tokens in 5
+    segments of 320 tokens (not a multiple of the 128-token correction blocks)."""
+    torch, kda = env
+    T, H, D = 1500, 2, 128
+    p = synth.prefill_inputs(35, T, H, D, True, s0_std=0.05, g_scale=0.02)
+    o, s, ro, rs = _run(torch, kda, p, D, True, 5, 64, with_s0=False)
+    assert_close(o, ro, True, (1,), "out")
+    assert_close(s, rs, True, (0,), "final state")
+
+
+@pytest.mark.parametrize("segments", [0, 19])
+def test_scan_longer_sequence_mild_gates(env, segments):
+    """8192 tokens, 2 heads, gates scaled by 0.02 so that the carried state matters across every segment;
+    19 segments of 448 tokens (and the automatic count, which fills the GPU's SMs once)."""
+    torch, kda = env
+    T, H, D = 8192, 2, 128
+    p = synth.prefill_inputs(36, T, H, D, True, s0_std=0.05, g_scale=0.02)
+    o, s, ro, rs = _run(torch, kda, p, D, True, segments, 64)
+    assert_close(o, ro, True, (1,), "out")
+    assert_close(s, rs, True, (0,), "final state")
