@@ -669,8 +669,11 @@ def bench_long_sequence(torch, kda, dev, stream, ws, T=65536, Hs=8, segments=0, 
         b.record(stream)
         torch.cuda.synchronize(dev)
         return max_over_ranks(a.elapsed_time(b) / n, dev)
+    # an empty workspace keeps kda_chunk_prefill on the serial path (with the workspace it asks for, the
+    # call would split this sequence itself)
+    no_ws = torch.empty(0, dtype=torch.uint8, device=dev)
     ms_serial = timed(lambda: kda.kda_chunk_prefill(q, k, v, g, beta, out, final_state=sf[None], chunk_size=64,
-                                                    stream=stream))
+                                                    workspace=no_ws, stream=stream))
     ms_scan = timed(lambda: kda.kda_chunk_prefill_scan(q, k, v, g, beta, out, segments, final_state=sf,
                                                        workspace=wsb, stream=stream))
     kda.kda_sync_status(stream)

@@ -333,7 +333,14 @@ size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int
  *                 tensor-core path; every other combination runs on CUDA cores)
  *   workspace     device buffer of at least
  *                 kda_chunk_prefill_workspace_bytes(T, N, H, D, C) bytes
- *                 (NULL allowed when that is 0); contents are scratch.
+ *                 (NULL allowed when that is 0); contents are scratch. For
+ *                 one sequence (N = 1) whose serial chunk chain would leave
+ *                 most SMs idle (floor(SMs / H) >= 4 and at least 8 chunks
+ *                 per segment), that size makes room for the automatic split
+ *                 of kda_chunk_prefill_scan, which the call then uses when
+ *                 cu_seqlens is NULL; with a smaller workspace (or NULL) the
+ *                 same call runs the serial prefill. The size depends on the
+ *                 current device.
  * Invalid cu_seqlens contents are found on the device: the affected
  * sequences are skipped and kda_sync_status() reports KDA_ERR_DEVICE_CHECK.
  */

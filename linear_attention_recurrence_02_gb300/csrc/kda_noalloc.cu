@@ -44,7 +44,9 @@ extern "C" kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, co
     if (N > KDA_NOALLOC_MAX_SEQS)
         return invalid("N exceeds the allocation-free maximum of " + std::to_string(KDA_NOALLOC_MAX_SEQS) +
                        " sequences; use kda_chunk_prefill with a workspace");
-    const size_t need = kda_chunk_prefill_workspace_bytes(T, N, H, D, C);
+    // only the launch order of a mixed-length batch lives in the static array
+    // (a single sequence needs none and then runs the serial prefill)
+    const size_t need = N >= 2 ? kda_chunk_prefill_workspace_bytes(T, N, H, D, C) : 0;
     void *ws = nullptr;
     if (need > 0) {
         kda_status st = bind_stream_device(stream);

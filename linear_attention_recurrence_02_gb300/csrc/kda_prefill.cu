@@ -250,14 +250,19 @@ kda_status launch_prefill_order(const int64_t *cu_seqlens, int N, int *order, cu
 
 using namespace kda;
 
-extern "C" size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C) {
-    (void)total_tokens;
-    (void)H;
-    (void)D;
-    (void)C;
-    // the launch order of a mixed-length batch: int32 per sequence
+// the launch order of a mixed-length batch: int32 per sequence
+static size_t order_bytes(int num_seqs) {
     if (num_seqs < 2 || num_seqs > ORDER_MAX_SEQS) return 0;
     return ((size_t)num_seqs * sizeof(int) + 255) & ~(size_t)255;
+}
+
+extern "C" size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C) {
+    // one long sequence with few heads: room for the automatic split
+    if (num_seqs == 1) {
+        const int P = prefill_auto_segments(total_tokens, H, C);
+        if (P > 0) return kda_chunk_prefill_scan_workspace_bytes(total_tokens, H, D, C, P);
+    }
+    return order_bytes(num_seqs);
 }
 
 // The gated prefill, followed by the output epilogue (a pass of
@@ -282,7 +287,7 @@ static kda_status prefill_entry(const void *q, const void *k, const void *v, con
     if (!(l2_eps >= 0.f)) return invalid("l2_eps must be >= 0");
     if (cu_seqlens == nullptr && N != 1) return invalid("cu_seqlens is NULL but N != 1");
     if ((long long)N * H * 2 > 0x7fffffffLL) return invalid("N*H too large for one launch");
-    const size_t need = kda_chunk_prefill_workspace_bytes(T, N, H, D, C);
+    const size_t need = order_bytes(N);
     if (workspace_bytes < need) return invalid("workspace too small");
     kda_status st;
     if (T > 0 && ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
@@ -296,6 +301,18 @@ static kda_status prefill_entry(const void *q, const void *k, const void *v, con
     if (T > 0 && (out == q || out == k || out == v)) return invalid("out must not alias q, k or v");
     if (T == 0 && final_state == nullptr) return KDA_OK;
     if ((st = bind_stream_device(stream))) return st;
+    // One sequence (no cu_seqlens) whose serial chunk chain would leave most
+    // SMs idle: split it into segments when the workspace has room for that
+    // (kda_chunk_prefill_workspace_bytes asks for it).
+    if (cu_seqlens == nullptr && T > 0) {
+        const int P = prefill_auto_segments(T, H, C);
+        if (P > 0 && workspace != nullptr && workspace_bytes >= kda_chunk_prefill_scan_workspace_bytes(T, H, D, C, P)) {
+            st = kda_chunk_prefill_scan(q, k, v, g, beta, initial_state, final_state, out, T, H, D, C, dtype, gate,
+                                        l2_eps, P, workspace, workspace_bytes, stream);
+            if (st != KDA_OK || epi_gate == nullptr) return st;
+            return kda_gated_rmsnorm(out, epi_gate, epi_w, out, T, H, D, dtype, epi_act, epi_eps, stream);
+        }
+    }
     PrefillArgs a{q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C,
                   dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word(), nullptr, (int)gate};
     if (a.err == nullptr) return fail(KDA_ERR_CUDA, "device error word unavailable");

@@ -38,6 +38,10 @@ kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_applicable(const PrefillArgs &a);
 kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s);
 
+// Segments of the automatic long-sequence split for one sequence of T tokens
+// with H heads on the current device, or 0 when the serial prefill is kept.
+int prefill_auto_segments(int64_t T, int H, int C);
+
 namespace tcp {
 // 2-D tiled TMA map over a row-major [rows][inner] tensor of `elem`-byte
 // elements with a box of box_inner x box_rows; false if the encoder fails.

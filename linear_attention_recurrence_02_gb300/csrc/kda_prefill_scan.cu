@@ -367,6 +367,19 @@ static int requested_segments(int segments, int H) {
     return p < 2 ? 2 : (p > 4096 ? 4096 : p);
 }
 
+// The automatic split of one long sequence inside kda_chunk_prefill: with
+// P = floor(SMs / H) segments one pass over them fills the GPU once, and the
+// split (two passes of 1/P of the chain each, the scan, the correction)
+// pays when P >= 4 and every segment keeps at least 8 chunks. 0: no split.
+int prefill_auto_segments(int64_t T, int H, int C) {
+    if (T <= 0 || H < 1 || C < 1) return 0;
+    const int sms = current_sms();
+    const int P = H > 0 ? sms / H : 0;
+    if (P < 4) return 0;
+    const int64_t chunks = (T + C - 1) / C;
+    return chunks >= 8LL * P ? (P > 4096 ? 4096 : P) : 0;
+}
+
 // segments actually used for P requested over T tokens in chunks of C
 static int scan_segments(int64_t T, int C, int P, int64_t *seg_tokens) {
     const int64_t nch = (T + C - 1) / C;

@@ -121,3 +121,35 @@ def test_scan_longer_sequence_mild_gates(env, segments):
     o, s, ro, rs = _run(torch, kda, p, D, True, segments, 64)
     assert_close(o, ro, True, (1,), "out")
     assert_close(s, rs, True, (0,), "final state")
+
+
+def test_prefill_splits_one_long_sequence_automatically(env):
+    """kda_chunk_prefill on one 12,288-token sequence with 8 heads: with the workspace that
+    kda_chunk_prefill_workspace_bytes asks for, the call takes the segmented path (floor(SMs / 8) segments);
+    without one, the serial path. Both against the fp64 oracle with mild gates and a carry-in state, and
+    against each other (an empty workspace keeps the serial path)."""
+    torch, kda = env
+    T, H, D = 12288, 8, 128
+    need = kda.kda_chunk_prefill_workspace_bytes(T, 1, H, D, 64)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms // H < 4:
+        pytest.skip("too few SMs for the automatic split at 8 heads")
+    assert need > 0
+    p = synth.prefill_inputs(37, T, H, D, True, s0_std=0.05, g_scale=0.02)
+    bf = torch.bfloat16
+    q, k, v = (to_dev(p[n], bf, torch) for n in "qkv")
+    g, b = to_dev(p["g"], torch.float32, torch), to_dev(p["beta"], torch.float32, torch)
+    s0 = to_dev(p["s0"], torch.float32, torch)
+    outs = []
+    # the binding allocates the asked-for workspace when given none: an empty one keeps the serial path
+    for ws in (torch.empty(need, dtype=torch.uint8, device="cuda"), torch.empty(0, dtype=torch.uint8, device="cuda")):
+        o = torch.full_like(q, float("nan"))
+        sf = torch.full((1, H, D, D), float("nan"), device="cuda")
+        kda.kda_chunk_prefill(q, k, v, g, b, o, initial_state=s0, final_state=sf, chunk_size=64, workspace=ws)
+        kda.kda_sync_status()
+        outs.append((to_np(o), to_np(sf)))
+    ro, rs = oracle.recurrence(p["q"], p["k"], p["v"], p["g"], p["beta"], s_init=p["s0"])
+    for o, sf in outs:
+        assert_close(o, ro, True, (1,), "out")
+        assert_close(sf, rs, True, (0, 1), "final state")
+    assert_close(outs[0][0], outs[1][0], True, (1,), "split vs serial")
