@@ -4,8 +4,10 @@
 // sections "KDA 递推公式先衰减再差分" and "414MB 的 KDA 状态从哪来").
 //
 // Memory-bound elementwise work: each thread owns 16 bytes of channels of one
-// (b, projection, h) row: it reads x and the three ring slots with 128-bit
-// loads, the 4 taps per channel as float4, writes y and the shifted ring.
+// (projection, h) pair for two sequences: it loads the 4 taps per channel
+// once (float4), issues the 128-bit loads of x and the three ring slots of
+// both sequences before using any, and writes y and the shifted ring (the
+// ring's stored vectors move unchanged).
 // y is written projection-major, [3,B,H,D], so that y[0], y[1], y[2] are the
 // contiguous q, k, v operands of the decode step.
 //
@@ -42,40 +44,71 @@ __device__ __forceinline__ void store16(T *p, const float (&in)[Vec16<T>::N]) {
     __stcs(reinterpret_cast<uint4 *>(p), raw);
 }
 
+// One thread per 16 bytes of channels of one (projection, head) and a group
+// of STEP_BPT sequences: the taps of its channels are loaded once and kept in
+// registers for every sequence of the group, and the group's loads are all
+// issued before any is used (one 16-byte x vector and three ring slots each).
+// Measured at 64 sequences x 96 heads (bf16): 1 sequence per thread 14.4 us,
+// 2 sequences 12.4 us, 4 sequences 14.4 us (133 registers: 1.3 waves); the
+// first form, one thread per (sequence, projection, head) vector re-reading
+// the taps for every sequence in 256-thread blocks, 16.4 us.
+constexpr int STEP_BPT = 2;
+constexpr int STEP_NT = 128;
 template <typename T>
-__global__ void __launch_bounds__(256) shortconv_step_kernel(const T *__restrict__ x, T *__restrict__ ring,
+__global__ void __launch_bounds__(STEP_NT) shortconv_step_kernel(const T *__restrict__ x, T *__restrict__ ring,
                                                              const float *__restrict__ w, T *__restrict__ y,
                                                              int B, int H, int D) {
     constexpr int V = Vec16<T>::N;
     const int nvec = D / V;
-    const size_t total = (size_t)B * 3 * H * nvec;
+    const int ngroups = (B + STEP_BPT - 1) / STEP_BPT;
+    const size_t total = (size_t)ngroups * 3 * H * nvec;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const int cv = (int)(idx % nvec);
-    const size_t row = idx / nvec;  // (b*3 + p)*H + h
-    const int h = (int)(row % H);
-    const int p = (int)((row / H) % 3);
-    const size_t b = row / ((size_t)3 * H);
-    const size_t xoff = row * D + (size_t)cv * V;
-    const size_t yoff = (((size_t)p * B + b) * H + h) * D + (size_t)cv * V;
-    const size_t roff = row * 3 * D + (size_t)cv * V;
-    const float *wt = w + (((size_t)p * H + h) * D + (size_t)cv * V) * 4;
-
-    float xv[V], r0[V], r1[V], r2[V], yv[V];
-    load16(x + xoff, xv);
-    load16(ring + roff, r0);
-    load16(ring + roff + D, r1);
-    load16(ring + roff + 2 * (size_t)D, r2);
+    const size_t r = idx / nvec;
+    const int h = (int)(r % H);
+    const int p = (int)((r / H) % 3);
+    const int b0 = (int)(r / ((size_t)3 * H)) * STEP_BPT;
+    const float4 *wt = reinterpret_cast<const float4 *>(w + (((size_t)p * H + h) * D + (size_t)cv * V) * 4);
+    float4 tap[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-        float4 tap = __ldg(reinterpret_cast<const float4 *>(wt) + i);
-        float z = tap.x * r0[i] + tap.y * r1[i] + tap.z * r2[i] + tap.w * xv[i];
-        yv[i] = z / (1.0f + expf(-z));
+    for (int i = 0; i < V; ++i) tap[i] = __ldg(wt + i);
+
+    // raw 16-byte vectors in flight: x and the three slots of every sequence of the group
+    uint4 xr[STEP_BPT], rr[STEP_BPT][3];
+#pragma unroll
+    for (int bb = 0; bb < STEP_BPT; ++bb) {
+        if (b0 + bb >= B) break;
+        const size_t row = ((size_t)(b0 + bb) * 3 + p) * H + h;  // (b*3 + p)*H + h
+        const size_t xoff = row * D + (size_t)cv * V, roff = row * 3 * D + (size_t)cv * V;
+        xr[bb] = __ldcs(reinterpret_cast<const uint4 *>(x + xoff));
+#pragma unroll
+        for (int k = 0; k < 3; ++k) rr[bb][k] = __ldcs(reinterpret_cast<const uint4 *>(ring + roff + (size_t)k * D));
     }
-    store16(y + yoff, yv);
-    store16(ring + roff, r1);
-    store16(ring + roff + D, r2);
-    store16(ring + roff + 2 * (size_t)D, xv);
+#pragma unroll
+    for (int bb = 0; bb < STEP_BPT; ++bb) {
+        const int b = b0 + bb;
+        if (b >= B) break;
+        const size_t row = ((size_t)b * 3 + p) * H + h;
+        const size_t roff = row * 3 * D + (size_t)cv * V;
+        const size_t yoff = (((size_t)p * B + b) * H + h) * D + (size_t)cv * V;
+        const T *xe = reinterpret_cast<const T *>(&xr[bb]);
+        const T *e0 = reinterpret_cast<const T *>(&rr[bb][0]);
+        const T *e1 = reinterpret_cast<const T *>(&rr[bb][1]);
+        const T *e2 = reinterpret_cast<const T *>(&rr[bb][2]);
+        float yv[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const float z = tap[i].x * Elem<T>::load(e0 + i) + tap[i].y * Elem<T>::load(e1 + i) +
+                            tap[i].z * Elem<T>::load(e2 + i) + tap[i].w * Elem<T>::load(xe + i);
+            yv[i] = z / (1.0f + expf(-z));
+        }
+        store16(y + yoff, yv);
+        // the ring shifts: its stored values move unchanged
+        __stcs(reinterpret_cast<uint4 *>(ring + roff), rr[bb][1]);
+        __stcs(reinterpret_cast<uint4 *>(ring + roff + D), rr[bb][2]);
+        __stcs(reinterpret_cast<uint4 *>(ring + roff + 2 * (size_t)D), xr[bb]);
+    }
 }
 
 constexpr int CONV_TILE = 64;  // tokens per prefill tile
@@ -269,14 +302,14 @@ extern "C" kda_status kda_shortconv_step(const void *x, void *ring, const float 
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int V = dtype == KDA_BF16 ? 8 : 4;
-    const size_t total = (size_t)B * 3 * H * (D / V);
-    const unsigned blocks = (unsigned)((total + 255) / 256);
+    const size_t total = (size_t)((B + STEP_BPT - 1) / STEP_BPT) * 3 * H * (D / V);
+    const unsigned blocks = (unsigned)((total + STEP_NT - 1) / STEP_NT);
     if (dtype == KDA_BF16)
-        shortconv_step_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        shortconv_step_kernel<__nv_bfloat16><<<blocks, STEP_NT, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(ring), w,
             static_cast<__nv_bfloat16 *>(y), B, H, D);
     else
-        shortconv_step_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(x),
+        shortconv_step_kernel<float><<<blocks, STEP_NT, 0, s>>>(static_cast<const float *>(x),
                                                             static_cast<float *>(ring), w,
                                                             static_cast<float *>(y), B, H, D);
     return check_launch("shortconv_step_kernel");
