@@ -214,6 +214,12 @@ kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s) {
     return a.bf16 ? dispatch_simt<__nv_bfloat16>(a, s) : dispatch_simt<float>(a, s);
 }
 
+kda_status prefill_run(const PrefillArgs &a, cudaStream_t s) {
+    if (prefill_tc_applicable(a)) return prefill_tc(a, s);
+    if (prefill_f32_applicable(a)) return prefill_f32(a, s);
+    return prefill_simt(a, s);
+}
+
 // Longest sequences first: a sequence's chunks are walked serially by its
 // CTAs, so starting the long chains first shortens the tail of a mixed-length
 // batch (greedy longest-processing-time order). order[rank] = n, where rank
@@ -322,7 +328,7 @@ static kda_status prefill_entry(const void *q, const void *k, const void *v, con
         if ((st = launch_prefill_order(cu_seqlens, N, order, s))) return st;
         a.order = order;
     }
-    if ((st = prefill_tc_applicable(a) ? prefill_tc(a, s) : prefill_simt(a, s))) return st;
+    if ((st = prefill_run(a, s))) return st;
     if (epi_gate == nullptr || T == 0) return KDA_OK;
     return kda_gated_rmsnorm(out, epi_gate, epi_w, out, T, H, D, dtype, epi_act, epi_eps, stream);
 }

@@ -37,6 +37,11 @@ kda_status launch_prefill_order(const int64_t *cu_seqlens, int N, int *order, cu
 kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_applicable(const PrefillArgs &a);
 kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s);
+bool prefill_f32_applicable(const PrefillArgs &a);
+kda_status prefill_f32(const PrefillArgs &a, cudaStream_t s);
+// The kernel for these arguments: tensor cores (bf16, d = 128, C = 64), the
+// register-tiled fp32 kernel (d = 128, any C), else the general CUDA-core one.
+kda_status prefill_run(const PrefillArgs &a, cudaStream_t s);
 
 // Segments of the automatic long-sequence split for one sequence of T tokens
 // with H heads on the current device, or 0 when the serial prefill is kept.

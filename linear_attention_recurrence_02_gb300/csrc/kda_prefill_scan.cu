@@ -533,7 +533,7 @@ extern "C" kda_status kda_chunk_prefill_scan(const void *q, const void *k, const
     // the segments are equally long except the last, so natural order is longest-first enough
     PrefillArgs a{q, k, v, g, beta, nullptr, w.Bs, out, w.cu, P, T, H, D, C, bf16, l2_eps, nullptr, 0,
                   err, nullptr, (int)gate};
-    auto run = [&](const PrefillArgs &x) { return prefill_tc_applicable(x) ? prefill_tc(x, s) : prefill_simt(x, s); };
+    auto run = [&](const PrefillArgs &x) { return prefill_run(x, s); };
     if ((st = run(a))) return st;  // 1. B of each segment; outputs from zero states into out
     PrefillArgs ai = a;
     ai.s_init = w.Id;

@@ -262,3 +262,53 @@ def test_prefill_full_size_varlen_sampled_heads(env):
     ro, rs = oracle_prefill(d)
     check(got_o, got_s, ro, rs, cu, True, "varlen full size")
     report_rows(got_o, ro, "varlen prefill outputs (sampled heads)")
+
+
+def test_prefill_full_size_4k_fp32(env):
+    """The 4K workload's shape in fp32 (T=4096, H=96, d=128, C=64, zero initial state): the register-tiled
+    fp32 kernel, every output and final state within the fp32 bar (max abs 1e-4)."""
+    torch, kda = env
+    c = synth.PREFILL
+    d = synth.prefill_inputs(c["seed"], c["T"], c["H"], c["D"], bf16=False)
+    o, s = run_prefill(torch, kda, d, False, c["C"])
+    ro, rs = oracle_prefill(d, init=False)
+    check(o, s, ro, rs, d["cu_seqlens"], False, "4K prefill fp32")
+    print(f"4K fp32 prefill: max abs error out {np.max(np.abs(o - ro)):.2e}, state {np.max(np.abs(s - rs)):.2e}")
+
+
+@pytest.mark.parametrize("gate", ["head", "none"])
+@pytest.mark.parametrize("C", [64, 48])
+def test_prefill_fp32_gate_forms_d128(env, gate, C):
+    """fp32, d=128 (the register-tiled kernel) with a per-head gate or none, carry-in states, ragged chunks."""
+    torch, kda = env
+    cu = np.array([0, 150, 150, 333], dtype=np.int64)
+    d = synth.prefill_inputs(60, 333, 3, 128, False, cu_seqlens=cu, s0_std=0.3, g_scale=0.1)
+    if gate == "head":
+        gk, go = np.ascontiguousarray(d["g"][..., 0]), np.repeat(d["g"][..., :1], 128, axis=-1)
+    else:
+        gk, go = None, np.zeros_like(d["g"])
+    f32 = torch.float32
+    q, k, v = (to_dev(d[n], f32, torch) for n in ("q", "k", "v"))
+    out = torch.full_like(q, float("nan"))
+    sf = torch.full((3, 3, 128, 128), float("nan"), device="cuda")
+    kda.kda_chunk_prefill_gated(q, k, v, None if gk is None else to_dev(gk, f32, torch),
+                                to_dev(d["beta"], f32, torch), out, gate=gate,
+                                initial_state=to_dev(d["s0"], f32, torch), final_state=sf,
+                                cu_seqlens=torch.from_numpy(cu).cuda(), chunk_size=C)
+    kda.kda_sync_status()
+    ro, rs = oracle.recurrence(d["q"], d["k"], d["v"], go, d["beta"], s_init=d["s0"], cu_seqlens=cu)
+    check(to_np(out), to_np(sf), ro, rs, cu, False, f"gate={gate} C={C}")
+
+
+def test_prefill_fp32_some_chunks_exact(env):
+    """fp32, d=128: a gate spike of -200 in one token makes that chunk's decay span exceed the range the
+    factored form covers, so that chunk (and only it) takes the exact pairwise path; the others stay on the
+    factored one. With mild gates elsewhere the carried state matters across the spike's neighbours."""
+    torch, kda = env
+    d = synth.prefill_inputs(61, 256, 2, 128, False, s0_std=0.3, g_scale=0.02)
+    g = d["g"].copy()
+    g[100, 0, :64] = -200.0  # head 0, half the channels, in the second chunk
+    d1 = dict(d, g=g)
+    o, s = run_prefill(torch, kda, d1, False, 64)
+    ro, rs = oracle_prefill(d1)
+    check(o, s, ro, rs, d1["cu_seqlens"], False, "spike")
