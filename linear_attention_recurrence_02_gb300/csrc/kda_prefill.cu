@@ -216,6 +216,7 @@ kda_status prefill_simt(const PrefillArgs &a, cudaStream_t s) {
 
 kda_status prefill_run(const PrefillArgs &a, cudaStream_t s) {
     if (prefill_tc_applicable(a)) return prefill_tc(a, s);
+    if (prefill_tf32_applicable(a)) return prefill_tf32(a, s);
     if (prefill_f32_applicable(a)) return prefill_f32(a, s);
     return prefill_simt(a, s);
 }

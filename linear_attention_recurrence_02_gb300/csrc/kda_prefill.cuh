@@ -39,6 +39,8 @@ bool prefill_tc_applicable(const PrefillArgs &a);
 kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_f32_applicable(const PrefillArgs &a);
 kda_status prefill_f32(const PrefillArgs &a, cudaStream_t s);
+bool prefill_tf32_applicable(const PrefillArgs &a);
+kda_status prefill_tf32(const PrefillArgs &a, cudaStream_t s);
 // The kernel for these arguments: tensor cores (bf16, d = 128, C = 64), the
 // register-tiled fp32 kernel (d = 128, any C), else the general CUDA-core one.
 kda_status prefill_run(const PrefillArgs &a, cudaStream_t s);

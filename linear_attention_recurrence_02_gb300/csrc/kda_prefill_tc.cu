@@ -142,11 +142,6 @@ __device__ __forceinline__ void unpack8(uint4 u, float *f) {
     }
 }
 
-__device__ __forceinline__ void sync_tc() {
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-}
 
 
 // ------------------------------------------------- MMA groups, issued by one elected lane
