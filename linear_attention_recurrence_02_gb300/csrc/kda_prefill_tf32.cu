@@ -61,13 +61,14 @@ constexpr uint32_t RKH = 131072, RKL = 163840;  // Rk hi / lo: 64 rows x 128 (fo
 constexpr uint32_t TH = 0, TL = 16384, PH = 32768, PL = 49152;  // T, P hi / lo: 64 rows x 64 (two 8 KB blocks)
 constexpr uint32_t AF = 65536;                  // A fp32 [64][65]
 constexpr uint32_t NI = AF + 64 * 65 * 4;       // (I + A)^-1 fp32 [64][65]
-constexpr uint32_t YS = NI + 64 * 65 * 4;       // block products [3][16][17]
-// exact chunks: k^, q^, G fp32 [64][129] in the [Lk; Lq] area before it is built, A | P fp32 [128][65] over Rk
+constexpr uint32_t AT = NI + 64 * 65 * 4;       // D_i A_ik below the diagonal blocks, fp32 [64][65]
+constexpr uint32_t RTH = 65536, RTL = 98304;    // once T is formed: Rk^T (Kb^T) hi / lo, 128 rows x 64 (two 16 KB blocks)
+// exact chunks: k^, q^, G fp32 [64][129] in the [Lk; Lq] area before it is built
 constexpr int XLD = 129;
-constexpr uint32_t XK = 0, XQ = 64 * XLD * 4, XG = 2 * 64 * XLD * 4, XAP = RKH;
+constexpr uint32_t XK = 0, XQ = 64 * XLD * 4, XG = 2 * 64 * XLD * 4;
 constexpr uint32_t SMALL = 196608;
-constexpr uint32_t SMEM = SMALL + 3344 + 1024;
-static_assert(YS + 3 * 16 * 17 * 4 <= RKH && XG + 64 * XLD * 4 <= RKH, "scratch overlaps Rk");
+constexpr uint32_t SMEM = SMALL + 3344 + 16 + 2048 + 1024;  // vectors, barrier, norm partials, alignment
+static_assert(AT + 64 * 65 * 4 <= RKH && XG + 64 * XLD * 4 <= RKH && PL + 16384 <= RTH, "tile overlap");
 static_assert(SMEM <= 232448, "shared memory of the tf32 prefill");
 // TMEM columns
 constexpr uint32_t T_S = 0;    // S~^T (fp32 accumulator; also the hi part of G0's A operand)
@@ -111,25 +112,31 @@ __device__ __forceinline__ bool elect_one() {
 template <int NK, uint32_t ABLK, uint32_t BBLK>
 __device__ __forceinline__ void prod_ss(uint32_t d, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl,
                                         uint32_t idesc, bool acc) {
+#pragma unroll 1
+    for (int kb = 0; kb < NK / 4; ++kb) {
 #pragma unroll
-    for (int ks = 0; ks < NK; ++ks) {
-        const uint64_t oa = (uint64_t)(((ks >> 2) * ABLK + (ks & 3) * 32) >> 4);
-        const uint64_t ob = (uint64_t)(((ks >> 2) * BBLK + (ks & 3) * 32) >> 4);
-        mma_tf32(d, ah + oa, bh + ob, idesc, (acc || ks > 0) ? 1u : 0u);
-        mma_tf32(d, ah + oa, bl + ob, idesc, 1u);
-        mma_tf32(d, al + oa, bh + ob, idesc, 1u);
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const uint64_t oa = (uint64_t)((kb * ABLK + k4 * 32) >> 4), ob = (uint64_t)((kb * BBLK + k4 * 32) >> 4);
+            mma_tf32(d, ah + oa, bh + ob, idesc, (acc || kb > 0 || k4 > 0) ? 1u : 0u);
+            mma_tf32(d, ah + oa, bl + ob, idesc, 1u);
+            mma_tf32(d, al + oa, bh + ob, idesc, 1u);
+        }
     }
 }
 // The same with A in TMEM (hi / lo columns ah / al, one element per column).
 template <int NK, uint32_t BBLK>
 __device__ __forceinline__ void prod_ts(uint32_t d, uint32_t ah, uint32_t al, uint64_t bh, uint64_t bl,
                                         uint32_t idesc, bool acc) {
+#pragma unroll 1
+    for (int kb = 0; kb < NK / 4; ++kb) {
 #pragma unroll
-    for (int ks = 0; ks < NK; ++ks) {
-        const uint64_t ob = (uint64_t)(((ks >> 2) * BBLK + (ks & 3) * 32) >> 4);
-        mma_tf32_ts(d, ah + 8 * ks, bh + ob, idesc, (acc || ks > 0) ? 1u : 0u);
-        mma_tf32_ts(d, ah + 8 * ks, bl + ob, idesc, 1u);
-        mma_tf32_ts(d, al + 8 * ks, bh + ob, idesc, 1u);
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const uint64_t ob = (uint64_t)((kb * BBLK + k4 * 32) >> 4);
+            const uint32_t ka = 32 * kb + 8 * k4;
+            mma_tf32_ts(d, ah + ka, bh + ob, idesc, (acc || kb > 0 || k4 > 0) ? 1u : 0u);
+            mma_tf32_ts(d, ah + ka, bl + ob, idesc, 1u);
+            mma_tf32_ts(d, al + ka, bh + ob, idesc, 1u);
+        }
     }
 }
 
@@ -149,6 +156,7 @@ __global__ void __launch_bounds__(tfp::NT, 1)
     float *vec = reinterpret_cast<float *>(sm + SMALL);
     float *s_rk = vec, *s_rq = vec + 64, *s_beta = vec + 128, *s_part = vec + 192;
     float *s_fac = vec + 448, *s_fpend = vec + 576, *s_egl = vec + 704;
+    float *s_nrm = reinterpret_cast<float *>(sm + SMALL + 3344 + 16);  // [4 channel groups][2][64] squared norms
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + SMALL + 3328);
     uint32_t *s_taddr = reinterpret_cast<uint32_t *>(sm + SMALL + 3336);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, half = warp >> 2;
@@ -198,60 +206,74 @@ __global__ void __launch_bounds__(tfp::NT, 1)
         tc_fence_after();
     };
 
+    // g of (row r of the chunk at c0, this thread's channel ci), 0 past the chunk's L rows
+    auto gload = [&](int64_t c0, int r, int L) -> float {
+        if (r >= L) return 0.f;
+        if constexpr (GCH) return g[((size_t)(c0 + r) * H + h) * D + ci];
+        else if constexpr (GHD) return g[(size_t)(c0 + r) * H + h];
+        else return 0.f;
+    };
     for (int64_t c0 = start; c0 < end; c0 += Cc) {
         const int L = (int)((end - c0) < (int64_t)Cc ? (end - c0) : (int64_t)Cc);
-        // ---- row norms of k and q (warp w: rows 8w..8w+7), beta, and the decay scan
-        {
-            float4 a[8], b[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int r = 8 * warp + m;
-                a[m] = b[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (r < L) {
-                    const size_t o = ((size_t)(c0 + r) * H + h) * D + 4 * lane;
-                    a[m] = *reinterpret_cast<const float4 *>(k + o);
-                    b[m] = *reinterpret_cast<const float4 *>(q + o);
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float sk = a[m].x * a[m].x + a[m].y * a[m].y + a[m].z * a[m].z + a[m].w * a[m].w;
-                float sq = b[m].x * b[m].x + b[m].y * b[m].y + b[m].z * b[m].z + b[m].w * b[m].w;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
-                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                }
-                const int r = 8 * warp + m;
-                if (lane == 0) {
-                    s_rk[r] = r < L ? inv_norm(sk, eps) : 0.f;
-                    s_rq[r] = r < L ? inv_norm(sq, eps) : 0.f;
-                }
-            }
-            if (tid < 64) s_beta[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        // ---- the next chunk's rows of q, k, v (and g) into L2 while this one is processed
+        if (c0 + Cc < end) {
+            const int64_t n0 = c0 + Cc;
+            const int Ln = (int)((end - n0) < (int64_t)Cc ? (end - n0) : (int64_t)Cc);
+            const int which = tid >> 6, r = tid & 63;
+            const float *src = which == 0 ? q : which == 1 ? k : which == 2 ? (v_zero ? nullptr : v)
+                                                                            : (GCH ? g : nullptr);
+            if (r < Ln && src != nullptr) prefetch_l2_bulk(src + ((size_t)(n0 + r) * H + h) * D, D * 4);
         }
-        float G[32];
+        // ---- this thread's g, k, q (rows 32 ch.., channel ci) in one round trip; beta
+        float gr[32], kr[32], qr[32];
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const int r = 32 * ch + m;
+            gr[m] = gload(c0, r, L);
+            kr[m] = qr[m] = 0.f;
+            if (r < L) {
+                const size_t o = ((size_t)(c0 + r) * H + h) * D + ci;
+                kr[m] = k[o];
+                qr[m] = q[o];
+            }
+        }
+        if (tid < 64) s_beta[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        // squared row norms over this warp's 32 channels: a butterfly leaves row 32 ch + lane's sum on lane
+        {
+            float a[32], b[32];
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+                a[m] = kr[m] * kr[m];
+                b[m] = qr[m] * qr[m];
+            }
+#pragma unroll
+            for (int w = 16; w > 0; w >>= 1) {
+                const bool up = (lane & w) != 0;
+#pragma unroll
+                for (int m = 0; m < w; ++m) {
+                    const float sa = up ? a[m] : a[m + w], sb = up ? b[m] : b[m + w];
+                    const float ra = __shfl_xor_sync(0xffffffffu, sa, w), rb = __shfl_xor_sync(0xffffffffu, sb, w);
+                    a[m] = (up ? a[m + w] : a[m]) + ra;
+                    b[m] = (up ? b[m + w] : b[m]) + rb;
+                }
+            }
+            s_nrm[(warp & 3) * 128 + 32 * ch + lane] = a[0];
+            s_nrm[(warp & 3) * 128 + 64 + 32 * ch + lane] = b[0];
+        }
         {
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const int r = 32 * ch + m;
-                float gv = 0.f;
-                if (r < L) {
-                    if constexpr (GCH) gv = g[((size_t)(c0 + r) * H + h) * D + ci];
-                    else if constexpr (GHD) gv = g[(size_t)(c0 + r) * H + h];
-                }
-                acc += gv;
-                G[m] = acc;
-            }
+            for (int m = 0; m < 32; ++m) acc += gr[m];
             s_part[ch * 128 + ci] = acc;
         }
         __syncthreads();
-        const float p0 = s_part[ci], GL = p0 + s_part[128 + ci];
-        if (ch == 1) {
-#pragma unroll
-            for (int m = 0; m < 32; ++m) G[m] += p0;
+        if (tid < 128) {  // inverse norms: k rows (tid < 64), q rows
+            const float ss = s_nrm[tid] + s_nrm[128 + tid] + s_nrm[256 + tid] + s_nrm[384 + tid];
+            const int r = tid & 63;
+            (tid < 64 ? s_rk : s_rq)[r] = r < L ? inv_norm(ss, eps) : 0.f;
         }
+        // G of row r runs as acc = (G of the rows before this thread's half) + its g, in row order
+        const float p0 = s_part[ci], GL = p0 + s_part[128 + ci], gbase = ch ? p0 : 0.f;
         const bool exact = __syncthreads_or(!(GL >= -SPAN_MAX)) != 0;
         const float cI = exact ? 0.f : fminf(0.f, GL + ANCHOR);
         if (ch == 0) {
@@ -259,71 +281,62 @@ __global__ void __launch_bounds__(tfp::NT, 1)
             s_egl[ci] = expf(GL);
         }
 
-        // ---- operand tiles: [Lk; Lq] and Rk (hi / lo), Rk^T (Kb^T) kept in registers
-        float rkt[32];
+        // ---- operand tiles: [Lk; Lq] and, row-major, the state-update operand Rk (Kb on exact chunks)
         if (!exact) {
+            float acc = gbase;
 #pragma unroll
             for (int m = 0; m < 32; ++m) {
                 const int r = 32 * ch + m;
-                float kk = 0.f, qq = 0.f;
-                if (r < L) {
-                    const size_t o = ((size_t)(c0 + r) * H + h) * D + ci;
-                    kk = k[o];
-                    qq = q[o];
-                }
-                const float kh = kk * s_rk[r], qh = qq * s_rq[r];
-                const float e1 = expf(G[m] - cI), e2 = expf(cI - G[m]);
-                rkt[m] = e2 * kh;
+                acc += gr[m];
+                const float kh = kr[m] * s_rk[r], qh = qr[m] * s_rq[r];
+                const float e1 = expf(acc - cI), e2 = expf(cI - acc);
                 put_hilo(sm, KQH, KQL, kmaj(r, ci, 128), e1 * kh);
                 put_hilo(sm, KQH, KQL, kmaj(64 + r, ci, 128), e1 * qh);
-                put_hilo(sm, RKH, RKL, kmaj(r, ci, 64), rkt[m]);
+                put_hilo(sm, RKH, RKL, kmaj(r, ci, 64), e2 * kh);
             }
         } else {
-            // exact pairwise decays: stage k^, q^, G, form A and P, then build [Lk; Lq] with c = 0
+            // exact pairwise decays: stage k^, q^, G; A_raw and P_raw straight into TMEM; then [Lk; Lq], c = 0
             float *xk = reinterpret_cast<float *>(sm + XK), *xq = reinterpret_cast<float *>(sm + XQ);
-            float *xg = reinterpret_cast<float *>(sm + XG), *ap = reinterpret_cast<float *>(sm + XAP);
+            float *xg = reinterpret_cast<float *>(sm + XG);
+            float acc = gbase;
 #pragma unroll
             for (int m = 0; m < 32; ++m) {
                 const int r = 32 * ch + m;
-                float kk = 0.f, qq = 0.f;
-                if (r < L) {
-                    const size_t o = ((size_t)(c0 + r) * H + h) * D + ci;
-                    kk = k[o];
-                    qq = q[o];
-                }
-                const float kh = kk * s_rk[r];
+                acc += gr[m];
+                gr[m] = acc;  // G from here on
+                const float kh = kr[m] * s_rk[r];
                 xk[r * XLD + ci] = kh;
-                xq[r * XLD + ci] = qq * s_rq[r];
-                xg[r * XLD + ci] = G[m];
-                rkt[m] = expf(GL - G[m]) * kh;
+                xq[r * XLD + ci] = qr[m] * s_rq[r];
+                xg[r * XLD + ci] = acc;
+                put_hilo(sm, RKH, RKL, kmaj(r, ci, 64), expf(GL - acc) * kh);
             }
             __syncthreads();
-            for (int p = tid; p < C * C; p += NT) {
-                const int r = p >> 6, s = p & 63;
-                float a = 0.f, pq = 0.f;
-                if (s <= r && r < L) {
-                    for (int i = 0; i < D; ++i) {
-                        const float ks = xk[s * XLD + i] * expf(xg[r * XLD + i] - xg[s * XLD + i]);
-                        a = fmaf(xk[r * XLD + i], ks, a);
-                        pq = fmaf(xq[r * XLD + i], ks, pq);
+            {
+                // lane = row of [A_raw; P_raw] (key row r for A, query row r for P), 32 columns s
+                const int rr = jl & 63;
+                const float *xa = jl < 64 ? xk : xq;
+                uint32_t o[32];
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int s = 32 * half + m;
+                    float a = 0.f;
+                    if (s <= rr) {
+#pragma unroll 4
+                        for (int i = 0; i < D; ++i)
+                            a = fmaf(xa[rr * XLD + i], xk[s * XLD + i] * expf(xg[rr * XLD + i] - xg[s * XLD + i]), a);
                     }
+                    o[m] = f2u(a);
                 }
-                ap[r * 65 + s] = s < r ? s_beta[r] * a : 0.f;
-                ap[(64 + r) * 65 + s] = pq;
+                tmem_st32(tbase + lq + T_AP + 32 * half, o);
+                tmem_st_wait();
             }
             __syncthreads();
 #pragma unroll
             for (int m = 0; m < 32; ++m) {
                 const int r = 32 * ch + m;
-                float kk = 0.f, qq = 0.f;
-                if (r < L) {
-                    const size_t o = ((size_t)(c0 + r) * H + h) * D + ci;
-                    kk = k[o];
-                    qq = q[o];
-                }
-                const float e1 = expf(G[m]);
-                put_hilo(sm, KQH, KQL, kmaj(r, ci, 128), e1 * kk * s_rk[r]);
-                put_hilo(sm, KQH, KQL, kmaj(64 + r, ci, 128), e1 * qq * s_rq[r]);
+                const float e1 = expf(gr[m]);
+                put_hilo(sm, KQH, KQL, kmaj(r, ci, 128), e1 * kr[m] * s_rk[r]);
+                put_hilo(sm, KQH, KQL, kmaj(64 + r, ci, 128), e1 * qr[m] * s_rq[r]);
             }
         }
         fence_async_smem();
@@ -358,6 +371,12 @@ __global__ void __launch_bounds__(tfp::NT, 1)
                                sdesc_sw128(sb + KQL, 16, 1024), ID_N128, false);
             mma_commit(bar);
         });
+        // v^T of this thread's value channel (warps 4-7), loaded while G0 runs
+        float vv[64];
+        if (half == 1) {
+#pragma unroll
+            for (int s = 0; s < 64; ++s) vv[s] = (s < L && !v_zero) ? v[((size_t)(c0 + s) * H + h) * D + jl] : 0.f;
+        }
         wait_mma();
         if (!ok) break;
 
@@ -366,16 +385,12 @@ __global__ void __launch_bounds__(tfp::NT, 1)
 #pragma unroll 1
             for (int part = 0; part < 2; ++part) {
                 float a[32];
-                if (!exact) {
+                {
                     uint32_t r0[32];
                     tmem_ld32(tbase + lq + T_AP + 32 * part, r0);
                     tmem_ld_wait();
 #pragma unroll
                     for (int m = 0; m < 32; ++m) a[m] = u2f(r0[m]);
-                } else {
-                    const float *ap = reinterpret_cast<const float *>(sm + XAP);
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) a[m] = ap[jl * 65 + 32 * part + m];
                 }
                 if (jl < 64) {
                     float *af = reinterpret_cast<float *>(sm + AF);
@@ -383,7 +398,7 @@ __global__ void __launch_bounds__(tfp::NT, 1)
 #pragma unroll
                     for (int m = 0; m < 32; ++m) {
                         const int s = 32 * part + m;
-                        af[jl * 65 + s] = exact ? a[m] : (s < jl ? br * a[m] : 0.f);
+                        af[jl * 65 + s] = s < jl ? br * a[m] : 0.f;
                     }
                 } else {
                     const int r = jl - 64;
@@ -400,20 +415,14 @@ __global__ void __launch_bounds__(tfp::NT, 1)
                 }
             }
         } else {
-#pragma unroll 1
-            for (int part = 0; part < 2; ++part) {
-                float vv[32];
 #pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int s = 32 * part + m;
-                    vv[m] = (s < L && !v_zero) ? v[((size_t)(c0 + s) * H + h) * D + jl] : 0.f;
-                }
+            for (int part = 0; part < 2; ++part) {
                 uint32_t x[32], hi[32];
                 tmem_ld32(tbase + lq + T_XO + 32 * part, x);
                 tmem_ld_wait();
 #pragma unroll
                 for (int m = 0; m < 32; ++m) {
-                    const float w = vv[m] - u2f(x[m]);
+                    const float w = vv[32 * part + m] - u2f(x[m]);
                     const float wh = tf32_hi(w);
                     hi[m] = f2u(wh);
                     x[m] = f2u(w - wh);
@@ -429,9 +438,9 @@ __global__ void __launch_bounds__(tfp::NT, 1)
         //      (warp b, lane = column), then block row by block row
         {
             const float *af = reinterpret_cast<const float *>(sm + AF);
-            float *ni = reinterpret_cast<float *>(sm + NI), *ys = reinterpret_cast<float *>(sm + YS);
-            if (warp < 4) {
-                const int b0 = 16 * warp, c = lane & 15;
+            float *ni = reinterpret_cast<float *>(sm + NI), *at = reinterpret_cast<float *>(sm + AT);
+            if (warp < 4 && lane < 16) {
+                const int b0 = 16 * warp, c = lane;  // column c of D_b, rows in order
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
@@ -440,31 +449,31 @@ __global__ void __launch_bounds__(tfp::NT, 1)
                     for (int t = 0; t < r; ++t) acc = fmaf(-af[(b0 + r) * 65 + b0 + t], x[t], acc);
                     x[r] = acc;
                 }
-                if (lane < 16)
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) ni[(b0 + r) * 65 + b0 + c] = x[r];
+                for (int r = 0; r < 16; ++r) ni[(b0 + r) * 65 + b0 + c] = x[r];
             }
             __syncthreads();
+            // At_ik = D_i A_ik for the six blocks below the diagonal (i > k)
+            for (int e = tid; e < 6 * 256; e += NT) {
+                const int pb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                const int i = pb < 1 ? 1 : pb < 3 ? 2 : 3, kb = pb - (i * (i - 1)) / 2;
+                float y = 0.f;
+#pragma unroll 4
+                for (int t = 0; t < 16; ++t)
+                    if (t <= rr) y = fmaf(ni[(16 * i + rr) * 65 + 16 * i + t], af[(16 * i + t) * 65 + 16 * kb + cc], y);
+                at[(16 * i + rr) * 65 + 16 * kb + cc] = y;
+            }
+            __syncthreads();
+            // block row i: Ninv_ij = -sum_{j <= kb < i} At_i,kb Ninv_kb,j for j < i
 #pragma unroll 1
-            for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                // Y_ij = sum_{j <= kb < i} A_i,kb Ninv_kb,j  (i = j + d)
-                for (int e = tid; e < nb * 256; e += NT) {
-                    const int j = e >> 8, i = j + d, rr = (e >> 4) & 15, cc = e & 15;
+            for (int i = 1; i < 4; ++i) {
+                for (int e = tid; e < i * 256; e += NT) {
+                    const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
                     float y = 0.f;
                     for (int kb = j; kb < i; ++kb)
-#pragma unroll
+#pragma unroll 4
                         for (int t = 0; t < 16; ++t)
-                            y = fmaf(af[(16 * i + rr) * 65 + 16 * kb + t], ni[(16 * kb + t) * 65 + 16 * j + cc], y);
-                    ys[j * 272 + rr * 17 + cc] = y;
-                }
-                __syncthreads();
-                // Ninv_ij = -Ninv_ii Y_ij
-                for (int e = tid; e < nb * 256; e += NT) {
-                    const int j = e >> 8, i = j + d, rr = (e >> 4) & 15, cc = e & 15;
-                    float y = 0.f;
-                    for (int t = 0; t <= rr; ++t)
-                        y = fmaf(ni[(16 * i + rr) * 65 + 16 * i + t], ys[j * 272 + t * 17 + cc], y);
+                            y = fmaf(at[(16 * i + rr) * 65 + 16 * kb + t], ni[(16 * kb + t) * 65 + 16 * j + cc], y);
                     ni[(16 * i + rr) * 65 + 16 * j + cc] = -y;
                 }
                 __syncthreads();
@@ -504,10 +513,22 @@ __global__ void __launch_bounds__(tfp::NT, 1)
             tmem_st32(tbase + lq + T_W + 32 * half, hi);
             tmem_st32(tbase + lq + T_W + 64 + 32 * half, u);
         }
-#pragma unroll
+        // Rk^T (Kb^T) from the row-major tile: thread (channel ci, rows 32 ch..), 16-byte groups of 4 rows
+#pragma unroll 2
         for (int g4 = 0; g4 < 8; ++g4) {
-            const float x[4] = {rkt[4 * g4], rkt[4 * g4 + 1], rkt[4 * g4 + 2], rkt[4 * g4 + 3]};
-            put_hilo4(sm, RKH, RKL, (uint32_t)(ch * 16384 + ci * 128 + ((g4 ^ (ci & 7)) << 4)), x);
+            const int r0 = 32 * ch + 4 * g4;
+            float4 hv, lv;
+            hv.x = *reinterpret_cast<const float *>(sm + RKH + kmaj(r0, ci, 64));
+            hv.y = *reinterpret_cast<const float *>(sm + RKH + kmaj(r0 + 1, ci, 64));
+            hv.z = *reinterpret_cast<const float *>(sm + RKH + kmaj(r0 + 2, ci, 64));
+            hv.w = *reinterpret_cast<const float *>(sm + RKH + kmaj(r0 + 3, ci, 64));
+            lv.x = *reinterpret_cast<const float *>(sm + RKL + kmaj(r0, ci, 64));
+            lv.y = *reinterpret_cast<const float *>(sm + RKL + kmaj(r0 + 1, ci, 64));
+            lv.z = *reinterpret_cast<const float *>(sm + RKL + kmaj(r0 + 2, ci, 64));
+            lv.w = *reinterpret_cast<const float *>(sm + RKL + kmaj(r0 + 3, ci, 64));
+            const uint32_t off = kmaj(ci, r0, 128);
+            *reinterpret_cast<float4 *>(sm + RTH + off) = hv;
+            *reinterpret_cast<float4 *>(sm + RTL + off) = lv;
         }
         if (exact) {
 #pragma unroll 1
@@ -528,8 +549,8 @@ __global__ void __launch_bounds__(tfp::NT, 1)
         issue([&] {
             prod_ts<8, 8192>(tbase + T_XO + 64, tbase + T_W, tbase + T_W + 64, sdesc_sw128(sb + PH, 16, 1024),
                              sdesc_sw128(sb + PL, 16, 1024), ID_N64, true);
-            prod_ts<8, 16384>(tbase + T_S, tbase + T_W, tbase + T_W + 64, sdesc_sw128(sb + RKH, 16, 1024),
-                              sdesc_sw128(sb + RKL, 16, 1024), ID_N128, true);
+            prod_ts<8, 16384>(tbase + T_S, tbase + T_W, tbase + T_W + 64, sdesc_sw128(sb + RTH, 16, 1024),
+                              sdesc_sw128(sb + RTL, 16, 1024), ID_N128, true);
             mma_commit(bar);
         });
         wait_mma();

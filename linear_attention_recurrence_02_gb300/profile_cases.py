@@ -1,12 +1,12 @@
 """Run one workload of the library a fixed number of times, for profiler captures.
 
     python -m linear_attention_recurrence_02_gb300.profile_cases CASE [--B 64] [--T 4096] [--H 96]
-        [--gate channel|head|none] [--warmup 3] [--reps 2]
+        [--gate channel|head|none] [--dtype bf16|f32] [--warmup 3] [--reps 2]
 
 Every call goes through the C ABI exactly as a user's does. Inputs are drawn
 on the device by a seeded torch generator with the workloads' distributions
 (q, k, v, x ~ N(0,1) in bf16, g = -softplus(N(0,1)), beta = sigmoid(N(0,1)),
-state ~ N(0, 0.02^2)); nothing is checked, the point is a known launch
+state ~ N(0, 0.02^2); --dtype f32 keeps the prefill's q, k, v in fp32); nothing is checked, the point is a known launch
 sequence: `warmup` calls, then `reps` calls, one launch of the named kernel
 each (the prefill adds no other launch for one sequence). Cases:
 
@@ -34,6 +34,7 @@ def main(argv=None) -> int:
     ap.add_argument("--H", type=int, default=96)
     ap.add_argument("--D", type=int, default=128)
     ap.add_argument("--gate", default="channel", choices=["channel", "head", "none"])
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f32"])
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--reps", type=int, default=2)
     a = ap.parse_args(argv)
@@ -70,7 +71,8 @@ def main(argv=None) -> int:
             else:
                 kda.kda_shortconv_step(x, ring, w, y)
     else:
-        q, k, v = rnd(T, H, D).to(bf), rnd(T, H, D).to(bf), rnd(T, H, D).to(bf)
+        dt = bf if a.dtype == "bf16" else torch.float32
+        q, k, v = rnd(T, H, D).to(dt), rnd(T, H, D).to(dt), rnd(T, H, D).to(dt)
         g, beta = gate_of((T, H, D)), torch.sigmoid(rnd(T, H))
         out = torch.empty_like(q)
         sf = torch.empty((1, H, D, D), device=dev)
