@@ -479,7 +479,7 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
         gates[name] = {"value": ws * toks / (gms * 1e-3), "unit": "tokens/s", "ms_per_call": gms,
                        "roofline_hbm": {"achieved": gby / (gms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                                         "frac": gby / (gms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": gby}}
-    # the same workload in fp32, which runs the CUDA-core (reference-grade) kernel
+    # the same workload in fp32: the tensor-core kernel in tf32 with a 3-term hi/lo split per product
     simt = None
     try:
         q32, k32, v32 = (t_.float() for t_ in (q, k, v))
@@ -499,10 +499,17 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
         torch.cuda.synchronize(dev)
         sms = max_over_ranks(statistics.mean(a0.elapsed_time(b0) for a0, b0 in se), dev)
         sby = T * H * (3 * D * 4 + D * 4 + 4 + D * 4) + H * D * D * 4
+        # tensor-pipe work as issued: per chunk-head the five products (G1 128x64x128, G0 128x128x128,
+        # G2, G3 128x64x64, G4 128x128x64) at 2 flops per multiply-add, three tf32 MMAs each
+        sfl = 3 * 2 * (128 * 64 * 128 + 128 * 128 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64) * (T // C) * H
+        tf32_peak = tc_peak / 2.0  # dense tf32 runs at half the bf16 rate (nominal 1.1 vs 2.25 PFLOP/s)
         simt = {"value": ws * toks / (sms * 1e-3), "unit": "tokens/s", "ms_per_call": sms,
-                "kernel": "prefill_simt_kernel (fp32 q/k/v/out)",
+                "kernel": "prefill_tf32_kernel (fp32 q/k/v/out; tcgen05 kind::tf32, 3xTF32 products)",
                 "roofline_hbm": {"achieved": sby / (sms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                                 "frac": sby / (sms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": sby}}
+                                 "frac": sby / (sms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": sby},
+                "roofline_tensor": {"achieved": sfl / (sms * 1e-3) / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
+                                    "frac": sfl / (sms * 1e-3) / 1e12 / tf32_peak, "flops_issued": sfl,
+                                    "peak_source": f"{peak_src} bf16_tflops (burst) x 1/2 (tf32 : bf16 nominal)"}}
         del q32, k32, v32, o32
     except kda.KdaError as e:
         simt = {"unavailable": str(e)}

@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(BULK_NT, 3)
     using namespace tc;
     constexpr int D = 128, NW = BULK_NT / 32;
     extern __shared__ uint8_t smem_raw[];
-    float *Ss = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+    // 16-byte aligned base derived from the shared array itself (accesses compile to shared-memory instructions)
+    float *Ss = reinterpret_cast<float *>(
+        smem_raw + ((16u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 15u)) & 15u));
     __shared__ float s_y[3][D];
     __shared__ float s_qa[D], s_ka[D], s_kh[D], s_a[D], s_delta[D];
     __shared__ float s_red[NW][3];

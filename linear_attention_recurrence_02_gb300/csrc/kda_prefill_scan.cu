@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(fixtc::NT) scan_fixup_tc_kernel(const __grid_c
     using namespace fixtc;
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base derived from the shared array itself (accesses compile to shared-memory instructions)
+    uint8_t *sm = smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + BAR), *bar_m = bar_a + 1;
     uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bar_a + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

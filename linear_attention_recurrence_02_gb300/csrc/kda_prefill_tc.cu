@@ -361,7 +361,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
     constexpr int BAR_CHAIN = 2, BAR_BACK = 3, BAR_FRONT = 4;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base derived from the shared array itself (accesses compile to shared-memory instructions)
+    uint8_t *sm = smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
     float *s_rq = reinterpret_cast<float *>(sm + SMALL);
     float *s_rk = s_rq + 64;
     float *s_beta = s_rk + 64;

@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(tfp::NT, 1)
     using namespace tfp;
     constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base derived from the shared array itself (accesses compile to shared-memory instructions)
+    uint8_t *sm = smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
     float *vec = reinterpret_cast<float *>(sm + SMALL);
     float *s_rk = vec, *s_rq = vec + 64, *s_beta = vec + 128, *s_part = vec + 192;
     float *s_fac = vec + 448, *s_fpend = vec + 576, *s_egl = vec + 704;
