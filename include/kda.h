@@ -310,6 +310,14 @@ kda_status kda_chunk_prefill_epi(const void *q, const void *k, const void *v, co
                                  const float *norm_weight, kda_gate_act act, float norm_eps,
                                  void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
+/* Name of the kernel kda_chunk_prefill (and the gated, epilogue and scan
+ * entry points, per segment) runs for head dimension D, chunk size C and
+ * dtype: "prefill_tc_pipe_kernel" (tcgen05, bf16), "prefill_tf32_kernel"
+ * (tcgen05 kind::tf32, fp32), "prefill_f32_kernel" (CUDA cores, D = 128) or
+ * "prefill_simt_kernel" (CUDA cores, any shape). A static string; NULL when
+ * D, C or dtype is not one kda_chunk_prefill accepts. Needs no GPU. */
+const char *kda_chunk_prefill_route(int D, int C, kda_dtype dtype);
+
 /* Workspace bytes kda_chunk_prefill needs for these sizes (may be 0). */
 size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H, int D, int C);
 
@@ -329,8 +337,14 @@ size_t kda_chunk_prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int
  *                 (then N must be 1). Chunks never straddle sequences; a
  *                 sequence's last chunk may be short; empty sequences pass
  *                 their initial state through.
- *   C             chunk size: 1..64 (bf16 with D = 128 and C = 64 takes the
- *                 tensor-core path; every other combination runs on CUDA cores)
+ *   C             chunk size: 1..64. The kernel each shape runs on is what
+ *                 kda_chunk_prefill_route names: bf16 with D = 128 or 64 and
+ *                 C = 16, 32 or 64 takes the bf16 tensor-core kernel, which
+ *                 always works in 64-token chunks (the chunked form is an exact
+ *                 rewrite of the recurrence, so the chunk length changes only
+ *                 the rounding); fp32 with D = 128 and C >= 16 the tf32
+ *                 tensor-core kernel; other D = 128 shapes a register-tiled
+ *                 CUDA-core kernel; the rest the general CUDA-core kernel
  *   workspace     device buffer of at least
  *                 kda_chunk_prefill_workspace_bytes(T, N, H, D, C) bytes
  *                 (NULL allowed when that is 0); contents are scratch. For

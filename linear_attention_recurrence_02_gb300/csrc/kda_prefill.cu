@@ -221,6 +221,19 @@ kda_status prefill_run(const PrefillArgs &a, cudaStream_t s) {
     return prefill_simt(a, s);
 }
 
+extern "C" const char *kda_chunk_prefill_route(int D, int C, kda_dtype dtype) {
+    if (!valid_head_dim(D) || C < 1 || C > SIMT_CMAX || (dtype != KDA_F32 && dtype != KDA_BF16)) return nullptr;
+    PrefillArgs a{};
+    a.D = D;
+    a.C = C;
+    a.T = 1;
+    a.bf16 = dtype == KDA_BF16;
+    if (prefill_tc_applicable(a)) return "prefill_tc_pipe_kernel";
+    if (prefill_tf32_applicable(a)) return "prefill_tf32_kernel";
+    if (prefill_f32_applicable(a)) return "prefill_f32_kernel";
+    return "prefill_simt_kernel";
+}
+
 // Longest sequences first: a sequence's chunks are walked serially by its
 // CTAs, so starting the long chains first shortens the tail of a mixed-length
 // batch (greedy longest-processing-time order). order[rank] = n, where rank

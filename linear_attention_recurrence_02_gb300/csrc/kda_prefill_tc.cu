@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                            const float *__restrict__ g_head, const float *__restrict__ beta, const float *s_init,
                            float *s_final, __nv_bfloat16 *__restrict__ out, const int64_t *__restrict__ cu_seqlens,
                            int N, int64_t Ttot, int H, float eps, unsigned *err, const int *__restrict__ order,
-                           int v_zero) {
+                           int v_zero, int dg) {
+    // dg: the head dimension in memory (128, or 64 with channels 64..127 zero-filled by the loads)
     using namespace pipe;
     constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
     constexpr int BAR_CHAIN = 2, BAR_BACK = 3, BAR_FRONT = 4;
@@ -401,22 +402,21 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     const int h = blockIdx.x % H, n = order ? order[blockIdx.x / H] : (int)(blockIdx.x / H);
     int64_t start, end;
     if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
-    const int x0 = h * D;
     const int nchunks = (int)((end - start + C - 1) / C);
 
     auto issue_qk = [&](int y, int b) {
         uint8_t *xb = sm + X0 + 32768 * b;
         s_armed[b] += 1;
         mbar_arrive_expect_tx(bar_qk + b, QK_BYTES);
-        tma_load_2d(xb, &tm_k, bar_qk + b, x0, y);
-        tma_load_2d(xb + 16384, &tm_k, bar_qk + b, x0 + 64, y);
-        tma_load_2d(xb + 8192, &tm_q, bar_qk + b, x0, y);
-        tma_load_2d(xb + 24576, &tm_q, bar_qk + b, x0 + 64, y);
+        tma_load_3d(xb, &tm_k, bar_qk + b, 0, h, y);
+        tma_load_3d(xb + 16384, &tm_k, bar_qk + b, 64, h, y);
+        tma_load_3d(xb + 8192, &tm_q, bar_qk + b, 0, h, y);
+        tma_load_3d(xb + 24576, &tm_q, bar_qk + b, 64, h, y);
     };
     auto issue_g = [&](int y) {
         s_armed[2] += 1;
         mbar_arrive_expect_tx(bar_g, G_BYTES);
-        tma_load_2d(sm + G_, &tm_g, bar_g, x0, y);
+        tma_load_3d(sm + G_, &tm_g, bar_g, 0, h, y);
     };
     auto issue_v = [&](int y) {
         s_armed[3] += 1;
@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             return;
         }
         mbar_arrive_expect_tx(bar_v, V_BYTES);
-        tma_load_2d(sm + V_, &tm_v, bar_v, x0, y);
-        tma_load_2d(sm + V_ + 8192, &tm_v, bar_v, x0 + 64, y);
+        tma_load_3d(sm + V_, &tm_v, bar_v, 0, h, y);
+        tma_load_3d(sm + V_ + 8192, &tm_v, bar_v, 64, h, y);
     };
 
     if (tid == 0) {
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     const uint32_t lrow = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
     const uint32_t sbase = smem_u32(sm);
     const int jl = 32 * q4 + lane;                    // this thread's TMEM lane (channel)
-    const size_t soff = ((size_t)n * H + h) * D * D;
+    const size_t soff = ((size_t)n * H + h) * dg * dg;  // the state of this (sequence, head): [dg][dg]
     bool ok = true;
 
     if (is_prep) {
@@ -496,13 +496,15 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                     // inside the pipeline's dependency cycle: stage their tiles in L2
                     if (ci + 2 < nchunks) {
                         const int y2 = (int)(c0 + 2 * C);
-                        tma_prefetch_l2_2d(&tm_k, x0, y2);
-                        tma_prefetch_l2_2d(&tm_k, x0 + 64, y2);
-                        tma_prefetch_l2_2d(&tm_q, x0, y2);
-                        tma_prefetch_l2_2d(&tm_q, x0 + 64, y2);
-                        tma_prefetch_l2_2d(&tm_v, x0, y2);
-                        tma_prefetch_l2_2d(&tm_v, x0 + 64, y2);
-                        if constexpr (GCH) tma_prefetch_l2_2d(&tm_g, x0, y2);
+                        tma_prefetch_l2_3d(&tm_k, 0, h, y2);
+                        tma_prefetch_l2_3d(&tm_q, 0, h, y2);
+                        tma_prefetch_l2_3d(&tm_v, 0, h, y2);
+                        if (dg > 64) {
+                            tma_prefetch_l2_3d(&tm_k, 64, h, y2);
+                            tma_prefetch_l2_3d(&tm_q, 64, h, y2);
+                            tma_prefetch_l2_3d(&tm_v, 64, h, y2);
+                        }
+                        if constexpr (GCH) tma_prefetch_l2_3d(&tm_g, 0, h, y2);
                     }
                 }
                 float *sb = s_beta + 64 * b;
@@ -1024,9 +1026,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
 #pragma unroll
         for (int part = 0; part < 4; ++part) {
             uint32_t r[32];
+            // dg is 64 or 128, so a 32-row part lies wholly inside or outside the stored state
+            const bool in = s_init != nullptr && jl < dg && 32 * part < dg;
 #pragma unroll
             for (int m = 0; m < 32; ++m)
-                r[m] = s_init ? __float_as_uint(s_init[soff + (size_t)(32 * part + m) * D + jl]) : 0u;
+                r[m] = in ? __float_as_uint(s_init[soff + (size_t)(32 * part + m) * dg + jl]) : 0u;
             tmem_st32(tbase + lrow + T_S + 32 * part, r);
         }
         tmem_st_wait();
@@ -1152,8 +1156,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 // a whole chunk: one bulk store per 64-channel box; the staging is
                 // rewritten once the copy engine has read it (next chunk)
                 if (ct == 0) {
-                    tma_store_2d(&tm_o, ost, x0, (int)c0);
-                    tma_store_2d(&tm_o, ost + 8192, x0 + 64, (int)c0);
+                    tma_store_3d(&tm_o, ost, 0, h, (int)c0);
+                    if (dg > 64) tma_store_3d(&tm_o, ost + 8192, 64, h, (int)c0);
                     bulk_commit();
                 }
             } else {
@@ -1168,7 +1172,8 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
 #pragma unroll
                 for (int k8 = 0; k8 < 8; ++k8) {
                     const int p = ct + 128 * k8, r = p >> 4, c16 = p & 15;
-                    if (r < L) *reinterpret_cast<uint4 *>(out + ((size_t)(c0 + r) * H + h) * D + c16 * 8) = orow[k8];
+                    if (r < L && 8 * c16 < dg)
+                        *reinterpret_cast<uint4 *>(out + ((size_t)(c0 + r) * H + h) * dg + c16 * 8) = orow[k8];
                 }
             }
             last_b = b;
@@ -1181,10 +1186,11 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 uint32_t r[32];
                 tmem_ld32(tbase + lrow + T_S + 32 * part, r);
                 tmem_ld_wait();
+                if (jl < dg && 32 * part < dg)
 #pragma unroll
-                for (int m = 0; m < 32; ++m)
-                    s_final[soff + (size_t)(32 * part + m) * D + jl] =
-                        __uint_as_float(r[m]) * (sg ? sg[32 * part + m] : 1.f);
+                    for (int m = 0; m < 32; ++m)
+                        s_final[soff + (size_t)(32 * part + m) * dg + jl] =
+                            __uint_as_float(r[m]) * (sg ? sg[32 * part + m] : 1.f);
             }
         }
         if (!ok) {
@@ -1238,10 +1244,29 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over [T][H][d] (dims innermost first: d, H, T), box box_d x 1 x box_t. A box reaching
+// past d (d = 64, box_d = 128) reads zeros there.
+static bool make_map3(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t elem, uint64_t d, uint64_t H,
+                      uint64_t T, uint32_t box_d, uint32_t box_t, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d, H, T};
+    const cuuint64_t strides[2] = {d * elem, H * d * elem};
+    const cuuint32_t box[3] = {box_d, 1, box_t};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tcp
 
+// bf16, d = 128 or 64 (64: the kernel's channels 64..127 read as zeros, which leaves every
+// product of the chunk algebra unchanged), C = 16, 32 or 64. The kernel always works in chunks of
+// 64 tokens: the chunked form is an exact rewrite of the recurrence, so the chunk length changes
+// only the rounding.
 bool prefill_tc_applicable(const PrefillArgs &a) {
-    return a.bf16 && a.D == 128 && a.C == 64 && a.T > 0 && a.T <= 0x7fffffffLL;
+    return a.bf16 && (a.D == 128 || a.D == 64) && (a.C == 64 || a.C == 32 || a.C == 16) && a.T > 0 &&
+           a.T <= 0x7fffffffLL;
 }
 
 // The pipelined kernel runs every gate form (4K workload, per-channel gate:
@@ -1254,8 +1279,8 @@ static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const C
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out);
     // the kernel stores whole output chunks through this map
     CUtensorMap mo;
-    if (!make_map(&mo, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.H * D, (uint64_t)a.T, 64, 64,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_map3(&mo, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.D, (uint64_t)a.H, (uint64_t)a.T, 64,
+                   64, CU_TENSOR_MAP_SWIZZLE_NONE))
         return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     // the register split only adds up for the launch register count it was made for
     static std::atomic<int> regs_ok{0};  // 0 unknown, 1 checked, -1 mismatch
@@ -1275,7 +1300,7 @@ static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const C
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
     prefill_tc_pipe_kernel<GM><<<(unsigned)a.N * a.H, pipe::NTP, pipe::SMEM, s>>>(
         mq, mk, mv, mg, mo, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order,
-        a.v_zero ? 1 : 0);
+        a.v_zero ? 1 : 0, a.D);
     return check_launch("prefill_tc_pipe_kernel");
 }
 
@@ -1283,12 +1308,13 @@ kda_status prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     using namespace tcp;
     CUtensorMap mq, mk, mv, mg;
     memset(&mg, 0, sizeof(mg));  // not read unless the gate is per channel
-    const uint64_t inner = (uint64_t)a.H * D, rows = (uint64_t)a.T;
-    if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        (a.gate == KDA_GATE_CHANNEL &&
-         !make_map(&mg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, inner, rows, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
+    const uint64_t d = (uint64_t)a.D, hh = (uint64_t)a.H, rows = (uint64_t)a.T;
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map3(&mq, a.q, bf, 2, d, hh, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map3(&mk, a.k, bf, 2, d, hh, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map3(&mv, a.v, bf, 2, d, hh, rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        (a.gate == KDA_GATE_CHANNEL && !make_map3(&mg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, hh, rows, 128, 64,
+                                                  CU_TENSOR_MAP_SWIZZLE_NONE)))
         return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     if (a.gate == KDA_GATE_HEAD) return launch_tc<KDA_GATE_HEAD>(a, mq, mk, mv, mg, s);
     if (a.gate == KDA_GATE_NONE) return launch_tc<KDA_GATE_NONE>(a, mq, mk, mv, mg, s);

@@ -72,6 +72,7 @@ _SIGNATURES = {
     "kda_shortconv_decode_step_epi": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci,
                                        _cf, _cf, ctypes.c_uint, _vp], _ci),
     "kda_chunk_prefill_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
+    "kda_chunk_prefill_route": ([_ci, _ci, _ci], ctypes.c_char_p),
     "kda_chunk_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
                            _cf, _vp, _sz, _vp], _ci),
     "kda_chunk_prefill_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci,
@@ -332,6 +333,18 @@ def kda_chunk_prefill_scan(q, k, v, g, beta, out, segments, initial_state=None, 
                                         float(l2_eps), int(segments), _ptr(workspace),
                                         0 if workspace is None else workspace.numel() * workspace.element_size(),
                                         _stream(stream, q.device)))
+
+
+def kda_chunk_prefill_route(D, C, dtype) -> str | None:
+    """Name of the kernel the chunked prefill runs for this head dimension, chunk size and dtype
+    (torch.bfloat16 / torch.float32 or the KDA_* dtype code); None for an unsupported shape."""
+    if isinstance(dtype, int):
+        code = dtype
+    else:
+        import torch
+        code = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32}[dtype]
+    r = lib().kda_chunk_prefill_route(int(D), int(C), int(code))
+    return None if r is None else r.decode()
 
 
 def kda_chunk_prefill_workspace_bytes(total_tokens, num_seqs, H, D, C) -> int:

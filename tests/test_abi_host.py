@@ -284,3 +284,24 @@ def test_prefill_epi_argument_checks(kda):
     assert st == kda.KDA_ERR_INVALID_ARG and "norm_weight is NULL" in L.kda_last_error_detail().decode()
     st = L.kda_chunk_prefill_epi(*base, 0x60000, 0x80000, kda.KDA_ACT_SIGMOID, 1e-6, None, 0, None)
     assert st == kda.KDA_ERR_INVALID_ARG and "out_gate must not alias" in L.kda_last_error_detail().decode()
+
+
+def test_prefill_route_table(kda):
+    """Which kernel each prefill shape runs on (no GPU needed): bf16 d in {64, 128} with C in {16, 32, 64}
+    on the tcgen05 kernel, fp32 d = 128 with C >= 16 on the tf32 tensor-core kernel, other d = 128 shapes
+    on the register-tiled CUDA-core kernel, everything else on the general one; invalid shapes give None."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    route = kda.kda_chunk_prefill_route
+    for D in (64, 128):
+        for C in (16, 32, 64):
+            assert route(D, C, bf) == "prefill_tc_pipe_kernel", (D, C)
+    for C in (16, 48, 64):
+        assert route(128, C, f32) == "prefill_tf32_kernel", C
+    assert route(128, 7, f32) == "prefill_f32_kernel"
+    assert route(128, 48, bf) == "prefill_f32_kernel"
+    assert route(64, 64, f32) == "prefill_simt_kernel"
+    assert route(32, 64, bf) == "prefill_simt_kernel"
+    assert route(64, 7, bf) == "prefill_simt_kernel"
+    assert route(48, 64, bf) is None and route(128, 0, bf) is None and route(128, 65, f32) is None
+    assert route(128, 64, 7) is None

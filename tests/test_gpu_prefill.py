@@ -312,3 +312,32 @@ def test_prefill_fp32_some_chunks_exact(env):
     o, s = run_prefill(torch, kda, d1, False, 64)
     ro, rs = oracle_prefill(d1)
     check(o, s, ro, rs, d1["cu_seqlens"], False, "spike")
+
+
+@pytest.mark.parametrize("gate", ["channel", "head", "none"])
+@pytest.mark.parametrize("D,C", [(64, 64), (64, 32), (64, 16), (128, 32), (128, 16)])
+def test_prefill_bf16_tensor_core_shapes(env, D, C, gate):
+    """bf16 shapes the tcgen05 kernel takes besides d=128/C=64: d=64 (its channels 64..127 read as zeros)
+    and C=16/32 (64-token chunks inside). Ragged varlen batch with an empty sequence, carry-in states,
+    several 64-token chunks per sequence and short last chunks; every gate form; against the oracle."""
+    torch, kda = env
+    assert kda.kda_chunk_prefill_route(D, C, torch.bfloat16) == "prefill_tc_pipe_kernel"
+    cu = np.array([0, 150, 150, 333, 397], dtype=np.int64)
+    d = synth.prefill_inputs(700 + D + C, int(cu[-1]), 3, D, True, cu_seqlens=cu, s0_std=0.3, g_scale=0.1)
+    bf = torch.bfloat16
+    q, k, v = (to_dev(d[n], bf, torch) for n in ("q", "k", "v"))
+    if gate == "channel":
+        gk, go = to_dev(d["g"], torch.float32, torch), d["g"]
+    elif gate == "head":
+        gk, go = to_dev(np.ascontiguousarray(d["g"][..., 0]), torch.float32, torch), np.repeat(d["g"][..., :1], D, axis=-1)
+    else:
+        gk, go = None, np.zeros_like(d["g"])
+    out = torch.full_like(q, float("nan"))
+    N = len(cu) - 1
+    sf = torch.full((N, 3, D, D), float("nan"), device="cuda")
+    kda.kda_chunk_prefill_gated(q, k, v, gk, to_dev(d["beta"], torch.float32, torch), out, gate=gate,
+                                initial_state=to_dev(d["s0"], torch.float32, torch), final_state=sf,
+                                cu_seqlens=torch.from_numpy(cu).cuda(), chunk_size=C)
+    kda.kda_sync_status()
+    ro, rs = oracle.recurrence(d["q"], d["k"], d["v"], go, d["beta"], s_init=d["s0"], cu_seqlens=cu)
+    check(to_np(out), to_np(sf), ro, rs, cu, True, f"D={D} C={C} gate={gate}")
