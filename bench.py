@@ -506,7 +506,11 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
         simt = {"value": ws * toks / (sms * 1e-3), "unit": "tokens/s", "ms_per_call": sms,
                 "kernel": "prefill_tf32_kernel (fp32 q/k/v/out; tcgen05 kind::tf32, 3xTF32 products)",
                 "roofline_hbm": {"achieved": sby / (sms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                                 "frac": sby / (sms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": sby},
+                                 "frac": sby / (sms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": sby,
+                                 **_traffic_fields(_traffic("prefill_tf32_kernel",
+                                                            ["kda_prefill_tf32.cu", "kda_tc.cuh", "kda_prefill.cuh",
+                                                             "kda_common.cuh"], T * H),
+                                                   T * H * D * 4 + H * D * D * 4)},
                 "roofline_tensor": {"achieved": sfl / (sms * 1e-3) / 1e12, "peak": tf32_peak, "unit": "TFLOP/s",
                                     "frac": sfl / (sms * 1e-3) / 1e12 / tf32_peak, "flops_issued": sfl,
                                     "peak_source": f"{peak_src} bf16_tflops (burst) x 1/2 (tf32 : bf16 nominal)"}}
