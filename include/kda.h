@@ -310,6 +310,45 @@ kda_status kda_chunk_prefill_epi(const void *q, const void *k, const void *v, co
                                  const float *norm_weight, kda_gate_act act, float norm_eps,
                                  void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
+/* Chunked prefill of a packed batch in which some sequences are long
+ * ("为什么 Kimi K3 敢把 KV Cache 扔掉？" section 5, the chunk-to-chunk state
+ * hand-off, which is affine in the state: the same scan as
+ * kda_chunk_prefill_scan, applied per sequence). The host-side lengths let
+ * the call plan the split without a device round trip:
+ * kda_chunk_prefill_split_plan gives each sequence its segment count.
+ *   - A sequence is split when its serial chain of chunks is longer than
+ *     the batch's work per SM would be with every chunk-head spread evenly
+ *     (and than 8 chunks), into P = min(chunks / that balance, 4096)
+ *     segments when P >= 4. Sequences are never split when H is not a
+ *     multiple of 4.
+ *   - The sequences kept whole run in one prefill launch, longest first; each
+ *     split one then runs through kda_chunk_prefill_scan over its own rows,
+ *     with its own initial and final state.
+ *   - With nothing to split this is kda_chunk_prefill_gated.
+ * Arguments as kda_chunk_prefill_gated, plus host_cu_seqlens: a host copy of
+ * cu_seqlens (both required; they must agree, which is not checked on the
+ * device side). The results equal kda_chunk_prefill_gated's up to rounding.
+ *   workspace  device buffer of kda_chunk_prefill_split_workspace_bytes(
+ *              host_cu_seqlens, N, H, D, C) bytes.
+ * The split uses the current device's SM count; plan, workspace and call
+ * must see the same device. Errors: KDA_ERR_INVALID_ARG for bad lengths
+ * (host_cu_seqlens[0] != 0, decreasing, host_cu_seqlens[N] != T) or a short
+ * workspace, the callees' errors otherwise. */
+kda_status kda_chunk_prefill_split(const void *q, const void *k, const void *v, const float *g,
+                                   const float *beta, const float *initial_state, float *final_state,
+                                   void *out, const int64_t *cu_seqlens, const int64_t *host_cu_seqlens,
+                                   int N, int64_t T, int H, int D, int C, kda_dtype dtype, kda_gate gate,
+                                   float l2_eps, void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Workspace bytes kda_chunk_prefill_split needs (0 for invalid lengths). */
+size_t kda_chunk_prefill_split_workspace_bytes(const int64_t *host_cu_seqlens, int N, int H, int D, int C);
+
+/* The split kda_chunk_prefill_split makes: segments[i] = the segment count of
+ * sequence i (1: kept whole). sms: the SM count to plan for, or <= 0 for the
+ * current device's (then no GPU means no split). Returns the number of split
+ * sequences, or -1 for invalid lengths. Needs no GPU. */
+int kda_chunk_prefill_split_plan(const int64_t *host_cu_seqlens, int N, int H, int C, int sms, int *segments);
+
 /* Name of the kernel kda_chunk_prefill (and the gated, epilogue and scan
  * entry points, per segment) runs for head dimension D, chunk size C and
  * dtype: "prefill_tc_pipe_kernel" (tcgen05, bf16), "prefill_tf32_kernel"

@@ -22,6 +22,7 @@
 // to any finite gate; it is the reference-grade fp32 path, not the fast one.
 #include <algorithm>
 #include <string>
+#include <vector>
 
 #include "kda_common.cuh"
 #include "kda_prefill.cuh"
@@ -192,7 +193,7 @@ static kda_status launch_simt(const PrefillArgs &a, cudaStream_t s) {
     auto kern = a.v_zero ? prefill_simt_kernel<D, T, true> : prefill_simt_kernel<D, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    const unsigned grid = (unsigned)a.N * a.H * (D / simt_js(D));
+    const unsigned grid = launch_seqs(a) * a.H * (D / simt_js(D));
     kern<<<grid, SIMT_NT, smem, s>>>(static_cast<const T *>(a.q), static_cast<const T *>(a.k),
                                      static_cast<const T *>(a.v), a.g, a.beta, a.s_init, a.s_final,
                                      static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err,
@@ -295,7 +296,8 @@ static kda_status prefill_entry(const void *q, const void *k, const void *v, con
                                 const int64_t *cu_seqlens, int N, int64_t T, int H, int D, int C, kda_dtype dtype,
                                 kda_gate gate, float l2_eps, void *workspace, size_t workspace_bytes,
                                 kda_stream_t stream, const void *epi_gate, const float *epi_w, kda_gate_act epi_act,
-                                float epi_eps) {
+                                float epi_eps, const int *ext_order = nullptr, int ext_nlaunch = 0) {
+    // ext_order (device, ext_nlaunch entries): launch only these sequences, in this order
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE)
         return invalid("gate must be KDA_GATE_CHANNEL, KDA_GATE_HEAD or KDA_GATE_NONE");
     if (N < 1) return invalid("N must be >= 1");
@@ -307,7 +309,7 @@ static kda_status prefill_entry(const void *q, const void *k, const void *v, con
     if (!(l2_eps >= 0.f)) return invalid("l2_eps must be >= 0");
     if (cu_seqlens == nullptr && N != 1) return invalid("cu_seqlens is NULL but N != 1");
     if ((long long)N * H * 2 > 0x7fffffffLL) return invalid("N*H too large for one launch");
-    const size_t need = order_bytes(N);
+    const size_t need = ext_order ? 0 : order_bytes(N);
     if (workspace_bytes < need) return invalid("workspace too small");
     kda_status st;
     if (T > 0 && ((st = check_ptr(q, "q")) || (st = check_ptr(k, "k")) || (st = check_ptr(v, "v")) ||
@@ -324,7 +326,7 @@ static kda_status prefill_entry(const void *q, const void *k, const void *v, con
     // One sequence (no cu_seqlens) whose serial chunk chain would leave most
     // SMs idle: split it into segments when the workspace has room for that
     // (kda_chunk_prefill_workspace_bytes asks for it).
-    if (cu_seqlens == nullptr && T > 0) {
+    if (cu_seqlens == nullptr && T > 0 && ext_order == nullptr) {
         const int P = prefill_auto_segments(T, H, C);
         if (P > 0 && workspace != nullptr && workspace_bytes >= kda_chunk_prefill_scan_workspace_bytes(T, H, D, C, P)) {
             st = kda_chunk_prefill_scan(q, k, v, g, beta, initial_state, final_state, out, T, H, D, C, dtype, gate,
@@ -337,7 +339,10 @@ static kda_status prefill_entry(const void *q, const void *k, const void *v, con
                   dtype == KDA_BF16, l2_eps, workspace, workspace_bytes, device_error_word(), nullptr, (int)gate};
     if (a.err == nullptr) return fail(KDA_ERR_CUDA, "device error word unavailable");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (need > 0 && cu_seqlens != nullptr) {
+    if (ext_order != nullptr) {
+        a.order = ext_order;
+        a.nlaunch = ext_nlaunch;
+    } else if (need > 0 && cu_seqlens != nullptr) {
         int *order = static_cast<int *>(workspace);
         if ((st = launch_prefill_order(cu_seqlens, N, order, s))) return st;
         a.order = order;
@@ -382,4 +387,128 @@ extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void
                                         size_t workspace_bytes, kda_stream_t stream) {
     return kda_chunk_prefill_gated(q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C,
                                    dtype, KDA_GATE_CHANNEL, l2_eps, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- batches with long sequences
+// Segments per sequence for kda_chunk_prefill_split. The batch's work is W
+// chunk-heads (every sequence's chunks times H); spread evenly it keeps each
+// of the `sms` SMs busy for ceil(W / sms) chunk steps. A sequence whose serial
+// chain of chunks is longer than that (and than 8 chunks) gets
+// P = min(chunks / balance, 4096) segments when P >= 4: its two scan passes
+// then take 1/P of its chain each, and the scan and the correction pay. The
+// per-head arrays of a segment start 16-byte aligned only when H is a
+// multiple of 4, so other H are never split. -1 for invalid lengths.
+static int split_plan(const int64_t *cu, int N, int H, int C, int sms, int *seg) {
+    if (cu == nullptr || seg == nullptr || N < 1 || H < 1 || C < 1 || cu[0] != 0) return -1;
+    int64_t W = 0;
+    for (int i = 0; i < N; ++i) {
+        if (cu[i + 1] < cu[i]) return -1;
+        W += (cu[i + 1] - cu[i] + C - 1) / C;
+    }
+    if (sms <= 0) sms = current_sms();
+    const int64_t bal = sms > 0 ? std::max<int64_t>((W * H + sms - 1) / sms, 8) : 0;
+    int n = 0;
+    for (int i = 0; i < N; ++i) {
+        const int64_t ch = (cu[i + 1] - cu[i] + C - 1) / C;
+        const int64_t P = (bal > 0 && H % 4 == 0) ? std::min<int64_t>(ch / bal, 4096) : 0;
+        seg[i] = P >= 4 ? (int)P : 1;
+        n += P >= 4 ? 1 : 0;
+    }
+    return n;
+}
+
+static size_t align256_(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// workspace: the largest split sequence's scan workspace, then the launch order of the rest
+static size_t split_ws(const int64_t *cu, const int *seg, int N, int H, int D, int C, size_t *scan_bytes) {
+    size_t scan = 0;
+    for (int i = 0; i < N; ++i)
+        if (seg[i] > 1)
+            scan = std::max(scan, kda_chunk_prefill_scan_workspace_bytes(cu[i + 1] - cu[i], H, D, C, seg[i]));
+    scan = align256_(scan);
+    if (scan_bytes) *scan_bytes = scan;
+    return scan + align256_((size_t)N * sizeof(int));
+}
+
+extern "C" int kda_chunk_prefill_split_plan(const int64_t *host_cu_seqlens, int N, int H, int C, int sms,
+                                            int *segments) {
+    return split_plan(host_cu_seqlens, N, H, C, sms, segments);
+}
+
+extern "C" size_t kda_chunk_prefill_split_workspace_bytes(const int64_t *host_cu_seqlens, int N, int H, int D,
+                                                          int C) {
+    if (N < 1 || N > (1 << 24)) return 0;
+    std::vector<int> seg((size_t)N);
+    if (split_plan(host_cu_seqlens, N, H, C, 0, seg.data()) < 0) return 0;
+    return split_ws(host_cu_seqlens, seg.data(), N, H, D, C, nullptr);
+}
+
+extern "C" kda_status kda_chunk_prefill_split(const void *q, const void *k, const void *v, const float *g,
+                                              const float *beta, const float *initial_state, float *final_state,
+                                              void *out, const int64_t *cu_seqlens, const int64_t *host_cu_seqlens,
+                                              int N, int64_t T, int H, int D, int C, kda_dtype dtype, kda_gate gate,
+                                              float l2_eps, void *workspace, size_t workspace_bytes,
+                                              kda_stream_t stream) {
+    clear_detail();
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE)
+        return invalid("gate must be KDA_GATE_CHANNEL, KDA_GATE_HEAD or KDA_GATE_NONE");
+    if (N < 1 || N > (1 << 24)) return invalid("N must be in 1..2^24");
+    if (T < 0) return invalid("T must be >= 0");
+    if (H < 1) return invalid("H must be >= 1");
+    if (!valid_head_dim(D)) return invalid("D must be one of 16, 32, 64, 128");
+    if (C < 1 || C > SIMT_CMAX) return invalid("C must be in 1..64");
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return invalid("dtype must be KDA_F32 or KDA_BF16");
+    if (cu_seqlens == nullptr || host_cu_seqlens == nullptr)
+        return invalid("cu_seqlens and host_cu_seqlens are both required");
+    std::vector<int> seg((size_t)N);
+    const int nsplit = split_plan(host_cu_seqlens, N, H, C, 0, seg.data());
+    if (nsplit < 0) return invalid("host_cu_seqlens must start at 0 and be non-decreasing");
+    if (host_cu_seqlens[N] != T) return invalid("host_cu_seqlens[N] must equal T");
+    if (nsplit == 0)  // nothing to split: the ordinary prefill
+        return kda_chunk_prefill_gated(q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C,
+                                       dtype, gate, l2_eps, workspace, workspace_bytes, stream);
+    size_t scan_bytes = 0;
+    const size_t need = split_ws(host_cu_seqlens, seg.data(), N, H, D, C, &scan_bytes);
+    if (workspace_bytes < need) return invalid("workspace too small");
+    kda_status st;
+    if ((st = check_ptr(workspace, "workspace"))) return st;
+    if ((st = bind_stream_device(stream))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // 1. the sequences that stay whole: one launch, longest first
+    std::vector<int> keep;
+    for (int i = 0; i < N; ++i)
+        if (seg[i] == 1) keep.push_back(i);
+    std::stable_sort(keep.begin(), keep.end(), [&](int a, int b) {
+        return host_cu_seqlens[a + 1] - host_cu_seqlens[a] > host_cu_seqlens[b + 1] - host_cu_seqlens[b];
+    });
+    if (!keep.empty()) {
+        int *order = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + scan_bytes);
+        // from pageable memory: the call returns once the list is staged, so `keep` may go
+        cudaError_t e = cudaMemcpyAsync(order, keep.data(), keep.size() * sizeof(int), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
+        if ((st = prefill_entry(q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C, dtype,
+                                gate, l2_eps, nullptr, 0, stream, nullptr, nullptr, KDA_ACT_SIGMOID, 0.f, order,
+                                (int)keep.size())))
+            return st;
+    }
+    // 2. each long sequence through the chunk-state scan over its own rows
+    const size_t elt = dtype == KDA_BF16 ? 2 : 4;
+    for (int i = 0; i < N; ++i) {
+        if (seg[i] == 1) continue;
+        const int64_t t0 = host_cu_seqlens[i], len = host_cu_seqlens[i + 1] - t0;
+        const size_t row = (size_t)t0 * H * D, sst = (size_t)i * H * D * D;
+        const float *gi = g == nullptr ? nullptr
+                          : gate == KDA_GATE_CHANNEL ? g + row
+                          : gate == KDA_GATE_HEAD ? g + (size_t)t0 * H
+                                                  : g;
+        if ((st = kda_chunk_prefill_scan(static_cast<const uint8_t *>(q) + row * elt,
+                                         static_cast<const uint8_t *>(k) + row * elt,
+                                         static_cast<const uint8_t *>(v) + row * elt, gi, beta + (size_t)t0 * H,
+                                         initial_state ? initial_state + sst : nullptr,
+                                         final_state ? final_state + sst : nullptr,
+                                         static_cast<uint8_t *>(out) + row * elt, len, H, D, C, dtype, gate, l2_eps,
+                                         seg[i], workspace, scan_bytes, stream)))
+            return st;
+    }
+    return KDA_OK;
 }

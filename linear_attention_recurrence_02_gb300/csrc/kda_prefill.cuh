@@ -26,7 +26,11 @@ struct PrefillArgs {
     const int *order;  // sequences by descending length (device), or NULL = natural order
     int gate;          // kda_gate: g is [T,H,D], [T,H], or unused
     bool v_zero = false;  // read v as all zeros (v is not loaded)
+    int nlaunch = 0;      // sequences launched (order[0..nlaunch) when set; 0: all N)
 };
+
+// (sequence, head) CTAs per head of a prefill launch
+inline unsigned launch_seqs(const PrefillArgs &a) { return (unsigned)(a.nlaunch > 0 ? a.nlaunch : a.N); }
 
 // Largest batch the length sort handles; bigger batches keep their order.
 constexpr int ORDER_MAX_SEQS = 4096;
@@ -47,6 +51,8 @@ kda_status prefill_run(const PrefillArgs &a, cudaStream_t s);
 
 // Segments of the automatic long-sequence split for one sequence of T tokens
 // with H heads on the current device, or 0 when the serial prefill is kept.
+// Streaming multiprocessors of the current device (0 if unknown).
+int current_sms();
 int prefill_auto_segments(int64_t T, int H, int C);
 
 namespace tcp {

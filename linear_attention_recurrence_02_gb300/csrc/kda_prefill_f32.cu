@@ -464,7 +464,7 @@ static kda_status launch_f32(const PrefillArgs &a, cudaStream_t s) {
     auto kern = prefill_f32_kernel<T, GM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f32p::SMEM);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    kern<<<(unsigned)a.N * a.H, f32p::NT, f32p::SMEM, s>>>(
+    kern<<<launch_seqs(a) * a.H, f32p::NT, f32p::SMEM, s>>>(
         static_cast<const T *>(a.q), static_cast<const T *>(a.k), static_cast<const T *>(a.v), a.g, a.beta,
         a.s_init, a.s_final, static_cast<T *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err, a.order,
         a.v_zero ? 1 : 0);

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(fixtc::NT) scan_fixup_tc_kernel(const __grid_c
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Streaming multiprocessors of the current device (0 if unknown).
-static int current_sms() {
+int current_sms() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
                                                    cudaSuccess) {

@@ -1298,7 +1298,7 @@ static kda_status launch_tc(const PrefillArgs &a, const CUtensorMap &mq, const C
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_pipe_kernel<GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pipe::SMEM);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    prefill_tc_pipe_kernel<GM><<<(unsigned)a.N * a.H, pipe::NTP, pipe::SMEM, s>>>(
+    prefill_tc_pipe_kernel<GM><<<launch_seqs(a) * a.H, pipe::NTP, pipe::SMEM, s>>>(
         mq, mk, mv, mg, mo, gh, a.beta, a.s_init, a.s_final, o, a.cu_seqlens, a.N, a.T, a.H, a.eps, a.err, a.order,
         a.v_zero ? 1 : 0, a.D);
     return check_launch("prefill_tc_pipe_kernel");

@@ -601,7 +601,7 @@ static kda_status launch_tf32(const PrefillArgs &a, cudaStream_t s) {
     auto kern = prefill_tf32_kernel<GM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tfp::SMEM);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    kern<<<(unsigned)a.N * a.H, tfp::NT, tfp::SMEM, s>>>(
+    kern<<<launch_seqs(a) * a.H, tfp::NT, tfp::SMEM, s>>>(
         static_cast<const float *>(a.q), static_cast<const float *>(a.k), static_cast<const float *>(a.v), a.g,
         a.beta, a.s_init, a.s_final, static_cast<float *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err,
         a.order, a.v_zero ? 1 : 0);

@@ -79,6 +79,10 @@ _SIGNATURES = {
                                    _ci, _cf, _vp], _ci),
     "kda_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i64, _ci, _ci, _ci, _ci, _cf, _vp], _ci),
     "kda_chunk_prefill_scan_workspace_bytes": ([_i64, _ci, _ci, _ci, _ci], _sz),
+    "kda_chunk_prefill_split": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci,
+                                 _ci, _cf, _vp, _sz, _vp], _ci),
+    "kda_chunk_prefill_split_workspace_bytes": ([_vp, _ci, _ci, _ci, _ci], _sz),
+    "kda_chunk_prefill_split_plan": ([_vp, _ci, _ci, _ci, _ci, _vp], _ci),
     "kda_chunk_prefill_epi": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _i64, _ci, _ci, _ci, _ci, _ci,
                                _cf, _vp, _vp, _ci, _cf, _vp, _sz, _vp], _ci),
     "kda_chunk_prefill_scan": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _ci, _ci, _ci, _ci, _ci, _cf, _ci,
@@ -382,6 +386,47 @@ def kda_chunk_prefill_gated(q, k, v, g, beta, out, gate="channel", initial_state
     _check(lib().kda_chunk_prefill_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
                                          _ptr(final_state), _ptr(out), _ptr(cu_seqlens), N, T, H, D, chunk_size,
                                          _dtype_code(q), code, float(l2_eps), _ptr(workspace), wsz,
+                                         _stream(stream, q.device)))
+
+
+def _host_cu(cu_seqlens):
+    import numpy as np
+    a = cu_seqlens.detach().cpu().numpy() if hasattr(cu_seqlens, "detach") else cu_seqlens
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def kda_chunk_prefill_split_plan(cu_seqlens, H, chunk_size=64, sms=0):
+    """Segment count per sequence that kda_chunk_prefill_split uses (1: kept whole) and the number of
+    split sequences; `sms` <= 0 plans for the current device."""
+    import numpy as np
+    cu = _host_cu(cu_seqlens)
+    N = cu.shape[0] - 1
+    seg = np.zeros(max(N, 1), dtype=np.int32)
+    n = lib().kda_chunk_prefill_split_plan(cu.ctypes.data, N, H, chunk_size, sms, seg.ctypes.data)
+    if n < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "invalid cu_seqlens")
+    return seg[:N], n
+
+
+def kda_chunk_prefill_split(q, k, v, g, beta, out, cu_seqlens, gate="channel", initial_state=None,
+                            final_state=None, chunk_size=64, l2_eps=1e-6, workspace=None, stream=None):
+    """Chunked prefill of a packed batch that splits its long sequences through the chunk-state scan.
+    cu_seqlens: the [N+1] offsets, on the host or the device (a host copy is taken here, a device
+    copy made when it lives on the host); other arguments as kda_chunk_prefill_gated."""
+    import torch
+    T, H, D = q.shape
+    code = _check_gate(g, gate, (T,), H, D)
+    host = _host_cu(cu_seqlens)
+    dev_cu = cu_seqlens if (hasattr(cu_seqlens, "is_cuda") and cu_seqlens.is_cuda) else \
+        torch.from_numpy(host).to(q.device)
+    N = host.shape[0] - 1
+    need = int(lib().kda_chunk_prefill_split_workspace_bytes(host.ctypes.data, N, H, D, chunk_size))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kda_chunk_prefill_split(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                         _ptr(final_state), _ptr(out), _ptr(dev_cu), host.ctypes.data, N, T, H, D,
+                                         chunk_size, _dtype_code(q), code, float(l2_eps), _ptr(workspace), wsz,
                                          _stream(stream, q.device)))
 
 

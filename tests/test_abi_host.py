@@ -305,3 +305,40 @@ def test_prefill_route_table(kda):
     assert route(64, 7, bf) == "prefill_simt_kernel"
     assert route(48, 64, bf) is None and route(128, 0, bf) is None and route(128, 65, f32) is None
     assert route(128, 64, 7) is None
+
+
+def test_split_plan(kda):
+    """The long-sequence split of kda_chunk_prefill_split, planned on the host for a given SM count: only a
+    sequence whose chain outlasts the evenly spread work is split (here the 65,536-token one at 8 heads,
+    into 1024 // 57 = 17 segments), never at H not a multiple of 4, never the bench's varlen batch at 96
+    heads (its longest chain is shorter than its work per SM); invalid lengths give -1 (an error)."""
+    import numpy as np
+    cu = np.array([0, 65536, 66036, 69036, 69156], dtype=np.int64)
+    seg, n = kda.kda_chunk_prefill_split_plan(cu, 8, 64, sms=152)
+    assert n == 1 and list(seg) == [17, 1, 1, 1]
+    seg, n = kda.kda_chunk_prefill_split_plan(cu, 6, 64, sms=152)
+    assert n == 0 and list(seg) == [1, 1, 1, 1]
+    varlen = np.cumsum([0, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536]).astype(np.int64)
+    assert kda.kda_chunk_prefill_split_plan(varlen, 96, 64, sms=152)[1] == 0
+    # one sequence: floor(chunks / max(ceil(chunks * H / SMs), 8)) segments
+    seg, n = kda.kda_chunk_prefill_split_plan(np.array([0, 65536], dtype=np.int64), 8, 64, sms=152)
+    assert n == 1 and seg[0] == 1024 // -(-1024 * 8 // 152)
+    # a sequence of fewer than 4 x 8 chunks stays whole whatever the SM count
+    assert kda.kda_chunk_prefill_split_plan(np.array([0, 1984], dtype=np.int64), 4, 64, sms=1024)[1] == 0
+    with pytest.raises(kda.KdaError):
+        kda.kda_chunk_prefill_split_plan(np.array([0, 10, 5], dtype=np.int64), 8, 64, sms=152)
+    with pytest.raises(kda.KdaError):
+        kda.kda_chunk_prefill_split_plan(np.array([3, 10], dtype=np.int64), 8, 64, sms=152)
+
+
+def test_split_rejects_bad_lengths_without_a_gpu(kda):
+    import numpy as np
+    lib = kda.lib()
+    cu = np.array([0, 10, 20], dtype=np.int64)
+    st = lib.kda_chunk_prefill_split(None, None, None, None, None, None, None, None, 8, cu.ctypes.data, 2, 21,
+                                     8, 128, 64, kda.KDA_BF16, 0, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    assert "host_cu_seqlens[N]" in lib.kda_last_error_detail().decode()
+    st = lib.kda_chunk_prefill_split(None, None, None, None, None, None, None, None, None, cu.ctypes.data, 2, 20,
+                                     8, 128, 64, kda.KDA_BF16, 0, 1e-6, None, 0, None)
+    assert st == kda.KDA_ERR_INVALID_ARG

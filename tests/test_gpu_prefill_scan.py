@@ -153,3 +153,43 @@ def test_prefill_splits_one_long_sequence_automatically(env):
         assert_close(o, ro, True, (1,), "out")
         assert_close(sf, rs, True, (0, 1), "final state")
     assert_close(outs[0][0], outs[1][0], True, (1,), "split vs serial")
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_split_batch_with_a_long_sequence(env, bf16):
+    """kda_chunk_prefill_split on a packed batch with an empty sequence, short ones and one long one, with
+    carry-in states and mild gates (g_scale 0.02: the carried state matters across the long sequence's
+    segments). The plan for this GPU splits the long sequence (and only it); every output and final state
+    against the fp64 recurrence, and against kda_chunk_prefill_gated of the same batch."""
+    torch, kda = env
+    H, D = 8, 128
+    lens = [300, 0, 9000, 50, 1500]
+    cu = np.cumsum([0] + lens).astype(np.int64)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    seg, nsplit = kda.kda_chunk_prefill_split_plan(cu, H, 64)
+    expect, _ = kda.kda_chunk_prefill_split_plan(cu, H, 64, sms=sms)
+    assert list(seg) == list(expect)
+    assert nsplit == 1 and seg[2] >= 4 and all(seg[i] == 1 for i in (0, 1, 3, 4)), seg
+    p = synth.prefill_inputs(41, int(cu[-1]), H, D, bf16, cu_seqlens=cu, s0_std=0.05, g_scale=0.02)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    q, k, v = (to_dev(p[n], dt, torch) for n in "qkv")
+    g, b = to_dev(p["g"], torch.float32, torch), to_dev(p["beta"], torch.float32, torch)
+    s0 = to_dev(p["s0"], torch.float32, torch)
+    N = len(lens)
+    res = []
+    for split in (True, False):
+        o = torch.full_like(q, float("nan"))
+        sf = torch.full((N, H, D, D), float("nan"), device="cuda")
+        if split:
+            kda.kda_chunk_prefill_split(q, k, v, g, b, o, torch.from_numpy(cu), initial_state=s0, final_state=sf,
+                                        chunk_size=64)
+        else:
+            kda.kda_chunk_prefill_gated(q, k, v, g, b, o, initial_state=s0, final_state=sf,
+                                        cu_seqlens=torch.from_numpy(cu).cuda(), chunk_size=64)
+        kda.kda_sync_status()
+        res.append((to_np(o), to_np(sf)))
+    ro, rs = oracle.recurrence(p["q"], p["k"], p["v"], p["g"], p["beta"], s_init=p["s0"], cu_seqlens=cu)
+    for o, sf in res:
+        assert_close(o, ro, bf16, (1,), "out")
+        assert_close(sf, rs, bf16, (0, 1), "final state")
+    assert_close(res[0][0], res[1][0], bf16, (1,), "split vs whole")
