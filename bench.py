@@ -687,9 +687,25 @@ def bench_long_sequence(torch, kda, dev, stream, ws, T=65536, Hs=8, segments=0, 
                                                     workspace=no_ws, stream=stream))
     ms_scan = timed(lambda: kda.kda_chunk_prefill_scan(q, k, v, g, beta, out, segments, final_state=sf,
                                                        workspace=wsb, stream=stream))
+    # the same rows as a packed batch of five sequences, one of them long: kda_chunk_prefill_split
+    # (host-side lengths; it splits the long one and runs the rest in one launch) against one
+    # kda_chunk_prefill_gated call over the batch
+    lens = [59904, 512, 3000, 120, 2000]
+    cu_h = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int64)
+    cu_d = cu_h.to(dev)
+    sfb = torch.empty((len(lens), Hs, D, D), device=dev)
+    seg, _ = kda.kda_chunk_prefill_split_plan(cu_h, Hs, 64)
+    ms_batch_whole = timed(lambda: kda.kda_chunk_prefill_gated(q, k, v, g, beta, out, final_state=sfb,
+                                                               cu_seqlens=cu_d, chunk_size=64, stream=stream))
+    ms_batch_split = timed(lambda: kda.kda_chunk_prefill_split(q, k, v, g, beta, out, cu_h, final_state=sfb,
+                                                               chunk_size=64, stream=stream))
     kda.kda_sync_status(stream)
+    mixed = {"ms_per_call": ms_batch_split, "whole_ms_per_call": ms_batch_whole,
+             "speedup": ms_batch_whole / ms_batch_split, "segments": [int(x) for x in seg],
+             "config": {"workload": f"packed batch of {len(lens)} sequences {lens} (65,536 tokens), H={Hs}, d={D}, "
+                                    "C=64, bf16: kda_chunk_prefill_split vs kda_chunk_prefill_gated"}}
     return {"value": ws * T / (ms_scan * 1e-3), "unit": "tokens/s", "ms_per_call": ms_scan,
-            "serial_ms_per_call": ms_serial, "speedup": ms_serial / ms_scan,
+            "serial_ms_per_call": ms_serial, "speedup": ms_serial / ms_scan, "mixed_batch": mixed,
             "config": {"workload": f"one sequence of {T} tokens, H={Hs}, d={D}, C=64, bf16, per-channel gate: "
                                    "kda_chunk_prefill_scan vs kda_chunk_prefill",
                        "segments": segments if segments else max(2, torch.cuda.get_device_properties(dev)
