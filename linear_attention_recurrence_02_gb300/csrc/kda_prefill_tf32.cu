@@ -214,19 +214,10 @@ __global__ void __launch_bounds__(tfp::NT, 1)
         else if constexpr (GHD) return g[(size_t)(c0 + r) * H + h];
         else return 0.f;
     };
-    for (int64_t c0 = start; c0 < end; c0 += Cc) {
-        const int L = (int)((end - c0) < (int64_t)Cc ? (end - c0) : (int64_t)Cc);
-        // ---- the next chunk's rows of q, k, v (and g) into L2 while this one is processed
-        if (c0 + Cc < end) {
-            const int64_t n0 = c0 + Cc;
-            const int Ln = (int)((end - n0) < (int64_t)Cc ? (end - n0) : (int64_t)Cc);
-            const int which = tid >> 6, r = tid & 63;
-            const float *src = which == 0 ? q : which == 1 ? k : which == 2 ? (v_zero ? nullptr : v)
-                                                                            : (GCH ? g : nullptr);
-            if (r < Ln && src != nullptr) prefetch_l2_bulk(src + ((size_t)(n0 + r) * H + h) * D, D * 4);
-        }
-        // ---- this thread's g, k, q (rows 32 ch.., channel ci) in one round trip; beta
-        float gr[32], kr[32], qr[32];
+    // this thread's g, k, q (rows 32 ch.., channel ci) and beta of the chunk at c0 into registers in one
+    // round trip; the loads of the next chunk are issued once G3/G4 of this one are under way
+    float gr[32], kr[32], qr[32], br = 0.f;
+    auto load_chunk = [&](int64_t c0, int L) {
 #pragma unroll
         for (int m = 0; m < 32; ++m) {
             const int r = 32 * ch + m;
@@ -238,7 +229,21 @@ __global__ void __launch_bounds__(tfp::NT, 1)
                 qr[m] = q[o];
             }
         }
-        if (tid < 64) s_beta[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        if (tid < 64) br = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+    };
+    if (start < end) load_chunk(start, (int)((end - start) < (int64_t)Cc ? (end - start) : (int64_t)Cc));
+    for (int64_t c0 = start; c0 < end; c0 += Cc) {
+        const int L = (int)((end - c0) < (int64_t)Cc ? (end - c0) : (int64_t)Cc);
+        // ---- the next chunk's rows of q, k, v (and g) into L2 while this one is processed
+        if (c0 + Cc < end) {
+            const int64_t n0 = c0 + Cc;
+            const int Ln = (int)((end - n0) < (int64_t)Cc ? (end - n0) : (int64_t)Cc);
+            const int which = tid >> 6, r = tid & 63;
+            const float *src = which == 0 ? q : which == 1 ? k : which == 2 ? (v_zero ? nullptr : v)
+                                                                            : (GCH ? g : nullptr);
+            if (r < Ln && src != nullptr) prefetch_l2_bulk(src + ((size_t)(n0 + r) * H + h) * D, D * 4);
+        }
+        if (tid < 64) s_beta[tid] = br;
         // squared row norms over this warp's 32 channels: a butterfly leaves row 32 ch + lane's sum on lane
         {
             float a[32], b[32];
@@ -455,28 +460,34 @@ __global__ void __launch_bounds__(tfp::NT, 1)
             }
             __syncthreads();
             // At_ik = D_i A_ik for the six blocks below the diagonal (i > k)
-            for (int e = tid; e < 6 * 256; e += NT) {
-                const int pb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            // every thread one element (row rr, column cc) of each of the six blocks: six independent chains
+            const int rr = tid >> 4, cc = tid & 15;
+#pragma unroll
+            for (int pb = 0; pb < 6; ++pb) {
                 const int i = pb < 1 ? 1 : pb < 3 ? 2 : 3, kb = pb - (i * (i - 1)) / 2;
                 float y = 0.f;
-#pragma unroll 4
+#pragma unroll
                 for (int t = 0; t < 16; ++t)
                     if (t <= rr) y = fmaf(ni[(16 * i + rr) * 65 + 16 * i + t], af[(16 * i + t) * 65 + 16 * kb + cc], y);
                 at[(16 * i + rr) * 65 + 16 * kb + cc] = y;
             }
             __syncthreads();
             // block row i: Ninv_ij = -sum_{j <= kb < i} At_i,kb Ninv_kb,j for j < i
-#pragma unroll 1
+#pragma unroll
             for (int i = 1; i < 4; ++i) {
-                for (int e = tid; e < i * 256; e += NT) {
-                    const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                    float y = 0.f;
+                float y[3];
+#pragma unroll
+                for (int j = 0; j < i; ++j) {  // element (rr, cc) of block (i, j): i independent chains
+                    float acc = 0.f;
+#pragma unroll
                     for (int kb = j; kb < i; ++kb)
-#pragma unroll 4
+#pragma unroll
                         for (int t = 0; t < 16; ++t)
-                            y = fmaf(at[(16 * i + rr) * 65 + 16 * kb + t], ni[(16 * kb + t) * 65 + 16 * j + cc], y);
-                    ni[(16 * i + rr) * 65 + 16 * j + cc] = -y;
+                            acc = fmaf(at[(16 * i + rr) * 65 + 16 * kb + t], ni[(16 * kb + t) * 65 + 16 * j + cc], acc);
+                    y[j] = acc;
                 }
+#pragma unroll
+                for (int j = 0; j < i; ++j) ni[(16 * i + rr) * 65 + 16 * j + cc] = -y[j];
                 __syncthreads();
             }
             for (int e = tid; e < C * 16; e += NT) {
@@ -554,6 +565,7 @@ __global__ void __launch_bounds__(tfp::NT, 1)
                               sdesc_sw128(sb + RTL, 16, 1024), ID_N128, true);
             mma_commit(bar);
         });
+        if (c0 + Cc < end) load_chunk(c0 + Cc, (int)((end - c0 - Cc) < (int64_t)Cc ? (end - c0 - Cc) : (int64_t)Cc));
         wait_mma();
         if (!ok) break;
 
