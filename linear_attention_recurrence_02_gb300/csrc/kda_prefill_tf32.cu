@@ -67,7 +67,7 @@ constexpr uint32_t RTH = 65536, RTL = 98304;    // once T is formed: Rk^T (Kb^T)
 constexpr int XLD = 129;
 constexpr uint32_t XK = 0, XQ = 64 * XLD * 4, XG = 2 * 64 * XLD * 4;
 constexpr uint32_t SMALL = 196608;
-constexpr uint32_t SMEM = SMALL + 3344 + 16 + 2048 + 1024;  // vectors, barrier, norm partials, alignment
+constexpr uint32_t SMEM = SMALL + 3344 + 16 + 4096 + 1024;  // vectors, barrier, norm partials, alignment
 static_assert(AT + 64 * 65 * 4 <= RKH && XG + 64 * XLD * 4 <= RKH && PL + 16384 <= RTH, "tile overlap");
 static_assert(SMEM <= 232448, "shared memory of the tf32 prefill");
 // TMEM columns
@@ -155,13 +155,13 @@ __global__ void __launch_bounds__(tfp::NT, 1)
     // 1024-byte aligned base derived from the shared array itself (accesses compile to shared-memory instructions)
     uint8_t *sm = smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
     float *vec = reinterpret_cast<float *>(sm + SMALL);
-    float *s_rk = vec, *s_rq = vec + 64, *s_beta = vec + 128, *s_part = vec + 192;
+    float *s_rk = vec, *s_rq = vec + 64, *s_beta = vec + 128;
     float *s_fac = vec + 448, *s_fpend = vec + 576, *s_egl = vec + 704;
-    float *s_nrm = reinterpret_cast<float *>(sm + SMALL + 3344 + 16);  // [4 channel groups][2][64] squared norms
+    float *s_part = reinterpret_cast<float *>(sm + SMALL + 3344 + 16);  // [8 row groups][128] decay totals
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + SMALL + 3328);
     uint32_t *s_taddr = reinterpret_cast<uint32_t *>(sm + SMALL + 3336);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, q4 = warp & 3, half = warp >> 2;
-    const int ci = tid & 127, ch = tid >> 7;  // operand builder: channel, half of the chunk's rows
+    // front (loads, norms, decay, operand build): warp = 8-row group, lane = 4-channel group
     const int h = blockIdx.x % H, n = order ? order[blockIdx.x / H] : (int)(blockIdx.x / H);
     int64_t start, end;
     if (!seq_range(cu_seqlens, n, N, Ttot, err, start, end)) return;
@@ -207,30 +207,30 @@ __global__ void __launch_bounds__(tfp::NT, 1)
         tc_fence_after();
     };
 
-    // g of (row r of the chunk at c0, this thread's channel ci), 0 past the chunk's L rows
-    auto gload = [&](int64_t c0, int r, int L) -> float {
-        if (r >= L) return 0.f;
-        if constexpr (GCH) return g[((size_t)(c0 + r) * H + h) * D + ci];
-        else if constexpr (GHD) return g[(size_t)(c0 + r) * H + h];
-        else return 0.f;
-    };
-    // this thread's g, k, q (rows 32 ch.., channel ci) and beta of the chunk at c0 into registers in one
-    // round trip; the loads of the next chunk are issued once G3/G4 of this one are under way
-    float gr[32], kr[32], qr[32], br = 0.f;
+    // this thread's g, k, q (rows 8 warp.., channels 4 lane..) and beta of the chunk at c0 into registers,
+    // 16-byte loads in one round trip; the loads of the next chunk are issued once G3/G4 of this one run
+    float4 gr[8], kr[8], qr[8];
+    float br = 0.f;
     auto load_chunk = [&](int64_t c0, int L) {
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            const int r = 32 * ch + m;
-            gr[m] = gload(c0, r, L);
-            kr[m] = qr[m] = 0.f;
+        for (int m = 0; m < 8; ++m) {
+            const int r = 8 * warp + m;
+            gr[m] = kr[m] = qr[m] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (r < L) {
-                const size_t o = ((size_t)(c0 + r) * H + h) * D + ci;
-                kr[m] = k[o];
-                qr[m] = q[o];
+                const size_t o = ((size_t)(c0 + r) * H + h) * D + 4 * lane;
+                kr[m] = *reinterpret_cast<const float4 *>(k + o);
+                qr[m] = *reinterpret_cast<const float4 *>(q + o);
+                if constexpr (GCH) {
+                    gr[m] = *reinterpret_cast<const float4 *>(g + o);
+                } else if constexpr (GHD) {
+                    const float gv = g[(size_t)(c0 + r) * H + h];
+                    gr[m] = make_float4(gv, gv, gv, gv);
+                }
             }
         }
         if (tid < 64) br = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
     };
+    auto f4 = [](const float4 &x, int e) -> float { return e == 0 ? x.x : e == 1 ? x.y : e == 2 ? x.z : x.w; };
     if (start < end) load_chunk(start, (int)((end - start) < (int64_t)Cc ? (end - start) : (int64_t)Cc));
     for (int64_t c0 = start; c0 < end; c0 += Cc) {
         const int L = (int)((end - c0) < (int64_t)Cc ? (end - c0) : (int64_t)Cc);
@@ -244,16 +244,17 @@ __global__ void __launch_bounds__(tfp::NT, 1)
             if (r < Ln && src != nullptr) prefetch_l2_bulk(src + ((size_t)(n0 + r) * H + h) * D, D * 4);
         }
         if (tid < 64) s_beta[tid] = br;
-        // squared row norms over this warp's 32 channels: a butterfly leaves row 32 ch + lane's sum on lane
+        // row norms: the warp holds all 128 channels of its 8 rows; a halving butterfly over lane bits 2..0
+        // leaves row (lane & 7)'s partial on the lane, and lane bits 3, 4 finish the sum
         {
-            float a[32], b[32];
+            float a[8], b[8];
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                a[m] = kr[m] * kr[m];
-                b[m] = qr[m] * qr[m];
+            for (int m = 0; m < 8; ++m) {
+                a[m] = kr[m].x * kr[m].x + kr[m].y * kr[m].y + kr[m].z * kr[m].z + kr[m].w * kr[m].w;
+                b[m] = qr[m].x * qr[m].x + qr[m].y * qr[m].y + qr[m].z * qr[m].z + qr[m].w * qr[m].w;
             }
 #pragma unroll
-            for (int w = 16; w > 0; w >>= 1) {
+            for (int w = 4; w > 0; w >>= 1) {
                 const bool up = (lane & w) != 0;
 #pragma unroll
                 for (int m = 0; m < w; ++m) {
@@ -263,58 +264,92 @@ __global__ void __launch_bounds__(tfp::NT, 1)
                     b[m] = (up ? b[m + w] : b[m]) + rb;
                 }
             }
-            s_nrm[(warp & 3) * 128 + 32 * ch + lane] = a[0];
-            s_nrm[(warp & 3) * 128 + 64 + 32 * ch + lane] = b[0];
+            a[0] += __shfl_xor_sync(0xffffffffu, a[0], 8);
+            b[0] += __shfl_xor_sync(0xffffffffu, b[0], 8);
+            a[0] += __shfl_xor_sync(0xffffffffu, a[0], 16);
+            b[0] += __shfl_xor_sync(0xffffffffu, b[0], 16);
+            if (lane < 8) {
+                const int r = 8 * warp + lane;
+                s_rk[r] = r < L ? inv_norm(a[0], eps) : 0.f;
+                s_rq[r] = r < L ? inv_norm(b[0], eps) : 0.f;
+            }
         }
-        {
-            float acc = 0.f;
+        {  // decay totals of this row group per channel
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int m = 0; m < 32; ++m) acc += gr[m];
-            s_part[ch * 128 + ci] = acc;
+            for (int m = 0; m < 8; ++m) {
+                t.x += gr[m].x; t.y += gr[m].y; t.z += gr[m].z; t.w += gr[m].w;
+            }
+            *reinterpret_cast<float4 *>(s_part + warp * 128 + 4 * lane) = t;
         }
         __syncthreads();
-        if (tid < 128) {  // inverse norms: k rows (tid < 64), q rows
-            const float ss = s_nrm[tid] + s_nrm[128 + tid] + s_nrm[256 + tid] + s_nrm[384 + tid];
-            const int r = tid & 63;
-            (tid < 64 ? s_rk : s_rq)[r] = r < L ? inv_norm(ss, eps) : 0.f;
+        // G of row r runs as (G of the row groups before) + its g, in row order; G_L and the anchors per channel
+        float off[4] = {0.f, 0.f, 0.f, 0.f}, GL[4] = {0.f, 0.f, 0.f, 0.f}, cI[4];
+#pragma unroll
+        for (int w2 = 0; w2 < 8; ++w2) {
+            const float4 t = *reinterpret_cast<const float4 *>(s_part + w2 * 128 + 4 * lane);
+            const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (w2 < warp) off[e] += tv[e];
+                GL[e] += tv[e];
+            }
         }
-        // G of row r runs as acc = (G of the rows before this thread's half) + its g, in row order
-        const float p0 = s_part[ci], GL = p0 + s_part[128 + ci], gbase = ch ? p0 : 0.f;
-        const bool exact = __syncthreads_or(!(GL >= -SPAN_MAX)) != 0;
-        const float cI = exact ? 0.f : fminf(0.f, GL + ANCHOR);
-        if (ch == 0) {
-            s_fac[ci] = s_fpend[ci] * expf(cI);
-            s_egl[ci] = expf(GL);
+        const bool exact = __syncthreads_or(!(GL[0] >= -SPAN_MAX && GL[1] >= -SPAN_MAX && GL[2] >= -SPAN_MAX &&
+                                              GL[3] >= -SPAN_MAX)) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cI[e] = exact ? 0.f : fminf(0.f, GL[e] + ANCHOR);
+        if (warp == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s_fac[4 * lane + e] = s_fpend[4 * lane + e] * expf(cI[e]);
+                s_egl[4 * lane + e] = expf(GL[e]);
+            }
         }
 
         // ---- operand tiles: [Lk; Lq] and, row-major, the state-update operand Rk (Kb on exact chunks)
         if (!exact) {
-            float acc = gbase;
+            float acc[4] = {off[0], off[1], off[2], off[3]};
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const int r = 32 * ch + m;
-                acc += gr[m];
-                const float kh = kr[m] * s_rk[r], qh = qr[m] * s_rq[r];
-                const float e1 = expf(acc - cI), e2 = expf(cI - acc);
-                put_hilo(sm, KQH, KQL, kmaj(r, ci, 128), e1 * kh);
-                put_hilo(sm, KQH, KQL, kmaj(64 + r, ci, 128), e1 * qh);
-                put_hilo(sm, RKH, RKL, kmaj(r, ci, 64), e2 * kh);
+            for (int m = 0; m < 8; ++m) {
+                const int r = 8 * warp + m;
+                const float rk = s_rk[r], rq = s_rq[r];
+                float lk[4], lq[4], rkv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[e] += f4(gr[m], e);
+                    const float kh = f4(kr[m], e) * rk, qh = f4(qr[m], e) * rq;
+                    const float e1 = expf(acc[e] - cI[e]), e2 = expf(cI[e] - acc[e]);
+                    lk[e] = e1 * kh;
+                    lq[e] = e1 * qh;
+                    rkv[e] = e2 * kh;
+                }
+                put_hilo4(sm, KQH, KQL, kmaj(r, 4 * lane, 128), lk);
+                put_hilo4(sm, KQH, KQL, kmaj(64 + r, 4 * lane, 128), lq);
+                put_hilo4(sm, RKH, RKL, kmaj(r, 4 * lane, 64), rkv);
             }
         } else {
             // exact pairwise decays: stage k^, q^, G; A_raw and P_raw straight into TMEM; then [Lk; Lq], c = 0
             float *xk = reinterpret_cast<float *>(sm + XK), *xq = reinterpret_cast<float *>(sm + XQ);
             float *xg = reinterpret_cast<float *>(sm + XG);
-            float acc = gbase;
+            float acc[4] = {off[0], off[1], off[2], off[3]};
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const int r = 32 * ch + m;
-                acc += gr[m];
-                gr[m] = acc;  // G from here on
-                const float kh = kr[m] * s_rk[r];
-                xk[r * XLD + ci] = kh;
-                xq[r * XLD + ci] = qr[m] * s_rq[r];
-                xg[r * XLD + ci] = acc;
-                put_hilo(sm, RKH, RKL, kmaj(r, ci, 64), expf(GL - acc) * kh);
+            for (int m = 0; m < 8; ++m) {
+                const int r = 8 * warp + m;
+                const float rk = s_rk[r], rq = s_rq[r];
+                float kb[4], gg[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[e] += f4(gr[m], e);
+                    gg[e] = acc[e];
+                    const float kh = f4(kr[m], e) * rk;
+                    xk[r * XLD + 4 * lane + e] = kh;
+                    xq[r * XLD + 4 * lane + e] = f4(qr[m], e) * rq;
+                    xg[r * XLD + 4 * lane + e] = acc[e];
+                    kb[e] = expf(GL[e] - acc[e]) * kh;
+                }
+                gr[m] = make_float4(gg[0], gg[1], gg[2], gg[3]);  // G from here on
+                put_hilo4(sm, RKH, RKL, kmaj(r, 4 * lane, 64), kb);
             }
             __syncthreads();
             {
@@ -338,11 +373,18 @@ __global__ void __launch_bounds__(tfp::NT, 1)
             }
             __syncthreads();
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const int r = 32 * ch + m;
-                const float e1 = expf(gr[m]);
-                put_hilo(sm, KQH, KQL, kmaj(r, ci, 128), e1 * kr[m] * s_rk[r]);
-                put_hilo(sm, KQH, KQL, kmaj(64 + r, ci, 128), e1 * qr[m] * s_rq[r]);
+            for (int m = 0; m < 8; ++m) {
+                const int r = 8 * warp + m;
+                const float rk = s_rk[r], rq = s_rq[r];
+                float lk[4], lq[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float e1 = expf(f4(gr[m], e));
+                    lk[e] = e1 * f4(kr[m], e) * rk;
+                    lq[e] = e1 * f4(qr[m], e) * rq;
+                }
+                put_hilo4(sm, KQH, KQL, kmaj(r, 4 * lane, 128), lk);
+                put_hilo4(sm, KQH, KQL, kmaj(64 + r, 4 * lane, 128), lq);
             }
         }
         fence_async_smem();
@@ -526,6 +568,7 @@ __global__ void __launch_bounds__(tfp::NT, 1)
             tmem_st32(tbase + lq + T_W + 64 + 32 * half, u);
         }
         // Rk^T (Kb^T) from the row-major tile: thread (channel ci, rows 32 ch..), 16-byte groups of 4 rows
+        const int ci = tid & 127, ch = tid >> 7;
 #pragma unroll 2
         for (int g4 = 0; g4 < 8; ++g4) {
             const int r0 = 32 * ch + 4 * g4;
@@ -557,7 +600,9 @@ __global__ void __launch_bounds__(tfp::NT, 1)
         tmem_st_wait();
         fence_async_smem();
         sync_tc();
-        if (ch == 0) s_fpend[ci] = exact ? 1.f : expf(GL - cI);
+        if (warp == 0)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s_fpend[4 * lane + e] = exact ? 1.f : expf(GL[e] - cI[e]);
         issue([&] {
             prod_ts<8, 8192>(tbase + T_XO + 64, tbase + T_W, tbase + T_W + 64, sdesc_sw128(sb + PH, 16, 1024),
                              sdesc_sw128(sb + PL, 16, 1024), ID_N64, true);
