@@ -341,3 +341,25 @@ def test_prefill_bf16_tensor_core_shapes(env, D, C, gate):
     kda.kda_sync_status()
     ro, rs = oracle.recurrence(d["q"], d["k"], d["v"], go, d["beta"], s_init=d["s0"], cu_seqlens=cu)
     check(to_np(out), to_np(sf), ro, rs, cu, True, f"D={D} C={C} gate={gate}")
+
+
+@pytest.mark.parametrize("D,C", [(64, 64), (64, 16), (128, 32)])
+def test_prefill_bf16_tensor_core_exact_chunks(env, D, C):
+    """The tcgen05 kernel's exact-decay path at the shapes it takes besides d=128/C=64: g = -1e4 on every
+    token (each chunk's decay span far past the anchored range; memory cleared every token), and a single
+    spike of -200 in one chunk of otherwise mild gates (that chunk alone exact, the carried state mattering
+    across it). d=64 runs with the kernel's channels 64..127 zero."""
+    torch, kda = env
+    assert kda.kda_chunk_prefill_route(D, C, torch.bfloat16) == "prefill_tc_pipe_kernel"
+    cu = np.array([0, 100, 230], dtype=np.int64)
+    d = synth.prefill_inputs(57 + D + C, 230, 2, D, True, cu_seqlens=cu, s0_std=0.5, g_scale=0.02)
+    d1 = dict(d, g=np.full_like(d["g"], -1.0e4))
+    o, s = run_prefill(torch, kda, d1, True, C)
+    ro, rs = oracle_prefill(d1)
+    check(o, s, ro, rs, cu, True, f"D={D} C={C} g=-1e4")
+    g2 = d["g"].copy()
+    g2[170, 1, : D // 2] = -200.0
+    d2 = dict(d, g=g2)
+    o, s = run_prefill(torch, kda, d2, True, C)
+    ro, rs = oracle_prefill(d2)
+    check(o, s, ro, rs, cu, True, f"D={D} C={C} spike")
