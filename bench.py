@@ -289,7 +289,7 @@ def run_ours(args):
     dec_avg_ms = statistics.mean(dec_ms)
     dec_bytes = STEP_BYTES
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = _traffic("fused_decode_kernel", ["kda_fused_decode.cu", "kda_common.cuh"], UNITS)
+    traffic = _traffic("fused_decode_bulk_kernel", ["kda_fused_decode.cu", "kda_common.cuh", "kda_tc.cuh"], UNITS)
     # state written back, o, the shifted 3-slot ring
     dec_write = UNITS * (D * D * 4 + D * 2 + 9 * D * 2)
 
@@ -369,7 +369,7 @@ def run_ours(args):
                                    f"H={H}, d_k=d_v={D}, bf16 q/k/v, fp32 state (384 MiB), 1 layer",
                        "B": B, "H": H, "d": D, "l2": "state (384 MiB) larger than L2 (129 MB); no flush",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": "fused_decode_kernel", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": "fused_decode_bulk_kernel", "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                          **_traffic_fields(traffic, dec_write), "algorithmic_bytes": dec_bytes,
@@ -819,10 +819,10 @@ def bench_decode_epi(torch, kda, dev, stream, ws, hbm_peak, d, fused_ms, steps=2
     kda.kda_sync_status(stream)
     ms = max_over_ranks(a.elapsed_time(b) / steps, dev)
     by = STEP_BYTES + B * H * D * 2 + D * 4
-    tr = _traffic("fused_decode_kernel_epilogue", ["kda_fused_decode.cu", "kda_common.cuh"], B * H)
+    tr = _traffic("fused_decode_bulk_kernel_epilogue", ["kda_fused_decode.cu", "kda_common.cuh", "kda_tc.cuh"], B * H)
     return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "dram": _traffic_fields(tr, B * H * (D * D * 4 + D * 2 + 9 * D * 2)),
-            "fused_step_without_epilogue_ms": fused_ms, "kernel": "fused_decode_kernel (output epilogue)",
+            "fused_step_without_epilogue_ms": fused_ms, "kernel": "fused_decode_bulk_kernel (output epilogue)",
             "config": {"workload": f"fused conv + decode step with the gated RMSNorm epilogue (sigmoid gate) in "
                                    f"one launch: B={B}, H={H}, d={D}, bf16, fp32 state 384 MiB", "steps": steps},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
