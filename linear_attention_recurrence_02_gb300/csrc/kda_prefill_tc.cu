@@ -361,6 +361,7 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
     using namespace pipe;
     constexpr bool GCH = GM == KDA_GATE_CHANNEL, GHD = GM == KDA_GATE_HEAD, GNO = GM == KDA_GATE_NONE;
     constexpr int BAR_CHAIN = 2, BAR_BACK = 3, BAR_FRONT = 4;
+    constexpr int BAR_FRONT_N = 5, BAR_FRONT_S = 6;  // the front's norm half (ft < 128) and scan half
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base derived from the shared array itself (accesses compile to shared-memory instructions)
     uint8_t *sm = smem_raw + ((1024u - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023u)) & 1023u);
@@ -477,110 +478,200 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
                 const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
                 const bool has_next = ci + 1 < nchunks;
                 uint8_t *xb = sm + X0 + 32768 * b;
-                // ofree[b]: the chain is done with chunk ci - 2, hence the back warps too.
-                // One warp spins on the barriers; the others wait in the named
-                // barrier, which costs them no issue slots.
-                bool got = true;
-                if (ft < 32)
-                    got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
-                          (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
-                          (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
-                if (group_or(BAR_FRONT, 256, !got)) {
-                    ok = false;
-                    break;
-                }
-                if (ft == 0) {
-                    s_waited[b] += 1;
-                    if constexpr (GCH) s_waited[2] += 1;
-                    // the loads of chunk ci + 2 are issued one to two chunks from now,
-                    // inside the pipeline's dependency cycle: stage their tiles in L2
-                    if (ci + 2 < nchunks) {
-                        const int y2 = (int)(c0 + 2 * C);
-                        tma_prefetch_l2_3d(&tm_k, 0, h, y2);
-                        tma_prefetch_l2_3d(&tm_q, 0, h, y2);
-                        tma_prefetch_l2_3d(&tm_v, 0, h, y2);
-                        if (dg > 64) {
-                            tma_prefetch_l2_3d(&tm_k, 64, h, y2);
-                            tma_prefetch_l2_3d(&tm_q, 64, h, y2);
-                            tma_prefetch_l2_3d(&tm_v, 64, h, y2);
-                        }
-                        if constexpr (GCH) tma_prefetch_l2_3d(&tm_g, 0, h, y2);
-                    }
-                }
+                bool bad = false, got = true;
                 float *sb = s_beta + 64 * b;
-                if (ft < C) {
-                    sb[ft] = beta_reg;
-                    if constexpr (GHD) s_g1[ft] = gh_reg;
-                }
-                if (L < C) {  // rows past the end of the sequence contribute nothing
-                    const uint4 z4 = make_uint4(0, 0, 0, 0);
-                    for (int p = ft; p < (C - L) * 16; p += 256) {
-                        const int r = L + (p >> 4), cc = p & 15;
-                        *reinterpret_cast<uint4 *>(xb + swz(r, cc, 128)) = z4;
-                        *reinterpret_cast<uint4 *>(xb + swz(r + 64, cc, 128)) = z4;
-                    }
-                    if constexpr (GCH)
-                        for (int p = ft; p < (C - L) * 32; p += 256)
-                            *reinterpret_cast<uint4 *>(sm + G_ + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
-                }
-                named_bar_sync(BAR_FRONT, 256);
-
-                // ft < 128: L2 norm of one row (q rows for ft < 64, k rows after);
-                // ft >= 128: cumulative decay of key channel ft - 128
-                bool bad = false;
-                if (ft < 128) {
-                    const int r = ft & 63;
-                    const int row = ft < 64 ? r + 64 : r;  // q rows follow the k rows
-                    float ss[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (GCH) {
+                    // the decay scan needs only g, which comes on its own barrier well ahead: the scan half
+                    // (ft >= 128) starts on it at once, while the norm half waits for q/k and for ofree[b]
+                    // (the chain is done with chunk ci - 2, hence the back warps too). One warp per half
+                    // spins; the others wait in the half's named barrier at no issue cost.
+                    if (ft < 128) {
+                        if (ft < 32)
+                            got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
+                                  (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
+                        got = !group_or(BAR_FRONT_N, 128, !got);
+                        if (got) {
+                            if (ft == 0) {
+                                s_waited[b] += 1;
+                                // the loads of chunk ci + 2 are issued one to two chunks from now,
+                                // inside the pipeline's dependency cycle: stage their tiles in L2
+                                if (ci + 2 < nchunks) {
+                                    const int y2 = (int)(c0 + 2 * C);
+                                    tma_prefetch_l2_3d(&tm_k, 0, h, y2);
+                                    tma_prefetch_l2_3d(&tm_q, 0, h, y2);
+                                    tma_prefetch_l2_3d(&tm_v, 0, h, y2);
+                                    if (dg > 64) {
+                                        tma_prefetch_l2_3d(&tm_k, 64, h, y2);
+                                        tma_prefetch_l2_3d(&tm_q, 64, h, y2);
+                                        tma_prefetch_l2_3d(&tm_v, 64, h, y2);
+                                    }
+                                    if constexpr (GCH) tma_prefetch_l2_3d(&tm_g, 0, h, y2);
+                                }
+                            }
+                            if (ft < C) sb[ft] = beta_reg;
+                            if (L < C) {  // rows past the end of the sequence contribute nothing
+                                const uint4 z4 = make_uint4(0, 0, 0, 0);
+                                for (int p = ft; p < (C - L) * 16; p += 128) {
+                                    const int r = L + (p >> 4), cc = p & 15;
+                                    *reinterpret_cast<uint4 *>(xb + swz(r, cc, 128)) = z4;
+                                    *reinterpret_cast<uint4 *>(xb + swz(r + 64, cc, 128)) = z4;
+                                }
+                            }
+                            named_bar_sync(BAR_FRONT_N, 128);
+                            // L2 norm of one row (q rows for ft < 64, k rows after)
+                            const int r = ft & 63;
+                            const int row = ft < 64 ? r + 64 : r;  // q rows follow the k rows
+                            float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-                    for (int cc = 0; cc < 16; ++cc) {
-                        float f[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(xb + swz(row, cc, 128)), f);
+                            for (int cc = 0; cc < 16; ++cc) {
+                                float f[8];
+                                unpack8(*reinterpret_cast<const uint4 *>(xb + swz(row, cc, 128)), f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
-                    }
-                    (ft < 64 ? s_rq : s_rk)[r] = inv_norm((ss[0] + ss[1]) + (ss[2] + ss[3]), eps);
-                } else if constexpr (GCH) {
-                    const int i = ft - 128;
-                    // running sum down the 64 rows, 16 rows at a time
-                    float run = 0.f, G0 = 0.f;
+                                for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
+                            }
+                            (ft < 64 ? s_rq : s_rk)[r] = inv_norm((ss[0] + ss[1]) + (ss[2] + ss[3]), eps);
+                        }
+                    } else {
+                        if (ft < 160) got = wait_or_abort(bar_g, ci & 1, s_abort);
+                        got = !group_or(BAR_FRONT_S, 128, !got);
+                        if (got) {
+                            if (ft == 128) s_waited[2] += 1;
+                            if (L < C) {
+                                const uint4 z4 = make_uint4(0, 0, 0, 0);
+                                for (int p = ft - 128; p < (C - L) * 32; p += 128)
+                                    *reinterpret_cast<uint4 *>(sm + G_ + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
+                            }
+                            named_bar_sync(BAR_FRONT_S, 128);
+                            // cumulative decay of key channel ft - 128
+                            const int i = ft - 128;
+                            // running sum down the 64 rows, 16 rows at a time
+                            float run = 0.f, G0 = 0.f;
 #pragma unroll 1
-                    for (int r0 = 0; r0 < 64; r0 += 16) {
-                        float gv[16];
+                            for (int r0 = 0; r0 < 64; r0 += 16) {
+                                float gv[16];
 #pragma unroll
-                        for (int r = 0; r < 16; ++r) gv[r] = gt[(r0 + r) * 128 + i];
+                                for (int r = 0; r < 16; ++r) gv[r] = gt[(r0 + r) * 128 + i];
 #pragma unroll
-                        for (int r = 0; r < 16; ++r) {
-                            run = r0 + r == 0 ? gv[r] : run + gv[r];
-                            gv[r] = run;
+                                for (int r = 0; r < 16; ++r) {
+                                    run = r0 + r == 0 ? gv[r] : run + gv[r];
+                                    gv[r] = run;
+                                }
+                                if (r0 == 0) G0 = gv[0];
+#pragma unroll
+                                for (int r = 0; r < 16; ++r) gt[(r0 + r) * 128 + i] = gv[r] * LOG2E;
+                            }
+                            const float GL = run;
+                            bad = !(G0 - GL <= SPAN_MAX);
+                            s_gl[i] = GL;
                         }
-                        if (r0 == 0) G0 = gv[0];
-#pragma unroll
-                        for (int r = 0; r < 16; ++r) gt[(r0 + r) * 128 + i] = gv[r] * LOG2E;
                     }
-                    const float GL = run;
-                    bad = !(G0 - GL <= SPAN_MAX);
-                    s_gl[i] = GL;
-                } else if constexpr (GHD) {
-                    if (warp == 8) {
-                        const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
-                        float incl = g0 + g1;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += y;
-                        }
-                        const float G1v = incl, G0v = incl - g1;
-                        const float GL = __shfl_sync(0xffffffffu, incl, 31);
-                        const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
-                        bad = !(Gfirst - GL <= SPAN_MAX);
-                        s_g1[2 * lane] = G0v * LOG2E;
-                        s_g1[2 * lane + 1] = G1v * LOG2E;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
+                    if (group_or(BAR_FRONT, 256, !got)) {
+                        ok = false;
+                        break;
                     }
                 } else {
-                    s_gl[ft - 128] = 0.f;
+                    // ofree[b]: the chain is done with chunk ci - 2, hence the back warps too.
+                    // One warp spins on the barriers; the others wait in the named
+                    // barrier, which costs them no issue slots.
+                    if (ft < 32)
+                        got = wait_or_abort(bar_qk + b, (ci >> 1) & 1, s_abort) &&
+                              (!GCH || wait_or_abort(bar_g, ci & 1, s_abort)) &&
+                              (ci < 2 || wait_or_abort(bar_ofree + b, ((ci - 2) >> 1) & 1, s_abort));
+                    if (group_or(BAR_FRONT, 256, !got)) {
+                        ok = false;
+                        break;
+                    }
+                    if (ft == 0) {
+                        s_waited[b] += 1;
+                        if constexpr (GCH) s_waited[2] += 1;
+                        // the loads of chunk ci + 2 are issued one to two chunks from now,
+                        // inside the pipeline's dependency cycle: stage their tiles in L2
+                        if (ci + 2 < nchunks) {
+                            const int y2 = (int)(c0 + 2 * C);
+                            tma_prefetch_l2_3d(&tm_k, 0, h, y2);
+                            tma_prefetch_l2_3d(&tm_q, 0, h, y2);
+                            tma_prefetch_l2_3d(&tm_v, 0, h, y2);
+                            if (dg > 64) {
+                                tma_prefetch_l2_3d(&tm_k, 64, h, y2);
+                                tma_prefetch_l2_3d(&tm_q, 64, h, y2);
+                                tma_prefetch_l2_3d(&tm_v, 64, h, y2);
+                            }
+                            if constexpr (GCH) tma_prefetch_l2_3d(&tm_g, 0, h, y2);
+                        }
+                    }
+                    if (ft < C) {
+                        sb[ft] = beta_reg;
+                        if constexpr (GHD) s_g1[ft] = gh_reg;
+                    }
+                    if (L < C) {  // rows past the end of the sequence contribute nothing
+                        const uint4 z4 = make_uint4(0, 0, 0, 0);
+                        for (int p = ft; p < (C - L) * 16; p += 256) {
+                            const int r = L + (p >> 4), cc = p & 15;
+                            *reinterpret_cast<uint4 *>(xb + swz(r, cc, 128)) = z4;
+                            *reinterpret_cast<uint4 *>(xb + swz(r + 64, cc, 128)) = z4;
+                        }
+                        if constexpr (GCH)
+                            for (int p = ft; p < (C - L) * 32; p += 256)
+                                *reinterpret_cast<uint4 *>(sm + G_ + (L + (p >> 5)) * 512 + (p & 31) * 16) = z4;
+                    }
+                    named_bar_sync(BAR_FRONT, 256);
+
+                    // ft < 128: L2 norm of one row (q rows for ft < 64, k rows after);
+                    // ft >= 128: the decay of the per-head gate, or nothing
+                    if (ft < 128) {
+                        const int r = ft & 63;
+                        const int row = ft < 64 ? r + 64 : r;  // q rows follow the k rows
+                        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                        for (int cc = 0; cc < 16; ++cc) {
+                            float f[8];
+                            unpack8(*reinterpret_cast<const uint4 *>(xb + swz(row, cc, 128)), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
+                        }
+                        (ft < 64 ? s_rq : s_rk)[r] = inv_norm((ss[0] + ss[1]) + (ss[2] + ss[3]), eps);
+                    } else if constexpr (GCH) {
+                        const int i = ft - 128;
+                        // running sum down the 64 rows, 16 rows at a time
+                        float run = 0.f, G0 = 0.f;
+#pragma unroll 1
+                        for (int r0 = 0; r0 < 64; r0 += 16) {
+                            float gv[16];
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) gv[r] = gt[(r0 + r) * 128 + i];
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) {
+                                run = r0 + r == 0 ? gv[r] : run + gv[r];
+                                gv[r] = run;
+                            }
+                            if (r0 == 0) G0 = gv[0];
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) gt[(r0 + r) * 128 + i] = gv[r] * LOG2E;
+                        }
+                        const float GL = run;
+                        bad = !(G0 - GL <= SPAN_MAX);
+                        s_gl[i] = GL;
+                    } else if constexpr (GHD) {
+                        if (warp == 8) {
+                            const float g0 = s_g1[2 * lane], g1 = s_g1[2 * lane + 1];
+                            float incl = g0 + g1;
+#pragma unroll
+                            for (int o = 1; o < 32; o <<= 1) {
+                                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                                if (lane >= o) incl += y;
+                            }
+                            const float G1v = incl, G0v = incl - g1;
+                            const float GL = __shfl_sync(0xffffffffu, incl, 31);
+                            const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
+                            bad = !(Gfirst - GL <= SPAN_MAX);
+                            s_g1[2 * lane] = G0v * LOG2E;
+                            s_g1[2 * lane + 1] = G1v * LOG2E;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) s_gl[4 * lane + e] = GL;
+                        }
+                    } else {
+                        s_gl[ft - 128] = 0.f;
+                    }
                 }
                 const bool exact = GNO ? (named_bar_sync(BAR_FRONT, 256), false) : group_or(BAR_FRONT, 256, bad);
                 // per-channel anchor c and state scale sigma
