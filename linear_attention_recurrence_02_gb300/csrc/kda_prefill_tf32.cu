@@ -62,7 +62,8 @@ constexpr uint32_t TH = 0, TL = 16384, PH = 32768, PL = 49152;  // T, P hi / lo:
 constexpr uint32_t AF = 65536;                  // A fp32 [64][65]
 constexpr uint32_t NI = AF + 64 * 65 * 4;       // (I + A)^-1 fp32 [64][65]
 constexpr uint32_t AT = NI + 64 * 65 * 4;       // D_i A_ik below the diagonal blocks, fp32 [64][65]
-constexpr uint32_t RTH = 65536, RTL = 98304;    // once T is formed: Rk^T (Kb^T) hi / lo, 128 rows x 64 (two 16 KB blocks)
+constexpr uint32_t RTH = 65536, RTL = 98304;
+constexpr uint32_t OSTG = RKH;                  // once Rk^T is formed: a whole chunk of O, row-major [64][128] fp32    // once T is formed: Rk^T (Kb^T) hi / lo, 128 rows x 64 (two 16 KB blocks)
 // exact chunks: k^, q^, G fp32 [64][129] in the [Lk; Lq] area before it is built
 constexpr int XLD = 129;
 constexpr uint32_t XK = 0, XQ = 64 * XLD * 4, XG = 2 * 64 * XLD * 4;
@@ -144,7 +145,8 @@ __device__ __forceinline__ void prod_ts(uint32_t d, uint32_t ah, uint32_t al, ui
 
 template <int GM>
 __global__ void __launch_bounds__(tfp::NT, 1)
-    prefill_tf32_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
+    prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ q,
+                        const float *__restrict__ k, const float *__restrict__ v,
                         const float *__restrict__ g, const float *__restrict__ beta, const float *s_init,
                         float *s_final, float *__restrict__ out, const int64_t *__restrict__ cu_seqlens, int N,
                         int64_t Ttot, int H, int Cc, float eps, unsigned *err, const int *__restrict__ order,
@@ -243,6 +245,8 @@ __global__ void __launch_bounds__(tfp::NT, 1)
                                                                             : (GCH ? g : nullptr);
             if (r < Ln && src != nullptr) prefetch_l2_bulk(src + ((size_t)(n0 + r) * H + h) * D, D * 4);
         }
+        // the previous chunk's output copy has read its staging (the Rk area this chunk's build writes)
+        if (tid == 0) bulk_wait_read();
         if (tid < 64) s_beta[tid] = br;
         // row norms: the warp holds all 128 channels of its 8 rows; a halving butterfly over lane bits 2..0
         // leaves row (lane & 7)'s partial on the lane, and lane bits 3, 4 finish the sum
@@ -614,15 +618,29 @@ __global__ void __launch_bounds__(tfp::NT, 1)
         wait_mma();
         if (!ok) break;
 
-        // ---- O^T -> out (warp half: 32 rows)
+        // ---- O^T -> out (warp half: 32 rows). A whole chunk is staged row-major in the dead Rk area and
+        //      leaves by one tensor copy; a sequence's short last chunk by plain stores of its own rows
+        //      (the rows after it belong to the next sequence)
         {
             uint32_t o[32];
             tmem_ld32(tbase + lq + T_XO + 64 + 32 * half, o);
             tmem_ld_wait();
+            if (L == C) {
+                float *ost = reinterpret_cast<float *>(sm + OSTG);
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const int r = 32 * half + m;
-                if (r < L) out[((size_t)(c0 + r) * H + h) * D + jl] = u2f(o[m]);
+                for (int m = 0; m < 32; ++m) ost[(32 * half + m) * D + jl] = u2f(o[m]);
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tma_store_2d(&tm_o, ost, h * D, (int)c0);
+                    bulk_commit();
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int r = 32 * half + m;
+                    if (r < L) out[((size_t)(c0 + r) * H + h) * D + jl] = u2f(o[m]);
+                }
             }
         }
         __syncthreads();
@@ -639,6 +657,7 @@ __global__ void __launch_bounds__(tfp::NT, 1)
             for (int m = 0; m < 32; ++m) s_final[soff + (size_t)(i0 + m) * D + jl] = u2f(r[m]) * s_fpend[i0 + m];
         }
     }
+    if (tid == 0) bulk_wait_all();  // output copies complete before the CTA's shared memory goes away
     if (!ok) {
         if (tid == 0) {
             atomicOr(err, DEVERR_TIMEOUT);
@@ -658,8 +677,13 @@ static kda_status launch_tf32(const PrefillArgs &a, cudaStream_t s) {
     auto kern = prefill_tf32_kernel<GM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tfp::SMEM);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    // whole output chunks leave through this map: 64 rows x one head's 128 channels
+    CUtensorMap mo;
+    if (!tcp::make_map(&mo, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)a.H * tfp::D, (uint64_t)a.T, tfp::D,
+                       tfp::C, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     kern<<<launch_seqs(a) * a.H, tfp::NT, tfp::SMEM, s>>>(
-        static_cast<const float *>(a.q), static_cast<const float *>(a.k), static_cast<const float *>(a.v), a.g,
+        mo, static_cast<const float *>(a.q), static_cast<const float *>(a.k), static_cast<const float *>(a.v), a.g,
         a.beta, a.s_init, a.s_final, static_cast<float *>(a.out), a.cu_seqlens, a.N, a.T, a.H, a.C, a.eps, a.err,
         a.order, a.v_zero ? 1 : 0);
     return check_launch("prefill_tf32_kernel");
