@@ -668,8 +668,9 @@ __global__ void __launch_bounds__(tfp::NT, 1)
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// fp32, d = 128, C >= 16; the output copy's row coordinate is 32-bit
 bool prefill_tf32_applicable(const PrefillArgs &a) {
-    return !a.bf16 && a.D == 128 && a.C >= 16 && a.C <= 64 && a.T > 0;
+    return !a.bf16 && a.D == 128 && a.C >= 16 && a.C <= 64 && a.T > 0 && a.T <= 0x7fffffffLL;
 }
 
 template <int GM>
