@@ -193,3 +193,32 @@ def test_split_batch_with_a_long_sequence(env, bf16):
         assert_close(o, ro, bf16, (1,), "out")
         assert_close(sf, rs, bf16, (0, 1), "final state")
     assert_close(res[0][0], res[1][0], bf16, (1,), "split vs whole")
+
+
+@pytest.mark.parametrize("gate", ["channel", "head"])
+def test_split_batch_with_two_long_sequences(env, gate):
+    """kda_chunk_prefill_split with two sequences long enough to split (the scan workspace reused for
+    both, the per-head gate's rows offset per sequence) around short ones, bf16, carry-in states and mild
+    gates, against the fp64 recurrence."""
+    torch, kda = env
+    H, D = 8, 128
+    lens = [9000, 40, 8500, 300]
+    cu = np.cumsum([0] + lens).astype(np.int64)
+    seg, nsplit = kda.kda_chunk_prefill_split_plan(cu, H, 64)
+    assert nsplit == 2 and seg[0] >= 4 and seg[2] >= 4 and seg[1] == 1 and seg[3] == 1, seg
+    p = synth.prefill_inputs(43, int(cu[-1]), H, D, True, cu_seqlens=cu, s0_std=0.05, g_scale=0.02)
+    bf = torch.bfloat16
+    q, k, v = (to_dev(p[n], bf, torch) for n in "qkv")
+    if gate == "head":
+        gk, go = np.ascontiguousarray(p["g"][..., 0]), np.repeat(p["g"][..., :1], D, axis=-1)
+    else:
+        gk, go = p["g"], p["g"]
+    o = torch.full_like(q, float("nan"))
+    sf = torch.full((len(lens), H, D, D), float("nan"), device="cuda")
+    kda.kda_chunk_prefill_split(q, k, v, to_dev(gk, torch.float32, torch), to_dev(p["beta"], torch.float32, torch),
+                                o, torch.from_numpy(cu), gate=gate, initial_state=to_dev(p["s0"], torch.float32, torch),
+                                final_state=sf, chunk_size=64)
+    kda.kda_sync_status()
+    ro, rs = oracle.recurrence(p["q"], p["k"], p["v"], go, p["beta"], s_init=p["s0"], cu_seqlens=cu)
+    assert_close(to_np(o), ro, True, (1,), "out")
+    assert_close(to_np(sf), rs, True, (0, 1), "final state")
