@@ -363,3 +363,41 @@ def test_prefill_bf16_tensor_core_exact_chunks(env, D, C):
     o, s = run_prefill(torch, kda, d2, True, C)
     ro, rs = oracle_prefill(d2)
     check(o, s, ro, rs, cu, True, f"D={D} C={C} spike")
+
+
+def test_prefill_full_size_varlen_fp32_sampled_heads(env):
+    """The variable-length workload at full size in fp32 (8 sequences of 512..65536 tokens, 130,560 in
+    all, H=96, d=128, C=64, non-zero initial states): the tf32 tensor-core kernel walks the 65,536-token
+    sequence's 1024 chunks per head. Three sampled heads against the oracle at the fp32 bar (max abs
+    1e-4); the other heads are filled on the device with a seeded torch generator (same distributions)."""
+    torch, kda = env
+    c = synth.VARLEN
+    cu = synth.varlen_cu_seqlens()
+    T, H, D = int(cu[-1]), c["H"], c["D"]
+    assert kda.kda_chunk_prefill_route(D, c["C"], torch.float32) == "prefill_tf32_kernel"
+    heads = [1, 48, 94]
+    d = synth.prefill_inputs(c["seed"] + 100, T, H, D, bf16=False, cu_seqlens=cu, s0_std=0.02, heads=heads)
+    gen = torch.Generator(device="cuda").manual_seed(c["seed"] + 100)
+    f32 = torch.float32
+
+    def fill(shape):
+        return torch.randn(shape, generator=gen, device="cuda", dtype=f32)
+    q, k, v = fill((T, H, D)), fill((T, H, D)), fill((T, H, D))
+    g = -torch.nn.functional.softplus(fill((T, H, D)))
+    beta = torch.sigmoid(fill((T, H)))
+    s0 = fill((len(cu) - 1, H, D, D)) * 0.02
+    hs = torch.tensor(heads, device="cuda")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
+        t[:, hs] = to_dev(d[name], f32, torch)
+    beta[:, hs] = to_dev(d["beta"], f32, torch)
+    s0[:, hs] = to_dev(d["s0"], f32, torch)
+    out = torch.empty_like(q)
+    sf = torch.empty_like(s0)
+    kda.kda_chunk_prefill(q, k, v, g, beta, out, initial_state=s0, final_state=sf,
+                          cu_seqlens=torch.from_numpy(cu).cuda(), chunk_size=c["C"])
+    kda.kda_sync_status()
+    got_o, got_s = to_np(out[:, hs]), to_np(sf[:, hs])
+    ro, rs = oracle_prefill(d)
+    check(got_o, got_s, ro, rs, cu, False, "varlen full size fp32")
+    print(f"varlen fp32 (sampled heads): max abs error out {np.max(np.abs(got_o - ro)):.2e}, "
+          f"state {np.max(np.abs(got_s - rs)):.2e}")
