@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -45,6 +46,20 @@ struct SymbolCache {
     void *ctx[MAX_DEV] = {};
 };
 kda_status symbol_address(const void *symbol, SymbolCache &cache, void **out);
+
+// Opt a kernel into more than 48 KiB of dynamic shared memory, once per device.
+template <auto Kern>
+inline cudaError_t smem_attr_once(int bytes) {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // ---------------------------------------------------------------- device side
 template <typename T> struct Elem;

@@ -398,19 +398,6 @@ __global__ void __launch_bounds__(BULK_NT, 3)
     }
 }
 
-// Opt a kernel into more than 48 KiB of dynamic shared memory, once per device.
-template <auto Kern>
-static cudaError_t smem_attr_once(int bytes) {
-    static std::atomic<uint64_t> done{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
-    return e;
-}
 
 
 // Epilogue operands of one launch: the output gate [B, H, D] (storage dtype),

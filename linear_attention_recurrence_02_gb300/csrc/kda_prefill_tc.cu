@@ -1351,6 +1351,25 @@ static bool make_map3(CUtensorMap *m, const void *base, CUtensorMapDataType dt, 
 
 }  // namespace tcp
 
+namespace tc {
+bool make_map_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int rank, const uint64_t *dims,
+                 const uint64_t *strides, const uint32_t *box) {
+    tcp::EncodeTiledFn fn = tcp::encode_fn();
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return fn(m, dt, (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+}  // namespace tc
+
 // bf16, d = 128 or 64 (64: the kernel's channels 64..127 read as zeros, which leaves every
 // product of the chunk algebra unchanged), C = 16, 32 or 64. The kernel always works in chunks of
 // 64 tokens: the chunked form is an exact rewrite of the recurrence, so the chunk length changes

@@ -3,11 +3,12 @@
 // ("KV缓存从11.25GB缩到0.21GB: WARP中Kimi Delta Attention线性注意力原理剖析",
 // sections "KDA 递推公式先衰减再差分" and "414MB 的 KDA 状态从哪来").
 //
-// Memory-bound elementwise work: each thread owns 16 bytes of channels of one
-// (projection, h) pair for two sequences: it loads the 4 taps per channel
-// once (float4), issues the 128-bit loads of x and the three ring slots of
-// both sequences before using any, and writes y and the shifted ring (the
-// ring's stored vectors move unchanged).
+// Memory-bound elementwise work. A CTA owns one (projection, head) and a
+// block of sequences: one thread copies their x rows and 3-slot ring rows
+// into shared memory with two TMA tensor copies, the CTA reads the
+// (projection, head)'s taps once, and each thread then convolves 16-byte
+// vectors of channels and writes y and the shifted ring (the ring's stored
+// vectors move unchanged).
 // y is written projection-major, [3,B,H,D], so that y[0], y[1], y[2] are the
 // contiguous q, k, v operands of the decode step.
 //
@@ -20,6 +21,7 @@
 #include <string>
 
 #include "kda_common.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -44,58 +46,75 @@ __device__ __forceinline__ void store16(T *p, const float (&in)[Vec16<T>::N]) {
     __stcs(reinterpret_cast<uint4 *>(p), raw);
 }
 
-// One thread per 16 bytes of channels of one (projection, head) and a group
-// of STEP_BPT sequences: the taps of its channels are loaded once and kept in
-// registers for every sequence of the group, and the group's loads are all
-// issued before any is used (one 16-byte x vector and three ring slots each).
-// Measured at 64 sequences x 96 heads (bf16): 1 sequence per thread 14.4 us,
-// 2 sequences 12.4 us, 4 sequences 14.4 us (133 registers: 1.3 waves); the
-// first form, one thread per (sequence, projection, head) vector re-reading
-// the taps for every sequence in 256-thread blocks, 16.4 us.
-constexpr int STEP_BPT = 2;
-constexpr int STEP_NT = 128;
-template <typename T>
-__global__ void __launch_bounds__(STEP_NT) shortconv_step_kernel(const T *__restrict__ x, T *__restrict__ ring,
-                                                             const float *__restrict__ w, T *__restrict__ y,
-                                                             int B, int H, int D) {
-    constexpr int V = Vec16<T>::N;
-    const int nvec = D / V;
-    const int ngroups = (B + STEP_BPT - 1) / STEP_BPT;
-    const size_t total = (size_t)ngroups * 3 * H * nvec;
-    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= total) return;
-    const int cv = (int)(idx % nvec);
-    const size_t r = idx / nvec;
-    const int h = (int)(r % H);
-    const int p = (int)((r / H) % 3);
-    const int b0 = (int)(r / ((size_t)3 * H)) * STEP_BPT;
-    const float4 *wt = reinterpret_cast<const float4 *>(w + (((size_t)p * H + h) * D + (size_t)cv * V) * 4);
+// Decode step: one CTA per (projection, head) and sc_bc(D) consecutive
+// sequences (a tile of SC_TILE_BYTES of x and ring). One thread issues the two
+// tensor copies (the x rows and the 3-slot ring rows of those sequences) as
+// soon as the CTA starts, so the whole launch's input is in flight at once;
+// the (projection, head)'s taps are read once per CTA. Threads then own one
+// 16-byte vector of channels for a stride of sequences and write y and the
+// shifted ring with plain 16-byte stores. A tile reaching past B reads zeros
+// there and stores nothing.
+// Measured at 64 sequences x 96 heads (bf16, inputs rotating through six sets
+// so every call misses in L2, launches replayed from a CUDA graph): 8.2 us.
+// Tiles of 16 KB / 64 threads ran the same, 64 KB or 256 threads 8.7-9.6 us.
+// The earlier form, one thread per 16-byte vector and two sequences with all
+// loads in registers, ran 10.2 us: 1.9 waves with 64 KB of loads in flight
+// per SM, and its per-lane tap loads touched a different 128-byte line in
+// every lane (two thirds of its L1 sectors).
+constexpr int SC_NT = 128;
+constexpr int SC_TILE_BYTES = 32768;
+constexpr long long WAIT_LIMIT_CONV = 2000000000LL;  // clock cycles (about 1 s)
+__host__ __device__ constexpr int sc_bc(int D, int esize) {
+    return SC_TILE_BYTES / (4 * D * esize) > 256 ? 256 : SC_TILE_BYTES / (4 * D * esize);
+}
+template <typename T, int D>
+__global__ void __launch_bounds__(SC_NT) shortconv_step_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                               const __grid_constant__ CUtensorMap tm_r,
+                                                               T *__restrict__ ring, const float *__restrict__ w,
+                                                               T *__restrict__ y, int B, int H, unsigned *err) {
+    constexpr int V = Vec16<T>::N, NV = D / V, BC = sc_bc(D, (int)sizeof(T));
+    constexpr int BSTEP = SC_NT / NV;  // sequences handled per pass of the CTA
+    extern __shared__ __align__(128) unsigned char sc_smem[];
+    T *sx = reinterpret_cast<T *>(sc_smem);  // [BC][D]
+    T *sr = sx + BC * D;                     // [BC][3][D]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sr + 3 * BC * D);
+    const int H3 = 3 * H;
+    const int ph = (int)(blockIdx.x % (unsigned)H3);  // p * H + h
+    const int b0 = (int)(blockIdx.x / (unsigned)H3) * BC;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bar, 1);
+        tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(bar, (uint32_t)(BC * 4 * D * sizeof(T)));
+        tc::tma_load_3d(sx, &tm_x, bar, 0, ph, b0);
+        tc::tma_load_4d(sr, &tm_r, bar, 0, 0, ph, b0);
+    }
+    const int cv = threadIdx.x % NV, bs = threadIdx.x / NV;
     float4 tap[V];
+    const float4 *wt = reinterpret_cast<const float4 *>(w + ((size_t)ph * D + (size_t)cv * V) * 4);
 #pragma unroll
     for (int i = 0; i < V; ++i) tap[i] = __ldg(wt + i);
-
-    // raw 16-byte vectors in flight: x and the three slots of every sequence of the group
-    uint4 xr[STEP_BPT], rr[STEP_BPT][3];
-#pragma unroll
-    for (int bb = 0; bb < STEP_BPT; ++bb) {
-        if (b0 + bb >= B) break;
-        const size_t row = ((size_t)(b0 + bb) * 3 + p) * H + h;  // (b*3 + p)*H + h
-        const size_t xoff = row * D + (size_t)cv * V, roff = row * 3 * D + (size_t)cv * V;
-        xr[bb] = __ldcs(reinterpret_cast<const uint4 *>(x + xoff));
-#pragma unroll
-        for (int k = 0; k < 3; ++k) rr[bb][k] = __ldcs(reinterpret_cast<const uint4 *>(ring + roff + (size_t)k * D));
+    __syncthreads();  // the barrier's initialisation is visible to every waiting thread
+    const bool got = tc::mbar_wait(bar, 0, WAIT_LIMIT_CONV);
+    if (__syncthreads_or(!got)) {
+        if (threadIdx.x == 0) {
+            atomicOr(err, DEVERR_TIMEOUT);
+            tc::mbar_wait(bar, 0, WAIT_LIMIT_CONV);  // let the copies land before shared memory goes away
+        }
+        return;
     }
-#pragma unroll
-    for (int bb = 0; bb < STEP_BPT; ++bb) {
+    const int p = ph / H, h = ph - p * H;
+#pragma unroll 4
+    for (int bb = bs; bb < BC; bb += BSTEP) {
         const int b = b0 + bb;
         if (b >= B) break;
-        const size_t row = ((size_t)b * 3 + p) * H + h;
-        const size_t roff = row * 3 * D + (size_t)cv * V;
-        const size_t yoff = (((size_t)p * B + b) * H + h) * D + (size_t)cv * V;
-        const T *xe = reinterpret_cast<const T *>(&xr[bb]);
-        const T *e0 = reinterpret_cast<const T *>(&rr[bb][0]);
-        const T *e1 = reinterpret_cast<const T *>(&rr[bb][1]);
-        const T *e2 = reinterpret_cast<const T *>(&rr[bb][2]);
+        const uint4 xr = *reinterpret_cast<const uint4 *>(sx + bb * D + cv * V);
+        const uint4 r0 = *reinterpret_cast<const uint4 *>(sr + (bb * 3 + 0) * D + cv * V);
+        const uint4 r1 = *reinterpret_cast<const uint4 *>(sr + (bb * 3 + 1) * D + cv * V);
+        const uint4 r2 = *reinterpret_cast<const uint4 *>(sr + (bb * 3 + 2) * D + cv * V);
+        const T *xe = reinterpret_cast<const T *>(&xr);
+        const T *e0 = reinterpret_cast<const T *>(&r0);
+        const T *e1 = reinterpret_cast<const T *>(&r1);
+        const T *e2 = reinterpret_cast<const T *>(&r2);
         float yv[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) {
@@ -103,12 +122,36 @@ __global__ void __launch_bounds__(STEP_NT) shortconv_step_kernel(const T *__rest
                             tap[i].z * Elem<T>::load(e2 + i) + tap[i].w * Elem<T>::load(xe + i);
             yv[i] = z / (1.0f + expf(-z));
         }
-        store16(y + yoff, yv);
+        store16(y + (((size_t)p * B + b) * H + h) * D + (size_t)cv * V, yv);
         // the ring shifts: its stored values move unchanged
-        __stcs(reinterpret_cast<uint4 *>(ring + roff), rr[bb][1]);
-        __stcs(reinterpret_cast<uint4 *>(ring + roff + D), rr[bb][2]);
-        __stcs(reinterpret_cast<uint4 *>(ring + roff + 2 * (size_t)D), xr[bb]);
+        T *rp = ring + ((size_t)b * H3 + ph) * 3 * D + (size_t)cv * V;
+        __stcs(reinterpret_cast<uint4 *>(rp), r1);
+        __stcs(reinterpret_cast<uint4 *>(rp + D), r2);
+        __stcs(reinterpret_cast<uint4 *>(rp + 2 * D), xr);
     }
+}
+
+template <typename T, int D>
+static kda_status launch_conv_step(const T *x, T *ring, const float *w, T *y, int B, int H, cudaStream_t s) {
+    constexpr int BC = sc_bc(D, (int)sizeof(T));
+    const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const uint64_t e = sizeof(T), H3 = 3 * (uint64_t)H;
+    CUtensorMap mx, mr;
+    // x [B][3H][D] and ring [B][3H][3][D], dimensions innermost first
+    const uint64_t dx[3] = {(uint64_t)D, H3, (uint64_t)B}, sxs[2] = {D * e, H3 * D * e};
+    const uint32_t bx[3] = {(uint32_t)D, 1u, (uint32_t)BC};
+    const uint64_t dr[4] = {(uint64_t)D, 3u, H3, (uint64_t)B}, srs[3] = {D * e, 3 * D * e, 3 * H3 * D * e};
+    const uint32_t br[4] = {(uint32_t)D, 3u, 1u, (uint32_t)BC};
+    if (!tc::make_map_nd(&mx, x, dt, 3, dx, sxs, bx) || !tc::make_map_nd(&mr, ring, dt, 4, dr, srs, br))
+        return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the conv step");
+    const size_t smem = (size_t)BC * 4 * D * sizeof(T) + 16;
+    if (smem_attr_once<shortconv_step_kernel<T, D>>((int)smem) != cudaSuccess)
+        return check_launch("shortconv_step_kernel (shared memory attribute)");
+    const uint64_t blocks = (((uint64_t)B + BC - 1) / BC) * H3;
+    if (blocks > 0x7fffffffULL) return invalid("B * H too large for the conv step grid");
+    shortconv_step_kernel<T, D><<<(unsigned)blocks, SC_NT, smem, s>>>(mx, mr, ring, w, y, B, H,
+                                                                          device_error_word());
+    return check_launch("shortconv_step_kernel");
 }
 
 constexpr int CONV_TILE = 64;  // tokens per prefill tile
@@ -301,18 +344,24 @@ extern "C" kda_status kda_shortconv_step(const void *x, void *ring, const float 
     if (y == x || y == ring) return invalid("y must not alias x or ring");
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int V = dtype == KDA_BF16 ? 8 : 4;
-    const size_t total = (size_t)((B + STEP_BPT - 1) / STEP_BPT) * 3 * H * (D / V);
-    const unsigned blocks = (unsigned)((total + STEP_NT - 1) / STEP_NT);
-    if (dtype == KDA_BF16)
-        shortconv_step_kernel<__nv_bfloat16><<<blocks, STEP_NT, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(ring), w,
-            static_cast<__nv_bfloat16 *>(y), B, H, D);
-    else
-        shortconv_step_kernel<float><<<blocks, STEP_NT, 0, s>>>(static_cast<const float *>(x),
-                                                            static_cast<float *>(ring), w,
-                                                            static_cast<float *>(y), B, H, D);
-    return check_launch("shortconv_step_kernel");
+    if (dtype == KDA_BF16) {
+        const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+        __nv_bfloat16 *rb = static_cast<__nv_bfloat16 *>(ring), *yb = static_cast<__nv_bfloat16 *>(y);
+        switch (D) {
+        case 16: return launch_conv_step<__nv_bfloat16, 16>(xb, rb, w, yb, B, H, s);
+        case 32: return launch_conv_step<__nv_bfloat16, 32>(xb, rb, w, yb, B, H, s);
+        case 64: return launch_conv_step<__nv_bfloat16, 64>(xb, rb, w, yb, B, H, s);
+        default: return launch_conv_step<__nv_bfloat16, 128>(xb, rb, w, yb, B, H, s);
+        }
+    }
+    const float *xf = static_cast<const float *>(x);
+    float *rf = static_cast<float *>(ring), *yf = static_cast<float *>(y);
+    switch (D) {
+    case 16: return launch_conv_step<float, 16>(xf, rf, w, yf, B, H, s);
+    case 32: return launch_conv_step<float, 32>(xf, rf, w, yf, B, H, s);
+    case 64: return launch_conv_step<float, 64>(xf, rf, w, yf, B, H, s);
+    default: return launch_conv_step<float, 128>(xf, rf, w, yf, B, H, s);
+    }
 }
 
 extern "C" kda_status kda_shortconv_prefill(const void *x, const void *ring_in, const float *w, void *y,

@@ -154,6 +154,24 @@ def test_shortconv_matches_oracle(env, D, bf16):
     assert np.array_equal(ring, rring)  # the ring only moves stored values
 
 
+@pytest.mark.parametrize("B,H,D,bf16", [(70, 2, 128, True), (33, 3, 128, False), (37, 2, 64, False),
+                                        (300, 2, 16, True), (130, 1, 16, False), (1, 1, 128, True)])
+def test_shortconv_tiles(env, B, H, D, bf16):
+    """Batches spanning several sequence tiles of the conv step's CTAs (32 KB of x and ring per
+    tile: 32 bf16 or 16 fp32 sequences at d=128, up to 256 at d=16), each with a ragged last
+    tile, and a single sequence."""
+    torch, kda = env
+    d = synth.decode_inputs(300 + B, B, H, D, bf16, s0_std=None)
+    y, ring = _gpu_conv(torch, kda, d["x"], d["ring"], d["w"], bf16)
+    ry, rring = oracle.shortconv_step(d["x"], d["ring"], d["w"])
+    ry = ry.transpose(1, 0, 2, 3)
+    if bf16:
+        assert np.all(np.abs(y - ry) <= 4e-3 * np.abs(ry) + 1e-5)
+    else:
+        assert np.max(np.abs(y - ry)) <= 1e-5
+    assert np.array_equal(ring, rring)
+
+
 def test_shortconv_then_decode_full_size(env):
     """The decode workload end to end: short conv (bf16 ring of 3 tokens x
     3 projections x 128 per head, SiLU) feeding the decode step, against the
