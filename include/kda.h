@@ -105,7 +105,10 @@ size_t kda_shortconv_ring_bytes(int layers, int batch, int heads, int d, int ele
  *                          projection-major so that y[0], y[1], y[2] are the
  *                          contiguous [B,H,D] q, k, v of kda_decode_step
  * Requires B >= 0, H >= 1, D in {16,32,64,128}. y may not alias x or ring.
- * B = 0 is a no-op.
+ * B = 0 is a no-op. x and ring are read by TMA tensor copies: KDA_ERR_CUDA
+ * if the driver's tensor-map encoder rejects them. A copy that does not land
+ * within about a second sets the device error word (KDA_ERR_TIMEOUT from the
+ * next kda_sync_status) and the launch leaves y and ring untouched.
  */
 kda_status kda_shortconv_step(const void *x, void *ring, const float *w, void *y,
                               int B, int H, int D, kda_dtype dtype, kda_stream_t stream);
