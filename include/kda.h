@@ -108,7 +108,8 @@ size_t kda_shortconv_ring_bytes(int layers, int batch, int heads, int d, int ele
  * B = 0 is a no-op. x and ring are read by TMA tensor copies: KDA_ERR_CUDA
  * if the driver's tensor-map encoder rejects them. A copy that does not land
  * within about a second sets the device error word (KDA_ERR_TIMEOUT from the
- * next kda_sync_status) and the launch leaves y and ring untouched.
+ * next kda_sync_status); the sequences of that copy keep their y and ring
+ * contents.
  */
 kda_status kda_shortconv_step(const void *x, void *ring, const float *w, void *y,
                               int B, int H, int D, kda_dtype dtype, kda_stream_t stream);
