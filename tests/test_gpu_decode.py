@@ -230,6 +230,38 @@ def test_fused_conv_decode_matches_oracle(env, D, bf16):
     assert np.array_equal(to_np(tr), rring)
 
 
+@pytest.mark.parametrize("gate", ["channel", "head", "none"])
+@pytest.mark.parametrize("bf16,overlap", [(True, False), (False, False), (True, True)])
+def test_fused_conv_decode_gate_forms(env, gate, bf16, overlap):
+    """The staged d = 128 kernel on an odd batch (17 sequences x 3 heads) in every gate form, plain and
+    programmatic-dependent launches, against the oracle's conv feeding its recurrence."""
+    torch, kda = env
+    B, H, D = 17, 3, 128
+    d = synth.decode_inputs(820, B, H, D, bf16, s0_std=0.5)
+    if gate == "head":
+        g_in = np.ascontiguousarray(d["g"][..., 0])
+        g_or = np.repeat(g_in[..., None], D, axis=-1)
+    elif gate == "none":
+        g_in, g_or = None, np.zeros_like(d["g"])
+    else:
+        g_in = g_or = d["g"]
+    dt = torch.bfloat16 if bf16 else torch.float32
+    tx, tr = to_dev(d["x"], dt, torch), to_dev(d["ring"], dt, torch)
+    tw, tb = to_dev(d["w"], torch.float32, torch), to_dev(d["beta"], torch.float32, torch)
+    tg = to_dev(g_in, torch.float32, torch) if g_in is not None else None
+    ts = to_dev(d["s0"], torch.float32, torch)
+    out = torch.full((B, H, D), float("nan"), dtype=dt, device="cuda")
+    kda.kda_shortconv_decode_step_ex(tx, tr, tw, tg, tb, ts, out, gate=gate, overlap_prev=overlap)
+    torch.cuda.synchronize()
+    kda.kda_sync_status()
+    ry, rring = oracle.shortconv_step(d["x"], d["ring"], d["w"])
+    ro, rs = oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], g_or, d["beta"], d["s0"], nthreads=NCPU)
+    assert_close(to_np(out), ro, bf16, (0, 1), "out")
+    assert_close(to_np(ts), rs, bf16, (0, 1), "state")
+    assert np.max(np.abs(to_np(ts) - rs)) <= 1e-4
+    assert np.array_equal(to_np(tr), rring)
+
+
 def test_fused_conv_decode_consecutive_steps(env):
     """Four fused steps in a row (ring and state carried) against the oracle
     run step by step on the same inputs."""

@@ -209,6 +209,21 @@ def test_fused_decode_epilogue_gate_forms(env, gate, overlap):
     assert np.array_equal(ring, rring)
 
 
+@pytest.mark.parametrize("act", ["sigmoid", "silu"])
+@pytest.mark.parametrize("gate,overlap", [("channel", False), ("head", True), ("none", False)])
+def test_fused_decode_epilogue_acts_gates(env, act, gate, overlap):
+    """The staged d = 128 kernel with the epilogue, both activations, on 16 sequences x 5 heads (bf16) in
+    three gate and launch forms."""
+    torch, kda = env
+    d = synth.decode_inputs(720, 16, 5, 128, True, s0_std=0.3)
+    e = synth.epilogue_inputs(721, 16, 5, 128, True)
+    y, st, ring = _gpu_decode_epi(torch, kda, d, e, True, act, gate=gate, overlap=overlap)
+    ry, rs, rring = _oracle_decode_epi(d, e, act, gate=gate)
+    assert_close(y, ry, True, (0, 1), "y")
+    assert_close(st, rs, True, (0, 1), "state")
+    assert np.array_equal(ring, rring)
+
+
 def test_fused_decode_epilogue_zero_output_row(env):
     """A head whose output is exactly zero (zero state, zero v: o = 0) maps to zeros with norm eps = 0, as the
     oracle's reading fixes; the other heads are unaffected."""
@@ -234,7 +249,7 @@ def test_fused_decode_epilogue_zero_output_row(env):
 
 
 def test_fused_decode_epilogue_full_size(env):
-    """The decode workload at full size (B=64, H=96, d=128, bf16: the register kernel), every unit against
+    """The decode workload at full size (B=64, H=96, d=128, bf16: the staged kernel), every unit against
     the oracle."""
     torch, kda = env
     c = synth.DECODE
