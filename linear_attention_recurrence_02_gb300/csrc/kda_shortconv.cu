@@ -54,9 +54,13 @@ __device__ __forceinline__ void store16(T *p, const float (&in)[Vec16<T>::N]) {
 // 16-byte vector of channels for a stride of sequences and write y and the
 // shifted ring with plain 16-byte stores. A tile reaching past B reads zeros
 // there and stores nothing.
+// The SiLU takes the fast exponential and division intrinsics (a few ulp, as
+// the prefill form does): the CTA's compute sits between its tile landing and
+// its stores, on the launch's critical path.
 // Measured at 64 sequences x 96 heads (bf16, inputs rotating through six sets
-// so every call misses in L2, launches replayed from a CUDA graph): 8.2 us.
-// Tiles of 16 KB / 64 threads ran the same, 64 KB or 256 threads 8.7-9.6 us.
+// so every call misses in L2, launches replayed from a CUDA graph): 7.0 us,
+// 8.1 us with the exact expf and division. Tiles of 16 KB / 64 threads ran
+// about the same, 64 KB or 256 threads 8.7-9.6 us (exact forms).
 // The earlier form, one thread per 16-byte vector and two sequences with all
 // loads in registers, ran 10.2 us: 1.9 waves with 64 KB of loads in flight
 // per SM, and its per-lane tap loads touched a different 128-byte line in
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(SC_NT) shortconv_step_kernel(const __grid_cons
         for (int i = 0; i < V; ++i) {
             const float z = tap[i].x * Elem<T>::load(e0 + i) + tap[i].y * Elem<T>::load(e1 + i) +
                             tap[i].z * Elem<T>::load(e2 + i) + tap[i].w * Elem<T>::load(xe + i);
-            yv[i] = z / (1.0f + expf(-z));
+            yv[i] = __fdividef(z, 1.0f + __expf(-z));
         }
         store16(y + (((size_t)p * B + b) * H + h) * D + (size_t)cv * V, yv);
         // the ring shifts: its stored values move unchanged
