@@ -262,6 +262,39 @@ def test_fused_conv_decode_gate_forms(env, gate, bf16, overlap):
     assert np.array_equal(to_np(tr), rring)
 
 
+@pytest.mark.parametrize("gate", ["channel", "head", "none"])
+def test_fused_conv_decode_1248_heads(env, gate):
+    """The staged d = 128 kernel on 13 sequences x 96 heads (1248 CTAs: 2.7 waves at three per SM on 152
+    SMs) in every gate form, two steps in a row (ring and state carried), against the oracle."""
+    torch, kda = env
+    B, H, D = 13, 96, 128
+    d = synth.decode_inputs(840, B, H, D, True, s0_std=0.3)
+    if gate == "head":
+        g_in = np.ascontiguousarray(d["g"][..., 0])
+        g_or = np.repeat(g_in[..., None], D, axis=-1)
+    elif gate == "none":
+        g_in, g_or = None, np.zeros_like(d["g"])
+    else:
+        g_in = g_or = d["g"]
+    bf = torch.bfloat16
+    tr = to_dev(d["ring"], bf, torch)
+    tw, tb = to_dev(d["w"], torch.float32, torch), to_dev(d["beta"], torch.float32, torch)
+    tg = to_dev(g_in, torch.float32, torch) if g_in is not None else None
+    ts = to_dev(d["s0"], torch.float32, torch)
+    xs = [d["x"], synth.bf16_round(np.random.default_rng(841).standard_normal(d["x"].shape).astype(np.float32))]
+    ring, st = d["ring"], d["s0"]
+    for i, xi in enumerate(xs):
+        out = torch.full((B, H, D), float("nan"), dtype=bf, device="cuda")
+        kda.kda_shortconv_decode_step_gated(to_dev(xi, bf, torch), tr, tw, tg, tb, ts, out, gate=gate)
+        torch.cuda.synchronize()
+        kda.kda_sync_status()
+        ry, ring = oracle.shortconv_step(xi, ring, d["w"])
+        ro, st = oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], g_or, d["beta"], st, nthreads=NCPU)
+        assert_close(to_np(out), ro, True, (0, 1), f"out step {i}")
+        assert_close(to_np(ts), st, True, (0, 1), f"state step {i}")
+        assert np.array_equal(to_np(tr), ring)
+
+
 def test_fused_conv_decode_consecutive_steps(env):
     """Four fused steps in a row (ring and state carried) against the oracle
     run step by step on the same inputs."""

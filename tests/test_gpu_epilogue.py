@@ -224,6 +224,19 @@ def test_fused_decode_epilogue_acts_gates(env, act, gate, overlap):
     assert np.array_equal(ring, rring)
 
 
+@pytest.mark.parametrize("act", ["sigmoid", "silu"])
+def test_fused_decode_epilogue_1248_heads(env, act):
+    """The staged d = 128 kernel with the epilogue on 13 sequences x 96 heads (bf16), against the oracle."""
+    torch, kda = env
+    d = synth.decode_inputs(730, 13, 96, 128, True, s0_std=0.3)
+    e = synth.epilogue_inputs(731, 13, 96, 128, True)
+    y, st, ring = _gpu_decode_epi(torch, kda, d, e, True, act)
+    ry, rs, rring = _oracle_decode_epi(d, e, act)
+    assert_close(y, ry, True, (0, 1), "y")
+    assert_close(st, rs, True, (0, 1), "state")
+    assert np.array_equal(ring, rring)
+
+
 def test_fused_decode_epilogue_zero_output_row(env):
     """A head whose output is exactly zero (zero state, zero v: o = 0) maps to zeros with norm eps = 0, as the
     oracle's reading fixes; the other heads are unaffected."""
