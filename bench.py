@@ -573,7 +573,10 @@ def bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak, n=20):
             "config": {"workload": f"short conv + SiLU prefill T={T}, H={H}, d={D}, bf16, ring in and out",
                        "calls": n, "l2": "3 rotating input/output sets (450 MB)"},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by,
+                             **_traffic_fields(_traffic("shortconv_prefill_kernel",
+                                                        ["kda_shortconv.cu", "kda_common.cuh", "kda_tc.cuh"], T),
+                                               T * 3 * H * D * 2 + 9 * H * D * 2)}}
 
 
 def bench_shortconv_step(torch, kda, dev, stream, ws, hbm_peak, n=200, nsets=6, per_graph=60, replays=10):
@@ -673,7 +676,9 @@ def bench_epilogue(torch, kda, dev, stream, ws, hbm_peak, n=20):
             "config": {"workload": f"gated RMSNorm output epilogue T={T}, H={H}, d={D}, bf16, sigmoid gate",
                        "calls": n, "l2": "2 alternating sets (604 MB)"},
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
+                             "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by,
+                             **_traffic_fields(_traffic("gated_rmsnorm_kernel", ["kda_epilogue.cu", "kda_common.cuh"],
+                                                        T * H), T * H * D * 2)}}
 
 
 def bench_long_sequence(torch, kda, dev, stream, ws, T=65536, Hs=8, segments=0, n=3):

@@ -15,6 +15,8 @@ each (the prefill adds no other launch for one sequence). Cases:
   decode_unfused  the decode step alone (kda_decode_step)
   shortconv_step  the short conv decode step alone (kda_shortconv_step)
   prefill         chunked prefill of one T-token sequence (C = 64)
+  shortconv_prefill  the short conv over one T-token prompt with rings in and out
+  epilogue        the gated RMSNorm output epilogue over T x H rows (sigmoid gate)
 """
 from __future__ import annotations
 
@@ -28,7 +30,8 @@ from linear_attention_recurrence_02_gb300 import kda
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["decode", "decode_epi", "decode_unfused", "shortconv_step", "prefill"])
+    ap.add_argument("case", choices=["decode", "decode_epi", "decode_unfused", "shortconv_step", "prefill",
+                                     "shortconv_prefill", "epilogue"])
     ap.add_argument("--B", type=int, default=64)
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=96)
@@ -70,6 +73,19 @@ def main(argv=None) -> int:
                 kda.kda_decode_step_gated(qkv[0], qkv[1], qkv[2], g, beta, state, out, gate=a.gate)
             else:
                 kda.kda_shortconv_step(x, ring, w, y)
+    elif a.case == "shortconv_prefill":
+        x, w = rnd(T, 3, H, D).to(bf), rnd(3, H, D, 4, scale=0.5)
+        rin, rout = rnd(1, 3, H, 3, D).to(bf), torch.empty((1, 3, H, 3, D), dtype=bf, device=dev)
+        y = torch.empty((3, T, H, D), dtype=bf, device=dev)
+
+        def call():
+            kda.kda_shortconv_prefill(x, w, y, ring_in=rin, ring_out=rout)
+    elif a.case == "epilogue":
+        o, og = rnd(T, H, D).to(bf), rnd(T, H, D, scale=2.0).to(bf)
+        nw, y = torch.rand((D,), generator=gen, device=dev) + 0.5, torch.empty((T, H, D), dtype=bf, device=dev)
+
+        def call():
+            kda.kda_gated_rmsnorm(o, og, nw, y)
     else:
         dt = bf if a.dtype == "bf16" else torch.float32
         q, k, v = rnd(T, H, D).to(dt), rnd(T, H, D).to(dt), rnd(T, H, D).to(dt)
