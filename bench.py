@@ -43,6 +43,7 @@ STATE_RW = 2 * D * D * 4
 DEC_UNIT_BYTES = STATE_RW + 3 * D * 2 + D * 4 + 4 + D * 2 + 3 * 3 * D * 2 + 3 * D * 2
 CONV_W_BYTES = 3 * H * D * 4 * 4
 STEP_BYTES = UNITS * DEC_UNIT_BYTES + CONV_W_BYTES
+GRAPH_STEPS = 100  # decode steps per CUDA graph in the headline's timed region
 # prefill per token-head: q,k,v bf16 in, g fp32, beta, o bf16 out
 PREFILL_TOKEN_HEAD_BYTES = 3 * D * 2 + D * 4 + 4 + D * 2
 PREFILL_TOKEN_HEAD_FLOPS = 6 * D * D + 5 * PRE["C"] * D
@@ -253,16 +254,39 @@ def run_ours(args):
     out = torch.empty((B, H, D), dtype=bf, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(st=None):
         # one launch: short conv + decode (kda_shortconv_decode_step)
-        kda.kda_shortconv_decode_step(x, ring, w, g, beta, state, out, stream=stream)
+        kda.kda_shortconv_decode_step(x, ring, w, g, beta, state, out, stream=stream if st is None else st)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the same steps issued one by one from the host, reported beside the graph-timed value
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    one_by_one_ms = start.elapsed_time(end) / args.steps
+    # The timed steps run from CUDA graphs of up to GRAPH_STEPS launches (a serving loop's decode
+    # form): each launch is the same call on the same resident state, and the graph removes the
+    # host's launch gap between steps (about 2 us on this part), not any work.
+    G = min(GRAPH_STEPS, args.steps)
+    graphs = []
+    for n_g in sorted({G, args.steps % G} - {0}, reverse=True):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            cs = torch.cuda.current_stream(dev)
+            for _ in range(n_g):
+                step(cs)
+        graphs.append((n_g, gr))
+    for _, gr in graphs:
+        gr.replay()  # warm-up of the graphs themselves
+    torch.cuda.synchronize(dev)
+    replays = [graphs[0][1]] * (args.steps // G) + ([graphs[1][1]] if len(graphs) > 1 else [])
     if ws > 1:
         dist.barrier()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -271,8 +295,8 @@ def run_ours(args):
     with ClockSampler(uuid) as clk:
         torch.cuda.synchronize(dev)
         start.record(stream)
-        for _ in range(args.steps):
-            step()
+        for gr in replays:
+            gr.replay()
         end.record(stream)
         torch.cuda.synchronize(dev)
     clocks = clk.summary()
@@ -368,7 +392,11 @@ def run_ours(args):
             "config": {"workload": f"KDA decode step with short conv (fused, one launch): B={B} sequences, "
                                    f"H={H}, d_k=d_v={D}, bf16 q/k/v, fp32 state (384 MiB), 1 layer",
                        "B": B, "H": H, "d": D, "l2": "state (384 MiB) larger than L2 (129 MB); no flush",
+                       "launch": f"the K steps replayed from CUDA graphs of {min(GRAPH_STEPS, args.steps)} launches",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "one_by_one": {"ms_per_step": one_by_one_ms,
+                           "value": ws * STEP_BYTES / (one_by_one_ms * 1e-3) / 1e9, "unit": "GB/s",
+                           "note": "the same K steps issued one by one from the host, before the graph-timed region"},
             "roofline": {"bound": "hbm", "kernel": "fused_decode_bulk_kernel", "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "peak_source": f"{peak_src} hbm_gbs (burst copy)",
@@ -532,7 +560,7 @@ def bench_prefill(args, torch, kda, dev, stream, ws, hbm_peak, tc_peak, peak_src
                                 "peak_source": f"{peak_src} bf16_tflops (burst)"}}
 
 
-def bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak, n=20):
+def bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak, n=30):
     """Short conv + SiLU over one 4096-token prompt (96 heads, d=128, bf16)
     with the ring handed in and out. Timing only; inputs drawn on the device
     by a seeded torch generator. Three input/output sets are rotated so that
@@ -550,28 +578,24 @@ def bench_conv_prefill(torch, kda, dev, stream, ws, hbm_peak, n=20):
     rout = torch.empty_like(rin)
     w = torch.randn((3, H, D, 4), generator=gen, device=dev) * 0.5
 
-    def call(i):
+    def call(st, i):
         x, y = sets[i % 3]
-        kda.kda_shortconv_prefill(x, w, y, ring_in=rin, ring_out=rout, stream=stream)
+        kda.kda_shortconv_prefill(x, w, y, ring_in=rin, ring_out=rout, stream=st)
     try:
-        call(0)
+        call(stream, 0)
     except kda.KdaError as e:
         return {"unavailable": str(e)}
     for i in range(6):
-        call(i)
+        call(stream, i)
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    for i, (a, b) in enumerate(evs):
-        a.record(stream)
-        call(i)
-        b.record(stream)
-    torch.cuda.synchronize(dev)
+    ms, loop_ms = _graph_and_loop_ms(torch, dev, stream, call, n, per_graph=n)
     kda.kda_sync_status(stream)
-    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
+    ms = max_over_ranks(ms, dev)
     by = 2 * (T * 3 * H * D * 2) + 2 * (9 * H * D * 2) + 3 * H * D * 16
     return {"value": ws * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
             "config": {"workload": f"short conv + SiLU prefill T={T}, H={H}, d={D}, bf16, ring in and out",
-                       "calls": n, "l2": "3 rotating input/output sets (450 MB)"},
+                       "calls": n, "l2": "3 rotating input/output sets (450 MB)", "launch": f"CUDA graph of {n} calls"},
+            "one_by_one_ms_per_call": loop_ms,
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by,
                              **_traffic_fields(_traffic("shortconv_prefill_kernel",
@@ -657,24 +681,20 @@ def bench_epilogue(torch, kda, dev, stream, ws, hbm_peak, n=20):
              torch.empty((T, H, D), dtype=bf, device=dev)) for _ in range(2)]
     w = torch.rand((D,), generator=gen, device=dev) + 0.5
 
-    def call(i):
+    def call(st, i):
         o, gt, y = sets[i % 2]
-        kda.kda_gated_rmsnorm(o, gt, w, y, stream=stream)
+        kda.kda_gated_rmsnorm(o, gt, w, y, stream=st)
     for i in range(4):
-        call(i)
+        call(stream, i)
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    for i, (a, b) in enumerate(evs):
-        a.record(stream)
-        call(i)
-        b.record(stream)
-    torch.cuda.synchronize(dev)
+    ms, loop_ms = _graph_and_loop_ms(torch, dev, stream, call, n, per_graph=n)
     kda.kda_sync_status(stream)
-    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dev)
+    ms = max_over_ranks(ms, dev)
     by = 3 * T * H * D * 2 + D * 4
     return {"value": ws * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
             "config": {"workload": f"gated RMSNorm output epilogue T={T}, H={H}, d={D}, bf16, sigmoid gate",
-                       "calls": n, "l2": "2 alternating sets (604 MB)"},
+                       "calls": n, "l2": "2 alternating sets (604 MB)", "launch": f"CUDA graph of {n} calls"},
+            "one_by_one_ms_per_call": loop_ms,
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by,
                              **_traffic_fields(_traffic("gated_rmsnorm_kernel", ["kda_epilogue.cu", "kda_common.cuh"],
@@ -785,6 +805,33 @@ def bench_varlen(torch, kda, dev, stream, ws, hbm_peak):
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 
 
+def _graph_and_loop_ms(torch, dev, stream, call, steps, per_graph=GRAPH_STEPS):
+    """ms per call of `call(st, i)` (the i-th call, on stream st) issued one by one on `stream`, then
+    replayed from a CUDA graph of `per_graph` calls (steps // per_graph replays, at least one):
+    (graph_ms, one_by_one_ms)."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        call(stream, i)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    loop_ms = a.elapsed_time(b) / steps
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        cs = torch.cuda.current_stream(dev)
+        for i in range(per_graph):
+            call(cs, i)
+    gr.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, steps // per_graph)
+    a.record(stream)
+    for _ in range(reps):
+        gr.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / (reps * per_graph), loop_ms
+
+
 def bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d, steps=200):
     """The decode step alone (kda_decode_step, post-conv q/k/v, no conv) on
     the headline workload: B=64, H=96, d=128, bf16 q/k/v, its own 384 MiB
@@ -797,25 +844,22 @@ def bench_decode_unfused(torch, kda, dev, stream, ws, hbm_peak, d, steps=200):
     g, beta, state = up(d["g"], torch.float32), up(d["beta"], torch.float32), up(d["s0"], torch.float32)
     out = torch.empty_like(q)
 
-    def step():
-        kda.kda_decode_step(q, k, v, g, beta, state, out, stream=stream)
+    def step(st, i=0):
+        kda.kda_decode_step(q, k, v, g, beta, state, out, stream=st)
     for _ in range(5):
-        step()
+        step(stream)
     torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
+    ms, loop_ms = _graph_and_loop_ms(torch, dev, stream, step, steps)
     kda.kda_sync_status(stream)
-    ms = max_over_ranks(a.elapsed_time(b) / steps, dev)
+    ms = max_over_ranks(ms, dev)
     by = B * H * (2 * D * D * 4 + 3 * D * 2 + D * 4 + 4 + D * 2)
     tr = _traffic("decode_step_kernel", ["kda_decode.cu", "kda_common.cuh"], B * H)
     return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "kernel": "decode_step_kernel", "dram": _traffic_fields(tr, B * H * (D * D * 4 + D * 2)),
             "config": {"workload": f"decode step without conv (kda_decode_step): B={B}, H={H}, d={D}, bf16 q/k/v, "
-                                   "fp32 state 384 MiB", "steps": steps},
+                                   "fp32 state 384 MiB", "steps": steps,
+                       "launch": f"CUDA graph of {GRAPH_STEPS} calls, as the headline"},
+            "one_by_one_ms_per_step": loop_ms,
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 
@@ -835,26 +879,23 @@ def bench_decode_epi(torch, kda, dev, stream, ws, hbm_peak, d, fused_ms, steps=2
     og, nw = up(e["gate"], bf), up(e["weight"], torch.float32)
     y = torch.empty((B, H, D), dtype=bf, device=dev)
 
-    def step():
-        kda.kda_shortconv_decode_step_epi(x, ring, w, g, beta, state, og, nw, y, stream=stream)
+    def step(st, i=0):
+        kda.kda_shortconv_decode_step_epi(x, ring, w, g, beta, state, og, nw, y, stream=st)
     for _ in range(5):
-        step()
+        step(stream)
     torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
+    ms, loop_ms = _graph_and_loop_ms(torch, dev, stream, step, steps)
     kda.kda_sync_status(stream)
-    ms = max_over_ranks(a.elapsed_time(b) / steps, dev)
+    ms = max_over_ranks(ms, dev)
     by = STEP_BYTES + B * H * D * 2 + D * 4
     tr = _traffic("fused_decode_bulk_kernel_epilogue", ["kda_fused_decode.cu", "kda_common.cuh", "kda_tc.cuh"], B * H)
     return {"value": ws * by / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "dram": _traffic_fields(tr, B * H * (D * D * 4 + D * 2 + 9 * D * 2)),
             "fused_step_without_epilogue_ms": fused_ms, "kernel": "fused_decode_bulk_kernel (output epilogue)",
             "config": {"workload": f"fused conv + decode step with the gated RMSNorm epilogue (sigmoid gate) in "
-                                   f"one launch: B={B}, H={H}, d={D}, bf16, fp32 state 384 MiB", "steps": steps},
+                                   f"one launch: B={B}, H={H}, d={D}, bf16, fp32 state 384 MiB", "steps": steps,
+                       "launch": f"CUDA graph of {GRAPH_STEPS} calls, as the headline"},
+            "one_by_one_ms_per_step": loop_ms,
             "roofline_hbm": {"achieved": by / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": by / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": by}}
 
