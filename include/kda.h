@@ -324,10 +324,17 @@ kda_status kda_chunk_prefill_epi(const void *q, const void *k, const void *v, co
  *     the batch's work per SM would be with every chunk-head spread evenly
  *     (and than 8 chunks), into P = min(chunks / that balance, 4096)
  *     segments when P >= 4. Sequences are never split when H is not a
- *     multiple of 4.
- *   - The sequences kept whole run in one prefill launch, longest first; each
- *     split one then runs through kda_chunk_prefill_scan over its own rows,
- *     with its own initial and final state.
+ *     multiple of 4. When some sequences stay whole, P is capped at
+ *     (SMs - whole sequences x H) / H if that is still >= 4, so that the
+ *     whole sequences' CTAs find SMs of their own beside the first split
+ *     sequence's passes.
+ *   - The sequences kept whole run in one prefill launch, longest first, on
+ *     an internal side stream forked from `stream` by an event; each split
+ *     one runs through kda_chunk_prefill_scan over its own rows, with its own
+ *     initial and final state, on `stream`, which then waits for the side
+ *     stream. The side stream and its two events are created on the first
+ *     such call on a device and kept for the process; the enqueueing is
+ *     serialised across host threads. Fork and join are stream-capture safe.
  *   - With nothing to split this is kda_chunk_prefill_gated.
  * Arguments as kda_chunk_prefill_gated, plus host_cu_seqlens: a host copy of
  * cu_seqlens (both required; they must agree, which is not checked on the

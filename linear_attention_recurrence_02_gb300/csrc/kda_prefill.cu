@@ -21,6 +21,7 @@
 // sequence. A and P use exact pairwise exponentials, so the kernel is robust
 // to any finite gate; it is the reference-grade fp32 path, not the fast one.
 #include <algorithm>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -396,6 +397,9 @@ extern "C" kda_status kda_chunk_prefill(const void *q, const void *k, const void
 // chain of chunks is longer than that (and than 8 chunks) gets
 // P = min(chunks / balance, 4096) segments when P >= 4: its two scan passes
 // then take 1/P of its chain each, and the scan and the correction pay. The
+// sequences that stay whole run beside the first split sequence's passes, one
+// CTA per (sequence, head), so P is capped where that leaves them SMs of their
+// own: P * H + (whole sequences) * H <= sms, as long as P stays >= 4. The
 // per-head arrays of a segment start 16-byte aligned only when H is a
 // multiple of 4, so other H are never split. -1 for invalid lengths.
 static int split_plan(const int64_t *cu, int N, int H, int C, int sms, int *seg) {
@@ -408,14 +412,31 @@ static int split_plan(const int64_t *cu, int N, int H, int C, int sms, int *seg)
     if (sms <= 0) sms = current_sms();
     const int64_t bal = sms > 0 ? std::max<int64_t>((W * H + sms - 1) / sms, 8) : 0;
     int n = 0;
+    int64_t whole = 0;  // sequences with tokens that stay whole
     for (int i = 0; i < N; ++i) {
         const int64_t ch = (cu[i + 1] - cu[i] + C - 1) / C;
         const int64_t P = (bal > 0 && H % 4 == 0) ? std::min<int64_t>(ch / bal, 4096) : 0;
         seg[i] = P >= 4 ? (int)P : 1;
         n += P >= 4 ? 1 : 0;
+        whole += (P < 4 && ch > 0) ? 1 : 0;
     }
+    const int64_t cap = sms > 0 ? ((int64_t)sms - whole * H) / H : 0;
+    if (n > 0 && whole > 0 && cap >= 4)
+        for (int i = 0; i < N; ++i)
+            if (seg[i] > cap) seg[i] = (int)cap;
     return n;
 }
+
+// The side stream on which kda_chunk_prefill_split runs the sequences that stay
+// whole, and the fork and join events around it: one set per device, created on
+// first use and kept for the process. The mutex serialises the calls' enqueueing
+// (the events are re-recorded by every call).
+struct SplitSide {
+    std::mutex mu;
+    cudaStream_t side[64] = {};
+    cudaEvent_t fork[64] = {}, join[64] = {};
+};
+static SplitSide g_split_side;
 
 static size_t align256_(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -474,26 +495,53 @@ extern "C" kda_status kda_chunk_prefill_split(const void *q, const void *k, cons
     if ((st = check_ptr(workspace, "workspace"))) return st;
     if ((st = bind_stream_device(stream))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // 1. the sequences that stay whole: one launch, longest first
+    // 1. the sequences that stay whole: one launch, longest first, on a side stream forked from
+    // `stream`, so that it runs beside the split sequences' passes; joined back at the end
     std::vector<int> keep;
     for (int i = 0; i < N; ++i)
         if (seg[i] == 1) keep.push_back(i);
     std::stable_sort(keep.begin(), keep.end(), [&](int a, int b) {
         return host_cu_seqlens[a + 1] - host_cu_seqlens[a] > host_cu_seqlens[b + 1] - host_cu_seqlens[b];
     });
+    std::unique_lock<std::mutex> lock(g_split_side.mu);
+    cudaEvent_t join = nullptr;
     if (!keep.empty()) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess || dev < 0 || dev >= 64)
+            return fail(KDA_ERR_CUDA, "cudaGetDevice failed or device index above 63");
+        if (g_split_side.side[dev] == nullptr) {
+            cudaStream_t ns = nullptr;
+            cudaEvent_t ef = nullptr, ej = nullptr;
+            if ((e = cudaStreamCreateWithFlags(&ns, cudaStreamNonBlocking)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&ef, cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&ej, cudaEventDisableTiming)) != cudaSuccess)
+                return fail(KDA_ERR_CUDA, std::string("side stream: ") + cudaGetErrorString(e));
+            g_split_side.side[dev] = ns;
+            g_split_side.fork[dev] = ef;
+            g_split_side.join[dev] = ej;
+        }
+        cudaStream_t side = g_split_side.side[dev];
+        join = g_split_side.join[dev];
         int *order = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + scan_bytes);
         // from pageable memory: the call returns once the list is staged, so `keep` may go
-        cudaError_t e = cudaMemcpyAsync(order, keep.data(), keep.size() * sizeof(int), cudaMemcpyHostToDevice, s);
+        e = cudaMemcpyAsync(order, keep.data(), keep.size() * sizeof(int), cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
+        if ((e = cudaEventRecord(g_split_side.fork[dev], s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(side, g_split_side.fork[dev], 0)) != cudaSuccess)
+            return fail(KDA_ERR_CUDA, std::string("fork: ") + cudaGetErrorString(e));
         if ((st = prefill_entry(q, k, v, g, beta, initial_state, final_state, out, cu_seqlens, N, T, H, D, C, dtype,
-                                gate, l2_eps, nullptr, 0, stream, nullptr, nullptr, KDA_ACT_SIGMOID, 0.f, order,
-                                (int)keep.size())))
+                                gate, l2_eps, nullptr, 0, reinterpret_cast<kda_stream_t>(side), nullptr, nullptr,
+                                KDA_ACT_SIGMOID, 0.f, order, (int)keep.size())))
             return st;
+        if ((e = cudaEventRecord(join, side)) != cudaSuccess)
+            return fail(KDA_ERR_CUDA, std::string("join: ") + cudaGetErrorString(e));
     }
-    // 2. each long sequence through the chunk-state scan over its own rows
+    // 2. each long sequence through the chunk-state scan over its own rows; `stream` then joins the
+    // side stream (also when a launch failed, so that nothing of the call runs unordered after it)
     const size_t elt = dtype == KDA_BF16 ? 2 : 4;
-    for (int i = 0; i < N; ++i) {
+    st = KDA_OK;
+    for (int i = 0; i < N && st == KDA_OK; ++i) {
         if (seg[i] == 1) continue;
         const int64_t t0 = host_cu_seqlens[i], len = host_cu_seqlens[i + 1] - t0;
         const size_t row = (size_t)t0 * H * D, sst = (size_t)i * H * D * D;
@@ -501,14 +549,17 @@ extern "C" kda_status kda_chunk_prefill_split(const void *q, const void *k, cons
                           : gate == KDA_GATE_CHANNEL ? g + row
                           : gate == KDA_GATE_HEAD ? g + (size_t)t0 * H
                                                   : g;
-        if ((st = kda_chunk_prefill_scan(static_cast<const uint8_t *>(q) + row * elt,
-                                         static_cast<const uint8_t *>(k) + row * elt,
-                                         static_cast<const uint8_t *>(v) + row * elt, gi, beta + (size_t)t0 * H,
-                                         initial_state ? initial_state + sst : nullptr,
-                                         final_state ? final_state + sst : nullptr,
-                                         static_cast<uint8_t *>(out) + row * elt, len, H, D, C, dtype, gate, l2_eps,
-                                         seg[i], workspace, scan_bytes, stream)))
-            return st;
+        st = kda_chunk_prefill_scan(static_cast<const uint8_t *>(q) + row * elt,
+                                    static_cast<const uint8_t *>(k) + row * elt,
+                                    static_cast<const uint8_t *>(v) + row * elt, gi, beta + (size_t)t0 * H,
+                                    initial_state ? initial_state + sst : nullptr,
+                                    final_state ? final_state + sst : nullptr,
+                                    static_cast<uint8_t *>(out) + row * elt, len, H, D, C, dtype, gate, l2_eps,
+                                    seg[i], workspace, scan_bytes, stream);
     }
-    return KDA_OK;
+    if (join != nullptr) {
+        cudaError_t e = cudaStreamWaitEvent(s, join, 0);
+        if (e != cudaSuccess && st == KDA_OK) return fail(KDA_ERR_CUDA, std::string("join: ") + cudaGetErrorString(e));
+    }
+    return st;
 }

@@ -310,12 +310,17 @@ def test_prefill_route_table(kda):
 def test_split_plan(kda):
     """The long-sequence split of kda_chunk_prefill_split, planned on the host for a given SM count: only a
     sequence whose chain outlasts the evenly spread work is split (here the 65,536-token one at 8 heads,
-    into 1024 // 57 = 17 segments), never at H not a multiple of 4, never the bench's varlen batch at 96
+    into 1024 // 57 = 17 segments, capped at (152 - 3 x 8) / 8 = 16 so that the three whole sequences'
+    CTAs have SMs of their own), never at H not a multiple of 4, never the bench's varlen batch at 96
     heads (its longest chain is shorter than its work per SM); invalid lengths give -1 (an error)."""
     import numpy as np
     cu = np.array([0, 65536, 66036, 69036, 69156], dtype=np.int64)
     seg, n = kda.kda_chunk_prefill_split_plan(cu, 8, 64, sms=152)
-    assert n == 1 and list(seg) == [17, 1, 1, 1]
+    assert n == 1 and list(seg) == [16, 1, 1, 1]
+    # the cap is skipped where it would leave fewer than 4 segments (36 whole sequences x 4 heads)
+    many = np.concatenate([[0, 65536], 65536 + 64 * np.arange(1, 37)]).astype(np.int64)
+    seg, n = kda.kda_chunk_prefill_split_plan(many, 4, 64, sms=152)
+    assert n == 1 and seg[0] == 1024 // -(-(1024 + 36) * 4 // 152) and list(seg[1:]) == [1] * 36
     seg, n = kda.kda_chunk_prefill_split_plan(cu, 6, 64, sms=152)
     assert n == 0 and list(seg) == [1, 1, 1, 1]
     varlen = np.cumsum([0, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536]).astype(np.int64)
