@@ -948,7 +948,31 @@ def bench_stack(torch, kda, dev, ws, hbm_peak, steps_per_graph=16, replays=8):
     kda.kda_sync_status()
     ms_step = max_over_ranks(a.elapsed_time(b) / (replays * G), dev)
     by = L * (Bs * H * DEC_UNIT_BYTES + CONV_W_BYTES)
+    del graph, x, g, beta, out
+
+    # Upper bound: the same 69 x 8 sequences' states in one tensor, stepped by one fused launch (one set
+    # of conv weights), so that no layer boundary stands between the heads
+    Bu = L * Bs
+    xu, ringu = rnd((Bu, 3, H, D)).to(torch.bfloat16), rnd((Bu, 3, H, 3, D)).to(torch.bfloat16)
+    gu, betau = -torch.nn.functional.softplus(rnd((Bu, H, D))), torch.sigmoid(rnd((Bu, H)))
+    stu, outu = rnd((Bu, H, D, D)) * 0.02, torch.empty((Bu, H, D), dtype=torch.bfloat16, device=dev)
+
+    def one(st, i=0):
+        kda.kda_shortconv_decode_step(xu, ringu, w[0], gu, betau, stu, outu, stream=st)
+    cs = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        one(cs)
+    torch.cuda.synchronize(dev)
+    ub_ms, _ = _graph_and_loop_ms(torch, dev, cs, one, 20, per_graph=10)
+    kda.kda_sync_status()
+    ub_ms = max_over_ranks(ub_ms, dev)
+    by_ub = Bu * H * DEC_UNIT_BYTES + CONV_W_BYTES
+    del xu, ringu, gu, betau, stu, outu
     return {"value": ws * by / (ms_step * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_step,
+            "upper_bound_single_launch": {
+                "ms_per_step": ub_ms, "frac": by_ub / (ub_ms * 1e-3) / 1e9 / hbm_peak,
+                "workload": f"the {Bu} sequences' states ({L} layers x {Bs}) in one [{Bu},{H},{D},{D}] tensor, one "
+                            "fused launch per step with one layer's conv weights, CUDA graph of 10 steps"},
             "config": {"workload": f"full-stack decode: {L} layers x {Bs} sequences x {H} heads, d={D}, bf16 q/k/v, "
                                    f"fp32 state 3.3 GB, {L} fused launches per step in a CUDA graph of {G} steps, "
                                    f"each a programmatic dependent launch overlapping the previous layer's tail",
