@@ -193,9 +193,16 @@ def cpu_baseline(d, budget_s=12.0):
         elapsed += _oracle_decode_sample(d, n, cores)
         reps += 1
     bytes_done = reps * (n * H * DEC_UNIT_BYTES + CONV_W_BYTES)
+    # the same oracle on one thread, over a smaller sample (about 2 s)
+    t_one = _oracle_decode_sample(d, 1, 1)
+    n1 = int(max(1, min(B, 2.0 / max(t_one, 1e-4))))
+    e1 = _oracle_decode_sample(d, n1, 1)
     return {"value": bytes_done / elapsed / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} x conv+decode step of {n} of {B} sequences x {H} heads (d={D}), fp64, "
-                      f"{cores} threads over (sequence, head) units, {elapsed:.1f} s"}
+                      f"{cores} threads over (sequence, head) units, {elapsed:.1f} s",
+            "single_thread": {"value": (n1 * H * DEC_UNIT_BYTES + CONV_W_BYTES) / e1 / 1e9, "unit": "GB/s",
+                              "sample": f"conv+decode step of {n1} of {B} sequences x {H} heads, 1 thread, "
+                                        f"{e1:.1f} s"}}
 
 
 def run_reference(args):
