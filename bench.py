@@ -184,6 +184,16 @@ def _oracle_decode_sample(d, n_seqs, nthreads):
     return time.perf_counter() - t0
 
 
+def _oracle_prefill_sample(n_heads, nthreads):
+    """Oracle token recurrence over the 4096-token prefill workload's first n_heads heads (the
+    workload's own seeded inputs for those heads); returns seconds."""
+    import oracle
+    p = synth.prefill_inputs(PRE["seed"], PRE["T"], H, D, True, heads=list(range(n_heads)))
+    t0 = time.perf_counter()
+    oracle.recurrence(p["q"], p["k"], p["v"], p["g"], p["beta"], nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(d, budget_s=12.0):
     cores = len(os.sched_getaffinity(0))
     t1 = _oracle_decode_sample(d, 1, cores)  # calibration: 1 sequence x 96 heads
@@ -202,7 +212,21 @@ def cpu_baseline(d, budget_s=12.0):
                       f"{cores} threads over (sequence, head) units, {elapsed:.1f} s",
             "single_thread": {"value": (n1 * H * DEC_UNIT_BYTES + CONV_W_BYTES) / e1 / 1e9, "unit": "GB/s",
                               "sample": f"conv+decode step of {n1} of {B} sequences x {H} heads, 1 thread, "
-                                        f"{e1:.1f} s"}}
+                                        f"{e1:.1f} s"},
+            "prefill": _prefill_cpu(cores)}
+
+
+def _prefill_cpu(cores, budget_s=4.0):
+    """The prefill metric on the host: the oracle over a head sample of the 4096-token workload, as
+    tokens/s for all H heads (the heads are independent units)."""
+    nh = min(H, max(1, cores))
+    t = _oracle_prefill_sample(nh, cores)
+    if t < budget_s / 4 and nh < H:  # enough time left for a larger sample
+        nh = min(H, int(nh * budget_s / 2 / max(t, 1e-3)))
+        t = _oracle_prefill_sample(nh, cores)
+    T = PRE["T"]
+    return {"value": T / (t * H / nh), "unit": "tokens/s", "cores": cores,
+            "sample": f"fp64 token recurrence over {nh} of {H} heads x {T} tokens, {cores} threads, {t:.1f} s"}
 
 
 def run_reference(args):
