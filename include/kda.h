@@ -333,8 +333,10 @@ kda_status kda_chunk_prefill_epi(const void *q, const void *k, const void *v, co
  *     one runs through kda_chunk_prefill_scan over its own rows, with its own
  *     initial and final state, on `stream`, which then waits for the side
  *     stream. The side stream and its two events are created on the first
- *     such call on a device and kept for the process; the enqueueing is
- *     serialised across host threads. Fork and join are stream-capture safe.
+ *     such call on a device and kept for the process (make that first call
+ *     outside a stream capture); the enqueueing is serialised across host
+ *     threads. The call can be captured into a CUDA graph: the launch order
+ *     travels in kernel parameters, and fork and join are events.
  *   - With nothing to split this is kda_chunk_prefill_gated.
  * Arguments as kda_chunk_prefill_gated, plus host_cu_seqlens: a host copy of
  * cu_seqlens (both required; they must agree, which is not checked on the

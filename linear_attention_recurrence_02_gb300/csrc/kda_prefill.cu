@@ -427,6 +427,18 @@ static int split_plan(const int64_t *cu, int N, int H, int C, int sms, int *seg)
     return n;
 }
 
+// The launch order of the sequences kda_chunk_prefill_split keeps whole travels
+// to the device in kernel parameters, ORDER_SLICE entries per launch, so that a
+// captured graph holds the list itself rather than a host address to copy from.
+constexpr int ORDER_SLICE = 1000;
+struct OrderSlice {
+    int offset, n;
+    int idx[ORDER_SLICE];
+};
+__global__ void order_fill_kernel(const __grid_constant__ OrderSlice sl, int *__restrict__ order) {
+    for (int i = threadIdx.x; i < sl.n; i += blockDim.x) order[sl.offset + i] = sl.idx[i];
+}
+
 // The side stream on which kda_chunk_prefill_split runs the sequences that stay
 // whole, and the fork and join events around it: one set per device, created on
 // first use and kept for the process. The mutex serialises the calls' enqueueing
@@ -524,9 +536,14 @@ extern "C" kda_status kda_chunk_prefill_split(const void *q, const void *k, cons
         cudaStream_t side = g_split_side.side[dev];
         join = g_split_side.join[dev];
         int *order = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + scan_bytes);
-        // from pageable memory: the call returns once the list is staged, so `keep` may go
-        e = cudaMemcpyAsync(order, keep.data(), keep.size() * sizeof(int), cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return fail(KDA_ERR_CUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
+        for (size_t o = 0; o < keep.size(); o += ORDER_SLICE) {
+            OrderSlice sl;
+            sl.offset = (int)o;
+            sl.n = (int)std::min<size_t>(ORDER_SLICE, keep.size() - o);
+            std::copy(keep.begin() + (ptrdiff_t)o, keep.begin() + (ptrdiff_t)(o + sl.n), sl.idx);
+            order_fill_kernel<<<1, 256, 0, s>>>(sl, order);
+            if ((st = check_launch("order_fill_kernel"))) return st;
+        }
         if ((e = cudaEventRecord(g_split_side.fork[dev], s)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(side, g_split_side.fork[dev], 0)) != cudaSuccess)
             return fail(KDA_ERR_CUDA, std::string("fork: ") + cudaGetErrorString(e));

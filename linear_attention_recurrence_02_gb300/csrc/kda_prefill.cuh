@@ -66,6 +66,10 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t
 // device error word and returns false (the caller skips the sequence).
 __device__ __forceinline__ bool seq_range(const int64_t *cu, int n, int N, int64_t T, unsigned *err,
                                           int64_t &start, int64_t &end) {
+    if (n < 0 || n >= N) {  // a launch-order entry that names no sequence
+        if (err) atomicOr(err, DEVERR_SEQLENS);
+        return false;
+    }
     if (cu == nullptr) {
         start = 0;
         end = T;

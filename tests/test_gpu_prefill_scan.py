@@ -195,6 +195,46 @@ def test_split_batch_with_a_long_sequence(env, bf16):
     assert_close(res[0][0], res[1][0], bf16, (1,), "split vs whole")
 
 
+def test_split_captured_in_a_cuda_graph(env):
+    """kda_chunk_prefill_split captured into a CUDA graph through the C ABI (its side stream forks from and
+    joins the capturing stream; the host lengths and every device buffer prepared before the capture) and
+    replayed: bit-identical outputs and final states to the direct call."""
+    torch, kda = env
+    H, D = 4, 128
+    lens = [4096, 100, 200]
+    cu = np.cumsum([0] + lens).astype(np.int64)
+    seg, nsplit = kda.kda_chunk_prefill_split_plan(cu, H, 64)
+    assert nsplit == 1 and seg[0] >= 4 and seg[1] == 1 and seg[2] == 1, seg
+    p = synth.prefill_inputs(47, int(cu[-1]), H, D, True, cu_seqlens=cu, s0_std=0.05, g_scale=0.02)
+    bf = torch.bfloat16
+    q, k, v = (to_dev(p[n], bf, torch) for n in "qkv")
+    g, b = to_dev(p["g"], torch.float32, torch), to_dev(p["beta"], torch.float32, torch)
+    s0 = to_dev(p["s0"], torch.float32, torch)
+    dev_cu = torch.from_numpy(cu).cuda()
+    lib = kda.lib()
+    N, T = len(lens), int(cu[-1])
+    need = int(lib.kda_chunk_prefill_split_workspace_bytes(cu.ctypes.data, N, H, D, 64))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    outs = [(torch.full_like(q, float("nan")), torch.full((N, H, D, D), float("nan"), device="cuda"))
+            for _ in range(2)]
+
+    def call(o, sf, stream):
+        return lib.kda_chunk_prefill_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), b.data_ptr(),
+                                           s0.data_ptr(), sf.data_ptr(), o.data_ptr(), dev_cu.data_ptr(),
+                                           cu.ctypes.data, N, T, H, D, 64, kda.KDA_BF16, 0, 1e-6, ws.data_ptr(),
+                                           ws.numel(), stream)
+    assert call(*outs[0], torch.cuda.current_stream().cuda_stream) == kda.KDA_OK
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        st = call(*outs[1], torch.cuda.current_stream().cuda_stream)
+    assert st == kda.KDA_OK, lib.kda_last_error_detail().decode()
+    graph.replay()
+    torch.cuda.synchronize()
+    kda.kda_sync_status()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 @pytest.mark.parametrize("gate", ["channel", "head"])
 def test_split_batch_with_two_long_sequences(env, gate):
     """kda_chunk_prefill_split with two sequences long enough to split (the scan workspace reused for
