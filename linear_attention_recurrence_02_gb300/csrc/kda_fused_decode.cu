@@ -6,13 +6,15 @@
 // front of q/k/v, then decay, delta correction and readout), except that the
 // post-conv q, k, v stay in fp32 on chip instead of being stored and read back.
 //
-// One CTA per (sequence, head) owns the whole D x D state slice in registers
-// (D=128: 256 threads x 16 rows x one float4) and every ring channel of that
-// head, so the in-place ring shift cannot race with another CTA's read. The
-// state loads are issued first and stay in flight while the conv, the norms
-// and the decay run; column sums of S'^T k^ and S'^T q^ are reduced through
-// shared memory across the row groups; S is written once. The gate form
-// (per channel, per head, none) is a template parameter as in kda_decode.cu.
+// One CTA per (sequence, head) owns the head's whole D x D state and every
+// ring channel of that head, so the in-place ring shift cannot race with
+// another CTA's read. For D < 128 the state lives in registers; for D = 128
+// one bulk copy stages it in shared memory (fused_decode_bulk_kernel, three
+// heads per SM). Either way the state's loads are issued first and stay in
+// flight while the conv, the norms and the decay run; column sums of S'^T k^
+// and S'^T q^ are reduced through shared memory across the row groups; S is
+// written once. The gate form (per channel, per head, none) is a template
+// parameter as in kda_decode.cu.
 //
 // With an output epilogue (template parameter EP = the gate activation), the
 // head's output vector o never leaves the CTA: it is normalised by its RMS,
@@ -24,7 +26,6 @@
 // channels: y = o / sqrt(mean(o^2) + eps) * weight * act(gate), a row whose
 // mean square plus eps is zero giving zeros. o is taken in fp32, before any
 // rounding to the storage type.
-#include <atomic>
 #include <string>
 
 #include "kda_common.cuh"
@@ -36,7 +37,6 @@ template <int D> struct FusedShape;
 template <> struct FusedShape<16> { static constexpr int NT = 32; };
 template <> struct FusedShape<32> { static constexpr int NT = 64; };
 template <> struct FusedShape<64> { static constexpr int NT = 128; };
-template <> struct FusedShape<128> { static constexpr int NT = 256; };
 
 // Output epilogue selector: no epilogue (o is stored), or the gate
 // activation of the gated RMSNorm (KDA_ACT_SIGMOID, KDA_ACT_SILU).
@@ -415,7 +415,7 @@ static void launch_fused(const void *x, void *ring, const float *w, const float 
     const T *gi = static_cast<const T *>(ea.gate);
     // d = 128: the staged kernel at every batch size (B=64, H=96: 131.9 us against 133.1 us for the
     // register kernel, once its shared-memory accesses compiled to shared-memory instructions)
-    if (D == 128) {
+    if constexpr (D == 128) {
         if (smem_attr_once<fused_decode_bulk_kernel<T, GM, EP>>((int)BULK_SMEM) != cudaSuccess)
             return;  // reported by check_launch
         if (overlap) {  // programmatic dependent launch: may start while the previous kernel drains

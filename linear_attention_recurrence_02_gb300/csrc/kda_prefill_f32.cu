@@ -1,6 +1,7 @@
 // kda_prefill_f32.cu -- chunked prefill for d = 128 on CUDA cores in fp32
-// arithmetic: the fast path for fp32 q/k/v (and for bf16 chunk sizes the
-// tensor-core kernel does not take).
+// arithmetic: the d = 128 path for the shapes neither tensor-core kernel
+// takes (fp32 q/k/v with a chunk below 16, bf16 with a chunk other than 16,
+// 32 or 64, and an empty token range).
 //
 // Chunk algebra ("为什么 Kimi K3 敢把 KV Cache 扔掉？一篇讲透 GPT-2 到 K3 的架构进化",
 // section 5: attention-like work inside a chunk, the state handed from chunk

@@ -1,5 +1,7 @@
 // kda_prefill_tc.cu -- chunked KDA prefill on the 5th-generation tensor
-// cores (tcgen05 + TMEM + TMA) for bf16 q/k/v, d_k = d_v = 128, chunk 64.
+// cores (tcgen05 + TMEM + TMA) for bf16 q/k/v, d_k = d_v = 128 or 64 (the
+// latter as zero channels of the 128-channel layout), in chunks of 64 tokens
+// (a requested C of 16 or 32 runs the same 64-token algebra).
 //
 // Method: the chunk algebra of the general kernel (kda_prefill.cu; "为什么 Kimi
 // K3 敢把 KV Cache 扔掉？一篇讲透 GPT-2 到 K3 的架构进化", section 5: attention-
@@ -9,7 +11,7 @@
 // cumulative log decay inside the chunk and a per-channel anchor c:
 //   Lk = e^{G-c} k^,  Lq = e^{G-c} q^,  Rk = e^{c-G} k^,  S~ = Diag(e^c) S
 //   [A_raw; P_raw] = [Lk; Lq] Rk^T            (G1)   A = mask_<(beta A_raw)
-//   T = (I + A)^-1 Diag(beta)                  (CUDA cores, fp32)
+//   T = (I + A)^-1 Diag(beta)                  (CUDA cores, fp32, and tf32 mma.sync merges)
 //   W' = T Lk,  U0 = T V                       (G2, G3)
 //   U = U0 - W' S~                             (G4)
 //   O = Lq S~ + P U                            (G5, G6)
