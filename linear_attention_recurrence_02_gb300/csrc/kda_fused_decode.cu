@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(BULK_NT, 3)
     fused_decode_bulk_kernel(const T *__restrict__ x, T *__restrict__ ring, const float *__restrict__ w,
                              const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ state,
                              T *__restrict__ out, int H, float eps, unsigned *err, const T *__restrict__ gate_in,
-                             const float *__restrict__ nweight, float neps) {
+                             const float *__restrict__ nweight, float neps, int prefetch_inputs) {
     using namespace tc;
     constexpr int D = 128, NW = BULK_NT / 32;
     extern __shared__ uint8_t smem_raw[];
@@ -259,6 +259,21 @@ __global__ void __launch_bounds__(BULK_NT, 3)
     // completed. Dependents are released only after the wait, so a kernel two
     // launches back has always completed before the next one starts its copy.
     // Launched plainly, both are no-ops.
+    // Before the wait, the head's x, ring, tap, g, beta (and output gate) rows
+    // are prefetched into L2 only. L2 is where the previous kernel's writes
+    // land, and every load of these rows comes after the wait, so a prefetch
+    // can bring them closer but never serve a stale value.
+    if (prefetch_inputs && t < 12) {
+        const size_t row = ((size_t)b * 3 + (t % 3)) * H + h;  // (b*3 + p)*H + h
+        if (t < 3) prefetch_l2_bulk(x + row * D, D * sizeof(T));
+        else if (t < 6) prefetch_l2_bulk(ring + row * 3 * D, 3 * D * sizeof(T));
+        else if (t >= 9) prefetch_l2_bulk(w + ((size_t)(t - 9) * H + h) * D * 4, D * 16);  // taps of projection t - 9
+        else if (t == 6) {
+            if constexpr (GM == KDA_GATE_CHANNEL) prefetch_l2_bulk(g + (size_t)unit * D, D * 4);
+            else if constexpr (GM == KDA_GATE_HEAD) asm volatile("prefetch.global.L2 [%0];" ::"l"(g + unit));
+        } else if (t == 7) asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + unit));
+        else if constexpr (EP != EP_NONE) prefetch_l2_bulk(gate_in + (size_t)unit * D, D * sizeof(T));
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -431,12 +446,12 @@ static void launch_fused(const void *x, void *ring, const float *w, const float 
             cfg.numAttrs = 1;
             cudaLaunchKernelEx(&cfg, fused_decode_bulk_kernel<T, GM, EP>, static_cast<const T *>(x),
                                static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
-                               device_error_word(), gi, ea.weight, ea.eps);  // an error is left for check_launch
+                               device_error_word(), gi, ea.weight, ea.eps, 1);  // an error is left for check_launch
             return;
         }
         fused_decode_bulk_kernel<T, GM, EP><<<(unsigned)B * H, BULK_NT, BULK_SMEM, s>>>(
             static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
-            device_error_word(), gi, ea.weight, ea.eps);
+            device_error_word(), gi, ea.weight, ea.eps, 0);
     } else {
         fused_decode_kernel<D, T, GM, EP><<<(unsigned)B * H, FusedShape<D>::NT, 0, s>>>(
             static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
