@@ -179,7 +179,12 @@ kda_status kda_decode_step_gated(const void *q, const void *k, const void *v, co
  *   x [B,3,H,D] dtype, ring [B,3,H,3,D] dtype (in/out), w [3,H,D,4] fp32,
  *   g [B,H,D] fp32, beta [B,H] fp32, state [B,H,D,D] fp32 (in/out),
  *   out [B,H,D] dtype
- * Same requirements and errors as the two calls it replaces.
+ * Same requirements and errors as the two calls it replaces. At D = 128 the
+ * launch is a programmatic dependent launch: it may start while the kernel
+ * before it on `stream` drains, but before that kernel has completed it only
+ * prefetches its state and input rows into L2 (which cannot serve a stale
+ * value); every read and write waits. So the results are those of a plain
+ * launch, and consecutive steps on one state overlap their launch boundary.
  */
 kda_status kda_shortconv_decode_step(const void *x, void *ring, const float *w, const float *g,
                                      const float *beta, float *state, void *out, int B, int H, int D,

@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(BULK_NT, 3)
     fused_decode_bulk_kernel(const T *__restrict__ x, T *__restrict__ ring, const float *__restrict__ w,
                              const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ state,
                              T *__restrict__ out, int H, float eps, unsigned *err, const T *__restrict__ gate_in,
-                             const float *__restrict__ nweight, float neps, int prefetch_inputs) {
+                             const float *__restrict__ nweight, float neps, int mode) {
     using namespace tc;
     constexpr int D = 128, NW = BULK_NT / 32;
     extern __shared__ uint8_t smem_raw[];
@@ -247,23 +247,32 @@ __global__ void __launch_bounds__(BULK_NT, 3)
     const int b = unit / H, h = unit % H;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     float *Sg = state + (size_t)unit * D * D;
+    // Every launch is a programmatic dependent launch: it may start while the
+    // kernel before it on the stream drains, and griddepcontrol.wait below
+    // holds the CTA until that kernel has completed. mode 1
+    // (KDA_DECODE_OVERLAP_PREV: that kernel does not write this state) issues
+    // the state copy before the wait; mode 2 (no promise) issues only L2
+    // prefetches before it and the copy after it.
     if (t == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bar, D * D * 4);
-        bulk_load(Ss, Sg, D * D * 4, &bar);
+        if (mode != 2) {
+            mbar_arrive_expect_tx(&bar, D * D * 4);
+            bulk_load(Ss, Sg, D * D * 4, &bar);
+        }
     }
-    // Launched as a programmatic dependent (KDA_DECODE_OVERLAP_PREV), the state
-    // copy above overlaps the previous kernel's tail, and this wait holds every
-    // read of x, ring, g and beta (that kernel's possible outputs) until it has
-    // completed. Dependents are released only after the wait, so a kernel two
-    // launches back has always completed before the next one starts its copy.
-    // Launched plainly, both are no-ops.
-    // Before the wait, the head's x, ring, tap, g, beta (and output gate) rows
-    // are prefetched into L2 only. L2 is where the previous kernel's writes
-    // land, and every load of these rows comes after the wait, so a prefetch
-    // can bring them closer but never serve a stale value.
-    if (prefetch_inputs && t < 12) {
+    // In mode 1 the state copy above overlaps the previous kernel's tail. In
+    // both modes the wait below holds every read of x, ring, g and beta (that
+    // kernel's possible outputs), and in mode 2 also the state copy, until it
+    // has completed. Dependents are released only after the wait, so a kernel
+    // two launches back has always completed before the next one starts.
+    // Before the wait, the head's state (mode 2) and its x, ring, tap, g, beta
+    // (and output gate) rows are prefetched into L2 only. L2 is where the
+    // previous kernel's writes land, and every load of these rows comes after
+    // the wait, so a prefetch can bring them closer but never serve a stale
+    // value.
+    if (mode == 2 && t >= 12 && t < 16) prefetch_l2_bulk(Sg + (t - 12) * (D * D / 4), D * D);  // the state, 4 x 16 KB
+    if (t < 12) {
         const size_t row = ((size_t)b * 3 + (t % 3)) * H + h;  // (b*3 + p)*H + h
         if (t < 3) prefetch_l2_bulk(x + row * D, D * sizeof(T));
         else if (t < 6) prefetch_l2_bulk(ring + row * 3 * D, 3 * D * sizeof(T));
@@ -275,6 +284,10 @@ __global__ void __launch_bounds__(BULK_NT, 3)
         else if constexpr (EP != EP_NONE) prefetch_l2_bulk(gate_in + (size_t)unit * D, D * sizeof(T));
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (mode == 2 && t == 0) {
+        mbar_arrive_expect_tx(&bar, D * D * 4);
+        bulk_load(Ss, Sg, D * D * 4, &bar);
+    }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // 1. width-4 causal conv + SiLU for q, k, v; shift the ring
@@ -429,29 +442,26 @@ static void launch_fused(const void *x, void *ring, const float *w, const float 
                          cudaStream_t s) {
     const T *gi = static_cast<const T *>(ea.gate);
     // d = 128: the staged kernel at every batch size (B=64, H=96: 131.9 us against 133.1 us for the
-    // register kernel, once its shared-memory accesses compiled to shared-memory instructions)
+    // register kernel, once its shared-memory accesses compiled to shared-memory instructions;
+    // 124.5 us once every launch became a dependent launch that prefetches its state into L2)
     if constexpr (D == 128) {
         if (smem_attr_once<fused_decode_bulk_kernel<T, GM, EP>>((int)BULK_SMEM) != cudaSuccess)
             return;  // reported by check_launch
-        if (overlap) {  // programmatic dependent launch: may start while the previous kernel drains
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)B * H);
-            cfg.blockDim = dim3(BULK_NT);
-            cfg.dynamicSmemBytes = BULK_SMEM;
-            cfg.stream = s;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            cudaLaunchKernelEx(&cfg, fused_decode_bulk_kernel<T, GM, EP>, static_cast<const T *>(x),
-                               static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
-                               device_error_word(), gi, ea.weight, ea.eps, 1);  // an error is left for check_launch
-            return;
-        }
-        fused_decode_bulk_kernel<T, GM, EP><<<(unsigned)B * H, BULK_NT, BULK_SMEM, s>>>(
-            static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
-            device_error_word(), gi, ea.weight, ea.eps, 0);
+        // a programmatic dependent launch: it may start while the previous kernel drains
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)B * H);
+        cfg.blockDim = dim3(BULK_NT);
+        cfg.dynamicSmemBytes = BULK_SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, fused_decode_bulk_kernel<T, GM, EP>, static_cast<const T *>(x),
+                           static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
+                           device_error_word(), gi, ea.weight, ea.eps,
+                           overlap ? 1 : 2);  // an error is left for check_launch
     } else {
         fused_decode_kernel<D, T, GM, EP><<<(unsigned)B * H, FusedShape<D>::NT, 0, s>>>(
             static_cast<const T *>(x), static_cast<T *>(ring), w, g, beta, state, static_cast<T *>(out), H, eps,
