@@ -295,6 +295,38 @@ def test_fused_conv_decode_1248_heads(env, gate):
         assert np.array_equal(to_np(tr), ring)
 
 
+def test_fused_decode_after_a_kernel_that_writes_the_state(env):
+    """Every d = 128 fused step is a programmatic dependent launch that may start while the kernel
+    before it drains, touching only L2 prefetches until that kernel completes. Here a torch kernel
+    halves the state (and shifts the ring's newest slot) between two fused steps on the same state;
+    the second step must see those writes: both steps against the oracle doing the same."""
+    torch, kda = env
+    B, H, D = 16, 96, 128
+    d = synth.decode_inputs(860, B, H, D, True, s0_std=0.3)
+    bf = torch.bfloat16
+    tx, tr = to_dev(d["x"], bf, torch), to_dev(d["ring"], bf, torch)
+    tw, tg, tb = (to_dev(d[n], torch.float32, torch) for n in ("w", "g", "beta"))
+    ts = to_dev(d["s0"], torch.float32, torch)
+    outs = [torch.empty((B, H, D), dtype=bf, device="cuda") for _ in range(2)]
+    kda.kda_shortconv_decode_step(tx, tr, tw, tg, tb, ts, outs[0])
+    ts.mul_(0.5)                         # a plain torch kernel writing the state
+    tr[:, :, :, 2].mul_(-1.0)            # and the ring's newest slot
+    kda.kda_shortconv_decode_step(tx, tr, tw, tg, tb, ts, outs[1])
+    torch.cuda.synchronize()
+    kda.kda_sync_status()
+    ry, ring = oracle.shortconv_step(d["x"], d["ring"], d["w"])
+    ro0, st = oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], d["g"], d["beta"], d["s0"], nthreads=NCPU)
+    st = st * 0.5
+    ring = ring.copy()
+    ring[:, :, :, 2] = -ring[:, :, :, 2]
+    ry, ring = oracle.shortconv_step(d["x"], ring, d["w"])
+    ro1, st = oracle.decode_step(ry[:, 0], ry[:, 1], ry[:, 2], d["g"], d["beta"], st, nthreads=NCPU)
+    assert_close(to_np(outs[0]), ro0, True, (0, 1), "out step 0")
+    assert_close(to_np(outs[1]), ro1, True, (0, 1), "out step 1")
+    assert_close(to_np(ts), st, True, (0, 1), "state")
+    assert np.array_equal(to_np(tr), ring)
+
+
 def test_fused_conv_decode_consecutive_steps(env):
     """Four fused steps in a row (ring and state carried) against the oracle
     run step by step on the same inputs."""
