@@ -281,7 +281,8 @@ __device__ __forceinline__ void mma44_ts(uint32_t d1, uint64_t b1, uint32_t ides
 //   chain, warps 12-15: the state chain of chunk c (S~ conversion, G4/G5, U,
 //     G6/G7, output).
 // The hand-offs are mbarriers in shared memory:
-//   fr[b]     front -> back: operand tiles of chunk parity b built
+//   fr[b]     front -> back: operand tiles of chunk parity b built (with the
+//             per-channel gate the chain waits on it too: the S~ factors)
 //   ready[b]  back -> chain: chunk of parity b fully prepared
 //   c45[b]    G4/G5 of chunk parity b done (tcgen05.commit): its W' / Lq
 //             tile may be reloaded; the chain itself then issues the q/k
@@ -1144,7 +1145,12 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             const int b = ci & 1;
             const int64_t c0 = start + (int64_t)ci * C;
             const int L = (int)((end - c0) < (int64_t)C ? (end - c0) : (int64_t)C);
-            bool got = ct >= 32 || wait_or_abort(bar_ready + b, (ci >> 1) & 1, s_abort);
+            // S~ needs only the front's factors of this chunk, published with its operand
+            // tiles. With the per-channel gate the chain converts it while the back still
+            // works on the chunk (4K 283 -> 280 us, 8 x 8192 tokens 3.21 -> 3.15 ms). With a
+            // per-head gate or none the early conversion competes with the back's solve and
+            // is slower (259 -> 265 us, 240 -> 252 us), so those forms wait for the back first.
+            bool got = ct >= 32 || wait_or_abort((GCH ? bar_fr : bar_ready) + b, (ci >> 1) & 1, s_abort);
             if (group_or(BAR_CHAIN, 128, !got)) {
                 ok = false;
                 break;
@@ -1189,7 +1195,15 @@ __global__ void __launch_bounds__(pipe::NTP, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            named_bar_sync(BAR_CHAIN, 128);
+            if constexpr (GCH) {
+                got = ct >= 32 || wait_or_abort(bar_ready + b, (ci >> 1) & 1, s_abort);
+                if (group_or(BAR_CHAIN, 128, !got)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                named_bar_sync(BAR_CHAIN, 128);
+            }
             tc_fence_after();
             // G4: X^T = S~^T W'^T (W' channel-major), G5: O^T = S~^T Lq^T, one commit
             if (ct < 32)
