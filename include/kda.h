@@ -109,7 +109,10 @@ size_t kda_shortconv_ring_bytes(int layers, int batch, int heads, int d, int ele
  * if the driver's tensor-map encoder rejects them. A copy that does not land
  * within about a second sets the device error word (KDA_ERR_TIMEOUT from the
  * next kda_sync_status); the sequences of that copy keep their y and ring
- * contents.
+ * contents. The launch is a programmatic dependent launch: it may start while
+ * the kernel before it on the stream drains, but reads x, ring and w only once
+ * that kernel has completed (before that it only prefetches them into L2), so
+ * stream order holds as for a plain launch.
  */
 kda_status kda_shortconv_step(const void *x, void *ring, const float *w, void *y,
                               int B, int H, int D, kda_dtype dtype, kda_stream_t stream);

@@ -94,6 +94,11 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x
                  "r"(z)
                  : "memory");
 }
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(z), "r"(w)
+                 : "memory");
+}
 // 3-D tiled store shared -> global (bulk-group completion); no coordinate may be negative.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
